@@ -1,0 +1,272 @@
+"""numpy front end of the plain CPU oracle (``oracle/pq_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+(``w4a8_rotated_int4_gb300``) never imports it, and this package never imports
+the product.
+
+Every function follows one step of the method described on the page
+"ParoQuant (PARO) W4A8 on gfx1201 -- engineering log" (sections "Format",
+"Inference identity", "Design" 1-4, "Gates passed"); the C file's header
+lists the readings taken where the page is silent.
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py
+(closed forms, library routines, exhaustive enumeration, brute force).  The
+one exception is bit-level agreement of the fp32 rotation with the pages' own
+kernel, which prints no worked values: parity unpinned against the pages for
+that detail; it is pinned against the stated operation order only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        vp, i32, u64 = C.c_void_p, C.c_int, C.c_uint64
+        L.orc_f16_to_double.restype = C.c_double
+        L.orc_f16_to_double.argtypes = [C.c_uint16]
+        L.orc_f16_from_double.restype = C.c_uint16
+        L.orc_f16_from_double.argtypes = [C.c_double]
+        L.orc_e4m3_decode.restype = C.c_double
+        L.orc_e4m3_decode.argtypes = [C.c_uint8]
+        L.orc_e4m3_encode.restype = C.c_uint8
+        L.orc_e4m3_encode.argtypes = [C.c_float]
+        L.orc_unpack_awq.argtypes = [i32, i32, vp, vp]
+        L.orc_check_pairs.argtypes = [i32, i32, vp]
+        L.orc_records.argtypes = [i32, i32, vp, vp, vp]
+        L.orc_sz.argtypes = [i32, i32, vp, vp, vp]
+        L.orc_repack.argtypes = [i32, i32, vp, vp]
+        L.orc_rotate_group_f32.argtypes = [vp, i32, i32, i32, vp]
+        L.orc_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_gemm_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.orc_gemm_f64_sampled.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32,
+                                           vp, vp, vp, vp, vp, vp]
+        L.orc_gemm_format_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.orc_linear_rotx_f64.argtypes = [i32] * 6 + [vp] * 6
+        L.orc_linear_rotw_f64.argtypes = [i32] * 6 + [vp] * 6
+        L.orc_e4m3_check_range.restype = C.c_longlong
+        L.orc_e4m3_check_range.argtypes = [u64, u64, C.POINTER(C.c_uint32)]
+        L.orc_num_threads.restype = i32
+        L.orc_set_num_threads.argtypes = [i32]
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- scalars
+def f16_to_double(h: int) -> float:
+    return lib().orc_f16_to_double(int(h))
+
+
+def f16_from_double(x: float) -> int:
+    return int(lib().orc_f16_from_double(float(x)))
+
+
+def e4m3_decode(c: int) -> float:
+    return lib().orc_e4m3_decode(int(c))
+
+
+def e4m3_encode(q: float) -> int:
+    return int(lib().orc_e4m3_encode(float(q)))
+
+
+def e4m3_decode_table() -> np.ndarray:
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_check_range(lo: int, hi: int):
+    """(#disagreements, first bad pattern) of the encoder against nearest-value
+    search over binary32 patterns [lo, hi)."""
+    first = C.c_uint32(0)
+    bad = lib().orc_e4m3_check_range(lo, hi, C.byref(first))
+    return int(bad), int(first.value)
+
+
+def num_threads() -> int:
+    return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    lib().orc_set_num_threads(int(n))
+
+
+# ---------------------------------------------------------------- format
+def unpack_awq(packed: np.ndarray, N: int) -> np.ndarray:
+    packed = _c(packed, np.int32)
+    rows = packed.shape[0]
+    out = np.empty((rows, N), dtype=np.uint8)
+    lib().orc_unpack_awq(rows, N, _p(packed), _p(out))
+    return out
+
+
+def check_pairs(pairs: np.ndarray) -> bool:
+    pairs = _c(pairs, np.int16)
+    P, _, K = pairs.shape
+    return lib().orc_check_pairs(P, K, _p(pairs)) == 0
+
+
+def records(pairs: np.ndarray, theta: np.ndarray) -> np.ndarray:
+    """Rotation records [P, 8, G, 64] x 8 bytes (as uint8 [P, 8, G, 64, 8])."""
+    pairs = _c(pairs, np.int16)
+    theta = _c(theta, np.uint16)
+    P, _, K = pairs.shape
+    out = np.zeros((P, 8, K // 128, 64, 8), dtype=np.uint8)
+    rc = lib().orc_records(P, K, _p(pairs), _p(theta), _p(out))
+    if rc != 0:
+        raise ValueError("orc_records failed with code %d" % rc)
+    return out
+
+
+def sz_table(scales: np.ndarray, qzeros: np.ndarray) -> np.ndarray:
+    """SZ table [G, N, 2] f16 bit patterns (scale, scale*(zp-8))."""
+    scales = _c(scales, np.uint16)
+    qzeros = _c(qzeros, np.int32)
+    G, N = scales.shape
+    out = np.empty((G, N, 2), dtype=np.uint16)
+    lib().orc_sz(G, N, _p(scales), _p(qzeros), _p(out))
+    return out
+
+
+def repack(qweight: np.ndarray) -> np.ndarray:
+    """Kernel weight bytes [N, K/2]."""
+    qweight = _c(qweight, np.int32)
+    K, N8 = qweight.shape
+    out = np.empty((N8 * 8, K // 2), dtype=np.uint8)
+    lib().orc_repack(K, N8 * 8, _p(qweight), _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- prologue
+def rotate_group_f32(rec: np.ndarray, p: int, g: int, v: np.ndarray) -> np.ndarray:
+    rec = _c(rec, np.uint8)
+    G = rec.shape[2]
+    v = _c(v, np.float32).copy()
+    lib().orc_rotate_group_f32(_p(rec), G, p, g, _p(v))
+    return v
+
+
+def rotate_quant(x: np.ndarray, cs: np.ndarray, rec: np.ndarray, want_v: bool = False):
+    """(a e4m3 [P,M,K], asg f32 [P,G,M], rs f32 [P,G,M][, v f32 [P,M,K]])."""
+    x = _c(x, np.uint16)
+    cs = _c(cs, np.uint16)
+    rec = _c(rec, np.uint8)
+    M, ldx = x.shape
+    P, K = cs.shape
+    G = K // 128
+    a = np.empty((P, M, K), dtype=np.uint8)
+    asg = np.empty((P, G, M), dtype=np.float32)
+    rs = np.empty((P, G, M), dtype=np.float32)
+    v = np.empty((P, M, K), dtype=np.float32) if want_v else None
+    lib().orc_rotate_quant(M, K, ldx, P, _p(x), _p(cs), _p(rec), _p(a), _p(asg), _p(rs),
+                           _p(v) if want_v else None)
+    return (a, asg, rs, v) if want_v else (a, asg, rs)
+
+
+# ---------------------------------------------------------------- GEMM
+def gemm_f64(a, asg, rs, codes, sz, pb1, pb2) -> np.ndarray:
+    a = _c(a, np.uint8); asg = _c(asg, np.float32); rs = _c(rs, np.float32)
+    codes = _c(codes, np.uint8); sz = _c(sz, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_gemm_f64(M, N, K, pb1, pb2, _p(a), _p(asg), _p(rs), _p(codes), _p(sz), _p(y))
+    return y
+
+
+def gemm_f64_sampled(ms, ns, a, asg, rs, codes, sz, pb1, pb2) -> np.ndarray:
+    ms = _c(ms, np.int32); ns = _c(ns, np.int32)
+    a = _c(a, np.uint8); asg = _c(asg, np.float32); rs = _c(rs, np.float32)
+    codes = _c(codes, np.uint8); sz = _c(sz, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty(len(ms), dtype=np.float64)
+    lib().orc_gemm_f64_sampled(len(ms), _p(ms), _p(ns), M, N, K, pb1, pb2, _p(a), _p(asg),
+                               _p(rs), _p(codes), _p(sz), _p(y))
+    return y
+
+
+def gemm_format_f64(a, asg, codes, zp, scales, pb1, pb2) -> np.ndarray:
+    a = _c(a, np.uint8); asg = _c(asg, np.float32); codes = _c(codes, np.uint8)
+    zp = _c(zp, np.uint8); scales = _c(scales, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_gemm_format_f64(M, N, K, pb1, pb2, _p(a), _p(asg), _p(codes), _p(zp), _p(scales),
+                              _p(y))
+    return y
+
+
+def linear_rotx_f64(x, cs, pairs, theta, W, pb1, pb2) -> np.ndarray:
+    x = _c(x, np.uint16); cs = _c(cs, np.uint16); pairs = _c(pairs, np.int16)
+    theta = _c(theta, np.uint16); W = _c(W, np.float64)
+    M, K = x.shape
+    N = W.shape[0]
+    P = cs.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_linear_rotx_f64(M, K, N, P, pb1, pb2, _p(x), _p(cs), _p(pairs), _p(theta), _p(W),
+                              _p(y))
+    return y
+
+
+def linear_rotw_f64(x, cs, pairs, theta, W, pb1, pb2) -> np.ndarray:
+    x = _c(x, np.uint16); cs = _c(cs, np.uint16); pairs = _c(pairs, np.int16)
+    theta = _c(theta, np.uint16); W = _c(W, np.float64)
+    M, K = x.shape
+    N = W.shape[0]
+    P = cs.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_linear_rotw_f64(M, K, N, P, pb1, pb2, _p(x), _p(cs), _p(pairs), _p(theta), _p(W),
+                              _p(y))
+    return y
+
+
+# ---------------------------------------------------------------- whole layer
+def pack(prob) -> dict:
+    """Oracle's own load-time tables for a generated problem."""
+    return dict(rec=records(prob["pairs"], prob["theta"]),
+                sz=sz_table(prob["scales"], prob["qzeros"]),
+                w=repack(prob["qweight"]),
+                codes=unpack_awq(prob["qweight"], prob["N"]),
+                zp=unpack_awq(prob["qzeros"], prob["N"]))
+
+
+def layer(prob, tables=None):
+    """Prologue + fp64 GEMM on a generated problem: (a, asg, rs, y64)."""
+    t = tables or pack(prob)
+    a, asg, rs = rotate_quant(prob["x"], prob["cs"], t["rec"])
+    y = gemm_f64(a, asg, rs, t["codes"], t["sz"], prob["pb1"], prob["pb2"])
+    return a, asg, rs, y
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def rel_err(y, y64) -> float:
+    """Norm-wise relative error ||y - y64||_F / ||y64||_F."""
+    y = np.asarray(y, dtype=np.float64)
+    d = np.linalg.norm((y - y64).ravel())
+    n = np.linalg.norm(np.asarray(y64, dtype=np.float64).ravel())
+    return float(d / n) if n > 0 else float(d)
+
+
+__all__ = [k for k in dir() if not k.startswith("_")]

@@ -1,0 +1,570 @@
+/*
+ * pq_oracle.c -- plain, slow CPU oracle for the ParoQuant (PARO) W4A8
+ * rotated-int4 linear layer  y = ((x * channel_scales) R^T) dequant(Q)^T.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code with the CUDA
+ * library (w4a8_rotated_int4_gb300/csrc).
+ *
+ * Sources (web page titles and sections):
+ *   [LOG]  "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log"
+ *          section "Format" (tensor layouts, nibble order 0,2,4,6,1,3,5,7,
+ *          zeros not offset by one, pairs local to each 128 group,
+ *          channel_scales pre-inverted), the "Inference identity" paragraph,
+ *          "Design" items 1-4 (zero point as a row-sum correction, SZ table,
+ *          per-group fp8 scales, fused prologue, records {i|j<<8, cos f16,
+ *          sin f16}, software e4m3 encode RNE/OCP/saturating, row-sums of the
+ *          decoded codes, partition select) and "Gates passed"
+ *          (scale = amax * (1/448.f)).
+ *   [CVT]  same page, section "2026-09-15: hardware e4m3 convert in the
+ *          producers" (NaN -> 0, -0 -> +0, clamp +-448, then RNE convert).
+ *
+ * Readings of points the pages leave open (each also listed in the design doc):
+ *   R1 pairs: entries 2t and 2t+1 of a layer's 128-group form pair t, and the
+ *      angle of pair t is theta[layer][64*g + t].
+ *   R2 rotation: x_i' = c*x_i + s*x_j, x_j' = -s*x_i + c*x_j, layers 0..7,
+ *      evaluated as separate fp32 multiplies and adds (no fused multiply-add):
+ *      x_i' = fl(fl(c*x_i) + fl(s*x_j)), x_j' = fl(fl(c*x_j) - fl(s*x_i)).
+ *   R3 record cos/sin: the f16 values nearest (RNE) to cos/sin of the f16
+ *      angle evaluated in double precision; record bytes little-endian
+ *      uint32 (i | j<<8), uint16 cos, uint16 sin.
+ *   R4 scale: asg = fl32(amax * fl32(1/448)); if asg == 0 every code of the
+ *      group is 0x00 and its row-sum is 0.
+ *   R5 quotient: q = fl32(v / asg) (an IEEE division, not a reciprocal).
+ *   R6 encode: NaN -> 0x00; clamp |q| to 448; round to nearest, ties to
+ *      even, onto the e4m3 grid (subnormals m*2^-9 included); any result
+ *      equal to zero is emitted as 0x00 (0x80 is never produced).
+ *   R7 row-sum: rs = fl32(exact sum of the decoded codes of the group).
+ *   R8 SZ: zscale = f16_RNE(fl32(sc * (zp - 8))) (the fp32 product is exact).
+ *   R9 GEMM: y = sum_g asg * (sc * D - zscale * rs) with
+ *      D = sum_{k in g} dec(A[k]) * (c[k] - 8), in fp64, using the f16 table
+ *      values ("table-true").
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_SHAPE 2
+#define ORC_ERR_PAIRS 4
+
+/* ------------------------------------------------------------------ */
+/* scalar formats                                                      */
+/* ------------------------------------------------------------------ */
+
+/* IEEE binary16 bit pattern -> double (exact). */
+double orc_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0x1F)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* double -> IEEE binary16, round to nearest, ties to even, overflow -> inf. */
+uint16_t orc_f16_from_double(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x))
+        return 0x7E00;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);                 /* a in [2^(e-1), 2^e) */
+    int eb = e - 1;               /* binade of a */
+    if (eb < -14)
+        eb = -14;                 /* the subnormal range shares the spacing 2^-24 */
+    double quantum = ldexp(1.0, eb - 10);
+    double n = nearbyint(a / quantum);       /* a/quantum is exact; nearbyint is RNE */
+    double v = n * quantum;                  /* rounded magnitude */
+    if (v > 65504.0)
+        return sign | 0x7C00;
+    if (v < ldexp(1.0, -14))
+        return sign | (uint16_t)(v / ldexp(1.0, -24));
+    frexp(v, &e);
+    eb = e - 1;
+    uint16_t mant = (uint16_t)(v / ldexp(1.0, eb - 10) - 1024.0);
+    return sign | (uint16_t)((eb + 15) << 10) | mant;
+}
+
+/* bf16 bit pattern -> float (exact: bf16 is the top half of a binary32). */
+float orc_bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* OCP FP8 E4M3FN code -> value: bias 7, no infinities, 0x7F/0xFF are NaN. */
+double orc_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7;
+    int e = (c >> 3) & 0xF;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);                  /* subnormal: m/8 * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* float -> OCP FP8 E4M3FN (readings R6): NaN -> 0, saturate at 448,
+ * RNE onto the e4m3 grid, zero results always +0. */
+uint8_t orc_e4m3_encode(float q)
+{
+    if (isnan(q))
+        return 0x00;
+    int neg = signbit(q) ? 1 : 0;
+    double a = fabs((double)q);
+    if (a > 448.0)
+        a = 448.0;
+    if (a == 0.0)
+        return 0x00;
+    int e;
+    frexp(a, &e);
+    int eb = e - 1;
+    if (eb < -6)
+        eb = -6;                  /* subnormals: spacing 2^-9 below 2^-6 */
+    double quantum = ldexp(1.0, eb - 3);
+    double n = nearbyint(a / quantum);
+    double v = n * quantum;       /* <= 448 because 448 is on the grid */
+    if (v == 0.0)
+        return 0x00;
+    uint8_t code;
+    if (v < ldexp(1.0, -6)) {
+        code = (uint8_t)(v / ldexp(1.0, -9));          /* 1..7 */
+    } else {
+        frexp(v, &e);
+        eb = e - 1;                                      /* -6..8 */
+        int mant = (int)(v / ldexp(1.0, eb - 3)) - 8;  /* 0..7 */
+        code = (uint8_t)(((eb + 7) << 3) | mant);
+    }
+    return neg ? (uint8_t)(code | 0x80) : code;
+}
+
+/* fp32 arithmetic helpers: one IEEE operation each, never contracted
+ * (the file is compiled with -ffp-contract=off). */
+static float f_mul(float a, float b) { return a * b; }
+static float f_add(float a, float b) { return a + b; }
+static float f_sub(float a, float b) { return a - b; }
+static float f_div(float a, float b) { return a / b; }
+
+/* ------------------------------------------------------------------ */
+/* checkpoint format: AWQ nibble order                                 */
+/* ------------------------------------------------------------------ */
+
+/* [LOG] Format: word slot i holds column order[i] with order 0,2,4,6,1,3,5,7,
+ * so column j sits in slot awq_slot[j]. */
+static const int awq_slot[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+
+/* qweight int32 [K, N/8] -> codes uint8 [K, N] (0..15). */
+void orc_unpack_awq(int rows, int N, const int32_t *packed, uint8_t *out)
+{
+    for (int r = 0; r < rows; r++)
+        for (int n = 0; n < N; n++) {
+            uint32_t w = (uint32_t)packed[(size_t)r * (N / 8) + n / 8];
+            out[(size_t)r * N + n] = (uint8_t)((w >> (4 * awq_slot[n % 8])) & 15u);
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* load-time tables                                                    */
+/* ------------------------------------------------------------------ */
+
+/* Check that every (p, layer, group) row of pairs is a permutation of 0..127. */
+int orc_check_pairs(int P, int K, const int16_t *pairs)
+{
+    int G = K / 128;
+    for (int p = 0; p < P; p++)
+        for (int r = 0; r < 8; r++)
+            for (int g = 0; g < G; g++) {
+                int seen[128] = {0};
+                for (int t = 0; t < 128; t++) {
+                    int v = pairs[((size_t)p * 8 + r) * K + 128 * g + t];
+                    if (v < 0 || v > 127 || seen[v])
+                        return ORC_ERR_PAIRS;
+                    seen[v] = 1;
+                }
+            }
+    return ORC_OK;
+}
+
+/* Rotation records [P][8][G][64] x 8 bytes (readings R1, R3). */
+int orc_records(int P, int K, const int16_t *pairs, const uint16_t *theta, uint8_t *rec)
+{
+    if (K <= 0 || K % 128 || P < 1)
+        return ORC_ERR_SHAPE;
+    if (orc_check_pairs(P, K, pairs) != ORC_OK)
+        return ORC_ERR_PAIRS;
+    int G = K / 128;
+    for (int p = 0; p < P; p++)
+        for (int r = 0; r < 8; r++)
+            for (int g = 0; g < G; g++)
+                for (int t = 0; t < 64; t++) {
+                    const int16_t *row = pairs + ((size_t)p * 8 + r) * K + 128 * g;
+                    uint32_t i = (uint32_t)row[2 * t], j = (uint32_t)row[2 * t + 1];
+                    double th = orc_f16_to_double(theta[((size_t)p * 8 + r) * (K / 2) + 64 * g + t]);
+                    uint16_t c16 = orc_f16_from_double(cos(th));
+                    uint16_t s16 = orc_f16_from_double(sin(th));
+                    uint32_t ij = i | (j << 8);
+                    uint8_t *o = rec + ((((size_t)p * 8 + r) * G + g) * 64 + t) * 8;
+                    o[0] = ij & 0xFF; o[1] = (ij >> 8) & 0xFF; o[2] = 0; o[3] = 0;
+                    o[4] = c16 & 0xFF; o[5] = c16 >> 8;
+                    o[6] = s16 & 0xFF; o[7] = s16 >> 8;
+                }
+    return ORC_OK;
+}
+
+/* SZ table [G][N][2] f16: (sc, zscale) with zscale = f16(sc * (zp - 8)) (R8). */
+void orc_sz(int G, int N, const uint16_t *scales, const int32_t *qzeros, uint16_t *sz)
+{
+    uint8_t *zp = (uint8_t *)malloc((size_t)G * N);
+    orc_unpack_awq(G, N, qzeros, zp);
+    for (int g = 0; g < G; g++)
+        for (int n = 0; n < N; n++) {
+            uint16_t sc = scales[(size_t)g * N + n];
+            float prod = f_mul((float)orc_f16_to_double(sc), (float)(zp[(size_t)g * N + n] - 8));
+            sz[((size_t)g * N + n) * 2 + 0] = sc;
+            sz[((size_t)g * N + n) * 2 + 1] = orc_f16_from_double((double)prod);
+        }
+    free(zp);
+}
+
+/* Kernel weight layout w[n][k/2]: low nibble = code at even k, high = odd k. */
+void orc_repack(int K, int N, const int32_t *qweight, uint8_t *w)
+{
+    uint8_t *c = (uint8_t *)malloc((size_t)K * N);
+    orc_unpack_awq(K, N, qweight, c);
+    for (int n = 0; n < N; n++)
+        for (int k = 0; k < K; k += 2)
+            w[(size_t)n * (K / 2) + k / 2] =
+                (uint8_t)(c[(size_t)k * N + n] | (c[(size_t)(k + 1) * N + n] << 4));
+    free(c);
+}
+
+/* ------------------------------------------------------------------ */
+/* prologue: channel scale, 8 Givens layers, per-group fp8 quantisation */
+/* ------------------------------------------------------------------ */
+
+/* Read record (p, r, g, t). */
+static void rec_get(const uint8_t *rec, int G, int p, int r, int g, int t,
+                    int *i, int *j, float *c, float *s)
+{
+    const uint8_t *o = rec + ((((size_t)p * 8 + r) * G + g) * 64 + t) * 8;
+    *i = o[0];
+    *j = o[1];
+    *c = (float)orc_f16_to_double((uint16_t)(o[4] | (o[5] << 8)));
+    *s = (float)orc_f16_to_double((uint16_t)(o[6] | (o[7] << 8)));
+}
+
+/* Rotate one 128-vector in fp32 with layers 0..7 of (p, g) (reading R2). */
+void orc_rotate_group_f32(const uint8_t *rec, int G, int p, int g, float *v)
+{
+    for (int r = 0; r < 8; r++)
+        for (int t = 0; t < 64; t++) {
+            int i, j;
+            float c, s;
+            rec_get(rec, G, p, r, g, t, &i, &j, &c, &s);
+            float vi = v[i], vj = v[j];
+            v[i] = f_add(f_mul(c, vi), f_mul(s, vj));
+            v[j] = f_sub(f_mul(c, vj), f_mul(s, vi));
+        }
+}
+
+/* fl32(1/448): the scale constant of [LOG] "Gates passed". */
+static float inv448(void)
+{
+    volatile float one = 1.0f, d = 448.0f;
+    return f_div(one, d);
+}
+
+/*
+ * pq_rotate_quant semantics.  x bf16 [M][ldx]; cs f16 [P][K]; rec from
+ * orc_records.  Outputs a e4m3 [P][M][K], asg f32 [P][G][M], rs f32 [P][G][M].
+ * Optional v_out f32 [P][M][K] receives the rotated, scaled activations.
+ */
+void orc_rotate_quant(int M, int K, int ldx, int P, const uint16_t *x, const uint16_t *cs,
+                      const uint8_t *rec, uint8_t *a, float *asg, float *rs, float *v_out)
+{
+    int G = K / 128;
+    float c448 = inv448();
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int p = 0; p < P; p++)
+        for (int m = 0; m < M; m++)
+            for (int g = 0; g < G; g++) {
+                float v[128];
+                for (int k = 0; k < 128; k++)
+                    v[k] = f_mul(orc_bf16_to_float(x[(size_t)m * ldx + 128 * g + k]),
+                                 (float)orc_f16_to_double(cs[(size_t)p * K + 128 * g + k]));
+                orc_rotate_group_f32(rec, G, p, g, v);
+                float amax = 0.0f;
+                for (int k = 0; k < 128; k++)
+                    if (fabsf(v[k]) > amax)
+                        amax = fabsf(v[k]);
+                float scale = f_mul(amax, c448);
+                int64_t sum512 = 0;             /* exact: sum of dec(code) * 2^9 */
+                uint8_t *arow = a + ((size_t)p * M + m) * K + 128 * g;
+                for (int k = 0; k < 128; k++) {
+                    uint8_t code = 0;
+                    if (scale != 0.0f)
+                        code = orc_e4m3_encode(f_div(v[k], scale));
+                    arow[k] = code;
+                    sum512 += (int64_t)llround(orc_e4m3_decode(code) * 512.0);
+                }
+                asg[((size_t)p * G + g) * M + m] = scale;
+                rs[((size_t)p * G + g) * M + m] = (float)((double)sum512 / 512.0);
+                if (v_out)
+                    memcpy(v_out + ((size_t)p * M + m) * K + 128 * g, v, sizeof v);
+            }
+}
+
+/* ------------------------------------------------------------------ */
+/* GEMM in fp64                                                        */
+/* ------------------------------------------------------------------ */
+
+static int part_of(int n, int pb1, int pb2) { return (n >= pb1) + (n >= pb2); }
+
+/* one output element, table-true (reading R9) */
+static double gemm_elem(int m, int n, int M, int N, int K, int pb1, int pb2,
+                        const uint8_t *a, const float *asg, const float *rs,
+                        const uint8_t *codes, const uint16_t *sz)
+{
+    int G = K / 128;
+    int p = part_of(n, pb1, pb2);
+    const uint8_t *arow = a + ((size_t)p * M + m) * K;
+    double y = 0.0;
+    for (int g = 0; g < G; g++) {
+        double D = 0.0;             /* exact: products and sums are multiples of 2^-9 below 2^53 */
+        for (int k = 128 * g; k < 128 * g + 128; k++)
+            D += orc_e4m3_decode(arow[k]) * (double)((int)codes[(size_t)k * N + n] - 8);
+        double sc = orc_f16_to_double(sz[((size_t)g * N + n) * 2 + 0]);
+        double zs = orc_f16_to_double(sz[((size_t)g * N + n) * 2 + 1]);
+        double s = asg[((size_t)p * G + g) * M + m];
+        double r = rs[((size_t)p * G + g) * M + m];
+        y += s * (sc * D - zs * r);
+    }
+    return y;
+}
+
+/*
+ * Full GEMM: a e4m3 [P][M][K], asg/rs f32 [P][G][M], codes uint8 [K][N]
+ * (unpacked qweight), sz [G][N][2] -> y f64 [M][N].
+ */
+void orc_gemm_f64(int M, int N, int K, int pb1, int pb2, const uint8_t *a, const float *asg,
+                  const float *rs, const uint8_t *codes, const uint16_t *sz, double *y)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++)
+            y[(size_t)m * N + n] = gemm_elem(m, n, M, N, K, pb1, pb2, a, asg, rs, codes, sz);
+}
+
+/* Sampled GEMM: y[i] = element (ms[i], ns[i]). */
+void orc_gemm_f64_sampled(int count, const int *ms, const int *ns, int M, int N, int K,
+                          int pb1, int pb2, const uint8_t *a, const float *asg, const float *rs,
+                          const uint8_t *codes, const uint16_t *sz, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < count; i++)
+        y[i] = gemm_elem(ms[i], ns[i], M, N, K, pb1, pb2, a, asg, rs, codes, sz);
+}
+
+/* "Format-true" diagnostic: sum_k dec(a)*asg * (c - zp)*sc, zero point exact. */
+void orc_gemm_format_f64(int M, int N, int K, int pb1, int pb2, const uint8_t *a,
+                         const float *asg, const uint8_t *codes, const uint8_t *zp,
+                         const uint16_t *scales, double *y)
+{
+    int G = K / 128;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            int p = part_of(n, pb1, pb2);
+            double acc = 0.0;
+            for (int k = 0; k < K; k++) {
+                int g = k / 128;
+                double av = orc_e4m3_decode(a[((size_t)p * M + m) * K + k]) *
+                            (double)asg[((size_t)p * G + g) * M + m];
+                double wv = (double)((int)codes[(size_t)k * N + n] - (int)zp[(size_t)g * N + n]) *
+                            orc_f16_to_double(scales[(size_t)g * N + n]);
+                acc += av * wv;
+            }
+            y[(size_t)m * N + n] = acc;
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* fp64 references for the inference identity (no quantisation)       */
+/* ------------------------------------------------------------------ */
+
+/* Apply the layers of (p, g) in fp64 to a 128-vector with exact cos/sin of
+ * the f16 angles; forward = layers 0..7, transpose = layers 7..0 with the
+ * angle negated. */
+static void rotate_group_f64(int K, int p, int g, const int16_t *pairs, const uint16_t *theta,
+                             double *v, int transpose)
+{
+    for (int rr = 0; rr < 8; rr++) {
+        int r = transpose ? 7 - rr : rr;
+        for (int t = 0; t < 64; t++) {
+            const int16_t *row = pairs + ((size_t)p * 8 + r) * K + 128 * g;
+            int i = row[2 * t], j = row[2 * t + 1];
+            double th = orc_f16_to_double(theta[((size_t)p * 8 + r) * (K / 2) + 64 * g + t]);
+            if (transpose)
+                th = -th;
+            double c = cos(th), s = sin(th);
+            double vi = v[i], vj = v[j];
+            v[i] = c * vi + s * vj;
+            v[j] = c * vj - s * vi;
+        }
+    }
+}
+
+/* y = ((x*cs) R^T) W^T with the rotation applied to the activations.
+ * W is the dequantised weight f64 [N][K]; x bf16 [M][K]. */
+void orc_linear_rotx_f64(int M, int K, int N, int P, int pb1, int pb2, const uint16_t *x,
+                         const uint16_t *cs, const int16_t *pairs, const uint16_t *theta,
+                         const double *W, double *y)
+{
+    int G = K / 128;
+    double *v = (double *)malloc(sizeof(double) * (size_t)P * K);
+    for (int m = 0; m < M; m++) {
+        for (int p = 0; p < P; p++)
+            for (int g = 0; g < G; g++) {
+                double *vg = v + (size_t)p * K + 128 * g;
+                for (int k = 0; k < 128; k++)
+                    vg[k] = (double)orc_bf16_to_float(x[(size_t)m * K + 128 * g + k]) *
+                            orc_f16_to_double(cs[(size_t)p * K + 128 * g + k]);
+                rotate_group_f64(K, p, g, pairs, theta, vg, 0);
+            }
+        for (int n = 0; n < N; n++) {
+            const double *vp = v + (size_t)part_of(n, pb1, pb2) * K;
+            double acc = 0.0;
+            for (int k = 0; k < K; k++)
+                acc += vp[k] * W[(size_t)n * K + k];
+            y[(size_t)m * N + n] = acc;
+        }
+    }
+    free(v);
+}
+
+/* Same y with R^T moved onto the weights: each weight row is rotated by the
+ * transposed layers, and the activations are only channel-scaled. */
+void orc_linear_rotw_f64(int M, int K, int N, int P, int pb1, int pb2, const uint16_t *x,
+                         const uint16_t *cs, const int16_t *pairs, const uint16_t *theta,
+                         const double *W, double *y)
+{
+    (void)P;                      /* the partition of each row comes from pb1/pb2 */
+    int G = K / 128;
+    double *Wr = (double *)malloc(sizeof(double) * (size_t)N * K);
+    memcpy(Wr, W, sizeof(double) * (size_t)N * K);
+    for (int n = 0; n < N; n++)
+        for (int g = 0; g < G; g++)
+            rotate_group_f64(K, part_of(n, pb1, pb2), g, pairs, theta, Wr + (size_t)n * K + 128 * g, 1);
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            int p = part_of(n, pb1, pb2);
+            double acc = 0.0;
+            for (int k = 0; k < K; k++)
+                acc += (double)orc_bf16_to_float(x[(size_t)m * K + k]) *
+                       orc_f16_to_double(cs[(size_t)p * K + k]) * Wr[(size_t)n * K + k];
+            y[(size_t)m * N + n] = acc;
+        }
+    free(Wr);
+}
+
+/* ------------------------------------------------------------------ */
+/* self-check: the encoder against nearest-value search on all 2^32    */
+/* ------------------------------------------------------------------ */
+
+/*
+ * For every binary32 bit pattern compare orc_e4m3_encode with the code found
+ * by searching the decoded table of the 127 non-negative finite values for the
+ * nearest one (ties to the even code, |q| saturated at 448, NaN -> 0, zero
+ * results as 0x00).  lo/hi bound the patterns (hi exclusive, up to 2^32).
+ * Returns the number of disagreements; *first_bad receives the first one.
+ */
+long long orc_e4m3_check_range(uint64_t lo, uint64_t hi, uint32_t *first_bad)
+{
+    double tab[127];
+    for (int c = 0; c < 127; c++)
+        tab[c] = orc_e4m3_decode((uint8_t)c);      /* increasing in c */
+    long long bad = 0;
+    unsigned long long first = ~0ull;
+#pragma omp parallel for schedule(static) reduction(+ : bad) reduction(min : first)
+    for (long long u = (long long)lo; u < (long long)hi; u++) {
+        uint32_t bits = (uint32_t)u;
+        float q;
+        memcpy(&q, &bits, 4);
+        uint8_t want;
+        if (isnan(q)) {
+            want = 0;
+        } else {
+            double a = fabs((double)q);
+            if (a > 448.0)
+                a = 448.0;
+            int lo_i = 0, hi_i = 126;                 /* tab[lo_i] <= a <= tab[hi_i] */
+            while (hi_i - lo_i > 1) {
+                int mid = (lo_i + hi_i) / 2;
+                if (tab[mid] <= a)
+                    lo_i = mid;
+                else
+                    hi_i = mid;
+            }
+            double dl = a - tab[lo_i], dh = tab[hi_i] - a;
+            int c;
+            if (dl < dh)
+                c = lo_i;
+            else if (dh < dl)
+                c = hi_i;
+            else
+                c = (lo_i % 2 == 0) ? lo_i : hi_i;   /* tie: the code with an even mantissa */
+            want = (uint8_t)c;
+            if (c != 0 && signbit(q))
+                want |= 0x80;
+        }
+        if (orc_e4m3_encode(q) != want) {
+            bad++;
+            if ((unsigned long long)bits < first)
+                first = bits;
+        }
+    }
+    if (first_bad)
+        *first_bad = (uint32_t)first;
+    return bad;
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
