@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of the PARO W4A8 linear layer (prologue + GEMM) on GB300.
+
+One step = one forward of the layer's hot path over one batch of synthetic
+input: pq_rotate_quant (fused rotate + quantise prologue) followed by pq_gemm
+(the uint4 x e4m3 group GEMM; CUDA-core kernel at M <= 16, tcgen05 above).
+Weights, tables and activations are resident in HBM when the timed region
+starts; every step uses the next of several input copies whose total size is
+more than twice the L2, so no step is served from L2.
+
+Headline (the JSON line's value): the decode gate_up layer, M=1, K=5120,
+N=17408, one partition -- microseconds per step (lower is better).  The other
+workloads (M=4, 16, prefill M=2048, down-projection M=8192 K=8704 N=5120,
+merged QKV M=512 with three rotations) are timed the same way and reported
+under "workloads".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pq|reference]
+For N > 1 launch with torchrun; ranks run independent replicas (the layer does
+not shard across GPUs in this build) and rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import pqgen  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "pq prologue+GEMM µs, TFLOP/s & HBM GB/s vs roofline at M=1/2048/8192"
+HEADLINE = ("decode", 1)
+EXTRA = [("decode", 4), ("decode", 16), ("prefill", None), ("down", None), ("qkv", None)]
+
+
+def describe(name, M=None):
+    c = dict(pqgen.CONFIGS[name])
+    if M is not None:
+        c["M"] = M
+    labels = {"decode": "decode gate_up", "prefill": "prefill gate_up", "down": "down-proj",
+              "qkv": "merged QKV", "tiny": "tiny"}
+    return c, "%s M=%d K=%d N=%d P=%d" % (labels[name], c["M"], c["K"], c["N"], c["P"])
+
+
+def algorithmic(c):
+    """Bytes each kernel must move and the GEMM's flops (per step)."""
+    M, K, N, P = c["M"], c["K"], c["N"], c["P"]
+    G = K // 128
+    gemm_bytes = N * K // 2 + 4 * G * N + P * M * K + 8 * P * M * G + 2 * M * N
+    pro_bytes = 2 * M * K + 2 * P * K + P * 8 * (K // 2) * 8 + P * M * K + 8 * P * M * G
+    return gemm_bytes, pro_bytes, 2.0 * M * N * K
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm=pk["hbm_gbs"], bf16=pk["bf16_tflops"],
+                    bf16_sus=pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our path
+class Workload:
+    def __init__(self, pq, torch, name, M, dev):
+        self.c, self.label = describe(name, M)
+        c = self.c
+        prob = pqgen.make_problem(**c)
+        self.prob = prob
+        rec, sz, w = pq.pq_pack(prob.qweight, prob.qzeros, prob.scales, prob.pairs, prob.theta)
+        gemm_bytes, pro_bytes, flops = algorithmic(c)
+        per_copy = w.nbytes + sz.nbytes + rec.nbytes + prob.x.nbytes + 2 * prob.cs.nbytes + \
+            2 * c["M"] * c["N"] + c["P"] * c["M"] * c["K"]
+        self.copies = max(2, min(16, -(-2 * L2_BYTES // per_copy) + 1))
+        t = torch
+
+        def u16(a):
+            return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+        self.w = [t.from_numpy(w).to(dev) for _ in range(self.copies)]
+        self.sz = [u16(sz) for _ in range(self.copies)]
+        self.rec = [t.from_numpy(rec).to(dev) for _ in range(self.copies)]
+        self.cs = [u16(prob.cs) for _ in range(self.copies)]
+        self.x = [u16(prob.x).view(t.bfloat16) for _ in range(self.copies)]
+        P, M, K, N, G = c["P"], c["M"], c["K"], c["N"], c["K"] // 128
+        self.a = [t.empty((P, M, K), dtype=t.uint8, device=dev) for _ in range(self.copies)]
+        self.asg = [t.empty((P, G, M), dtype=t.float32, device=dev) for _ in range(self.copies)]
+        self.rs = [t.empty((P, G, M), dtype=t.float32, device=dev) for _ in range(self.copies)]
+        self.y = [t.empty((M, N), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
+        self.pb1, self.pb2 = prob.pb1, prob.pb2
+        self.gemm_bytes, self.pro_bytes, self.flops = gemm_bytes, pro_bytes, flops
+        self.gemm_kernel = "skinny" if M_of(c) <= pq.pq_gemm_skinny_max_m() else "tcgen05"
+
+    def step(self, pq, i, stream):
+        j = i % self.copies
+        pq.pq_rotate_quant(self.x[j], self.rec[j], self.cs[j], a=self.a[j], asg=self.asg[j],
+                           rs=self.rs[j], stream=stream)
+        pq.pq_gemm(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1, self.pb2,
+                   y=self.y[j], stream=stream)
+
+
+def M_of(c):
+    return c["M"]
+
+
+def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=None):
+    """Returns dict with ms per step (total), per-kernel mean durations (ms)."""
+    for i in range(warmup):
+        wl.step(pq, i, stream)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * steps + 2)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        t0 = time.perf_counter()
+        ev[0].record(stream)
+        for i in range(steps):
+            j = i % wl.copies
+            e0, e1, e2 = ev[1 + 3 * i], ev[2 + 3 * i], ev[3 + 3 * i]
+            e0.record(stream)
+            pq.pq_rotate_quant(wl.x[j], wl.rec[j], wl.cs[j], a=wl.a[j], asg=wl.asg[j], rs=wl.rs[j],
+                               stream=stream)
+            e1.record(stream)
+            pq.pq_gemm(wl.a[j], wl.asg[j], wl.rs[j], wl.w[j], wl.sz[j], wl.pb1, wl.pb2, y=wl.y[j],
+                       stream=stream)
+            e2.record(stream)
+        ev[-1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if barrier:
+        barrier()
+    total_ms = ev[0].elapsed_time(ev[-1])
+    pro = [ev[1 + 3 * i].elapsed_time(ev[2 + 3 * i]) for i in range(steps)]
+    gem = [ev[2 + 3 * i].elapsed_time(ev[3 + 3 * i]) for i in range(steps)]
+    return dict(total_ms=total_ms, wall_s=wall, pro_ms=float(np.mean(pro)), gemm_ms=float(np.mean(gem)),
+                pro_med=float(np.median(pro)), gemm_med=float(np.median(gem)))
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        pass
+
+
+def e2e_workload(pq, torch, wl, steps, warmup, stream, dev):
+    """Same step through the public API from pinned host buffers: H2D of x,
+    prologue + GEMM, D2H of y, all inside the timed region."""
+    c = wl.c
+    xh = torch.from_numpy(wl.prob.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory()
+
+    def one(i):
+        j = i % wl.copies
+        wl.x[j].copy_(xh, non_blocking=True)
+        wl.step(pq, i, stream)
+        yh.copy_(wl.y[j], non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, xh.numel() * 2, yh.numel() * 2
+
+
+def roofline(wl, r, peaks, traffic=None):
+    if wl.gemm_kernel == "skinny":
+        achieved = wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9
+        return {"kernel": "pq_gemm_skinny", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                "peak_source": peaks["src"] + " (hbm_gbs)", "traffic": traffic}
+    fp8_peak = 2.0 * peaks["bf16"]
+    achieved = wl.flops / (r["gemm_ms"] * 1e-3) / 1e12
+    return {"kernel": "pq_gemm_tc", "bound": "tensor", "achieved": round(achieved, 1),
+            "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+            "peak_source": peaks["src"] + " bf16_tflops x 2 (dense fp8 : bf16 nominal ratio)",
+            "traffic": traffic}
+
+
+def summarize(wl, r, steps, peaks):
+    step_us = r["total_ms"] * 1e3 / steps
+    return {
+        "workload": wl.label, "us_per_step": round(step_us, 3),
+        "prologue_us": round(r["pro_ms"] * 1e3, 3), "gemm_us": round(r["gemm_ms"] * 1e3, 3),
+        "gemm_kernel": wl.gemm_kernel,
+        "gemm_tflops": round(wl.flops / (r["gemm_ms"] * 1e-3) / 1e12, 2),
+        "gemm_gbs": round(wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9, 1),
+        "prologue_gbs": round(wl.pro_bytes / (r["pro_ms"] * 1e-3) / 1e9, 1),
+        "roofline": roofline(wl, r, peaks), "copies": wl.copies,
+    }
+
+
+# ---------------------------------------------------------------- oracle timing
+class OracleSample:
+    """The CPU oracle (as it stands) on a bounded sample of the workload: the
+    full prologue for all tokens and the fp64 GEMM for a slice of output
+    columns, scaled to all columns.  Inputs are generated and packed once."""
+
+    def __init__(self, name, M=None, budget_s=10.0):
+        import oracle
+        self.oracle = oracle
+        c, self.label = describe(name, M)
+        self.c = c
+        self.prob = pqgen.make_problem(**c)
+        self.tab = oracle.pack(self.prob)
+        N = c["N"]
+        self.ncols = 128
+        # size the column slice so one step's GEMM takes about budget_s / 4
+        while True:
+            self._slice()
+            t = self._gemm()
+            if t > budget_s / 4 or self.ncols >= N:
+                break
+            self.ncols = min(N, self.ncols * 4)
+
+    def _slice(self):
+        self.codes = np.ascontiguousarray(self.tab["codes"][:, :self.ncols])
+        self.sz = np.ascontiguousarray(self.tab["sz"][:, :self.ncols])
+        self.a, self.asg, self.rs = self.oracle.rotate_quant(self.prob.x, self.prob.cs, self.tab["rec"])
+
+    def _gemm(self):
+        pb = min(self.prob.pb1, self.ncols), min(self.prob.pb2, self.ncols)
+        t0 = time.perf_counter()
+        self.oracle.gemm_f64(self.a, self.asg, self.rs, self.codes, self.sz, pb[0], pb[1])
+        return time.perf_counter() - t0
+
+    def step_us(self):
+        t0 = time.perf_counter()
+        self.a, self.asg, self.rs = self.oracle.rotate_quant(self.prob.x, self.prob.cs, self.tab["rec"])
+        t_pro = time.perf_counter() - t0
+        t_g = self._gemm()
+        return (t_pro + t_g * (self.c["N"] / self.ncols)) * 1e6
+
+    def describe(self):
+        return ("prologue on all %d tokens + fp64 GEMM on %d of %d output columns per step, "
+                "scaled to all columns" % (self.c["M"], self.ncols, self.c["N"]))
+
+    def cores(self):
+        return self.oracle.num_threads()
+
+
+# ---------------------------------------------------------------- main
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    backend = "nccl"
+    dist.init_process_group(backend=backend)
+    return rank, ws, dist
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pq", "reference"], default="pq")
+    ap.add_argument("--extra-steps", type=int, default=50)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, ws, dist = dist_init()
+    name, M = HEADLINE
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        orc = OracleSample(name, M, budget_s=4.0)
+        per_step = []
+        for i in range(args.warmup + args.steps):
+            us = orc.step_us()
+            if i >= args.warmup:
+                per_step.append(us)
+        v = float(np.mean(per_step))
+        cores, desc, label = orc.cores(), orc.describe(), orc.label
+        line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32 prologue, f64 GEMM (CPU oracle)",
+                "data": "synthetic", "config": {"workload": label},
+                "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": cores,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import w4a8_rotated_int4_gb300 as pq
+    import __graft_entry__
+    __graft_entry__.build_library()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    barrier = (lambda: dist.barrier()) if dist else None
+
+    wl = Workload(pq, torch, name, M, dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    r = time_workload(pq, torch, wl, args.steps, args.warmup, stream, barrier, sampler)
+    total_ms = r["total_ms"]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    step_us = total_ms * 1e3 / args.steps
+    value = step_us / ws            # whole-job time per step: ws replicas each ran `steps` steps
+    e2e_ms, h2d, d2h = e2e_workload(pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, dev)
+    head = summarize(wl, dict(r, total_ms=total_ms), args.steps, peaks)
+
+    extra = []
+    if not args.no_extra:
+        for en, em in EXTRA:
+            w2 = Workload(pq, torch, en, em, dev)
+            r2 = time_workload(pq, torch, w2, args.extra_steps, args.warmup, stream, barrier)
+            extra.append(summarize(w2, r2, args.extra_steps, peaks))
+            del w2
+            torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
+    clocks = sampler.summary() if sampler else {}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "us", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_us / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 prologue; e4m3 x u4 tensor/CUDA-core MMA, f32 accumulate; bf16 out",
+        "data": "synthetic",
+        "config": {"workload": wl.label, "M": wl.c["M"], "K": wl.c["K"], "N": wl.c["N"],
+                   "P": wl.c["P"], "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "%d rotating input copies (> 2x L2)" % wl.copies},
+        "prologue_us": head["prologue_us"], "gemm_us": head["gemm_us"],
+        "roofline": head["roofline"],
+        "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "workloads": extra,
+        "peaks": peaks,
+    }
+    if not args.no_cpu_baseline:
+        orc = OracleSample(name, M)
+        us = float(np.mean([orc.step_us() for _ in range(3)]))
+        line["cpu_baseline"] = {"value": round(us, 1), "unit": "us", "cores": orc.cores(),
+                                "kind": "oracle", "sample": orc.describe() + ", mean of 3"}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

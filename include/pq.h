@@ -1,0 +1,207 @@
+/*
+ * pq.h -- C ABI of libpq, a single-GPU (GB300, sm_103a) implementation of the
+ * ParoQuant (PARO) W4A8 rotated-int4 linear layer
+ *
+ *     y = ((x * channel_scales) R^T) dequant(Q)^T
+ *
+ * R is eight layers of pairwise Givens rotations local to each 128-channel
+ * group, Q is AWQ-packed uint4 with asymmetric zero points and group size 128.
+ *
+ * Source: the web page "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log":
+ *   [Format]   section "Format"
+ *   [Identity] the "Inference identity" paragraph of "Format"
+ *   [D1]..[D4] section "Design", items 1 (zero point as a row-sum correction,
+ *              SZ table), 2 (per-group fp8 activation scales), 3 (fused
+ *              prologue, rotation records, software e4m3), 4 (partition select)
+ *   [Gates]    section "Gates passed" (scale = amax * (1/448.f), rows past M
+ *              untouched, bf16-floor GEMM tolerance)
+ *   [CVT]      section "2026-09-15: hardware e4m3 convert in the producers"
+ *
+ * Conventions for every call:
+ *   - Sizes are element counts.  G = K / 128.  "f16" = IEEE binary16,
+ *     "bf16" = bfloat16, "e4m3" = OCP FP8 E4M3FN, all little-endian.
+ *   - Every buffer is owned by the caller, who allocates and frees it.  The
+ *     library allocates no memory (host or device), keeps no state besides a
+ *     per-thread error string, and may be called from several host threads.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream) and never synchronise.  All
+ *     argument checks run on the host before any launch; a failed check
+ *     returns a status and launches nothing.  A launch failure returns
+ *     PQ_ERR_CUDA.  Faults inside a kernel surface at the caller's next
+ *     synchronisation, as for any CUDA kernel.
+ *   - Device pointers must be 16-byte aligned unless stated otherwise.
+ *   - Inputs (x, channel scales, angles, scales) are finite; results for
+ *     non-finite inputs are unspecified.
+ *   - No call aborts, traps or prints.
+ */
+#ifndef PQ_H
+#define PQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PQ_ABI_VERSION 1
+
+/* Largest number of distinct rotations (partitions) one GEMM launch serves
+ * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
+ * rotations). */
+#define PQ_MAX_PARTITIONS 3
+
+typedef enum pq_status {
+    PQ_OK = 0,
+    PQ_ERR_NULL = 1,      /* a required pointer is NULL                         */
+    PQ_ERR_SHAPE = 2,     /* M/N/K/ld out of range, K or N not a multiple of 128 */
+    PQ_ERR_ALIGN = 3,     /* a pointer or leading dimension breaks alignment    */
+    PQ_ERR_PAIRS = 4,     /* a pairs row is not a permutation of 0..127         */
+    PQ_ERR_PARTITION = 5, /* P outside 1..3 or pb1/pb2 inconsistent with P      */
+    PQ_ERR_ARCH = 6,      /* no device, or the current device is not sm_103     */
+    PQ_ERR_CUDA = 7       /* a CUDA runtime call or launch failed               */
+} pq_status;
+
+/* ABI version of the loaded library (PQ_ABI_VERSION of its build). */
+int pq_abi_version(void);
+
+/* Static description of a status code; never NULL. */
+const char *pq_status_string(int status);
+
+/* Message of the last failed call on this host thread ("" if none). The
+ * pointer stays valid until the next pq_* call on the same thread. */
+const char *pq_last_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Load time (host)                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Byte sizes of pq_pack's three outputs for a K x N layer with P rotations:
+ *   rec_bytes = P * 8 * G * 64 * 8, sz_bytes = G * N * 4, w_bytes = N * K / 2.
+ * Any of the out pointers may be NULL.  Errors: PQ_ERR_SHAPE, PQ_ERR_PARTITION. */
+pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_t *sz_bytes,
+                        size_t *w_bytes);
+
+/*
+ * Host packer: turns one checkpoint projection into the kernels' load-time
+ * tables.  Pure and deterministic; all pointers are HOST memory, the outputs
+ * sized by pq_pack_sizes.
+ *
+ * Inputs, as stored by the checkpoint ([Format]):
+ *   qweight  int32 [K][N/8]   AWQ-packed codes: word slot i (bits 4i..4i+3)
+ *                             holds column 8w + order[i], order = 0,2,4,6,1,3,5,7
+ *   qzeros   int32 [G][N/8]   zero points, same packing, used raw (no +1)
+ *   scales   f16   [G][N]     group scales
+ *   pairs    int16 [P][8][K]  Givens pair indices local to each 128-group: in
+ *                             layer r, group g, entries 2t and 2t+1 form pair t;
+ *                             each (p, r, g) row is a permutation of 0..127
+ *   theta    f16   [P][8][K/2] angle of pair t of group g at index 64g + t
+ *
+ * Outputs:
+ *   rec  [P][8][G][64] records of 8 bytes ([D3]): uint32 (i | j << 8), then
+ *        uint16 f16(cos theta), uint16 f16(sin theta); cos/sin are evaluated in
+ *        double precision (host libm) and rounded once to f16 (nearest, ties
+ *        to even).
+ *   sz   [G][N][2] f16 ([D1]): (sc, f16(sc * (zp - 8))); the product is taken
+ *        in fp32 (exact) and rounded once to f16.
+ *   w    [N][K/2] bytes: byte k/2 of row n holds code c[k][n] in its low nibble
+ *        (even k) and c[k+1][n] in its high nibble (raw codes 0..15).
+ *
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE (K, N not positive multiples of 128),
+ * PQ_ERR_PARTITION (P outside 1..3), PQ_ERR_PAIRS (a pairs row is not a
+ * permutation; nothing useful is written in that case).
+ */
+pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
+                  const uint16_t *scales, const int16_t *pairs, const uint16_t *theta,
+                  void *rec, void *sz, void *w);
+
+/* ------------------------------------------------------------------------ */
+/* Per forward (device)                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Fused prologue ([D2], [D3], [Gates]): for every partition p, token m < M and
+ * group g, in one launch:
+ *   v[k]  = x[m][128g+k] * cs[p][128g+k]                  (fp32, exact)
+ *   for r = 0..7, for each pair t of (p, r, g) with record (i, j, c, s):
+ *       v[i], v[j] = fl(fl(c*v[i]) + fl(s*v[j])), fl(fl(c*v[j]) - fl(s*v[i]))
+ *   amax  = max_k |v[k]|,  asg = fl(amax * fl(1/448))
+ *   a[k]  = e4m3(fl(v[k] / asg))  -- RNE, |q| saturated at 448, NaN -> 0,
+ *           zero results as 0x00 ([CVT]); all codes 0x00 when asg == 0
+ *   rs    = fl32(exact sum of the values the 128 codes decode to)
+ * Every multiply, add and divide is a separately rounded IEEE fp32 operation,
+ * so the outputs are bit-identical to a CPU evaluation in that order.
+ *
+ *   x    bf16 [M][ldx] (device), ldx >= K, ldx a multiple of 8
+ *   rec  device copy of pq_pack's rec for these P rotations
+ *   cs   f16 [P][K] (device) channel scales, stored pre-inverted (multiplied)
+ *   a    e4m3 [P][M][K] (device, written)
+ *   asg  fp32 [P][G][M] (device, written; 4-byte aligned)
+ *   rs   fp32 [P][G][M] (device, written; 4-byte aligned)
+ * Exactly P*M*K code bytes and P*G*M scales/row-sums are written; nothing else.
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE (M < 1, K not a positive multiple of 128,
+ * ldx < K), PQ_ERR_ALIGN, PQ_ERR_PARTITION (P outside 1..3), PQ_ERR_ARCH,
+ * PQ_ERR_CUDA.
+ */
+pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
+                          const void *cs, void *a, float *asg, float *rs, void *stream);
+
+/*
+ * uint4 x e4m3 group GEMM ([D1], [D2], [D4]):
+ *   p(n)   = (n >= pb1) + (n >= pb2)
+ *   D      = sum_{k in g} dec(a[p(n)][m][k]) * (c[k][n] - 8)
+ *   y[m][n] = bf16( sum_g asg[p][g][m] * (sc[g][n] * D - zs[g][n] * rs[p][g][m]) )
+ * with (sc, zs) the f16 pair of sz[g][n].  Accumulation is fp32 (tensor-core
+ * fp32 accumulation within a 128-k group on the tensor-core path); the result
+ * is within the bf16 output floor of the fp64 value (norm-wise relative error
+ * <= 2e-3 is the gate).
+ *
+ *   a, asg, rs  as written by pq_rotate_quant (P partitions)
+ *   w, sz       device copies of pq_pack's outputs
+ *   y           bf16 [M][ldy] (device, written), ldy >= N, ldy a multiple of 8;
+ *               only y[0..M-1][0..N-1] is written
+ *   pb1, pb2    partition boundaries, multiples of 128:
+ *               P = 1: pb1 = pb2 = N;  P = 2: 0 < pb1 < pb2 = N;
+ *               P = 3: 0 < pb1 < pb2 < N
+ * Dispatch: M <= pq_gemm_skinny_max_m() runs the CUDA-core decode kernel,
+ * larger M the tcgen05 tensor-core kernel; one launch in both cases.
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE, PQ_ERR_ALIGN, PQ_ERR_PARTITION,
+ * PQ_ERR_ARCH, PQ_ERR_CUDA.
+ */
+pq_status pq_gemm(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
+                  int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
+                  void *stream);
+
+/* Largest M that pq_gemm sends to the CUDA-core decode kernel. */
+int pq_gemm_skinny_max_m(void);
+
+/*
+ * The two GEMM kernels behind pq_gemm, callable on their own (same arguments
+ * and result).  pq_gemm_skinny accepts 1 <= M <= 16 (PQ_ERR_SHAPE otherwise);
+ * pq_gemm_tc accepts any M >= 1.
+ *
+ * dev_status (device, 4-byte aligned, may be NULL): every wait inside the
+ * kernels is bounded; a wait that gives up (never expected) ORs a nonzero
+ * code into *dev_status, the affected output tile is filled with NaN, and the
+ * kernel returns.  The caller zeroes *dev_status beforehand.
+ */
+pq_status pq_gemm_skinny(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                         int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                         int ldy, unsigned int *dev_status, void *stream);
+pq_status pq_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                     int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
+                     unsigned int *dev_status, void *stream);
+
+/*
+ * The prologue's device e4m3 encoder applied to n fp32 values ([CVT]: NaN ->
+ * 0x00, clamp to +-448, round to nearest even, zero results as 0x00).  For the
+ * exhaustive check of the encoder; in/out device pointers, 4-byte and 1-byte
+ * alignment suffice.  Errors: PQ_ERR_NULL, PQ_ERR_ARCH, PQ_ERR_CUDA.
+ */
+pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQ_H */

@@ -57,6 +57,7 @@ def lib():
         L.orc_linear_rotw_f64.argtypes = [i32] * 6 + [vp] * 6
         L.orc_e4m3_check_range.restype = C.c_longlong
         L.orc_e4m3_check_range.argtypes = [u64, u64, C.POINTER(C.c_uint32)]
+        L.orc_e4m3_encode_range.argtypes = [u64, u64, vp]
         L.orc_num_threads.restype = i32
         L.orc_set_num_threads.argtypes = [i32]
         _lib = L
@@ -99,6 +100,13 @@ def e4m3_check_range(lo: int, hi: int):
     first = C.c_uint32(0)
     bad = lib().orc_e4m3_check_range(lo, hi, C.byref(first))
     return int(bad), int(first.value)
+
+
+def e4m3_encode_range(lo: int, hi: int) -> np.ndarray:
+    """Oracle codes of the binary32 patterns [lo, hi)."""
+    out = np.empty(hi - lo, dtype=np.uint8)
+    lib().orc_e4m3_encode_range(lo, hi, _p(out))
+    return out
 
 
 def num_threads() -> int:

@@ -568,3 +568,15 @@ void orc_set_num_threads(int n)
     (void)n;
 #endif
 }
+
+/* Encode the binary32 patterns [lo, hi) (as floats) into out[0 .. hi-lo). */
+void orc_e4m3_encode_range(uint64_t lo, uint64_t hi, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (long long u = (long long)lo; u < (long long)hi; u++) {
+        uint32_t bits = (uint32_t)u;
+        float q;
+        memcpy(&q, &bits, 4);
+        out[u - (long long)lo] = orc_e4m3_encode(q);
+    }
+}

@@ -53,9 +53,10 @@ def _rng(seed: int, name: str, p: int = 0) -> np.random.Generator:
 
 def to_bf16_bits(f: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns, round to nearest even (input preparation)."""
-    u = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    u = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    # finite inputs only: u + 0x7FFF + lsb cannot overflow 32 bits below the NaN range
+    r = (u + (np.uint32(0x7FFF) + lsb)) >> np.uint32(16)
     return r.astype(np.uint16)
 
 
@@ -97,26 +98,36 @@ def make_problem(M: int, K: int, N: int, P: int = 1, seed: int = 0,
     if K % 128 or N % 128:
         raise ValueError("K and N must be multiples of 128")
     G = K // 128
-    # activations
+    # activations, drawn and rounded to bf16 in row blocks (same stream as one draw)
     r = _rng(seed, "x")
-    if x_mode == "normal":
-        xf = r.standard_normal((M, K), dtype=np.float32) * np.float32(x_sigma)
-    elif x_mode == "sparse":
-        xf = r.standard_normal((M, K), dtype=np.float32) * np.float32(1e-5)
-        hot = r.integers(0, 128, size=(M, G))
-        vals = r.standard_normal((M, G), dtype=np.float32)
-        rows = np.repeat(np.arange(M), G)
-        cols = (np.tile(np.arange(G), M) * 128 + hot.reshape(-1))
-        xf[rows, cols] = vals.reshape(-1)
-    else:
-        raise ValueError(x_mode)
     if outlier_frac > 0:
         n_out = int(round(outlier_frac * K))
-        ch = _rng(seed, "outliers").choice(K, size=n_out, replace=False)
-        xf[:, ch] *= np.float32(20.0)
-    x = to_bf16_bits(xf)
+        out_ch = _rng(seed, "outliers").choice(K, size=n_out, replace=False)
+    x = np.empty((M, K), dtype=np.uint16)
+    if x_mode == "sparse":
+        hot = np.empty((0,), dtype=np.int64)
+    for r0 in range(0, M, 256):
+        rows = min(256, M - r0)
+        if x_mode == "normal":
+            xf = r.standard_normal((rows, K), dtype=np.float32)
+            if x_sigma != 1.0:
+                xf *= np.float32(x_sigma)
+        elif x_mode == "sparse":
+            xf = r.standard_normal((rows, K), dtype=np.float32) * np.float32(1e-5)
+            hot = r.integers(0, 128, size=(rows, G))
+            vals = r.standard_normal((rows, G), dtype=np.float32)
+            ri = np.repeat(np.arange(rows), G)
+            ci = np.tile(np.arange(G), rows) * 128 + hot.reshape(-1)
+            xf[ri, ci] = vals.reshape(-1)
+        else:
+            raise ValueError(x_mode)
+        if outlier_frac > 0:
+            xf[:, out_ch] *= np.float32(20.0)
+        x[r0:r0 + rows] = to_bf16_bits(xf)
     # weights (checkpoint format)
-    qweight = _nibble_words(_rng(seed, "qweight"), (K, N // 8), 0, 15)
+    # eight independent uniform codes 0..15 per word == one uniform 32-bit word
+    qweight = _rng(seed, "qweight").integers(0, 1 << 32, size=(K, N // 8),
+                                             dtype=np.uint64).astype(np.uint32).view(np.int32)
     qzeros = _nibble_words(_rng(seed, "qzeros"), (G, N // 8), 2, 14)
     scales = f16_bits(_rng(seed, "scales").uniform(0.002, 0.02, size=(G, N)))
     # rotations, one per partition

@@ -1,0 +1,326 @@
+"""GPU parity gates: the CUDA path through the C ABI against the CPU oracle.
+
+* prologue (codes, per-group scales, row-sums): byte-equal on every workload,
+  ragged M, three partitions, subnormal-heavy inputs;
+* device e4m3 encoder: equal to the oracle's encoder on all 2^32 fp32 patterns;
+* GEMM (CUDA-core decode kernel and tcgen05 kernel): norm-wise relative error
+  <= 2e-3 against the fp64 oracle (the bf16 output floor; the engineering log
+  reports 1.65-1.71e-3 for its kernels), plus an elementwise bound, on full
+  small problems and on sampled outputs at the full workload sizes;
+* metamorphic cases: merged P=3 == three sliced launches (bit-identical),
+  all-eight codes with zero point 8 give exactly 0, rows are independent,
+  rows past M and columns past N are never written.
+
+Source: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", "Gates passed"
+(prologue bit-exact vs CPU, GEMM at the bf16 floor on all shapes incl.
+3-partition QKV and subnormal-heavy codes, rows past M untouched) and
+"Traps hit" ("clear every output between variants": outputs here are
+pre-filled with a canary).
+"""
+import numpy as np
+import pytest
+
+import pqgen
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CANARY = 0xA5
+
+
+@pytest.fixture(scope="module")
+def pq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import w4a8_rotated_int4_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    return m
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+class Problem:
+    """A generated layer: device tables from the product packer, host tables
+    from the oracle's independent packer (checked byte-equal)."""
+
+    def __init__(self, pq, orc, prob, check_pack=True):
+        self.prob = prob
+        self.rec, self.sz, self.w = pq.pq_pack(prob.qweight, prob.qzeros, prob.scales,
+                                               prob.pairs, prob.theta)
+        self.t = orc.pack(prob)
+        if check_pack:
+            assert np.array_equal(self.rec, self.t["rec"])
+            assert np.array_equal(self.sz, self.t["sz"])
+            assert np.array_equal(self.w, self.t["w"])
+        self.rec_d = torch.from_numpy(self.rec).cuda()
+        self.sz_d = dev_u16(self.sz)
+        self.w_d = torch.from_numpy(self.w).cuda()
+        self.cs_d = dev_u16(prob.cs)
+        self.x_d = dev_u16(prob.x).view(torch.bfloat16)
+
+
+def canary_outputs(P, M, K, G, pad=64):
+    """Outputs inside larger canary-filled buffers (views keep 16-byte alignment)."""
+    a_buf = torch.full((P * M * K + 2 * pad,), CANARY, dtype=torch.uint8, device="cuda")
+    s_buf = torch.full((P * G * M + 2 * pad,), float("nan"), dtype=torch.float32, device="cuda")
+    r_buf = torch.full((P * G * M + 2 * pad,), float("nan"), dtype=torch.float32, device="cuda")
+    a = a_buf[pad:pad + P * M * K].view(P, M, K)
+    asg = s_buf[pad:pad + P * G * M].view(P, G, M)
+    rs = r_buf[pad:pad + P * G * M].view(P, G, M)
+    return (a_buf, s_buf, r_buf), (a, asg, rs), pad
+
+
+def check_guards(bufs, pad):
+    a_buf, s_buf, r_buf = [b.cpu() for b in bufs]
+    assert bool((a_buf[:pad] == CANARY).all()) and bool((a_buf[-pad:] == CANARY).all())
+    for b in (s_buf, r_buf):
+        assert bool(torch.isnan(b[:pad]).all()) and bool(torch.isnan(b[-pad:]).all())
+
+
+# ---------------------------------------------------------------- encoder
+def test_e4m3_device_encoder_all_2_32(pq, orc):
+    chunk = 1 << 28
+    for lo in range(0, 1 << 32, chunk):
+        bits = torch.arange(lo, lo + chunk, dtype=torch.int64, device="cuda").to(torch.int32)
+        got = pq.pq_e4m3_encode(bits.view(torch.float32)).cpu().numpy()
+        want = orc.e4m3_encode_range(lo, lo + chunk)
+        bad = np.flatnonzero(got != want)
+        assert bad.size == 0, "pattern 0x%08x: gpu %02x oracle %02x" % (
+            lo + bad[0], got[bad[0]], want[bad[0]])
+        del bits
+
+
+# ---------------------------------------------------------------- prologue
+PROLOGUE_CASES = [
+    ("tiny", dict()),
+    ("decode", dict(M=1)),
+    ("decode", dict(M=4)),
+    ("decode", dict(M=16)),
+    ("prefill", dict()),
+    ("prefill", dict(x_sigma=1e-4)),                          # literal N(0, 1e-4) variant
+    ("prefill", dict(M=333, x_mode="sparse", theta_range=1e-4)),   # subnormal-heavy codes
+    ("down", dict()),
+    ("qkv", dict()),
+    ("qkv", dict(M=33)),
+]
+
+
+@pytest.mark.parametrize("name,over", PROLOGUE_CASES,
+                         ids=["%s-%s" % (n, "-".join("%s%s" % kv for kv in o.items()))
+                              for n, o in PROLOGUE_CASES])
+def test_prologue_bit_exact(pq, orc, name, over):
+    c = dict(pqgen.CONFIGS[name])
+    c.update(over)
+    c["N"] = 128                                   # the prologue does not depend on N
+    c["pb"] = {1: (128, 128), 3: None}[c["P"]]
+    if c["P"] == 3:
+        c["N"] = 384
+        c["pb"] = (128, 256)
+    prob = pqgen.make_problem(**c)
+    P, M, K, G = prob.P, prob.M, prob.K, prob.G
+    rec = orc.records(prob.pairs, prob.theta)
+    rec_p, _, _ = pq.pq_pack(prob.qweight, prob.qzeros, prob.scales, prob.pairs, prob.theta)
+    assert np.array_equal(rec, rec_p)
+    bufs, (a, asg, rs), pad = canary_outputs(P, M, K, G)
+    pq.pq_rotate_quant(dev_u16(prob.x).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+                       dev_u16(prob.cs), a=a, asg=asg, rs=rs)
+    torch.cuda.synchronize()
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, rec)
+    a_g = a.cpu().numpy()
+    assert np.array_equal(a_g, a_o), "codes differ at %s" % (np.argwhere(a_g != a_o)[:3].tolist(),)
+    assert np.array_equal(asg.cpu().numpy().view(np.uint32), asg_o.view(np.uint32))
+    assert np.array_equal(rs.cpu().numpy().view(np.uint32), rs_o.view(np.uint32))
+    check_guards(bufs, pad)
+    if over.get("x_mode") == "sparse":
+        sub = ((a_o & 0x78) == 0) & ((a_o & 7) != 0)
+        assert sub.mean() > 0.5
+
+
+def test_prologue_strided_x(pq, orc):
+    """ldx > K: only the first K columns of each row are read."""
+    prob = pqgen.make_problem(37, 384, 128, seed=21)
+    xw = np.full((37, 384 + 64), 0x7FC0, dtype=np.uint16)     # NaN padding must never be read
+    xw[:, :384] = prob.x
+    rec = orc.records(prob.pairs, prob.theta)
+    a, asg, rs = pq.pq_rotate_quant(dev_u16(xw).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+                                    dev_u16(prob.cs))
+    a_o, asg_o, rs_o = orc.rotate_quant(xw, prob.cs, rec)
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    assert np.array_equal(asg.cpu().numpy(), asg_o) and np.array_equal(rs.cpu().numpy(), rs_o)
+
+
+# ---------------------------------------------------------------- GEMM helpers
+def gemm_paths(pq, M):
+    paths = [("tc", pq.pq_gemm_tc)]
+    if M <= pq.pq_gemm_skinny_max_m():
+        paths.append(("skinny", pq.pq_gemm_skinny))
+    return paths
+
+
+def run_gemm(fn, a, asg, rs, L, pb1, pb2, M, N, ldy=None, fill=float("nan")):
+    ldy = ldy or N
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ybuf = torch.full((M + 3, ldy), fill, dtype=torch.bfloat16, device="cuda")
+    y = ybuf[:M]
+    # a strided y view: pass the storage with its leading dimension
+    import ctypes as C
+    import w4a8_rotated_int4_gb300 as m
+    lib = m.lib()
+    name = "pq_gemm_tc" if fn is m.pq_gemm_tc else "pq_gemm_skinny"
+    P = a.shape[0]
+    K = a.shape[2]
+    st = getattr(lib, name)(C.c_void_p(a.data_ptr()), C.c_void_p(asg.data_ptr()),
+                            C.c_void_p(rs.data_ptr()), M, N, K, P, pb1, pb2,
+                            C.c_void_p(L.w_d.data_ptr()), C.c_void_p(L.sz_d.data_ptr()),
+                            C.c_void_p(y.data_ptr()), ldy, C.c_void_p(status.data_ptr()),
+                            C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    m._check(st, name)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %d" % int(status.item())
+    yb = ybuf.float().cpu().numpy()
+    # nothing outside [0, M) x [0, N) was written
+    assert np.isnan(yb[M:]).all()
+    if ldy > N:
+        assert np.isnan(yb[:M, N:]).all()
+    return yb[:M, :N]
+
+
+def assert_close(y, y64, what):
+    rel = float(np.linalg.norm(y - y64) / max(np.linalg.norm(y64), 1e-300))
+    rms = float(np.sqrt(np.mean(y64 ** 2)))
+    # elementwise: bf16 rounding (<= 2^-8 relative) plus fp32 accumulation noise
+    bound = 2.0 ** -8 * np.abs(y64) * 1.001 + 1e-3 * rms
+    worst = float(np.max(np.abs(y - y64) - bound))
+    assert np.isfinite(y).all(), what + ": non-finite output"
+    assert rel <= 2e-3, "%s: rel err %.3e" % (what, rel)
+    assert worst <= 0, "%s: elementwise excess %.3e (rms %.3e)" % (what, worst, rms)
+    return rel
+
+
+# ---------------------------------------------------------------- GEMM, full oracle
+GEMM_SMALL = [  # M, K, N, P, pb
+    (4, 256, 128, 1, None), (1, 1024, 256, 1, None), (3, 640, 384, 1, None),
+    (16, 1152, 512, 1, None), (7, 512, 384, 3, (128, 256)), (12, 384, 512, 2, (256, 512)),
+    (129, 512, 256, 1, None), (200, 896, 384, 3, (128, 256)), (256, 1024, 512, 1, None),
+    (33, 8704 // 8, 256, 1, None),
+]
+
+
+@pytest.mark.parametrize("M,K,N,P,pb", GEMM_SMALL)
+def test_gemm_full_vs_oracle(pq, orc, M, K, N, P, pb):
+    prob = pqgen.make_problem(M, K, N, P=P, pb=pb, seed=M * 7 + K + N)
+    L = Problem(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    y64 = orc.gemm_f64(a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
+    for name, fn in gemm_paths(pq, M):
+        y = run_gemm(fn, a, asg, rs, L, prob.pb1, prob.pb2, M, N, ldy=N + 64)
+        assert_close(y, y64, "%s M=%d K=%d N=%d P=%d" % (name, M, K, N, P))
+
+
+@pytest.mark.parametrize("subnormal", [False, True])
+def test_gemm_random_codes(pq, orc, subnormal):
+    """Codes drawn uniformly from all 254 finite e4m3 codes (incl. 0x80 and
+    subnormals), or only from the 16 zero/subnormal codes."""
+    M, K, N, P = 24, 1024, 384, 2
+    prob = pqgen.make_problem(M, K, N, P=P, pb=(128, 384), seed=5)
+    L = Problem(pq, orc, prob)
+    a_o = pqgen.random_codes(P, M, K, seed=6, subnormal_only=subnormal)
+    asg_o = pqgen.random_scales(P, K // 128, M, seed=7)
+    dec = orc.e4m3_decode_table()[a_o]
+    rs_o = dec.reshape(P, M, K // 128, 128).sum(axis=3).transpose(0, 2, 1).astype(np.float32)
+    y64 = orc.gemm_f64(a_o, asg_o, np.ascontiguousarray(rs_o), L.t["codes"], L.t["sz"], 128, 384)
+    a = torch.from_numpy(a_o).cuda()
+    asg = torch.from_numpy(asg_o).cuda()
+    rs = torch.from_numpy(np.ascontiguousarray(rs_o)).cuda()
+    for name, fn in gemm_paths(pq, M):
+        assert_close(run_gemm(fn, a, asg, rs, L, 128, 384, M, N), y64, name)
+
+
+def test_gemm_zero_point_eight_gives_zero(pq, orc):
+    M, K, N = 9, 512, 256
+    prob = pqgen.make_problem(M, K, N, seed=8)
+    eights = np.int32(np.uint32(0x88888888).view(np.int32))
+    prob["qweight"] = np.full_like(prob.qweight, eights)
+    prob["qzeros"] = np.full_like(prob.qzeros, eights)
+    L = Problem(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    for name, fn in gemm_paths(pq, M):
+        y = run_gemm(fn, a, asg, rs, L, N, N, M, N)
+        assert np.all(y == 0), name
+
+
+def test_gemm_merged_equals_sliced(pq, orc):
+    """One P=3 launch == three P=1 launches on the column slices, bit for bit."""
+    M, K, N = 40, 640, 512
+    prob = pqgen.make_problem(M, K, N, P=3, pb=(256, 384), seed=9)
+    L = Problem(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    for Mx in (M, 5):
+        for name, fn in gemm_paths(pq, Mx):
+            aa, ss, rr = a[:, :Mx].contiguous(), asg[:, :, :Mx].contiguous(), rs[:, :, :Mx].contiguous()
+            y = run_gemm(fn, aa, ss, rr, L, 256, 384, Mx, N)
+            for p, (lo, hi) in enumerate([(0, 256), (256, 384), (384, 512)]):
+                Ls = type("S", (), {})()
+                Ls.w_d = L.w_d[lo:hi].contiguous()
+                Ls.sz_d = L.sz_d[:, lo:hi].contiguous()
+                ys = run_gemm(fn, aa[p:p + 1].contiguous(), ss[p:p + 1].contiguous(),
+                              rr[p:p + 1].contiguous(), Ls, hi - lo, hi - lo, Mx, hi - lo)
+                assert np.array_equal(y[:, lo:hi], ys), (name, Mx, p)
+
+
+def test_gemm_rows_independent(pq, orc):
+    M, K, N = 150, 512, 256
+    prob = pqgen.make_problem(M, K, N, seed=10)
+    L = Problem(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    a2, asg2, rs2 = a.clone(), asg.clone(), rs.clone()
+    g = torch.Generator(device="cpu").manual_seed(0)
+    a2[:, 1::2] = torch.randint(0, 126, a2[:, 1::2].shape, generator=g).to(torch.uint8).cuda()
+    asg2[:, :, 1::2] *= 3
+    for Mx in (M, 16):
+        for name, fn in gemm_paths(pq, Mx):
+            y1 = run_gemm(fn, a[:, :Mx].contiguous(), asg[:, :, :Mx].contiguous(),
+                          rs[:, :, :Mx].contiguous(), L, N, N, Mx, N)
+            y2 = run_gemm(fn, a2[:, :Mx].contiguous(), asg2[:, :, :Mx].contiguous(),
+                          rs2[:, :, :Mx].contiguous(), L, N, N, Mx, N)
+            assert np.array_equal(y1[0::2], y2[0::2]), name
+
+
+# ---------------------------------------------------------------- full workloads, sampled
+FULL = [("decode", 1), ("decode", 4), ("decode", 16), ("prefill", None), ("down", None),
+        ("qkv", None), ("tiny", None)]
+
+
+def _samples(M, N, pb1, pb2, count, seed):
+    r = np.random.default_rng(seed)
+    ms = list(r.integers(0, M, count)) + [0, M - 1] * 4
+    ns = list(r.integers(0, N, count)) + [0, N - 1, pb1 - 1, min(pb1, N - 1), pb2 - 1,
+                                          min(pb2, N - 1), 127, 128]
+    return np.array(ms[:len(ns)]), np.array(ns)
+
+
+@pytest.mark.parametrize("name,M", FULL, ids=["%s-%s" % f for f in FULL])
+def test_full_workload_sampled(pq, orc, name, M):
+    """At the benchmarked sizes and launch configuration: prologue bit-exact
+    (full), GEMM on 3000 sampled outputs against the fp64 oracle."""
+    prob = pqgen.config_problem(name, M=M)
+    L = Problem(pq, orc, prob, check_pack=(name != "down"))
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    y = pq.pq_gemm(a, asg, rs, L.w_d, L.sz_d, prob.pb1, prob.pb2)
+    torch.cuda.synchronize()
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    assert np.array_equal(asg.cpu().numpy(), asg_o) and np.array_equal(rs.cpu().numpy(), rs_o)
+    ms, ns = _samples(prob.M, prob.N, prob.pb1, prob.pb2, 3000, 11)
+    y64 = orc.gemm_f64_sampled(ms, ns, a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1,
+                               prob.pb2)
+    yg = y.float().cpu().numpy()[ms, ns]
+    assert_close(yg, y64, "%s M=%d" % (name, prob.M))
+    if prob.M <= pq.pq_gemm_skinny_max_m():      # the other path on the same inputs
+        y2 = pq.pq_gemm_tc(a, asg, rs, L.w_d, L.sz_d, prob.pb1, prob.pb2)
+        assert_close(y2.float().cpu().numpy()[ms, ns], y64, "tc %s M=%d" % (name, prob.M))

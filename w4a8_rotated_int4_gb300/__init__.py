@@ -1,0 +1,240 @@
+"""Python binding of libpq: the ParoQuant (PARO) W4A8 rotated-int4 linear layer
+on one GB300 (sm_103a).
+
+    y = ((x * channel_scales) R^T) dequant(Q)^T
+
+The functions mirror the C ABI in include/pq.h one to one (same names, same
+argument order after marshalling).  This module only converts arguments:
+numpy arrays for the host packer, torch CUDA tensors (device memory) and the
+current torch stream for the device calls.  Every step of the layer runs in
+libpq's CUDA kernels; there is no fallback.  If libpq.so has not been built the
+first call raises PQError.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpq.so")
+
+# Every symbol include/pq.h declares.
+EXPORTS = (
+    "pq_abi_version", "pq_status_string", "pq_last_error", "pq_pack_sizes", "pq_pack",
+    "pq_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny", "pq_gemm_tc",
+    "pq_e4m3_encode",
+)
+
+STATUS = {0: "PQ_OK", 1: "PQ_ERR_NULL", 2: "PQ_ERR_SHAPE", 3: "PQ_ERR_ALIGN", 4: "PQ_ERR_PAIRS",
+          5: "PQ_ERR_PARTITION", 6: "PQ_ERR_ARCH", 7: "PQ_ERR_CUDA"}
+
+
+class PQError(RuntimeError):
+    """A libpq call returned a non-zero status (or the library is missing)."""
+
+    def __init__(self, msg, status=None):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded libpq.so (raises PQError when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise PQError("libpq.so is not built (run __graft_entry__.build() or "
+                      "python w4a8_rotated_int4_gb300/build.py)")
+    L = C.CDLL(LIB_PATH)
+    vp, i32, st, u64 = C.c_void_p, C.c_int, C.c_size_t, C.POINTER(C.c_size_t)
+    L.pq_abi_version.restype = i32
+    L.pq_abi_version.argtypes = []
+    L.pq_status_string.restype = C.c_char_p
+    L.pq_status_string.argtypes = [i32]
+    L.pq_last_error.restype = C.c_char_p
+    L.pq_last_error.argtypes = []
+    L.pq_pack_sizes.restype = i32
+    L.pq_pack_sizes.argtypes = [i32, i32, i32, u64, u64, u64]
+    L.pq_pack.restype = i32
+    L.pq_pack.argtypes = [i32, i32, i32] + [vp] * 8
+    L.pq_rotate_quant.restype = i32
+    L.pq_rotate_quant.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.pq_gemm.restype = i32
+    L.pq_gemm.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp]
+    L.pq_gemm_skinny_max_m.restype = i32
+    L.pq_gemm_skinny_max_m.argtypes = []
+    for name in ("pq_gemm_skinny", "pq_gemm_tc"):
+        f = getattr(L, name)
+        f.restype = i32
+        f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
+    L.pq_e4m3_encode.restype = i32
+    L.pq_e4m3_encode.argtypes = [vp, vp, st, vp]
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        L = lib()
+        raise PQError("%s: %s (%s): %s" % (what, STATUS.get(status, status),
+                                           L.pq_status_string(status).decode(),
+                                           L.pq_last_error().decode()), status)
+
+
+def pq_abi_version() -> int:
+    return int(lib().pq_abi_version())
+
+
+def pq_gemm_skinny_max_m() -> int:
+    return int(lib().pq_gemm_skinny_max_m())
+
+
+# ---------------------------------------------------------------- host packer
+def _np_ptr(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def pq_pack_sizes(K: int, N: int, P: int):
+    r, s, w = C.c_size_t(), C.c_size_t(), C.c_size_t()
+    _check(lib().pq_pack_sizes(K, N, P, C.byref(r), C.byref(s), C.byref(w)), "pq_pack_sizes")
+    return r.value, s.value, w.value
+
+
+def pq_pack(qweight: np.ndarray, qzeros: np.ndarray, scales: np.ndarray, pairs: np.ndarray,
+            theta: np.ndarray):
+    """Host packer.  Inputs in checkpoint layout (f16 tensors as uint16 bit
+    patterns); returns (rec uint8 [P,8,G,64,8], sz uint16 [G,N,2], w uint8 [N,K/2])."""
+    qweight = np.ascontiguousarray(qweight, dtype=np.int32)
+    qzeros = np.ascontiguousarray(qzeros, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int16)
+    theta = np.ascontiguousarray(theta, dtype=np.uint16)
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    if pairs.ndim == 2:
+        pairs = pairs[None]
+        theta = theta[None]
+    P = pairs.shape[0]
+    G = K // 128
+    nr, ns, nw = pq_pack_sizes(K, N, P)
+    rec = np.empty((P, 8, G, 64, 8), dtype=np.uint8)
+    sz = np.empty((G, N, 2), dtype=np.uint16)
+    w = np.empty((N, K // 2), dtype=np.uint8)
+    assert rec.nbytes == nr and sz.nbytes == ns and w.nbytes == nw
+    _check(lib().pq_pack(K, N, P, _np_ptr(qweight), _np_ptr(qzeros), _np_ptr(scales),
+                         _np_ptr(pairs), _np_ptr(theta), _np_ptr(rec), _np_ptr(sz), _np_ptr(w)),
+           "pq_pack")
+    return rec, sz, w
+
+
+# ---------------------------------------------------------------- device calls
+def _torch():
+    import torch
+    return torch
+
+
+def _dptr(t) -> C.c_void_p:
+    if not t.is_cuda:
+        raise PQError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise PQError("expected a contiguous tensor")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def pq_rotate_quant(x, rec, cs, a=None, asg=None, rs=None, stream=None):
+    """x bf16 [M, ldx>=K] (CUDA), rec uint8 (device copy of pq_pack's rec),
+    cs f16 [P, K].  Returns (a uint8 [P,M,K] e4m3 codes, asg f32 [P,G,M], rs f32 [P,G,M])."""
+    torch = _torch()
+    M, ldx = x.shape
+    P, K = cs.shape
+    G = K // 128
+    dev = x.device
+    if a is None:
+        a = torch.empty((P, M, K), dtype=torch.uint8, device=dev)
+    if asg is None:
+        asg = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    if rs is None:
+        rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _check(lib().pq_rotate_quant(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(a),
+                                 _dptr(asg), _dptr(rs), _stream(stream)), "pq_rotate_quant")
+    return a, asg, rs
+
+
+def _gemm_args(a, asg, rs, w, sz, pb1, pb2, y):
+    torch = _torch()
+    P, M, K = a.shape
+    N = w.shape[0]
+    if pb1 is None:
+        pb1 = pb2 = N
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    return P, M, K, N, pb1, pb2, y
+
+
+def pq_gemm(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, stream=None):
+    """y bf16 [M, N] = group GEMM of the prologue outputs with the packed weights."""
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
+    _check(lib().pq_gemm(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w),
+                         _dptr(sz), _dptr(y), y.stride(0), _stream(stream)), "pq_gemm")
+    return y
+
+
+def _gemm_path(fn, name, a, asg, rs, w, sz, pb1, pb2, y, dev_status, stream):
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
+    st = _dptr(dev_status) if dev_status is not None else None
+    _check(fn(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w), _dptr(sz),
+              _dptr(y), y.stride(0), st, _stream(stream)), name)
+    return y
+
+
+def pq_gemm_skinny(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    return _gemm_path(lib().pq_gemm_skinny, "pq_gemm_skinny", a, asg, rs, w, sz, pb1, pb2, y,
+                      dev_status, stream)
+
+
+def pq_gemm_tc(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    return _gemm_path(lib().pq_gemm_tc, "pq_gemm_tc", a, asg, rs, w, sz, pb1, pb2, y,
+                      dev_status, stream)
+
+
+def pq_e4m3_encode(x, out=None, stream=None):
+    """The prologue's device e4m3 encoder on an fp32 CUDA tensor."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().pq_e4m3_encode(_dptr(x), _dptr(out), x.numel(), _stream(stream)),
+           "pq_e4m3_encode")
+    return out
+
+
+class PQLinear:
+    """One packed projection resident in device memory: pq_pack once, then
+    forward(x) = pq_rotate_quant + pq_gemm on the current stream."""
+
+    def __init__(self, qweight, qzeros, scales, pairs, theta, cs, pb=None, device="cuda"):
+        torch = _torch()
+        rec, sz, w = pq_pack(qweight, qzeros, scales, pairs, theta)
+        self.P, self.K, self.N = rec.shape[0], w.shape[1] * 2, w.shape[0]
+        self.pb1, self.pb2 = pb if pb is not None else (self.N, self.N)
+        self.rec = torch.from_numpy(rec).to(device)
+        self.sz = torch.from_numpy(sz.view(np.int16)).to(device)
+        self.w = torch.from_numpy(w).to(device)
+        self.cs = torch.from_numpy(np.ascontiguousarray(cs, dtype=np.uint16).view(np.int16)
+                                   .reshape(self.P, self.K)).to(device)
+
+    def forward(self, x, y=None, stream=None):
+        a, asg, rs = pq_rotate_quant(x, self.rec, self.cs, stream=stream)
+        return pq_gemm(a, asg, rs, self.w, self.sz, self.pb1, self.pb2, y=y, stream=stream)
+
+    __call__ = forward

@@ -1,0 +1,328 @@
+// pq_abi.cpp -- host side of libpq: status strings, per-thread error text,
+// device checks, argument validation, the load-time packer and GEMM dispatch.
+//
+// Source: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", sections
+// "Format" (checkpoint layouts, nibble order 0,2,4,6,1,3,5,7, raw zero
+// points, pairs local to each 128 group) and "Design" items 1 (SZ table of
+// (scale, scale*(zp-8))), 3 (8-byte rotation records {i|j<<8, cos, sin}) and
+// 4 (partition select from two boundary columns).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pq_internal.h"
+
+namespace pq {
+
+namespace {
+thread_local std::string g_err;
+
+const char *kStatusText[] = {
+    "ok",
+    "a required pointer is NULL",
+    "a size or leading dimension is out of range",
+    "a pointer or leading dimension breaks the alignment rule",
+    "a pairs row is not a permutation of 0..127",
+    "partition count or boundaries are inconsistent",
+    "no sm_103 device is current",
+    "a CUDA runtime call failed",
+};
+}  // namespace
+
+pq_status fail(pq_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+void clear_error() { g_err.clear(); }
+
+pq_status check_device(int *sm_count) {
+    // Per-device cache of (checked, ok, SMs); devices are few and fixed.
+    static std::mutex mu;
+    static int cached_sm[64];
+    static int cached_ok[64];   // 0 unknown, 1 ok, -1 wrong arch
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return fail(PQ_ERR_ARCH, "cudaGetDevice: %s", cudaGetErrorString(e));
+    }
+    if (dev < 64) {
+        std::lock_guard<std::mutex> lk(mu);
+        if (cached_ok[dev] == 1) {
+            if (sm_count) *sm_count = cached_sm[dev];
+            return PQ_OK;
+        }
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        e = cudaGetLastError();
+        return fail(PQ_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    }
+    if (major != 10 || minor != 3)
+        return fail(PQ_ERR_ARCH, "device %d is sm_%d%d; libpq is built for sm_103a only", dev,
+                    major, minor);
+    if (dev < 64) {
+        std::lock_guard<std::mutex> lk(mu);
+        cached_ok[dev] = 1;
+        cached_sm[dev] = sms;
+    }
+    if (sm_count) *sm_count = sms;
+    return PQ_OK;
+}
+
+static pq_status check_partitions(int P, int N, int pb1, int pb2) {
+    if (P < 1 || P > PQ_MAX_PARTITIONS)
+        return fail(PQ_ERR_PARTITION, "P = %d outside 1..%d", P, PQ_MAX_PARTITIONS);
+    if (pb1 % 128 || pb2 % 128)
+        return fail(PQ_ERR_PARTITION, "pb1 = %d, pb2 = %d must be multiples of 128", pb1, pb2);
+    bool ok = false;
+    if (P == 1) ok = (pb1 == N && pb2 == N);
+    if (P == 2) ok = (pb1 > 0 && pb1 < N && pb2 == N);
+    if (P == 3) ok = (pb1 > 0 && pb1 < pb2 && pb2 < N);
+    if (!ok)
+        return fail(PQ_ERR_PARTITION, "pb1 = %d, pb2 = %d do not describe %d partitions of N = %d",
+                    pb1, pb2, P, N);
+    return PQ_OK;
+}
+
+pq_status check_gemm_args(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                          int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                          int ldy) {
+    if (!a || !asg || !rs || !w || !sz || !y) return fail(PQ_ERR_NULL, "NULL buffer");
+    if (M < 1 || N < 128 || K < 128 || N % 128 || K % 128)
+        return fail(PQ_ERR_SHAPE, "M = %d, N = %d, K = %d (need M >= 1, N and K positive "
+                    "multiples of 128)", M, N, K);
+    if ((long long)K * 128 > (1ll << 31) || (long long)M * N > (1ll << 40))
+        return fail(PQ_ERR_SHAPE, "sizes too large");
+    if (ldy < N) return fail(PQ_ERR_SHAPE, "ldy = %d < N = %d", ldy, N);
+    pq_status st = check_partitions(P, N, pb1, pb2);
+    if (st != PQ_OK) return st;
+    if (!aligned(a, 16) || !aligned(w, 16) || !aligned(sz, 16) || !aligned(y, 16) ||
+        !aligned(asg, 4) || !aligned(rs, 4) || ldy % 8)
+        return fail(PQ_ERR_ALIGN, "a, w, sz, y need 16-byte alignment, asg/rs 4-byte, ldy a "
+                    "multiple of 8");
+    return PQ_OK;
+}
+
+// ---------------------------------------------------------------------------
+// load-time packer
+// ---------------------------------------------------------------------------
+
+// double -> IEEE binary16 bits, round to nearest even, by integer manipulation
+// of the binary64 encoding.
+static uint16_t half_bits_rne(double d) {
+    uint64_t u;
+    std::memcpy(&u, &d, 8);
+    const uint16_t sign = (uint16_t)((u >> 48) & 0x8000u);
+    const uint64_t mag = u & 0x7FFFFFFFFFFFFFFFull;
+    if (mag > 0x7FF0000000000000ull) return sign | 0x7E00;          // NaN
+    if ((mag >> 52) == 0) return sign;                                // zero / binary64 subnormal
+    const int e = (int)(mag >> 52) - 1023;                            // value in [2^e, 2^(e+1))
+    if (e >= 16) return sign | 0x7C00;
+    const uint64_t sig = (mag & ((1ull << 52) - 1)) | (1ull << 52);   // 53-bit significand
+    const int qexp = (e < -14 ? -14 : e) - 10;                        // exponent of one f16 ulp
+    const int drop = qexp - (e - 52);                                 // >= 42
+    if (drop > 63) return sign;
+    uint64_t n = sig >> drop;
+    const uint64_t rem = sig & ((1ull << drop) - 1), half = 1ull << (drop - 1);
+    if (rem > half || (rem == half && (n & 1))) n++;
+    if (e < -14) return sign | (uint16_t)n;                           // n <= 1024 (1024 = min normal)
+    const uint32_t bits = ((uint32_t)(e + 15) << 10) + (uint32_t)(n - 1024);   // n == 2048 carries
+    return bits >= 0x7C00 ? (uint16_t)(sign | 0x7C00) : (uint16_t)(sign | bits);
+}
+
+static double half_value(uint16_t h) {
+    const int e = (h >> 10) & 31, m = h & 1023;
+    double v = e == 0 ? std::ldexp((double)m, -24) : std::ldexp((double)(m | 1024), e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
+// AWQ interleave: slot s of a packed word holds column kAwqOrder[s] of its octet.
+static const int kAwqOrder[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+}  // namespace pq
+
+using namespace pq;
+
+extern "C" int pq_abi_version(void) { return PQ_ABI_VERSION; }
+
+extern "C" const char *pq_status_string(int status) {
+    if (status < 0 || status > (int)PQ_ERR_CUDA) return "unknown status";
+    return kStatusText[status];
+}
+
+extern "C" const char *pq_last_error(void) { return g_err.c_str(); }
+
+extern "C" pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_t *sz_bytes,
+                                   size_t *w_bytes) {
+    clear_error();
+    if (K < 128 || N < 128 || K % 128 || N % 128)
+        return fail(PQ_ERR_SHAPE, "K = %d, N = %d must be positive multiples of 128", K, N);
+    if (P < 1 || P > PQ_MAX_PARTITIONS) return fail(PQ_ERR_PARTITION, "P = %d outside 1..3", P);
+    const size_t G = (size_t)K / 128;
+    if (rec_bytes) *rec_bytes = (size_t)P * 8 * G * 64 * 8;
+    if (sz_bytes) *sz_bytes = G * (size_t)N * 4;
+    if (w_bytes) *w_bytes = (size_t)N * (size_t)K / 2;
+    return PQ_OK;
+}
+
+extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
+                             const uint16_t *scales, const int16_t *pairs, const uint16_t *theta,
+                             void *rec, void *sz, void *w) {
+    clear_error();
+    if (!qweight || !qzeros || !scales || !pairs || !theta || !rec || !sz || !w)
+        return fail(PQ_ERR_NULL, "pq_pack: NULL pointer");
+    pq_status st = pq_pack_sizes(K, N, P, nullptr, nullptr, nullptr);
+    if (st != PQ_OK) return st;
+    const int G = K / 128, W8 = N / 8;
+
+    // pairs: every (p, layer, group) row a permutation of 0..127
+    for (int row = 0; row < P * 8 * G; ++row) {
+        const int16_t *pr = pairs + (size_t)row * 128;   // rows are contiguous 128-entry blocks
+        uint64_t seen[2] = {0, 0};
+        for (int t = 0; t < 128; ++t) {
+            const int v = pr[t];
+            if (v < 0 || v > 127 || ((seen[v >> 6] >> (v & 63)) & 1))
+                return fail(PQ_ERR_PAIRS, "pairs row (p=%d, layer=%d, group=%d) is not a "
+                            "permutation of 0..127", row / (8 * G), (row / G) % 8, row % G);
+            seen[v >> 6] |= 1ull << (v & 63);
+        }
+    }
+
+    // rotation records: [p][layer][g][t] = {i | j<<8, f16 cos, f16 sin}
+    uint8_t *ro = static_cast<uint8_t *>(rec);
+    for (int pl = 0; pl < P * 8; ++pl)
+        for (int g = 0; g < G; ++g)
+            for (int t = 0; t < 64; ++t) {
+                const int16_t *pr = pairs + (size_t)pl * K + 128 * g;
+                const double th = half_value(theta[(size_t)pl * (K / 2) + 64 * g + t]);
+                const uint16_t c = half_bits_rne(std::cos(th));
+                const uint16_t s = half_bits_rne(std::sin(th));
+                uint8_t *o = ro + (((size_t)pl * G + g) * 64 + t) * 8;
+                o[0] = (uint8_t)pr[2 * t];
+                o[1] = (uint8_t)pr[2 * t + 1];
+                o[2] = 0;
+                o[3] = 0;
+                o[4] = (uint8_t)(c & 0xFF);
+                o[5] = (uint8_t)(c >> 8);
+                o[6] = (uint8_t)(s & 0xFF);
+                o[7] = (uint8_t)(s >> 8);
+            }
+
+    // SZ table: (sc, f16(sc * (zp - 8))), the product exact in fp32
+    uint16_t *so = static_cast<uint16_t *>(sz);
+    for (int g = 0; g < G; ++g)
+        for (int w8 = 0; w8 < W8; ++w8) {
+            const uint32_t zw = (uint32_t)qzeros[(size_t)g * W8 + w8];
+            for (int s = 0; s < 8; ++s) {
+                const int n = 8 * w8 + kAwqOrder[s];
+                const int zp = (int)((zw >> (4 * s)) & 15u);
+                const uint16_t sc = scales[(size_t)g * N + n];
+                const float prod = (float)half_value(sc) * (float)(zp - 8);
+                so[((size_t)g * N + n) * 2 + 0] = sc;
+                so[((size_t)g * N + n) * 2 + 1] = half_bits_rne((double)prod);
+            }
+        }
+
+    // weights: w[n][k/2] = c[k][n] | c[k+1][n] << 4
+    uint8_t *wo = static_cast<uint8_t *>(w);
+    for (int k = 0; k < K; k += 2) {
+        const int32_t *r0 = qweight + (size_t)k * W8;
+        const int32_t *r1 = r0 + W8;
+        for (int w8 = 0; w8 < W8; ++w8) {
+            const uint32_t a0 = (uint32_t)r0[w8], a1 = (uint32_t)r1[w8];
+            for (int s = 0; s < 8; ++s) {
+                const int n = 8 * w8 + kAwqOrder[s];
+                wo[(size_t)n * (K / 2) + k / 2] =
+                    (uint8_t)(((a0 >> (4 * s)) & 15u) | (((a1 >> (4 * s)) & 15u) << 4));
+            }
+        }
+    }
+    return PQ_OK;
+}
+
+extern "C" pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
+                                     const void *cs, void *a, float *asg, float *rs,
+                                     void *stream) {
+    clear_error();
+    if (!x || !rec || !cs || !a || !asg || !rs) return fail(PQ_ERR_NULL, "NULL buffer");
+    if (M < 1 || K < 128 || K % 128 || ldx < K)
+        return fail(PQ_ERR_SHAPE, "M = %d, K = %d, ldx = %d", M, K, ldx);
+    if ((long long)M * K > (1ll << 40)) return fail(PQ_ERR_SHAPE, "sizes too large");
+    if (P < 1 || P > PQ_MAX_PARTITIONS) return fail(PQ_ERR_PARTITION, "P = %d outside 1..3", P);
+    if (!aligned(x, 16) || !aligned(rec, 16) || !aligned(cs, 16) || !aligned(a, 16) ||
+        !aligned(asg, 4) || !aligned(rs, 4) || ldx % 8)
+        return fail(PQ_ERR_ALIGN, "x, rec, cs, a need 16-byte alignment, asg/rs 4-byte, ldx a "
+                    "multiple of 8");
+    pq_status st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    return launch_rotate_quant(x, M, K, ldx, P, rec, cs, a, asg, rs, stream);
+}
+
+extern "C" pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream) {
+    clear_error();
+    if (!in || !out) return fail(PQ_ERR_NULL, "NULL buffer");
+    if (!aligned(in, 4)) return fail(PQ_ERR_ALIGN, "in needs 4-byte alignment");
+    pq_status st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    if (n == 0) return PQ_OK;
+    return launch_e4m3_encode(in, out, n, stream);
+}
+
+extern "C" int pq_gemm_skinny_max_m(void) { return kSkinnyMaxM; }
+
+extern "C" pq_status pq_gemm_skinny(const void *a, const float *asg, const float *rs, int M,
+                                    int N, int K, int P, int pb1, int pb2, const void *w,
+                                    const void *sz, void *y, int ldy, unsigned int *dev_status,
+                                    void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (M > kSkinnyMaxM) return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: M = %d > %d", M, kSkinnyMaxM);
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    return launch_gemm_skinny(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream,
+                              sms);
+}
+
+extern "C" pq_status pq_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N,
+                                int K, int P, int pb1, int pb2, const void *w, const void *sz,
+                                void *y, int ldy, unsigned int *dev_status, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, sms);
+}
+
+extern "C" pq_status pq_gemm(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                             int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                             int ldy, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    if (M <= kSkinnyMaxM)
+        return launch_gemm_skinny(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream,
+                                  sms);
+    return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, sms);
+}

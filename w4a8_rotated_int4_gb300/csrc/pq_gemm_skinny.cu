@@ -1,0 +1,334 @@
+// pq_gemm_skinny.cu -- decode-band (M <= 16) uint4 x e4m3 group GEMM on CUDA
+// cores, streaming the 4.25-bit/weight operands from HBM once.
+//
+// Source: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", "Design"
+// items 1 (zero point as a row-sum correction: per group
+// acc += asg * (sc * D - zscale * rowsum), SZ table in one 4-byte load),
+// 2 (per-group activation scales folded per 128-k group) and 4 (partition
+// of a column from two boundary columns, one launch for any P).
+//
+// Work split.  A CTA owns a run of column octets (8 output features) for an
+// M-tile of MT tokens.  Compute warp kw covers k in [1024 kw, 1024 kw + 1024):
+// lane l owns the 32 consecutive k at 1024 kw + 32 l (one quarter of group
+// 8 kw + l/4) and keeps that slice of the MT activation rows in registers for
+// the whole launch (as f16 pairs; e4m3 converts to f16 exactly).  A producer
+// warp streams each octet's weight rows (8 x K/2 contiguous bytes) and its SZ
+// words (G x 32 bytes) into a 4-stage shared-memory ring with bulk copies
+// (cp.async.bulk + mbarrier transaction counts), so the weight stream is
+// independent of register pressure.
+//
+// Arithmetic.  A weight nibble c is turned into an f16 *subnormal* whose bits
+// are the nibble (value c * 2^-24) by one AND per two nibbles -- no integer to
+// float conversion and no bias subtraction -- and multiplied into an fp32
+// accumulator with the mixed-precision fma.rn.f32.f16 (exact product, one
+// rounding per add).  Nibbles sitting in bits 4..7 of a half are used in place
+// as 16 * c * 2^-24.  So per group and token the lanes compute
+// D' = sum a * c = D + 8 * rs exactly up to fp32 addition, and the fold uses
+// sc * D - zscale * rs = sc * D' - (zscale + 8 sc) * rs, where zscale + 8 sc
+// is exact in fp32.  Each of the four lanes of a group adds a quarter of the
+// zero-point term; five xor-shuffles reduce a warp, shared memory reduces the
+// k-warps in a fixed order (deterministic), and the bf16 result is stored once.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pq_device.cuh"
+#include "pq_internal.h"
+
+namespace pq {
+namespace {
+
+constexpr int kMaxStages = 4;
+constexpr int kMaxK = 16384;          // 16 compute warps + producer; larger K uses the tcgen05 path
+constexpr int kSmemBudget = 200 * 1024;
+
+struct SkinnyParams {
+    const uint8_t *a;
+    const float *asg;
+    const float *rs;
+    const uint8_t *w;
+    const uint32_t *sz;     // [G][N] words: f16 scale | f16 zscale << 16
+    __nv_bfloat16 *y;
+    unsigned int *status;
+    int M, N, K, G, pb1, pb2, ldy;
+    int oct_per_cta, n_oct, nkw, stages;
+    uint32_t stage_bytes, w_bytes;
+};
+
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_codes));
+    return r;
+}
+
+// acc_lo += a.lo * b.lo, acc_hi += a.hi * b.hi with f16 operands and fp32 accumulators
+__device__ __forceinline__ void fma2_f32_f16(float &acc_lo, float &acc_hi, uint32_t a, uint32_t b) {
+    asm("{\n.reg .f16 al, ah, bl, bh;\n"
+        "mov.b32 {al, ah}, %2;\n"
+        "mov.b32 {bl, bh}, %3;\n"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n"
+        "fma.rn.f32.f16 %1, ah, bh, %1;\n}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(a), "r"(b));
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+    float f;
+    asm("{\n.reg .f16 l, h;\nmov.b32 {l, h}, %1;\ncvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(w));
+    return f;
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+    float f;
+    asm("{\n.reg .f16 l, h;\nmov.b32 {l, h}, %1;\ncvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(w));
+    return f;
+}
+
+template <int MT>
+__global__ void skinny_kernel(const SkinnyParams prm) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nkw = prm.nkw, S = prm.stages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * prm.stage_bytes);
+    uint64_t *empty = full + S;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + S);
+    float *ypart = reinterpret_cast<float *>(empty + S + 2);
+
+    const int oct0 = blockIdx.x * prm.oct_per_cta;
+    const int noct = min(prm.oct_per_cta, prm.n_oct - oct0);
+    const int ncol = prm.oct_per_cta * 8;
+    const int m0 = blockIdx.y * MT;
+    const int K = prm.K, G = prm.G, M = prm.M;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nkw);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == nkw) {
+        // ---------------- producer warp ----------------
+        int issued = 0;
+        for (int i = 0; i < noct; ++i) {
+            const int s = i % S, use = i / S;
+            if (*abort_flag) break;
+            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+                if (lane == 0) {
+                    if (prm.status) atomicOr(prm.status, kStatusWaitEmpty);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            uint8_t *st = smem + (size_t)s * prm.stage_bytes;
+            const int n0 = (oct0 + i) * 8;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], prm.stage_bytes);
+            __syncwarp();
+            if (lane == 0) bulk_g2s(st, prm.w + (size_t)n0 * (K / 2), prm.w_bytes, &full[s]);
+            for (int g = lane; g < G; g += 32)
+                bulk_g2s(st + prm.w_bytes + 32 * g, prm.sz + (size_t)g * prm.N + n0, 32, &full[s]);
+            issued = i + 1;
+        }
+        __syncwarp();
+        // on abort: let every copy already issued land before shared memory is released
+        if (*abort_flag && lane == 0) {
+            for (int s = 0; s < S && s < issued; ++s) {
+                const int last_use = (issued - 1 - s) / S;
+                if (!mbar_wait(&full[s], last_use & 1) && prm.status)
+                    atomicOr(prm.status, kStatusDrain);
+            }
+        }
+    } else {
+        // ---------------- compute warps ----------------
+        const int kw = warp;
+        const int k0 = 1024 * kw + 32 * lane;
+        const bool kvalid = k0 < K;
+        const int g = kvalid ? (k0 >> 7) : 0;
+        uint32_t A[MT][16];
+        float asg_r[MT], rs_r[MT];
+        int cur_p = -1;
+        for (int i = 0; i < noct; ++i) {
+            const int s = i % S, use = i / S;
+            const int n0 = (oct0 + i) * 8;
+            const int p = (n0 >= prm.pb1) + (n0 >= prm.pb2);
+            if (p != cur_p) {
+                cur_p = p;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const int row = m0 + m;
+                    uint32_t u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    asg_r[m] = 0.0f;
+                    rs_r[m] = 0.0f;
+                    if (kvalid && row < M) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            prm.a + ((size_t)p * M + row) * K + k0);
+                        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                        u[0] = v0.x; u[1] = v0.y; u[2] = v0.z; u[3] = v0.w;
+                        u[4] = v1.x; u[5] = v1.y; u[6] = v1.z; u[7] = v1.w;
+                        asg_r[m] = __ldg(prm.asg + ((size_t)p * G + g) * M + row);
+                        rs_r[m] = __ldg(prm.rs + ((size_t)p * G + g) * M + row);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        // bytes 8q..8q+7 -> pairs (k, k+4), (k+1, k+5), (k+2, k+6), (k+3, k+7)
+                        const uint32_t t01 = __byte_perm(u[2 * q], u[2 * q + 1], 0x5140);
+                        const uint32_t t23 = __byte_perm(u[2 * q], u[2 * q + 1], 0x7362);
+                        A[m][4 * q + 0] = f16x2_from_e4m3x2(t01 & 0xFFFF);
+                        A[m][4 * q + 1] = f16x2_from_e4m3x2(t01 >> 16);
+                        A[m][4 * q + 2] = f16x2_from_e4m3x2(t23 & 0xFFFF);
+                        A[m][4 * q + 3] = f16x2_from_e4m3x2(t23 >> 16);
+                    }
+                }
+            }
+            if (*abort_flag) break;
+            if (!mbar_wait(&full[s], use & 1)) {
+                if (lane == 0) {
+                    if (prm.status) atomicOr(prm.status, kStatusWaitFull);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const uint8_t *st = smem + (size_t)s * prm.stage_bytes;
+            const uint32_t *szs = reinterpret_cast<const uint32_t *>(st + prm.w_bytes) + 8 * g;
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j) {
+                uint4 wv = make_uint4(0, 0, 0, 0);
+                if (kvalid) wv = *reinterpret_cast<const uint4 *>(st + (size_t)j * (K / 2) + (k0 >> 1));
+                float acc[MT][4];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+                const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t x = wq[q], x8 = x >> 8;
+                    const uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
+                    const uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 0], lo);
+                        fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 1], hi);
+                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 2], lo2);
+                        fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 3], hi2);
+                    }
+                }
+                const uint32_t szw = szs[j];
+                const float sc = half_lo(szw), zs = half_hi(szw);
+                const float sc24 = sc * 16777216.0f;            // 2^24: undo the subnormal scaling
+                const float zs8 = zs + 8.0f * sc;               // exact in fp32
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float sum = (acc[m][0] + acc[m][1]) + 16.0f * (acc[m][2] + acc[m][3]);
+                    const float c1 = asg_r[m] * sc24;
+                    const float c0 = asg_r[m] * (zs8 * (rs_r[m] * 0.25f));
+                    float yl = kvalid ? fmaf(c1, sum, -c0) : 0.0f;
+                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 16);
+                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 8);
+                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 4);
+                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 2);
+                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 1);
+                    if (lane == 0) ypart[(kw * MT + m) * ncol + 8 * i + j] = yl;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+    __syncthreads();
+
+    // reduce the k-warps in a fixed order and store bf16 rows (NaN after an abort)
+    const bool bad = *abort_flag != 0;
+    const int cols = noct * 8;
+    for (int e = threadIdx.x; e < MT * cols; e += blockDim.x) {
+        const int m = e / cols, c = e - m * cols;
+        if (m0 + m >= M) continue;
+        float v = 0.0f;
+        for (int k = 0; k < nkw; ++k) v += ypart[(k * MT + m) * ncol + c];
+        if (bad) v = __int_as_float(0x7FC00000);
+        prm.y[(size_t)(m0 + m) * prm.ldy + oct0 * 8 + c] = __float2bfloat16_rn(v);
+    }
+}
+
+// Whether the MT-row instantiation fits the register file with nkw + 1 warps.
+template <int MT>
+bool fits_registers(int nkw) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, skinny_kernel<MT>) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const int regs = (fa.numRegs + 7) / 8 * 8;
+    return regs * 32 * (nkw + 1) <= 65536 && 32 * (nkw + 1) <= fa.maxThreadsPerBlock;
+}
+
+template <int MT>
+pq_status launch_mt(SkinnyParams prm, int sm_count, cudaStream_t stream) {
+    const int threads = 32 * (prm.nkw + 1);
+    const int mtiles = (prm.M + MT - 1) / MT;
+    // column octets per CTA: about one CTA per SM per M-tile, bounded by shared memory
+    int ctas = sm_count > 0 ? sm_count : 1;
+    if (ctas > prm.n_oct) ctas = prm.n_oct;
+    int opc = (prm.n_oct + ctas - 1) / ctas;
+    auto smem_for = [&](int o) {
+        return (size_t)prm.stages * prm.stage_bytes + 16 * prm.stages + 16 +
+               (size_t)prm.nkw * MT * o * 8 * 4;
+    };
+    while (opc > 1 && smem_for(opc) > (size_t)kSmemBudget) opc = (opc + 1) / 2;
+    if (smem_for(opc) > (size_t)kSmemBudget)
+        return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d needs too much shared memory", prm.K);
+    prm.oct_per_cta = opc;
+    const dim3 grid((prm.n_oct + opc - 1) / opc, mtiles);
+    const size_t smem = smem_for(opc);
+    cudaError_t e = cudaFuncSetAttribute(skinny_kernel<MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    skinny_kernel<MT><<<grid, threads, smem, stream>>>(prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
+    return PQ_OK;
+}
+
+}  // namespace
+
+pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                             int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                             int ldy, unsigned int *dev_status, void *stream, int sm_count) {
+    (void)P;
+    if (K > kMaxK) return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d > %d", K, kMaxK);
+    SkinnyParams prm{};
+    prm.a = static_cast<const uint8_t *>(a);
+    prm.asg = asg;
+    prm.rs = rs;
+    prm.w = static_cast<const uint8_t *>(w);
+    prm.sz = static_cast<const uint32_t *>(sz);
+    prm.y = static_cast<__nv_bfloat16 *>(y);
+    prm.status = dev_status;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.G = K / 128;
+    prm.pb1 = pb1;
+    prm.pb2 = pb2;
+    prm.ldy = ldy;
+    prm.n_oct = N / 8;
+    prm.nkw = (K + 1023) / 1024;
+    prm.w_bytes = (uint32_t)(8 * (K / 2));
+    prm.stage_bytes = prm.w_bytes + 32u * (uint32_t)prm.G;
+    prm.stages = kMaxStages;
+    while (prm.stages > 2 && (size_t)prm.stages * prm.stage_bytes > 160 * 1024) --prm.stages;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // rows per M-tile: the smallest power of two >= M (at most 8) whose
+    // instantiation fits the register file with this many k-warps
+    if (M == 1 && fits_registers<1>(prm.nkw)) return launch_mt<1>(prm, sm_count, st);
+    if (M <= 2 && fits_registers<2>(prm.nkw)) return launch_mt<2>(prm, sm_count, st);
+    if (M <= 4 && fits_registers<4>(prm.nkw)) return launch_mt<4>(prm, sm_count, st);
+    if (fits_registers<8>(prm.nkw)) return launch_mt<8>(prm, sm_count, st);
+    if (fits_registers<4>(prm.nkw)) return launch_mt<4>(prm, sm_count, st);
+    if (fits_registers<2>(prm.nkw)) return launch_mt<2>(prm, sm_count, st);
+    if (fits_registers<1>(prm.nkw)) return launch_mt<1>(prm, sm_count, st);
+    return fail(PQ_ERR_CUDA, "pq_gemm_skinny: no instantiation fits K = %d", K);
+}
+
+}  // namespace pq

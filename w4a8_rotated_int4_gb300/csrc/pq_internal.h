@@ -1,0 +1,43 @@
+// pq_internal.h -- declarations shared by the translation units of libpq.
+// Not part of the public ABI (that is include/pq.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "pq.h"
+
+namespace pq {
+
+// Records the message for pq_last_error() on this thread and returns `st`.
+pq_status fail(pq_status st, const char *fmt, ...);
+// Clears the thread's message (start of every public call).
+void clear_error();
+
+// PQ_OK if the current device is compute capability 10.3, else PQ_ERR_ARCH /
+// PQ_ERR_CUDA with a message.  Also returns the SM count of that device.
+pq_status check_device(int *sm_count);
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Validation shared by the GEMM entry points.
+pq_status check_gemm_args(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                          int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                          int ldy);
+
+// Kernel launchers (one per translation unit).
+pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
+                              const void *cs, void *a, float *asg, float *rs, void *stream);
+pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream);
+pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, int M, int N,
+                             int K, int P, int pb1, int pb2, const void *w, const void *sz,
+                             void *y, int ldy, unsigned int *dev_status, void *stream,
+                             int sm_count);
+pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                         int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                         int ldy, unsigned int *dev_status, void *stream, int sm_count);
+
+constexpr int kSkinnyMaxM = 16;   // largest M the CUDA-core decode kernel accepts
+
+}  // namespace pq
