@@ -153,51 +153,81 @@ class Workload:
         self.gemm_bytes, self.pro_bytes, self.flops = gemm_bytes, pro_bytes, flops
         self.gemm_kernel = "skinny" if M_of(c) <= pq.pq_gemm_skinny_max_m() else "tcgen05"
 
-    def step(self, pq, i, stream):
+    def prologue(self, pq, i, stream):
         j = i % self.copies
         pq.pq_rotate_quant(self.x[j], self.rec[j], self.cs[j], a=self.a[j], asg=self.asg[j],
                            rs=self.rs[j], stream=stream)
+
+    def gemm(self, pq, i, stream):
+        j = i % self.copies
         pq.pq_gemm(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1, self.pb2,
                    y=self.y[j], stream=stream)
+
+    def step(self, pq, i, stream):
+        self.prologue(pq, i, stream)
+        self.gemm(pq, i, stream)
 
 
 def M_of(c):
     return c["M"]
 
 
+def _capture(torch, fn):
+    """A CUDA graph of fn() (the library launches on torch's current stream,
+    which is the capture stream inside the context)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=None):
-    """Returns dict with ms per step (total), per-kernel mean durations (ms)."""
-    for i in range(warmup):
-        wl.step(pq, i, stream)
+    """Times exactly `steps` steps replayed from CUDA graphs (one graph holds one
+    step per input copy, so consecutive steps never share inputs), then the two
+    kernels on their own from graphs of the same shape.  Returns ms totals."""
+    for i in range(max(warmup, wl.copies)):
+        wl.step(pq, i, None)
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * steps + 2)]
+    C = wl.copies
+    g_full = _capture(torch, lambda: [wl.step(pq, j, None) for j in range(C)])
+    rem = steps % C
+    g_rem = _capture(torch, lambda: [wl.step(pq, j, None) for j in range(rem)]) if rem else None
+    g_pro = _capture(torch, lambda: [wl.prologue(pq, j, None) for j in range(C)])
+    g_gem = _capture(torch, lambda: [wl.gemm(pq, j, None) for j in range(C)])
+    for _ in range(2):
+        g_full.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if barrier:
         barrier()
     torch.cuda.synchronize()
     ctx = sampler if sampler is not None else _Null()
     with ctx:
         t0 = time.perf_counter()
-        ev[0].record(stream)
-        for i in range(steps):
-            j = i % wl.copies
-            e0, e1, e2 = ev[1 + 3 * i], ev[2 + 3 * i], ev[3 + 3 * i]
-            e0.record(stream)
-            pq.pq_rotate_quant(wl.x[j], wl.rec[j], wl.cs[j], a=wl.a[j], asg=wl.asg[j], rs=wl.rs[j],
-                               stream=stream)
-            e1.record(stream)
-            pq.pq_gemm(wl.a[j], wl.asg[j], wl.rs[j], wl.w[j], wl.sz[j], wl.pb1, wl.pb2, y=wl.y[j],
-                       stream=stream)
-            e2.record(stream)
-        ev[-1].record(stream)
+        e0.record(stream)
+        for _ in range(steps // C):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     if barrier:
         barrier()
-    total_ms = ev[0].elapsed_time(ev[-1])
-    pro = [ev[1 + 3 * i].elapsed_time(ev[2 + 3 * i]) for i in range(steps)]
-    gem = [ev[2 + 3 * i].elapsed_time(ev[3 + 3 * i]) for i in range(steps)]
-    return dict(total_ms=total_ms, wall_s=wall, pro_ms=float(np.mean(pro)), gemm_ms=float(np.mean(gem)),
-                pro_med=float(np.median(pro)), gemm_med=float(np.median(gem)))
+    total_ms = e0.elapsed_time(e1)
+    reps = max(1, steps // C // 2)
+    per = {}
+    for key, g in (("pro", g_pro), ("gemm", g_gem)):
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per[key] = a.elapsed_time(b) / (reps * C)
+    return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"])
 
 
 class _Null:
@@ -330,12 +360,18 @@ def main():
     ap.add_argument("--extra-steps", type=int, default=50)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="decode:1",
+                    help="headline workload NAME[:M], NAME in %s" % ", ".join(pqgen.CONFIGS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     rank, ws, dist = dist_init()
-    name, M = HEADLINE
+    name, _, m_txt = args.workload.partition(":")
+    M = int(m_txt) if m_txt else None
+    if name not in pqgen.CONFIGS:
+        raise SystemExit("unknown workload %r" % name)
 
     if args.impl == "reference":
         if rank != 0:
@@ -381,12 +417,15 @@ def main():
         total_ms = float(t.item())
     step_us = total_ms * 1e3 / args.steps
     value = step_us / ws            # whole-job time per step: ws replicas each ran `steps` steps
-    e2e_ms, h2d, d2h = e2e_workload(pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, dev)
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else e2e_workload(
+        pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, dev)
     head = summarize(wl, dict(r, total_ms=total_ms), args.steps, peaks)
 
     extra = []
     if not args.no_extra:
         for en, em in EXTRA:
+            if (en, em) == (name, M):
+                continue
             w2 = Workload(pq, torch, en, em, dev)
             r2 = time_workload(pq, torch, w2, args.extra_steps, args.warmup, stream, barrier)
             extra.append(summarize(w2, r2, args.extra_steps, peaks))
@@ -407,8 +446,10 @@ def main():
                    "l2": "%d rotating input copies (> 2x L2)" % wl.copies},
         "prologue_us": head["prologue_us"], "gemm_us": head["gemm_us"],
         "roofline": head["roofline"],
-        "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_ms is None else {
+            "value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "how": "public API per step: pinned H2D of x, "
+            "pq_rotate_quant + pq_gemm, D2H of y, host-driven launches"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "workloads": extra,

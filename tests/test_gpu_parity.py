@@ -8,7 +8,8 @@
   reports 1.65-1.71e-3 for its kernels), plus an elementwise bound, on full
   small problems and on sampled outputs at the full workload sizes;
 * metamorphic cases: merged P=3 == three sliced launches (bit-identical),
-  all-eight codes with zero point 8 give exactly 0, rows are independent,
+  all-eight codes with zero point 8 give 0 to within fp32 rounding, rows are
+  independent,
   rows past M and columns past N are never written.
 
 Source: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", "Gates passed"
@@ -205,7 +206,7 @@ GEMM_SMALL = [  # M, K, N, P, pb
     (4, 256, 128, 1, None), (1, 1024, 256, 1, None), (3, 640, 384, 1, None),
     (16, 1152, 512, 1, None), (7, 512, 384, 3, (128, 256)), (12, 384, 512, 2, (256, 512)),
     (129, 512, 256, 1, None), (200, 896, 384, 3, (128, 256)), (256, 1024, 512, 1, None),
-    (33, 8704 // 8, 256, 1, None),
+    (33, 1152, 256, 1, None), (18, 8704, 128, 1, None),
 ]
 
 
@@ -242,6 +243,9 @@ def test_gemm_random_codes(pq, orc, subnormal):
 
 
 def test_gemm_zero_point_eight_gives_zero(pq, orc):
+    """All codes 8 with zero point 8: every weight is 0, so y = 0.  The kernels
+    form D' = sum a*c and subtract 8*rs, so the zero is reached to within the
+    fp32 rounding of the two sums: |y| <= 2^-21 * sum_g asg * 8 sc |rs|."""
     M, K, N = 9, 512, 256
     prob = pqgen.make_problem(M, K, N, seed=8)
     eights = np.int32(np.uint32(0x88888888).view(np.int32))
@@ -249,9 +253,14 @@ def test_gemm_zero_point_eight_gives_zero(pq, orc):
     prob["qzeros"] = np.full_like(prob.qzeros, eights)
     L = Problem(pq, orc, prob)
     a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    sc = prob.scales.view(np.float16).astype(np.float64)                       # [G, N]
+    mag = np.einsum("gm,gn->mn", np.abs(asg[0].cpu().numpy().astype(np.float64) *
+                                        rs[0].cpu().numpy()), 8 * sc)
     for name, fn in gemm_paths(pq, M):
         y = run_gemm(fn, a, asg, rs, L, N, N, M, N)
-        assert np.all(y == 0), name
+        assert np.all(np.abs(y) <= 2.0 ** -21 * mag), name
+        # and a non-trivial weight moves it far away from zero
+        assert float(np.max(mag)) > 1e-3
 
 
 def test_gemm_merged_equals_sliced(pq, orc):
@@ -300,7 +309,7 @@ def _samples(M, N, pb1, pb2, count, seed):
     r = np.random.default_rng(seed)
     ms = list(r.integers(0, M, count)) + [0, M - 1] * 4
     ns = list(r.integers(0, N, count)) + [0, N - 1, pb1 - 1, min(pb1, N - 1), pb2 - 1,
-                                          min(pb2, N - 1), 127, 128]
+                                          min(pb2, N - 1), 127, min(128, N - 1)]
     return np.array(ms[:len(ns)]), np.array(ns)
 
 

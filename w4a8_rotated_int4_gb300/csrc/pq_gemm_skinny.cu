@@ -220,7 +220,8 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                 const float zs8 = zs + 8.0f * sc;               // exact in fp32
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    const float sum = (acc[m][0] + acc[m][1]) + 16.0f * (acc[m][2] + acc[m][3]);
+                    // the high-nibble halves already carry the factor 16: scale them back by 1/16
+                    const float sum = (acc[m][0] + acc[m][1]) + 0.0625f * (acc[m][2] + acc[m][3]);
                     const float c1 = asg_r[m] * sc24;
                     const float c0 = asg_r[m] * (zs8 * (rs_r[m] * 0.25f));
                     float yl = kvalid ? fmaf(c1, sum, -c0) : 0.0f;

@@ -190,10 +190,18 @@ __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsig
 // the low table, c >= 8 picks byte c-8 of the high table; PRMT's sign mode
 // (selector bit 3) turns the other table's byte into 0x00 since every entry
 // has a clear sign bit.
+// (PTX prmt in its default mode honours the sign-replicate bit of each
+// selector nibble; the __byte_perm intrinsic only uses the low three bits.)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t expand4(uint32_t sel, uint32_t sel_x8) {
     constexpr uint32_t kLo0 = 0x44403800u, kLo1 = 0x4E4C4A48u;   // e4m3(0..7)
     constexpr uint32_t kHi0 = 0x53525150u, kHi1 = 0x57565554u;   // e4m3(8..15)
-    return __byte_perm(kLo0, kLo1, sel) | __byte_perm(kHi0, kHi1, sel_x8);
+    return prmt(kLo0, kLo1, sel) | prmt(kHi0, kHi1, sel_x8);
 }
 
 __device__ __forceinline__ uint4 expand16(uint2 pk) {
