@@ -102,8 +102,12 @@ pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_t *sz_bytes
  *        uint16 f16(cos theta), uint16 f16(sin theta); cos/sin are evaluated in
  *        double precision (host libm) and rounded once to f16 (nearest, ties
  *        to even).
- *   sz   [G][N][2] f16 ([D1]): (sc, f16(sc * (zp - 8))); the product is taken
- *        in fp32 (exact) and rounded once to f16.
+ *   sz   the SZ table ([D1]): for column n and group g the f16 pair
+ *        (sc, f16(sc * (zp - 8))) -- the product is taken in fp32 (exact) and
+ *        rounded once to f16 -- stored as one 4-byte word (scale in the low
+ *        half) at word index ((n / 8) * G + g) * 8 + n % 8, i.e. laid out
+ *        [N/8][G][8]: the words of one column octet over all groups are
+ *        contiguous (one 32-byte sector per group and octet).
  *   w    [N][K/2] bytes: byte k/2 of row n holds code c[k][n] in its low nibble
  *        (even k) and c[k+1][n] in its high nibble (raw codes 0..15).
  *
@@ -151,7 +155,7 @@ pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P, const voi
  *   p(n)   = (n >= pb1) + (n >= pb2)
  *   D      = sum_{k in g} dec(a[p(n)][m][k]) * (c[k][n] - 8)
  *   y[m][n] = bf16( sum_g asg[p][g][m] * (sc[g][n] * D - zs[g][n] * rs[p][g][m]) )
- * with (sc, zs) the f16 pair of sz[g][n].  Accumulation is fp32 (tensor-core
+ * with (sc, zs) the f16 pair of column n, group g in the SZ table.  Accumulation is fp32 (tensor-core
  * fp32 accumulation within a 128-k group on the tensor-core path); the result
  * is within the bf16 output floor of the fp64 value (norm-wise relative error
  * <= 2e-3 is the gate).

@@ -154,6 +154,13 @@ def sz_table(scales: np.ndarray, qzeros: np.ndarray) -> np.ndarray:
     return out
 
 
+def sz_kernel_layout(sz: np.ndarray) -> np.ndarray:
+    """The SZ table [G, N, 2] rearranged into the library's storage order
+    [N/8, G, 8, 2] (one contiguous 32-byte run per column octet and group)."""
+    G, N, _ = sz.shape
+    return np.ascontiguousarray(sz.reshape(G, N // 8, 8, 2).transpose(1, 0, 2, 3))
+
+
 def repack(qweight: np.ndarray) -> np.ndarray:
     """Kernel weight bytes [N, K/2]."""
     qweight = _c(qweight, np.int32)
@@ -250,8 +257,9 @@ def linear_rotw_f64(x, cs, pairs, theta, W, pb1, pb2) -> np.ndarray:
 # ---------------------------------------------------------------- whole layer
 def pack(prob) -> dict:
     """Oracle's own load-time tables for a generated problem."""
+    sz = sz_table(prob["scales"], prob["qzeros"])
     return dict(rec=records(prob["pairs"], prob["theta"]),
-                sz=sz_table(prob["scales"], prob["qzeros"]),
+                sz=sz, sz_kernel=sz_kernel_layout(sz),
                 w=repack(prob["qweight"]),
                 codes=unpack_awq(prob["qweight"], prob["N"]),
                 zp=unpack_awq(prob["qzeros"], prob["N"]))

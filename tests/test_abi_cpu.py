@@ -47,7 +47,7 @@ def test_pack_byte_equal_to_oracle(L, orc, shape):
     rec, sz, w = pq.pq_pack(prob.qweight, prob.qzeros, prob.scales, prob.pairs, prob.theta)
     t = orc.pack(prob)
     assert np.array_equal(rec, t["rec"])
-    assert np.array_equal(sz, t["sz"])
+    assert np.array_equal(sz, t["sz_kernel"])
     assert np.array_equal(w, t["w"])
 
 
@@ -62,7 +62,7 @@ def test_pack_special_angles_and_scales(L, orc):
     sc.reshape(-1)[:6] = np.array([0x0001, 0x03FF, 0x0400, 0x7BFF, 0x3C00, 0x0000], dtype=np.uint16)
     rec, szt, w = pq.pq_pack(prob.qweight, prob.qzeros, sc, prob.pairs, th)
     assert np.array_equal(rec, orc.records(prob.pairs, th))
-    assert np.array_equal(szt, orc.sz_table(sc, prob.qzeros))
+    assert np.array_equal(szt, orc.sz_kernel_layout(orc.sz_table(sc, prob.qzeros)))
 
 
 def test_pack_sizes_and_errors(L):

@@ -54,7 +54,7 @@ class Problem:
         self.t = orc.pack(prob)
         if check_pack:
             assert np.array_equal(self.rec, self.t["rec"])
-            assert np.array_equal(self.sz, self.t["sz"])
+            assert np.array_equal(self.sz, self.t["sz_kernel"])
             assert np.array_equal(self.w, self.t["w"])
         self.rec_d = torch.from_numpy(self.rec).cuda()
         self.sz_d = dev_u16(self.sz)
@@ -106,6 +106,9 @@ PROLOGUE_CASES = [
     ("down", dict()),
     ("qkv", dict()),
     ("qkv", dict(M=33)),
+    ("qkv", dict(M=2)),                   # three partitions in the decode-band kernel
+    ("decode", dict(M=5)),
+    ("prefill", dict(M=17)),              # first size of the many-token kernel
 ]
 
 
@@ -276,7 +279,7 @@ def test_gemm_merged_equals_sliced(pq, orc):
             for p, (lo, hi) in enumerate([(0, 256), (256, 384), (384, 512)]):
                 Ls = type("S", (), {})()
                 Ls.w_d = L.w_d[lo:hi].contiguous()
-                Ls.sz_d = L.sz_d[:, lo:hi].contiguous()
+                Ls.sz_d = L.sz_d[lo // 8:hi // 8].contiguous()
                 ys = run_gemm(fn, aa[p:p + 1].contiguous(), ss[p:p + 1].contiguous(),
                               rr[p:p + 1].contiguous(), Ls, hi - lo, hi - lo, Mx, hi - lo)
                 assert np.array_equal(y[:, lo:hi], ys), (name, Mx, p)

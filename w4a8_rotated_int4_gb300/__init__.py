@@ -109,7 +109,8 @@ def pq_pack_sizes(K: int, N: int, P: int):
 def pq_pack(qweight: np.ndarray, qzeros: np.ndarray, scales: np.ndarray, pairs: np.ndarray,
             theta: np.ndarray):
     """Host packer.  Inputs in checkpoint layout (f16 tensors as uint16 bit
-    patterns); returns (rec uint8 [P,8,G,64,8], sz uint16 [G,N,2], w uint8 [N,K/2])."""
+    patterns); returns (rec uint8 [P,8,G,64,8], sz uint16 [N/8,G,8,2],
+    w uint8 [N,K/2])."""
     qweight = np.ascontiguousarray(qweight, dtype=np.int32)
     qzeros = np.ascontiguousarray(qzeros, dtype=np.int32)
     scales = np.ascontiguousarray(scales, dtype=np.uint16)
@@ -123,7 +124,7 @@ def pq_pack(qweight: np.ndarray, qzeros: np.ndarray, scales: np.ndarray, pairs: 
     G = K // 128
     nr, ns, nw = pq_pack_sizes(K, N, P)
     rec = np.empty((P, 8, G, 64, 8), dtype=np.uint8)
-    sz = np.empty((G, N, 2), dtype=np.uint16)
+    sz = np.empty((N // 8, G, 8, 2), dtype=np.uint16)
     w = np.empty((N, K // 2), dtype=np.uint8)
     assert rec.nbytes == nr and sz.nbytes == ns and w.nbytes == nw
     _check(lib().pq_pack(K, N, P, _np_ptr(qweight), _np_ptr(qzeros), _np_ptr(scales),

@@ -221,18 +221,19 @@ extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const 
                 o[7] = (uint8_t)(s >> 8);
             }
 
-    // SZ table: (sc, f16(sc * (zp - 8))), the product exact in fp32
-    uint16_t *so = static_cast<uint16_t *>(sz);
+    // SZ table: (sc, f16(sc * (zp - 8))), the product exact in fp32, one word
+    // per (column, group) at [n/8][g][n%8]
+    uint32_t *so = static_cast<uint32_t *>(sz);
     for (int g = 0; g < G; ++g)
         for (int w8 = 0; w8 < W8; ++w8) {
             const uint32_t zw = (uint32_t)qzeros[(size_t)g * W8 + w8];
             for (int s = 0; s < 8; ++s) {
-                const int n = 8 * w8 + kAwqOrder[s];
+                const int j = kAwqOrder[s];
+                const int n = 8 * w8 + j;
                 const int zp = (int)((zw >> (4 * s)) & 15u);
                 const uint16_t sc = scales[(size_t)g * N + n];
                 const float prod = (float)half_value(sc) * (float)(zp - 8);
-                so[((size_t)g * N + n) * 2 + 0] = sc;
-                so[((size_t)g * N + n) * 2 + 1] = half_bits_rne((double)prod);
+                so[((size_t)w8 * G + g) * 8 + j] = (uint32_t)sc | ((uint32_t)half_bits_rne((double)prod) << 16);
             }
         }
 

@@ -13,7 +13,7 @@
 // 8 kw + l/4) and keeps that slice of the MT activation rows in registers for
 // the whole launch (as f16 pairs; e4m3 converts to f16 exactly).  A producer
 // warp streams each octet's weight rows (8 x K/2 contiguous bytes) and its SZ
-// words (G x 32 bytes) into a 4-stage shared-memory ring with bulk copies
+// words (G x 32 contiguous bytes) into a 2..4-stage shared-memory ring with bulk copies
 // (cp.async.bulk + mbarrier transaction counts), so the weight stream is
 // independent of register pressure.
 //
@@ -26,8 +26,10 @@
 // D' = sum a * c = D + 8 * rs exactly up to fp32 addition, and the fold uses
 // sc * D - zscale * rs = sc * D' - (zscale + 8 sc) * rs, where zscale + 8 sc
 // is exact in fp32.  Each of the four lanes of a group adds a quarter of the
-// zero-point term; five xor-shuffles reduce a warp, shared memory reduces the
-// k-warps in a fixed order (deterministic), and the bf16 result is stored once.
+// zero-point term.  The lanes' partials of 8 (or 4) columns are then summed
+// over the warp by one butterfly that hands each column to a subset of lanes
+// (7 exchanges per 8 columns), shared memory reduces the k-warps in a fixed
+// order (deterministic), and the bf16 result is stored once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -39,16 +41,15 @@
 namespace pq {
 namespace {
 
-constexpr int kMaxStages = 4;
 constexpr int kMaxK = 16384;          // 16 compute warps + producer; larger K uses the tcgen05 path
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 220 * 1024;    // per SM, over all resident CTAs
 
 struct SkinnyParams {
     const uint8_t *a;
     const float *asg;
     const float *rs;
     const uint8_t *w;
-    const uint32_t *sz;     // [G][N] words: f16 scale | f16 zscale << 16
+    const uint32_t *sz;     // [N/8][G][8] words: f16 scale | f16 zscale << 16
     __nv_bfloat16 *y;
     unsigned int *status;
     int M, N, K, G, pb1, pb2, ldy;
@@ -84,8 +85,48 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
     return f;
 }
 
+// Sum a lane's partials of NC columns (NC = 8 or 4) over the 32 lanes of the
+// warp with one butterfly that splits the columns among the lanes on the way
+// down: NC - 1 exchanges instead of 5 * NC.  On return the lanes with
+// (lane & (32/NC - 1)) == 0 hold the total of column lane / (32/NC).
+template <int NC>
+__device__ __forceinline__ float transpose_reduce(const float (&v)[NC], int lane) {
+    float w[NC / 2];
+    const bool b4 = (lane & 16) != 0;
+#pragma unroll
+    for (int i = 0; i < NC / 2; ++i) {
+        const float send = b4 ? v[i] : v[i + NC / 2];
+        const float keep = b4 ? v[i + NC / 2] : v[i];
+        w[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    const bool b3 = (lane & 8) != 0;
+    float t;
+    if constexpr (NC == 8) {
+        float u[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = b3 ? w[i] : w[i + 2];
+            const float keep = b3 ? w[i + 2] : w[i];
+            u[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+        }
+        const bool b2 = (lane & 4) != 0;
+        const float send = b2 ? u[0] : u[1];
+        const float keep = b2 ? u[1] : u[0];
+        t = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+    } else {
+        const float send = b3 ? w[0] : w[1];
+        const float keep = b3 ? w[1] : w[0];
+        t = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+        t += __shfl_xor_sync(0xFFFFFFFFu, t, 4);
+    }
+    t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
+    t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
+    return t;
+}
+
 template <int MT>
 __global__ void skinny_kernel(const SkinnyParams prm) {
+    constexpr int NC = MT <= 2 ? 8 : 4;        // columns reduced together
     extern __shared__ __align__(128) uint8_t smem[];
     const int nkw = prm.nkw, S = prm.stages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,8 +135,9 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + S);
     float *ypart = reinterpret_cast<float *>(empty + S + 2);
 
-    const int oct0 = blockIdx.x * prm.oct_per_cta;
-    const int noct = min(prm.oct_per_cta, prm.n_oct - oct0);
+    // balanced contiguous octet range of this CTA
+    const int oct0 = (int)(((long long)blockIdx.x * prm.n_oct) / gridDim.x);
+    const int noct = (int)(((long long)(blockIdx.x + 1) * prm.n_oct) / gridDim.x) - oct0;
     const int ncol = prm.oct_per_cta * 8;
     const int m0 = blockIdx.y * MT;
     const int K = prm.K, G = prm.G, M = prm.M;
@@ -113,32 +155,29 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
     if (warp == nkw) {
         // ---------------- producer warp ----------------
         int issued = 0;
-        for (int i = 0; i < noct; ++i) {
-            const int s = i % S, use = i / S;
-            if (*abort_flag) break;
-            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-                if (lane == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < noct; ++i) {
+                const int s = i % S, use = i / S;
+                if (*abort_flag) break;
+                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
                     if (prm.status) atomicOr(prm.status, kStatusWaitEmpty);
                     *abort_flag = 1;
+                    break;
                 }
-                break;
+                uint8_t *st = smem + (size_t)s * prm.stage_bytes;
+                const int o = oct0 + i;
+                mbar_arrive_expect_tx(&full[s], prm.stage_bytes);
+                bulk_g2s(st, prm.w + (size_t)o * 8 * (K / 2), prm.w_bytes, &full[s]);
+                bulk_g2s(st + prm.w_bytes, prm.sz + (size_t)o * G * 8, 32u * (uint32_t)G, &full[s]);
+                issued = i + 1;
             }
-            uint8_t *st = smem + (size_t)s * prm.stage_bytes;
-            const int n0 = (oct0 + i) * 8;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], prm.stage_bytes);
-            __syncwarp();
-            if (lane == 0) bulk_g2s(st, prm.w + (size_t)n0 * (K / 2), prm.w_bytes, &full[s]);
-            for (int g = lane; g < G; g += 32)
-                bulk_g2s(st + prm.w_bytes + 32 * g, prm.sz + (size_t)g * prm.N + n0, 32, &full[s]);
-            issued = i + 1;
-        }
-        __syncwarp();
-        // on abort: let every copy already issued land before shared memory is released
-        if (*abort_flag && lane == 0) {
-            for (int s = 0; s < S && s < issued; ++s) {
-                const int last_use = (issued - 1 - s) / S;
-                if (!mbar_wait(&full[s], last_use & 1) && prm.status)
-                    atomicOr(prm.status, kStatusDrain);
+            // on abort: let every copy already issued land before shared memory is released
+            if (*abort_flag) {
+                for (int s = 0; s < S && s < issued; ++s) {
+                    const int last_use = (issued - 1 - s) / S;
+                    if (!mbar_wait(&full[s], last_use & 1) && prm.status)
+                        atomicOr(prm.status, kStatusDrain);
+                }
             }
         }
     } else {
@@ -148,7 +187,7 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
         const bool kvalid = k0 < K;
         const int g = kvalid ? (k0 >> 7) : 0;
         uint32_t A[MT][16];
-        float asg_r[MT], rs_r[MT];
+        float asg_r[MT], ar4_r[MT];        // asg and asg * rs / 4 of this lane's group
         int cur_p = -1;
         for (int i = 0; i < noct; ++i) {
             const int s = i % S, use = i / S;
@@ -161,7 +200,7 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                     const int row = m0 + m;
                     uint32_t u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                     asg_r[m] = 0.0f;
-                    rs_r[m] = 0.0f;
+                    ar4_r[m] = 0.0f;
                     if (kvalid && row < M) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(
                             prm.a + ((size_t)p * M + row) * K + k0);
@@ -169,7 +208,7 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                         u[0] = v0.x; u[1] = v0.y; u[2] = v0.z; u[3] = v0.w;
                         u[4] = v1.x; u[5] = v1.y; u[6] = v1.z; u[7] = v1.w;
                         asg_r[m] = __ldg(prm.asg + ((size_t)p * G + g) * M + row);
-                        rs_r[m] = __ldg(prm.rs + ((size_t)p * G + g) * M + row);
+                        ar4_r[m] = asg_r[m] * (__ldg(prm.rs + ((size_t)p * G + g) * M + row) * 0.25f);
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -192,49 +231,58 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                 break;
             }
             const uint8_t *st = smem + (size_t)s * prm.stage_bytes;
-            const uint32_t *szs = reinterpret_cast<const uint32_t *>(st + prm.w_bytes) + 8 * g;
-#pragma unroll 2
-            for (int j = 0; j < 8; ++j) {
-                uint4 wv = make_uint4(0, 0, 0, 0);
-                if (kvalid) wv = *reinterpret_cast<const uint4 *>(st + (size_t)j * (K / 2) + (k0 >> 1));
-                float acc[MT][4];
+            const uint4 *szv = reinterpret_cast<const uint4 *>(st + prm.w_bytes) + 2 * g;
+            const uint4 sz_lo = szv[0], sz_hi = szv[1];
+            const uint32_t szw[8] = {sz_lo.x, sz_lo.y, sz_lo.z, sz_lo.w,
+                                     sz_hi.x, sz_hi.y, sz_hi.z, sz_hi.w};
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
-                const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+            for (int jb = 0; jb < 8; jb += NC) {
+                float yl[MT][NC];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t x = wq[q], x8 = x >> 8;
-                    const uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
-                    const uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
+                for (int jj = 0; jj < NC; ++jj) {
+                    const int j = jb + jj;
+                    uint4 wv = make_uint4(0, 0, 0, 0);
+                    if (kvalid)
+                        wv = *reinterpret_cast<const uint4 *>(st + (size_t)j * (K / 2) + (k0 >> 1));
+                    float acc[MT][4];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+                    const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t x = wq[q], x8 = x >> 8;
+                        const uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
+                        const uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 0], lo);
+                            fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 1], hi);
+                            fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 2], lo2);
+                            fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 3], hi2);
+                        }
+                    }
+                    const float sc = half_lo(szw[j]), zs = half_hi(szw[j]);
+                    const float sc24 = sc * 16777216.0f;            // 2^24: undo the subnormal scaling
+                    const float zs8 = zs + 8.0f * sc;               // exact in fp32
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
-                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 0], lo);
-                        fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 1], hi);
-                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 2], lo2);
-                        fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 3], hi2);
+                        // the high-nibble halves already carry the factor 16: scale them back by 1/16
+                        const float sum = (acc[m][0] + acc[m][1]) + 0.0625f * (acc[m][2] + acc[m][3]);
+                        yl[m][jj] = kvalid ? fmaf(asg_r[m] * sc24, sum, -(ar4_r[m] * zs8)) : 0.0f;
                     }
                 }
-                const uint32_t szw = szs[j];
-                const float sc = half_lo(szw), zs = half_hi(szw);
-                const float sc24 = sc * 16777216.0f;            // 2^24: undo the subnormal scaling
-                const float zs8 = zs + 8.0f * sc;               // exact in fp32
+                if (jb + NC == 8) {            // every read of this stage has been issued and used
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    // the high-nibble halves already carry the factor 16: scale them back by 1/16
-                    const float sum = (acc[m][0] + acc[m][1]) + 0.0625f * (acc[m][2] + acc[m][3]);
-                    const float c1 = asg_r[m] * sc24;
-                    const float c0 = asg_r[m] * (zs8 * (rs_r[m] * 0.25f));
-                    float yl = kvalid ? fmaf(c1, sum, -c0) : 0.0f;
-                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 16);
-                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 8);
-                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 4);
-                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 2);
-                    yl += __shfl_xor_sync(0xFFFFFFFFu, yl, 1);
-                    if (lane == 0) ypart[(kw * MT + m) * ncol + 8 * i + j] = yl;
+                    const float t = transpose_reduce<NC>(yl[m], lane);
+                    constexpr int kLanesPerCol = 32 / NC;
+                    if ((lane & (kLanesPerCol - 1)) == 0)
+                        ypart[(kw * MT + m) * ncol + 8 * i + jb + lane / kLanesPerCol] = t;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
         }
     }
     __syncthreads();
@@ -268,27 +316,41 @@ template <int MT>
 pq_status launch_mt(SkinnyParams prm, int sm_count, cudaStream_t stream) {
     const int threads = 32 * (prm.nkw + 1);
     const int mtiles = (prm.M + MT - 1) / MT;
-    // column octets per CTA: about one CTA per SM per M-tile, bounded by shared memory
-    int ctas = sm_count > 0 ? sm_count : 1;
-    if (ctas > prm.n_oct) ctas = prm.n_oct;
-    int opc = (prm.n_oct + ctas - 1) / ctas;
-    auto smem_for = [&](int o) {
-        return (size_t)prm.stages * prm.stage_bytes + 16 * prm.stages + 16 +
-               (size_t)prm.nkw * MT * o * 8 * 4;
+    const int sms = sm_count > 0 ? sm_count : 1;
+    // Up to three CTAs per SM (the more compute warps per SM, the more load
+    // latency is hidden), each with its own 2..4-stage ring; shared memory per
+    // SM is kept under kSmemBudget.  CTAs per M-tile: a whole multiple of the
+    // SM count when there are enough octets, each with a balanced octet range.
+    int per_sm = 3;
+    auto smem_for = [&](int stages, int opc) {
+        return (size_t)stages * prm.stage_bytes + 16 * (size_t)stages + 16 +
+               (size_t)prm.nkw * MT * opc * 8 * 4;
     };
-    while (opc > 1 && smem_for(opc) > (size_t)kSmemBudget) opc = (opc + 1) / 2;
-    if (smem_for(opc) > (size_t)kSmemBudget)
-        return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d needs too much shared memory", prm.K);
-    prm.oct_per_cta = opc;
-    const dim3 grid((prm.n_oct + opc - 1) / opc, mtiles);
-    const size_t smem = smem_for(opc);
-    cudaError_t e = cudaFuncSetAttribute(skinny_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    skinny_kernel<MT><<<grid, threads, smem, stream>>>(prm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
-    return PQ_OK;
+    for (;;) {
+        int ctas = sms * per_sm / mtiles;
+        if (ctas < 1) ctas = 1;
+        if (ctas > prm.n_oct) ctas = prm.n_oct;
+        const int opc = (prm.n_oct + ctas - 1) / ctas;
+        int stages = 4;
+        while (stages > 2 && smem_for(stages, opc) * per_sm > (size_t)kSmemBudget) --stages;
+        if (smem_for(stages, opc) * per_sm <= (size_t)kSmemBudget || per_sm == 1) {
+            if (smem_for(stages, opc) > (size_t)kSmemBudget)
+                return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d needs too much shared memory", prm.K);
+            prm.stages = stages;
+            prm.oct_per_cta = opc;
+            const dim3 grid(ctas, mtiles);
+            const size_t smem = smem_for(stages, opc);
+            cudaError_t e = cudaFuncSetAttribute(skinny_kernel<MT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess)
+                return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            skinny_kernel<MT><<<grid, threads, smem, stream>>>(prm);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
+            return PQ_OK;
+        }
+        --per_sm;
+    }
 }
 
 }  // namespace
@@ -317,8 +379,6 @@ pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, i
     prm.nkw = (K + 1023) / 1024;
     prm.w_bytes = (uint32_t)(8 * (K / 2));
     prm.stage_bytes = prm.w_bytes + 32u * (uint32_t)prm.G;
-    prm.stages = kMaxStages;
-    while (prm.stages > 2 && (size_t)prm.stages * prm.stage_bytes > 160 * 1024) --prm.stages;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // rows per M-tile: the smallest power of two >= M (at most 8) whose
     // instantiation fits the register file with this many k-warps

@@ -12,7 +12,8 @@
 // 128-k group kb (a "slab"):
 //   TMA warp     loads A[p][m0:m0+128][128kb:+128] (e4m3, 128B-swizzled,
 //                zero-filled past M), the packed weight tile w[n0:n0+128]
-//                [64kb:+64] and the slab's 128 SZ words into stage s.
+//                [64kb:+64] and the slab's 128 SZ words (16 octets x 8 words
+//                of the [N/8][G][8] table) into stage s.
 //   expand warps turn each nibble c into the e4m3 code of c (0..15 are exact
 //                in e4m3) in the canonical K-major SWIZZLE_128B layout the MMA
 //                reads, and convert the SZ words to fp32 (sc, zscale + 8 sc).
@@ -221,7 +222,7 @@ __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushor
 // ---------------------------------------------------------------- kernel
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-          const TcParams prm) {
+          const __grid_constant__ CUtensorMap tmS, const TcParams prm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Stage *stg = reinterpret_cast<Stage *>(base);
@@ -263,6 +264,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (lane == 0) {
             prefetch_map(&tmA);
             prefetch_map(&tmB);
+            prefetch_map(&tmS);
             int issued = 0;
             for (int kb = 0; kb < G; ++kb) {
                 const int s = kb % kStages, use = kb / kStages;
@@ -273,7 +275,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 mbar_arrive_expect_tx(&ctl->full_tma[s], kTxBytes);
                 tma_load_3d(stg[s].a, &tmA, kb * BK, m0, p, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[s]);
-                bulk_g2s(stg[s].sz, prm.sz + (size_t)kb * N + n0, kSzBytes, &ctl->full_tma[s]);
+                tma_load_2d(stg[s].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[s]);
                 issued = kb + 1;
             }
             if (*abort_flag) {   // let issued copies land before shared memory is released
@@ -442,7 +444,7 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     (void)sm_count;
     auto enc = encode_fn();
     if (!enc) return fail(PQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmS;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M, (cuuint64_t)P};
         const cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)K * (cuuint64_t)M};
@@ -465,6 +467,18 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(PQ_ERR_CUDA, "tensor map for w: CUresult %d", (int)r);
     }
+    {
+        // SZ table [N/8][G][8] words: box = the 8 words of group kb for 16 octets
+        const cuuint64_t dims[2] = {(cuuint64_t)(8 * (K / 128)), (cuuint64_t)(N / 8)};
+        const cuuint64_t strides[1] = {(cuuint64_t)(32 * (K / 128))};
+        const cuuint32_t box[2] = {8, BN / 8};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUresult r = enc(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(sz), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PQ_ERR_CUDA, "tensor map for sz: CUresult %d", (int)r);
+    }
     TcParams prm{};
     prm.asg = asg;
     prm.rs = rs;
@@ -482,7 +496,7 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     cudaError_t e = cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    tc_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tmA, tmB, prm);
+    tc_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tmA, tmB, tmS, prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "tc launch: %s", cudaGetErrorString(e));
     return PQ_OK;

@@ -9,16 +9,21 @@
 // and "2026-09-15: hardware e4m3 convert" (NaN -> 0, -0 -> +0, clamp +-448,
 // then the hardware round-to-nearest-even convert).
 //
-// Layout on the GPU.  One CTA owns a tile of 32 tokens x one 128-group and
-// loops over the partitions.  The tile is held in shared memory as
+// Layout on the GPU (M > 16).  One CTA owns a tile of 32 tokens x one
+// 128-group and loops over the partitions; the records of (p, g) are decoded
+// once into shared-memory offsets and fp32 cos/sin.  The tile is held in shared memory as
 // v[k][token] (fp32), token fastest: in a Givens layer every warp works on one
 // pair (i, j) at a time with lane = token, so the 32 lanes read v[i][0..31]
 // and v[j][0..31] -- consecutive words, free of bank conflicts whatever the
 // pair permutation is.  Each of the 4 warps takes 16 of the 64 disjoint pairs
 // of a layer; the layers are separated by __syncthreads.  Every multiply, add,
 // subtract and divide is a separately rounded IEEE operation (explicit .rn
-// intrinsics; the packed f32x2 forms are .rn as well), so results are
-// bit-identical to an fp32 CPU evaluation in the same order.
+// intrinsics), so results are bit-identical to an fp32 CPU evaluation in the
+// same order.
+//
+// Decode band (M <= 16): 64 threads per token, thread t owns pair t of every
+// layer and keeps its 8 records in registers; one CTA per (token block, group,
+// partition), so at M = 1 the whole prologue is one short dependent chain.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,6 +33,18 @@
 namespace pq {
 namespace {
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float f;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f) : "r"(addr) : "memory");
+    return f;
+}
+__device__ __forceinline__ void sts_f32(uint32_t addr, float f) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(f) : "memory");
+}
+
 constexpr int kTok = 32;              // tokens per CTA (lane = token)
 constexpr int kWarps = 4;             // warp w rotates pairs 16w..16w+15 of each layer
 constexpr int kThreads = kTok * kWarps;
@@ -35,9 +52,9 @@ constexpr int kXsStride = 65;         // words per staged x row (64 + 1 pad)
 constexpr int kCodeStride = 144;      // bytes per staged code row
 
 struct __align__(16) Smem {
-    float v[128][kTok];               // 16 KB
+    float v[128][kTok];               // 16 KB, v[k][token]
     uint32_t xs[kTok][kXsStride];     // x tile, two bf16 per word
-    uint2 rec[8][64];                 // records of (p, g)
+    float4 rec[8][64];                // records of (p, g): byte offsets of v[i], v[j]; cos; sin
     float cs[128];
     uint8_t codes[kTok][kCodeStride];
     float red_max[kWarps][kTok];
@@ -74,6 +91,16 @@ __device__ __forceinline__ int e4m3_times512(uint32_t c) {
     return (c & 0x80) ? -mag : mag;
 }
 
+// One Givens pair, each product and sum rounded on its own:
+//   vi' = fl(fl(c*vi) + fl(s*vj)),  vj' = fl(fl(c*vj) - fl(s*vi))
+__device__ __forceinline__ void givens(float c, float s, float &vi, float &vj) {
+    const float ni = __fadd_rn(__fmul_rn(c, vi), __fmul_rn(s, vj));
+    const float nj = __fsub_rn(__fmul_rn(c, vj), __fmul_rn(s, vi));
+    vi = ni;
+    vj = nj;
+}
+
+// Many tokens: lane = token, warp w rotates pairs 16w..16w+15 of every layer.
 __global__ void __launch_bounds__(kThreads)
 rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P,
                     const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
@@ -81,28 +108,49 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
     __shared__ Smem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m0 = blockIdx.x * kTok, g = blockIdx.y, G = K >> 7;
-
-    // x tile -> shared (bf16 pairs); tokens past M read as zero
-    for (int c = tid; c < kTok * 16; c += kThreads) {
-        const int row = c >> 4, q = c & 15;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (m0 + row < M)
-            val = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + row) * ldx + 128 * g) + q);
-        uint32_t *d = &sm.xs[row][4 * q];
-        d[0] = val.x; d[1] = val.y; d[2] = val.z; d[3] = val.w;
-    }
     const float inv448 = __fdiv_rn(1.0f, 448.0f);
 
+    // x tile: issued together with the first partition's records and scales
+    uint4 xv[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
+        xv[it] = make_uint4(0, 0, 0, 0);
+        if (m0 + row < M)
+            xv[it] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + row) * ldx + 128 * g) + q);
+    }
+
     for (int p = 0; p < P; ++p) {
-        // records of (p, g): 8 layers x 64 x 8 B, and the group's channel scales
-        for (int c = tid; c < 8 * 32; c += kThreads) {
-            const int r = c >> 5, q = c & 31;
-            const uint4 val = __ldg(reinterpret_cast<const uint4 *>(
-                                        rec + ((size_t)(p * 8 + r) * G + g) * 64) + q);
-            sm.rec[r][2 * q] = make_uint2(val.x, val.y);
-            sm.rec[r][2 * q + 1] = make_uint2(val.z, val.w);
+        uint4 rv[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
+            rv[it] = __ldg(reinterpret_cast<const uint4 *>(rec + ((size_t)(p * 8 + r) * G + g) * 64) + q);
         }
-        sm.cs[tid] = half_to_float(__ldg(cs + (size_t)p * K + 128 * g + tid));
+        const uint16_t csv = __ldg(cs + (size_t)p * K + 128 * g + tid);
+        if (p == 0) {
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
+                uint32_t *d = &sm.xs[row][4 * q];
+                d[0] = xv[it].x; d[1] = xv[it].y; d[2] = xv[it].z; d[3] = xv[it].w;
+            }
+        }
+        // decoded records: shared-memory byte offsets of v[i][0], v[j][0]; cos, sin in fp32
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
+            const uint32_t w0[2] = {rv[it].x, rv[it].z}, w1[2] = {rv[it].y, rv[it].w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t i = w0[h] & 0xFF, j = (w0[h] >> 8) & 0xFF;
+                sm.rec[r][2 * q + h] = make_float4(__uint_as_float(i * (uint32_t)(kTok * 4)),
+                                                   __uint_as_float(j * (uint32_t)(kTok * 4)),
+                                                   half_to_float((uint16_t)(w1[h] & 0xFFFF)),
+                                                   half_to_float((uint16_t)(w1[h] >> 16)));
+            }
+        }
+        sm.cs[tid] = half_to_float(csv);
         __syncthreads();
 
         // v[k][t] = x[t][k] * cs[k] (exact: bf16 x f16 fits in 24 bits)
@@ -115,28 +163,27 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
         }
         __syncthreads();
 
-        // eight Givens layers; pairs of one layer are disjoint, so a warp reads
-        // all 32 operands of its 16 pairs before writing any result
+        // eight Givens layers; the pairs of one layer are disjoint, so a warp
+        // reads all 32 operands of its 16 pairs before writing any result
+        const uint32_t vlane = smem_addr(&sm.v[0][lane]);
         for (int r = 0; r < 8; ++r) {
-            float vi[16], vj[16];
-            int ii[16], jj[16];
-            float cc[16], ss[16];
+            float vi[16], vj[16], cc[16], ss[16];
+            uint32_t ai[16], aj[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-                const uint2 rr = sm.rec[r][16 * warp + q];
-                ii[q] = rr.x & 0xFF;
-                jj[q] = (rr.x >> 8) & 0xFF;
-                cc[q] = half_to_float((uint16_t)(rr.y & 0xFFFF));
-                ss[q] = half_to_float((uint16_t)(rr.y >> 16));
-                vi[q] = sm.v[ii[q]][lane];
-                vj[q] = sm.v[jj[q]][lane];
+                const float4 rr = sm.rec[r][16 * warp + q];
+                ai[q] = vlane + __float_as_uint(rr.x);
+                aj[q] = vlane + __float_as_uint(rr.y);
+                cc[q] = rr.z;
+                ss[q] = rr.w;
+                vi[q] = lds_f32(ai[q]);
+                vj[q] = lds_f32(aj[q]);
             }
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-                const float ni = __fadd_rn(__fmul_rn(cc[q], vi[q]), __fmul_rn(ss[q], vj[q]));
-                const float nj = __fsub_rn(__fmul_rn(cc[q], vj[q]), __fmul_rn(ss[q], vi[q]));
-                sm.v[ii[q]][lane] = ni;
-                sm.v[jj[q]][lane] = nj;
+                givens(cc[q], ss[q], vi[q], vj[q]);
+                sts_f32(ai[q], vi[q]);
+                sts_f32(aj[q], vj[q]);
             }
             __syncthreads();
         }
@@ -196,6 +243,66 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
     }
 }
 
+// Few tokens (decode): 64 threads per token, thread t owns pair t of every
+// layer (its 8 records live in registers) and channels 2t, 2t+1 for the
+// quantisation; grid.z runs the partitions side by side.
+template <int T>
+__global__ void __launch_bounds__(64 * T)
+rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
+                          const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
+                          uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
+    __shared__ float v[T][128];
+    __shared__ float red_max[T][2];
+    __shared__ int red_sum[T][2];
+    const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
+    const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
+    const bool live = m < M;
+
+    // every global load first: x pair, channel-scale pair, the 8 records of pair t
+    const uint32_t xw = live ? __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m * ldx + 128 * g) + t) : 0u;
+    const uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs + (size_t)p * K + 128 * g) + t);
+    uint2 r8[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
+
+    v[tt][2 * t] = __fmul_rn(bf16lo(xw), half_to_float((uint16_t)(cw & 0xFFFF)));
+    v[tt][2 * t + 1] = __fmul_rn(bf16hi(xw), half_to_float((uint16_t)(cw >> 16)));
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int i = r8[r].x & 0xFF, j = (r8[r].x >> 8) & 0xFF;
+        float vi = v[tt][i], vj = v[tt][j];
+        givens(half_to_float((uint16_t)(r8[r].y & 0xFFFF)), half_to_float((uint16_t)(r8[r].y >> 16)),
+               vi, vj);
+        v[tt][i] = vi;
+        v[tt][j] = vj;
+        __syncthreads();
+    }
+    const float e0 = v[tt][2 * t], e1 = v[tt][2 * t + 1];
+    float amax = fmaxf(fabsf(e0), fabsf(e1));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0) red_max[tt][half] = amax;
+    __syncthreads();
+    amax = fmaxf(red_max[tt][0], red_max[tt][1]);
+    const float scale = __fmul_rn(amax, __fdiv_rn(1.0f, 448.0f));
+    uint32_t c2 = 0;
+    if (scale != 0.0f) c2 = e4m3x2(__fdiv_rn(e1, scale), __fdiv_rn(e0, scale));
+    int sum512 = e4m3_times512(c2 & 0xFF) + e4m3_times512(c2 >> 8);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum512 += __shfl_xor_sync(0xFFFFFFFFu, sum512, o);
+    if (lane == 0) red_sum[tt][half] = sum512;
+    __syncthreads();
+    if (live) {
+        reinterpret_cast<uint16_t *>(a + ((size_t)p * M + m) * K + 128 * g)[t] = (uint16_t)c2;
+        if (t == 0) {
+            const size_t o = ((size_t)p * G + g) * M + m;
+            asg[o] = scale;
+            rs[o] = __fmul_rn(__int2float_rn(red_sum[tt][0] + red_sum[tt][1]), 1.0f / 512.0f);
+        }
+    }
+}
+
 __global__ void e4m3_encode_kernel(const float *__restrict__ in, uint8_t *__restrict__ out,
                                    size_t n) {
     const size_t stride = (size_t)gridDim.x * blockDim.x * 2;
@@ -212,12 +319,26 @@ __global__ void e4m3_encode_kernel(const float *__restrict__ in, uint8_t *__rest
 
 pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
                               const void *cs, void *a, float *asg, float *rs, void *stream) {
-    const dim3 grid((M + kTok - 1) / kTok, K / 128);
-    if (grid.x > 0x7FFFFFFF || grid.y > 65535)
-        return fail(PQ_ERR_SHAPE, "pq_rotate_quant: grid (%u, %u) too large", grid.x, grid.y);
-    rotate_quant_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), M, K, ldx, P, static_cast<const uint2 *>(rec),
-        static_cast<const uint16_t *>(cs), static_cast<uint8_t *>(a), asg, rs);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    const uint2 *rp = static_cast<const uint2 *>(rec);
+    const uint16_t *cp = static_cast<const uint16_t *>(cs);
+    uint8_t *ap = static_cast<uint8_t *>(a);
+    if (K / 128 > 65535) return fail(PQ_ERR_SHAPE, "pq_rotate_quant: K = %d too large", K);
+    if (M <= 16) {
+        // decode band: 64 threads per token, partitions in parallel
+        if (M == 1)
+            rotate_quant_small_kernel<1><<<dim3(1, K / 128, P), 64, 0, st>>>(xp, M, K, ldx, rp, cp, ap, asg, rs);
+        else if (M == 2)
+            rotate_quant_small_kernel<2><<<dim3(1, K / 128, P), 128, 0, st>>>(xp, M, K, ldx, rp, cp, ap, asg, rs);
+        else
+            rotate_quant_small_kernel<4><<<dim3((M + 3) / 4, K / 128, P), 256, 0, st>>>(xp, M, K, ldx, rp, cp, ap,
+                                                                                    asg, rs);
+    } else {
+        const dim3 grid((M + kTok - 1) / kTok, K / 128);
+        if (grid.x > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_rotate_quant: M = %d too large", M);
+        rotate_quant_kernel<<<grid, kThreads, 0, st>>>(xp, M, K, ldx, P, rp, cp, ap, asg, rs);
+    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_quant launch: %s", cudaGetErrorString(e));
     return PQ_OK;
