@@ -29,6 +29,14 @@
  *     returns a status and launches nothing.  A launch failure returns
  *     PQ_ERR_CUDA.  Faults inside a kernel surface at the caller's next
  *     synchronisation, as for any CUDA kernel.
+ *   - Kernels are launched as programmatic dependents (programmatic stream
+ *     serialization): pq_rotate_quant waits for the preceding kernel in the
+ *     stream before it reads anything; pq_gemm may begin streaming `w` and
+ *     `sz` (load-time tables) while the preceding kernel is still running if
+ *     that kernel signals early completion -- as pq_rotate_quant does -- and
+ *     waits for it before reading `a`, `asg`, `rs` or writing `y`.  So `w` and
+ *     `sz` must not be written by the kernel issued right before pq_gemm.
+ *     The relaxation survives CUDA-graph capture.
  *   - Device pointers must be 16-byte aligned unless stated otherwise.
  *   - Inputs (x, channel scales, angles, scales) are finite; results for
  *     non-finite inputs are unspecified.

@@ -5,8 +5,35 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 namespace pq {
+
+// Programmatic dependent launch.  pdl_wait(): block until the preceding grid
+// in the stream has completed and its writes are visible (a no-op when this
+// grid was not launched as a programmatic dependent).  pdl_trigger(): allow
+// the next grid in the stream, if launched with programmatic serialization,
+// to be scheduled before this one finishes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with the programmatic-stream-serialization attribute (works under
+// stream capture, where it becomes a programmatic graph edge).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Codes ORed into the optional device status word when a bounded wait gives up.
 enum : unsigned int {
@@ -50,12 +77,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// One try_wait; the thread may be suspended by the hardware for up to
+// kSuspendHintNs while the phase is incomplete (it resumes as soon as the
+// phase completes), so waiting warps do not spin on the issue slots.
+constexpr uint32_t kSuspendHintNs = 100000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -65,9 +97,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    for (uint32_t spin = 1;; ++spin) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 

@@ -22,14 +22,16 @@
 // float conversion and no bias subtraction -- and multiplied into an fp32
 // accumulator with the mixed-precision fma.rn.f32.f16 (exact product, one
 // rounding per add).  Nibbles sitting in bits 4..7 of a half are used in place
-// as 16 * c * 2^-24.  So per group and token the lanes compute
+// as 16 * c * 2^-24, against activations pre-divided by 16 (exact in f16), so
+// every product is a * c * 2^-24.  So per group and token the lanes compute
 // D' = sum a * c = D + 8 * rs exactly up to fp32 addition, and the fold uses
 // sc * D - zscale * rs = sc * D' - (zscale + 8 sc) * rs, where zscale + 8 sc
-// is exact in fp32.  Each of the four lanes of a group adds a quarter of the
-// zero-point term.  The lanes' partials of 8 (or 4) columns are then summed
-// over the warp by one butterfly that hands each column to a subset of lanes
-// (7 exchanges per 8 columns), shared memory reduces the k-warps in a fixed
-// order (deterministic), and the bf16 result is stored once.
+// is exact in fp32.  The four lanes of a group first sum their partials of the
+// octet's 8 columns with a butterfly that hands 2 columns to each lane, so
+// each lane folds only its 2 columns; a second butterfly over the 8 groups of
+// the warp finishes the sum (9 exchanges per 8 columns in all), shared memory
+// reduces the k-warps in a fixed order (deterministic), and the bf16 result is
+// stored once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -63,6 +65,13 @@ __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_codes) {
     return r;
 }
 
+// (a.lo / 16, a.hi / 16): exact for the e4m3 range (>= 2^-13 stays normal in f16)
+__device__ __forceinline__ uint32_t hmul2_sixteenth(uint32_t a) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x2C002C00u));
+    return r;
+}
+
 // acc_lo += a.lo * b.lo, acc_hi += a.hi * b.hi with f16 operands and fp32 accumulators
 __device__ __forceinline__ void fma2_f32_f16(float &acc_lo, float &acc_hi, uint32_t a, uint32_t b) {
     asm("{\n.reg .f16 al, ah, bl, bh;\n"
@@ -85,48 +94,22 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
     return f;
 }
 
-// Sum a lane's partials of NC columns (NC = 8 or 4) over the 32 lanes of the
-// warp with one butterfly that splits the columns among the lanes on the way
-// down: NC - 1 exchanges instead of 5 * NC.  On return the lanes with
-// (lane & (32/NC - 1)) == 0 hold the total of column lane / (32/NC).
+// Keep half of a lane's NC values, exchanging the other half with the lane
+// whose index differs in bit `mask`: out[i] = own kept value + partner's
+// value of the same column.  Lanes with the bit clear keep the lower half.
 template <int NC>
-__device__ __forceinline__ float transpose_reduce(const float (&v)[NC], int lane) {
-    float w[NC / 2];
-    const bool b4 = (lane & 16) != 0;
+__device__ __forceinline__ void split_step(const float (&in)[NC], float (&out)[NC / 2], int lane, int mask) {
+    const bool hi = (lane & mask) != 0;
 #pragma unroll
     for (int i = 0; i < NC / 2; ++i) {
-        const float send = b4 ? v[i] : v[i + NC / 2];
-        const float keep = b4 ? v[i + NC / 2] : v[i];
-        w[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+        const float send = hi ? in[i] : in[i + NC / 2];
+        const float keep = hi ? in[i + NC / 2] : in[i];
+        out[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, mask);
     }
-    const bool b3 = (lane & 8) != 0;
-    float t;
-    if constexpr (NC == 8) {
-        float u[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float send = b3 ? w[i] : w[i + 2];
-            const float keep = b3 ? w[i + 2] : w[i];
-            u[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-        }
-        const bool b2 = (lane & 4) != 0;
-        const float send = b2 ? u[0] : u[1];
-        const float keep = b2 ? u[1] : u[0];
-        t = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-    } else {
-        const float send = b3 ? w[0] : w[1];
-        const float keep = b3 ? w[1] : w[0];
-        t = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-        t += __shfl_xor_sync(0xFFFFFFFFu, t, 4);
-    }
-    t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
-    t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
-    return t;
 }
 
 template <int MT>
 __global__ void skinny_kernel(const SkinnyParams prm) {
-    constexpr int NC = MT <= 2 ? 8 : 4;        // columns reduced together
     extern __shared__ __align__(128) uint8_t smem[];
     const int nkw = prm.nkw, S = prm.stages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,8 +135,11 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
     }
     __syncthreads();
 
+    pdl_trigger();
     if (warp == nkw) {
         // ---------------- producer warp ----------------
+        // (weights and SZ words are load-time tables, not written by the
+        // preceding kernel, so they stream before its completion)
         int issued = 0;
         if (lane == 0) {
             for (int i = 0; i < noct; ++i) {
@@ -186,8 +172,10 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
         const int k0 = 1024 * kw + 32 * lane;
         const bool kvalid = k0 < K;
         const int g = kvalid ? (k0 >> 7) : 0;
+        pdl_wait();        // a, asg, rs are the preceding prologue's output
         uint32_t A[MT][16];
-        float asg_r[MT], ar4_r[MT];        // asg and asg * rs / 4 of this lane's group
+        // per row of this lane's group: 2^24 asg, asg * rs and 8 * asg * rs
+        float asg24_r[MT], ar_r[MT], ar8_r[MT];
         int cur_p = -1;
         for (int i = 0; i < noct; ++i) {
             const int s = i % S, use = i / S;
@@ -199,26 +187,32 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                 for (int m = 0; m < MT; ++m) {
                     const int row = m0 + m;
                     uint32_t u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    asg_r[m] = 0.0f;
-                    ar4_r[m] = 0.0f;
+                    asg24_r[m] = 0.0f;
+                    ar_r[m] = 0.0f;
+                    ar8_r[m] = 0.0f;
                     if (kvalid && row < M) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(
                             prm.a + ((size_t)p * M + row) * K + k0);
                         const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
                         u[0] = v0.x; u[1] = v0.y; u[2] = v0.z; u[3] = v0.w;
                         u[4] = v1.x; u[5] = v1.y; u[6] = v1.z; u[7] = v1.w;
-                        asg_r[m] = __ldg(prm.asg + ((size_t)p * G + g) * M + row);
-                        ar4_r[m] = asg_r[m] * (__ldg(prm.rs + ((size_t)p * G + g) * M + row) * 0.25f);
+                        const float sa = __ldg(prm.asg + ((size_t)p * G + g) * M + row);
+                        asg24_r[m] = sa * 16777216.0f;
+                        ar_r[m] = sa * __ldg(prm.rs + ((size_t)p * G + g) * M + row);
+                        ar8_r[m] = 8.0f * ar_r[m];
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         // bytes 8q..8q+7 -> pairs (k, k+4), (k+1, k+5), (k+2, k+6), (k+3, k+7)
                         const uint32_t t01 = __byte_perm(u[2 * q], u[2 * q + 1], 0x5140);
                         const uint32_t t23 = __byte_perm(u[2 * q], u[2 * q + 1], 0x7362);
+                        // the partners of the high nibbles (used in place as 16 c)
+                        // are divided by 16 -- exact in f16 -- so every product is
+                        // a * c * 2^-24
                         A[m][4 * q + 0] = f16x2_from_e4m3x2(t01 & 0xFFFF);
-                        A[m][4 * q + 1] = f16x2_from_e4m3x2(t01 >> 16);
+                        A[m][4 * q + 1] = hmul2_sixteenth(f16x2_from_e4m3x2(t01 >> 16));
                         A[m][4 * q + 2] = f16x2_from_e4m3x2(t23 & 0xFFFF);
-                        A[m][4 * q + 3] = f16x2_from_e4m3x2(t23 >> 16);
+                        A[m][4 * q + 3] = hmul2_sixteenth(f16x2_from_e4m3x2(t23 >> 16));
                     }
                 }
             }
@@ -231,57 +225,60 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                 break;
             }
             const uint8_t *st = smem + (size_t)s * prm.stage_bytes;
-            const uint4 *szv = reinterpret_cast<const uint4 *>(st + prm.w_bytes) + 2 * g;
-            const uint4 sz_lo = szv[0], sz_hi = szv[1];
-            const uint32_t szw[8] = {sz_lo.x, sz_lo.y, sz_lo.z, sz_lo.w,
-                                     sz_hi.x, sz_hi.y, sz_hi.z, sz_hi.w};
+            // dot products of the 8 columns: lane partials in units of 2^-24
+            float S[MT][8];
 #pragma unroll
-            for (int jb = 0; jb < 8; jb += NC) {
-                float yl[MT][NC];
+            for (int j = 0; j < 8; ++j) {
+                uint4 wv = make_uint4(0, 0, 0, 0);
+                if (kvalid) wv = *reinterpret_cast<const uint4 *>(st + (size_t)j * (K / 2) + (k0 >> 1));
+                float acc[MT][2];
 #pragma unroll
-                for (int jj = 0; jj < NC; ++jj) {
-                    const int j = jb + jj;
-                    uint4 wv = make_uint4(0, 0, 0, 0);
-                    if (kvalid)
-                        wv = *reinterpret_cast<const uint4 *>(st + (size_t)j * (K / 2) + (k0 >> 1));
-                    float acc[MT][4];
+                for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0.0f;
+                const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
-                    const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t x = wq[q], x8 = x >> 8;
-                        const uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
-                        const uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 0], lo);
-                            fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 1], hi);
-                            fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 2], lo2);
-                            fma2_f32_f16(acc[m][2], acc[m][3], A[m][4 * q + 3], hi2);
-                        }
-                    }
-                    const float sc = half_lo(szw[j]), zs = half_hi(szw[j]);
-                    const float sc24 = sc * 16777216.0f;            // 2^24: undo the subnormal scaling
-                    const float zs8 = zs + 8.0f * sc;               // exact in fp32
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t x = wq[q], x8 = x >> 8;
+                    const uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
+                    const uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
-                        // the high-nibble halves already carry the factor 16: scale them back by 1/16
-                        const float sum = (acc[m][0] + acc[m][1]) + 0.0625f * (acc[m][2] + acc[m][3]);
-                        yl[m][jj] = kvalid ? fmaf(asg_r[m] * sc24, sum, -(ar4_r[m] * zs8)) : 0.0f;
+                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 0], lo);
+                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 1], hi);
+                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 2], lo2);
+                        fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 3], hi2);
                     }
                 }
-                if (jb + NC == 8) {            // every read of this stage has been issued and used
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[s]);
-                }
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const float t = transpose_reduce<NC>(yl[m], lane);
-                    constexpr int kLanesPerCol = 32 / NC;
-                    if ((lane & (kLanesPerCol - 1)) == 0)
-                        ypart[(kw * MT + m) * ncol + 8 * i + jb + lane / kLanesPerCol] = t;
-                }
+                for (int m = 0; m < MT; ++m) S[m][j] = acc[m][0] + acc[m][1];
+            }
+            // this lane's group folds columns cb, cb+1 (cb even): the SZ words of
+            // (octet, group g) are contiguous, one 8-byte load
+            const int cb = 4 * ((lane >> 1) & 1) + 2 * (lane & 1);
+            const uint2 szp = *reinterpret_cast<const uint2 *>(st + prm.w_bytes + 32 * g + 4 * cb);
+            __syncwarp();                      // every read of this stage is done
+            if (lane == 0) mbar_arrive(&empty[s]);
+            const float sc0 = half_lo(szp.x), zs0 = half_hi(szp.x);
+            const float sc1 = half_lo(szp.y), zs1 = half_hi(szp.y);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                // sum the 4 lanes of the group, splitting the columns on the way:
+                // bit 1 keeps 4 of 8, bit 0 keeps 2 of 4 (columns cb, cb+1)
+                float h4[4], h2[2];
+                split_step<8>(S[m], h4, lane, 2);
+                split_step<4>(h4, h2, lane, 1);
+                // fold (once per group and column): asg * (sc * D' - (zs + 8 sc) * rs)
+                // with D' = 2^24 * sum
+                float f[2];
+                f[0] = fmaf(sc0 * asg24_r[m], h2[0], -fmaf(sc0, ar8_r[m], zs0 * ar_r[m]));
+                f[1] = fmaf(sc1 * asg24_r[m], h2[1], -fmaf(sc1, ar8_r[m], zs1 * ar_r[m]));
+                // sum the 8 groups of the warp: bit 4 keeps 1 of 2, bits 3 and 2 add
+                float h1[1];
+                split_step<2>(f, h1, lane, 16);
+                float t = h1[0];
+                t += __shfl_xor_sync(0xFFFFFFFFu, t, 8);
+                t += __shfl_xor_sync(0xFFFFFFFFu, t, 4);
+                if ((lane & 12) == 0)          // lanes 0-3 and 16-19 hold column cb + bit 4
+                    ypart[(kw * MT + m) * ncol + 8 * i + cb + ((lane >> 4) & 1)] = t;
             }
         }
     }
@@ -344,8 +341,8 @@ pq_status launch_mt(SkinnyParams prm, int sm_count, cudaStream_t stream) {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess)
                 return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            skinny_kernel<MT><<<grid, threads, smem, stream>>>(prm);
-            e = cudaGetLastError();
+            e = launch_pdl(skinny_kernel<MT>, grid, dim3(threads), smem, stream, prm);
+            if (e == cudaSuccess) e = cudaGetLastError();
             if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
             return PQ_OK;
         }

@@ -173,12 +173,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    for (uint32_t spin = 1;; ++spin) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitLimitNs) return false;
-        }
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -266,9 +264,20 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             prefetch_map(&tmB);
             prefetch_map(&tmS);
             int issued = 0;
-            for (int kb = 0; kb < G; ++kb) {
+            // first stages: weights and SZ (load-time tables) before the
+            // preceding kernel has finished, activations after pdl_wait
+            const int pre = G < kStages ? G : kStages;
+            for (int kb = 0; kb < pre; ++kb) {
+                mbar_arrive_expect_tx(&ctl->full_tma[kb], kTxBytes);
+                tma_load_2d(stg[kb].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[kb]);
+                tma_load_2d(stg[kb].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[kb]);
+            }
+            pdl_wait();
+            for (int kb = 0; kb < pre; ++kb) tma_load_3d(stg[kb].a, &tmA, kb * BK, m0, p, &ctl->full_tma[kb]);
+            issued = pre;
+            for (int kb = pre; kb < G; ++kb) {
                 const int s = kb % kStages, use = kb / kStages;
-                if (use > 0 && !wait_or_abort(&ctl->empty[s], (use - 1) & 1, abort_flag)) {
+                if (!wait_or_abort(&ctl->empty[s], (use - 1) & 1, abort_flag)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
@@ -356,6 +365,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        pdl_wait();        // asg and rs are the preceding prologue's output
         float sa_next = live ? __ldg(asg_p) : 0.0f, r_next = live ? __ldg(rs_p) : 0.0f;
         for (int kb = 0; kb < G; ++kb) {
             const int s = kb % kStages, use = kb / kStages;
@@ -394,6 +404,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->empty[s]);
         }
+        pdl_trigger();
         // epilogue: bf16 row segment of 64 columns
         if (live) {
             const bool bad = *abort_flag != 0;
@@ -496,8 +507,9 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     cudaError_t e = cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    tc_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tmA, tmB, tmS, prm);
-    e = cudaGetLastError();
+    e = launch_pdl(tc_kernel, grid, dim3(kThreads), kSmemBytes, static_cast<cudaStream_t>(stream), tmA, tmB,
+                   tmS, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "tc launch: %s", cudaGetErrorString(e));
     return PQ_OK;
 }

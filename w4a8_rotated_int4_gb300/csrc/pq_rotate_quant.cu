@@ -28,6 +28,7 @@
 
 #include <cstdint>
 
+#include "pq_device.cuh"
 #include "pq_internal.h"
 
 namespace pq {
@@ -109,6 +110,8 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m0 = blockIdx.x * kTok, g = blockIdx.y, G = K >> 7;
     const float inv448 = __fdiv_rn(1.0f, 448.0f);
+    pdl_wait();        // x may be the previous kernel's output
+    pdl_trigger();
 
     // x tile: issued together with the first partition's records and scales
     uint4 xv[4];
@@ -257,6 +260,8 @@ rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
     const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
     const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
     const bool live = m < M;
+    pdl_wait();        // x may be the previous kernel's output
+    pdl_trigger();
 
     // every global load first: x pair, channel-scale pair, the 8 records of pair t
     const uint32_t xw = live ? __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m * ldx + 128 * g) + t) : 0u;
@@ -325,21 +330,24 @@ pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const
     const uint16_t *cp = static_cast<const uint16_t *>(cs);
     uint8_t *ap = static_cast<uint8_t *>(a);
     if (K / 128 > 65535) return fail(PQ_ERR_SHAPE, "pq_rotate_quant: K = %d too large", K);
+    cudaError_t e;
     if (M <= 16) {
         // decode band: 64 threads per token, partitions in parallel
         if (M == 1)
-            rotate_quant_small_kernel<1><<<dim3(1, K / 128, P), 64, 0, st>>>(xp, M, K, ldx, rp, cp, ap, asg, rs);
+            e = launch_pdl(rotate_quant_small_kernel<1>, dim3(1, K / 128, P), dim3(64), 0, st, xp, M, K, ldx,
+                           rp, cp, ap, asg, rs);
         else if (M == 2)
-            rotate_quant_small_kernel<2><<<dim3(1, K / 128, P), 128, 0, st>>>(xp, M, K, ldx, rp, cp, ap, asg, rs);
+            e = launch_pdl(rotate_quant_small_kernel<2>, dim3(1, K / 128, P), dim3(128), 0, st, xp, M, K,
+                           ldx, rp, cp, ap, asg, rs);
         else
-            rotate_quant_small_kernel<4><<<dim3((M + 3) / 4, K / 128, P), 256, 0, st>>>(xp, M, K, ldx, rp, cp, ap,
-                                                                                    asg, rs);
+            e = launch_pdl(rotate_quant_small_kernel<4>, dim3((M + 3) / 4, K / 128, P), dim3(256), 0, st, xp,
+                           M, K, ldx, rp, cp, ap, asg, rs);
     } else {
         const dim3 grid((M + kTok - 1) / kTok, K / 128);
         if (grid.x > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_rotate_quant: M = %d too large", M);
-        rotate_quant_kernel<<<grid, kThreads, 0, st>>>(xp, M, K, ldx, P, rp, cp, ap, asg, rs);
+        e = launch_pdl(rotate_quant_kernel, grid, dim3(kThreads), 0, st, xp, M, K, ldx, P, rp, cp, ap, asg, rs);
     }
-    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_quant launch: %s", cudaGetErrorString(e));
     return PQ_OK;
 }
