@@ -8,23 +8,27 @@
 // (the per-slab fold is the cost to watch) and the A-tiled kernel's choice of
 // slab = scale group = 128 k.
 //
-// One CTA computes a 128 (tokens) x 128 (output features) tile of y.  Per
-// 128-k group kb (a "slab"):
-//   TMA warp     loads A[p][m0:m0+128][128kb:+128] (e4m3, 128B-swizzled,
+// One CTA computes a 256 (tokens) x 128 (output features) tile of y as two
+// M=128 halves that share the B tile.  Per 128-k group kb (a "slab"):
+//   TMA warp     loads A[p][m0:m0+256][128kb:+128] (e4m3, 128B-swizzled,
 //                zero-filled past M), the packed weight tile w[n0:n0+128]
 //                [64kb:+64] and the slab's 128 SZ words (16 octets x 8 words
 //                of the [N/8][G][8] table) into stage s.
 //   expand warps turn each nibble c into the e4m3 code of c (0..15 are exact
 //                in e4m3) in the canonical K-major SWIZZLE_128B layout the MMA
 //                reads, and convert the SZ words to fp32 (sc, zscale + 8 sc).
-//   MMA warp     issues 4 x tcgen05.mma m128n128k32 (kind::f8f6f4, fp32
-//                accumulate) into one of two TMEM accumulators, so the MMAs of
-//                slab kb+1 run while slab kb is folded.
-//   fold warps   tcgen05.ld the slab's D' = sum_k dec(a) * c and fold it into
-//                fp32 registers: acc += asg * (sc * D' - (zscale + 8 sc) * rs),
-//                which equals asg * (sc * D - zscale * rs) with D the sum over
-//                (c - 8): D' = D + 8 * rs exactly, and zscale + 8 sc is exact in
-//                fp32.
+//   MMA warp     issues 2 x 4 tcgen05.mma m128n128k32 (kind::f8f6f4, fp32
+//                accumulate), one chain per half, into one of two TMEM
+//                accumulator sets, so the MMAs of slab kb+1 run while slab kb
+//                is folded.
+//   fold warps   (one thread per row, 128 columns each) tcgen05.ld the slab's
+//                D' = sum_k dec(a) * c and fold it into fp32 registers with
+//                packed f32x2 operations:
+//                acc += asg * (sc * D' - (zscale + 8 sc) * rs), which equals
+//                asg * (sc * D - zscale * rs) with D the sum over (c - 8):
+//                D' = D + 8 * rs exactly, and zscale + 8 sc is exact in fp32.
+// The fold warpgroups raise their register budget (setmaxnreg) to hold the
+// 128 accumulators; the others lower theirs.
 // Epilogue: bf16 rows < M are stored; nothing else is written.
 //
 // Every wait is bounded (%globaltimer); a wait that gives up marks the CTA as
@@ -44,38 +48,47 @@
 namespace pq {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 128;
-constexpr int kStages = 4;
-constexpr int kFoldWarps = 8;     // warps 0..7: warp w folds rows 32(w%4).., columns 64(w/4)..
+constexpr int BM = 256, BN = 128, BK = 128;    // BM = two M=128 MMA halves
+constexpr int kStages = 3;
+constexpr int kFoldWarps = 8;     // warps 0..7: warp w folds rows 128(w/4) + 32(w%4)..+31, all columns
 constexpr int kExpWarps = 4;      // warps 8..11
-constexpr int kTmaWarp = 12, kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kTmaWarp = 12, kMmaWarp = 13;   // warps 14, 15 idle
+constexpr int kThreads = 16 * 32;
+constexpr uint32_t kFoldRegs = 216, kOtherRegs = 40;   // 256 * 216 + 256 * 40 = 65536
 constexpr uint32_t kABytes = BM * BK;
 constexpr uint32_t kBpBytes = BN * BK / 2;
 constexpr uint32_t kBxBytes = BN * BK;
 constexpr uint32_t kSzBytes = BN * 4;
 constexpr uint32_t kTxBytes = kABytes + kBpBytes + kSzBytes;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;    // 2 buffers x 2 halves x 128 columns
 
 struct __align__(1024) Stage {
-    uint8_t a[kABytes];       // 128 rows x 128 B, SWIZZLE_128B (TMA)
+    uint8_t a[kABytes];       // 256 rows x 128 B, SWIZZLE_128B (TMA); half h at 16 KB * h
     uint8_t bx[kBxBytes];     // 128 rows x 128 B, SWIZZLE_128B (expand warps)
     uint8_t bp[kBpBytes];     // 128 rows x 64 B packed nibbles (TMA)
-    uint32_t sz[BN];          // f16 (sc, zscale) per column (bulk copy)
-    float4 szf[BN / 2];       // (sc[n], sc[n+1], zs8[n], zs8[n+1]) for even n
+    uint32_t sz[BN];          // f16 (sc, zscale) per column
+};
+
+// fp32 column scales of one slab for the fold warps, in a ring of their own so
+// a stage is free as soon as its MMAs complete (the fold lags the MMA).
+constexpr int kSzfRing = 4;
+struct __align__(16) SzfSlot {
+    float4 v[BN / 2];         // (sc[n], sc[n+1], zs8[n], zs8[n+1]) for even n
 };
 
 struct Ctrl {
     uint64_t full_tma[kStages];
     uint64_t full_b[kStages];
     uint64_t empty[kStages];
+    uint64_t szf_full[kSzfRing];
+    uint64_t szf_empty[kSzfRing];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemBytes = kStages * sizeof(Stage) + sizeof(Ctrl) + 1024;
+constexpr size_t kSmemBytes = kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot) + sizeof(Ctrl) + 1024;
 
 struct TcParams {
     const float *asg;
@@ -124,9 +137,9 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 }
 
 // kind::f8f6f4 instruction descriptor: D fp32, A and B e4m3, both K-major,
-// N = 128, M = 128.
+// N = 128, M = 128 (one half).
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+                            ((uint32_t)(128 >> 4) << 24);
 
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
     asm volatile(
@@ -140,33 +153,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane; the wait carries
-// the registers so no use can be scheduled before the data has arrived.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
-                   "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -217,26 +203,115 @@ __device__ __forceinline__ uint4 expand16(uint2 pk) {
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFF))); }
 __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+// ---------------------------------------------------------------- fold pieces
+// Issue a 16-column TMEM load (no wait) / wait for it, carrying the registers
+// through the wait so their uses stay after it.
+__device__ __forceinline__ void tmem_issue16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+// One wait for two outstanding 16-column loads (tcgen05.wait::ld covers every
+// load the thread has issued), carrying all 32 registers through it.
+__device__ __forceinline__ void tmem_wait2x16(uint32_t (&a)[16], uint32_t (&b)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+                   "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
+                   "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]),
+                   "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
+                   "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+                 :
+                 : "memory");
+}
+
+// Packed ops, kept in program order (volatile) so each chunk's chains are
+// issued stage by stage.
+__device__ __forceinline__ uint64_t fmul2v(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm volatile("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t ffma2v(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm volatile("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// acc[j] += asg * (sc * D - zs8 * rs) for the 8 column pairs of one chunk,
+// issued stage by stage across all 8 pairs (8 independent chains per stage).
+__device__ __forceinline__ void fold_chunk(const uint32_t (&d)[16], const ulonglong2 *zf, uint64_t *acc,
+                                           uint64_t sa2, uint64_t nr2) {
+    uint64_t t[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        t[j] = fmul2v(f2pack(__uint_as_float(d[2 * j]), __uint_as_float(d[2 * j + 1])), zf[j].x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = ffma2v(zf[j].y, nr2, t[j]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = ffma2v(sa2, t[j], acc[j]);
+}
+
+// Tile i of this CTA: output-feature tile fastest, its partition from pb1/pb2.
+__device__ __forceinline__ void tile_coords(int i, int ntn, int pb1, int pb2, int &n0, int &m0, int &p) {
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    n0 = (t % ntn) * BN;
+    m0 = (t / ntn) * BM;
+    p = (n0 >= pb1) + (n0 >= pb2);
+}
+
 // ---------------------------------------------------------------- kernel
+// Persistent: CTA c walks tiles t = c, c + gridDim.x, ... (output-feature
+// tile fastest, so the CTAs running at once share activation rows and the
+// weight tiles stay L2-resident).  All pipelines run continuously across tile
+// boundaries; slab counter it = (tile index) * G + kb.
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmS, const TcParams prm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Stage *stg = reinterpret_cast<Stage *>(base);
-    Ctrl *ctl = reinterpret_cast<Ctrl *>(base + kStages * sizeof(Stage));
+    SzfSlot *szf = reinterpret_cast<SzfSlot *>(base + kStages * sizeof(Stage));
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(base + kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot));
     volatile int *abort_flag = &ctl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-    const int M = prm.M, N = prm.N, G = prm.K / BK;
-    const int p = (n0 >= prm.pb1) + (n0 >= prm.pb2);
+    const int M = prm.M, G = prm.K / BK;
+    const int ntn = prm.N / BN, ntiles = ntn * ((M + BM - 1) / BM);
+    const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_tiles * G;
+    const int pb1 = prm.pb1, pb2 = prm.pb2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full_tma[s], 1);
             mbar_init(&ctl->full_b[s], kExpWarps);
-            mbar_init(&ctl->empty[s], 1 + kFoldWarps);
+            mbar_init(&ctl->empty[s], 1);            // the MMA commit
+        }
+        for (int r = 0; r < kSzfRing; ++r) {
+            mbar_init(&ctl->szf_full[r], kExpWarps);
+            mbar_init(&ctl->szf_empty[r], kFoldWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
@@ -257,35 +332,43 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
+    if (warp >= kFoldWarps) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (warp == kTmaWarp) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_map(&tmA);
             prefetch_map(&tmB);
             prefetch_map(&tmS);
-            int issued = 0;
+            int n0, m0, p;
             // first stages: weights and SZ (load-time tables) before the
             // preceding kernel has finished, activations after pdl_wait
-            const int pre = G < kStages ? G : kStages;
-            for (int kb = 0; kb < pre; ++kb) {
-                mbar_arrive_expect_tx(&ctl->full_tma[kb], kTxBytes);
-                tma_load_2d(stg[kb].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[kb]);
-                tma_load_2d(stg[kb].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[kb]);
+            const int pre = total < kStages ? total : kStages;
+            for (int it = 0; it < pre; ++it) {
+                tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+                const int kb = it % G;
+                mbar_arrive_expect_tx(&ctl->full_tma[it], kTxBytes);
+                tma_load_2d(stg[it].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[it]);
+                tma_load_2d(stg[it].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[it]);
             }
             pdl_wait();
-            for (int kb = 0; kb < pre; ++kb) tma_load_3d(stg[kb].a, &tmA, kb * BK, m0, p, &ctl->full_tma[kb]);
-            issued = pre;
-            for (int kb = pre; kb < G; ++kb) {
-                const int s = kb % kStages, use = kb / kStages;
+            for (int it = 0; it < pre; ++it) {
+                tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+                tma_load_3d(stg[it].a, &tmA, (it % G) * BK, m0, p, &ctl->full_tma[it]);
+            }
+            int issued = pre;
+            for (int it = pre; it < total; ++it) {
+                const int s = it % kStages, use = it / kStages;
                 if (!wait_or_abort(&ctl->empty[s], (use - 1) & 1, abort_flag)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
+                tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+                const int kb = it % G;
                 mbar_arrive_expect_tx(&ctl->full_tma[s], kTxBytes);
                 tma_load_3d(stg[s].a, &tmA, kb * BK, m0, p, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[s]);
-                issued = kb + 1;
+                issued = it + 1;
             }
             if (*abort_flag) {   // let issued copies land before shared memory is released
                 for (int s = 0; s < kStages && s < issued; ++s) {
@@ -299,9 +382,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int committed = 0;
-            for (int kb = 0; kb < G; ++kb) {
-                const int s = kb % kStages, use = kb / kStages;
-                const int b = kb & 1, tuse = kb >> 1;
+            for (int it = 0; it < total; ++it) {
+                const int s = it % kStages, use = it / kStages;
+                const int b = it & 1, tuse = it >> 1;
                 if (!wait_or_abort(&ctl->full_tma[s], use & 1, abort_flag) ||
                     !wait_or_abort(&ctl->full_b[s], use & 1, abort_flag)) {
                     set_abort(ctl, prm.status, kStatusWaitFull);
@@ -312,37 +395,40 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = desc_sw128(smem_u32(stg[s].a));
+                const uint64_t ad0 = desc_sw128(smem_u32(stg[s].a));
+                const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
                 const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
+                const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
 #pragma unroll
-                for (int kk = 0; kk < BK / 32; ++kk)     // +32 bytes along K inside the swizzle row
-                    mma_f8(tmem + (uint32_t)(b * BN), ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
-                           kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K inside the swizzle row
+                    mma_f8(d0, ad0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kk > 0 ? 1u : 0u);
+                    mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kk > 0 ? 1u : 0u);
+                }
                 mma_commit(&ctl->empty[s]);
                 mma_commit(&ctl->tmem_full[b]);
-                committed = kb + 1;
+                committed = it + 1;
             }
             if (*abort_flag && committed > 0) {   // MMAs must finish before TMEM is freed
-                const int kb = committed - 1;
-                if (!mbar_wait(&ctl->tmem_full[kb & 1], (kb >> 1) & 1) && prm.status)
+                const int it = committed - 1;
+                if (!mbar_wait(&ctl->tmem_full[it & 1], (it >> 1) & 1) && prm.status)
                     atomicOr(prm.status, kStatusDrain);
             }
         }
-    } else if (warp >= kFoldWarps) {
+    } else if (warp >= kFoldWarps && warp < kFoldWarps + kExpWarps) {
         // ------------------------------------------------ nibble expansion
         const int et = threadIdx.x - kFoldWarps * 32;    // 0..127
         const int chunk = et & 7;
-        for (int kb = 0; kb < G; ++kb) {
-            const int s = kb % kStages, use = kb / kStages;
+        for (int it = 0; it < total; ++it) {
+            const int s = it % kStages, use = it / kStages;
             if (!wait_or_abort(&ctl->full_tma[s], use & 1, abort_flag)) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
             Stage &st = stg[s];
-            if (et < BN / 2) {
-                const uint32_t w0 = st.sz[2 * et], w1 = st.sz[2 * et + 1];
-                const float sc0 = f16lo(w0), sc1 = f16lo(w1);
-                st.szf[et] = make_float4(sc0, sc1, f16hi(w0) + 8.0f * sc0, f16hi(w1) + 8.0f * sc1);
+            uint32_t w0 = 0, w1 = 0;
+            if (et < BN / 2) {            // read the SZ words now: the stage may be refilled after full_b
+                w0 = st.sz[2 * et];
+                w1 = st.sz[2 * et + 1];
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -353,73 +439,104 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->full_b[s]);
-        }
-    } else {
-        // ------------------------------------------------ fold warps
-        const int q = warp & 3, h = warp >> 2;
-        const int row = 32 * q + lane;
-        const int m = m0 + row;
-        const bool live = m < M;
-        const float *asg_p = prm.asg + (size_t)p * G * M + m;
-        const float *rs_p = prm.rs + (size_t)p * G * M + m;
-        float acc[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        pdl_wait();        // asg and rs are the preceding prologue's output
-        float sa_next = live ? __ldg(asg_p) : 0.0f, r_next = live ? __ldg(rs_p) : 0.0f;
-        for (int kb = 0; kb < G; ++kb) {
-            const int s = kb % kStages, use = kb / kStages;
-            const int b = kb & 1, tuse = kb >> 1;
-            const float sa = sa_next, nr = -r_next;
-            if (kb + 1 < G && live) {
-                sa_next = __ldg(asg_p + (size_t)(kb + 1) * M);
-                r_next = __ldg(rs_p + (size_t)(kb + 1) * M);
-            }
-            if (!wait_or_abort(&ctl->full_b[s], use & 1, abort_flag) ||
-                !wait_or_abort(&ctl->tmem_full[b], tuse & 1, abort_flag)) {
+            // fp32 scales for the fold, into the ring slot of this slab
+            const int r = it % kSzfRing, ruse = it / kSzfRing;
+            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag)) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
-            tc_fence_after();
-            const float4 *zf = stg[s].szf + 32 * h;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float d[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 64 * h + 32 * half), d);
-                if (half == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->tmem_empty[b]);
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float4 z = zf[16 * half + j];
-                    const int c = 32 * half + 2 * j;
-                    const float t0 = fmaf(z.z, nr, d[2 * j] * z.x);
-                    const float t1 = fmaf(z.w, nr, d[2 * j + 1] * z.y);
-                    acc[c] = fmaf(sa, t0, acc[c]);
-                    acc[c + 1] = fmaf(sa, t1, acc[c + 1]);
-                }
+            if (et < BN / 2) {
+                const float sc0 = f16lo(w0), sc1 = f16lo(w1);
+                szf[r].v[et] = make_float4(sc0, sc1, f16hi(w0) + 8.0f * sc0, f16hi(w1) + 8.0f * sc1);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->empty[s]);
+            if (lane == 0) mbar_arrive(&ctl->szf_full[r]);
         }
-        pdl_trigger();
-        // epilogue: bf16 row segment of 64 columns
-        if (live) {
-            const bool bad = *abort_flag != 0;
-            uint4 *dst = reinterpret_cast<uint4 *>(prm.y + (size_t)m * prm.ldy + n0 + 64 * h);
+    } else if (warp < kFoldWarps) {
+        // ------------------------------------------------ fold warps
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFoldRegs));
+        const int q = warp & 3, h = warp >> 2;
+        const int row = 128 * h + 32 * q + lane;
+        pdl_wait();        // asg and rs are the preceding prologue's output
+        bool bad = false;
+        for (int i = 0; i < my_tiles; ++i) {
+            int n0, m0, p;
+            tile_coords(i, ntn, pb1, pb2, n0, m0, p);
+            const int m = m0 + row;
+            const bool live = m < M;
+            uint64_t acc[64];                 // column pairs (2c, 2c+1)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t wv[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float lo = acc[8 * i + 2 * j], hi = acc[8 * i + 2 * j + 1];
-                    if (bad) lo = hi = __int_as_float(0x7FC00000);
-                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(lo, hi);
-                    wv[j] = *reinterpret_cast<const uint32_t *>(&v2);
+            for (int c = 0; c < 64; ++c) acc[c] = 0;
+            const float *asg_p = prm.asg + (size_t)p * G * M + m;
+            const float *rs_p = prm.rs + (size_t)p * G * M + m;
+            // per-row scales, loaded two slabs ahead of their use
+            float sa0 = 0.0f, r0s = 0.0f, sa1 = 0.0f, r1s = 0.0f;
+            if (live && !bad) {
+                sa0 = __ldg(asg_p);
+                r0s = __ldg(rs_p);
+                if (G > 1) {
+                    sa1 = __ldg(asg_p + (size_t)M);
+                    r1s = __ldg(rs_p + (size_t)M);
                 }
-                dst[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+            for (int kb = 0; kb < G && !bad; ++kb) {
+                const int it = i * G + kb;
+                const int b = it & 1, tuse = it >> 1;
+                const uint64_t sa2 = f2pack(sa0, sa0), nr2 = f2pack(-r0s, -r0s);
+                sa0 = sa1;
+                r0s = r1s;
+                if (kb + 2 < G && live) {
+                    sa1 = __ldg(asg_p + (size_t)(kb + 2) * M);
+                    r1s = __ldg(rs_p + (size_t)(kb + 2) * M);
+                }
+                const int r = it % kSzfRing, ruse = it / kSzfRing;
+                if (!wait_or_abort(&ctl->szf_full[r], ruse & 1, abort_flag) ||
+                    !wait_or_abort(&ctl->tmem_full[b], tuse & 1, abort_flag)) {
+                    if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
+                    bad = true;
+                    break;
+                }
+                tc_fence_after();
+                const ulonglong2 *zf = reinterpret_cast<const ulonglong2 *>(szf[r].v);
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + h * BN);
+                // eight 16-column chunks; the load of chunk rd+1 is in flight
+                // while chunk rd is folded
+                uint32_t rbuf[2][16];
+                tmem_issue16(taddr, rbuf[0]);
+                tmem_wait16(rbuf[0]);
+#pragma unroll
+                for (int rd = 0; rd < BN / 16; ++rd) {
+                    const int cur = rd & 1;
+                    if (rd + 1 < BN / 16) {
+                        tmem_issue16(taddr + 16 * (rd + 1), rbuf[cur ^ 1]);
+                    } else {   // every load of this buffer has completed
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctl->tmem_empty[b]);
+                    }
+                    fold_chunk(rbuf[cur], zf + 8 * rd, acc + 8 * rd, sa2, nr2);
+                    if (rd + 1 < BN / 16) tmem_wait16(rbuf[cur ^ 1]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->szf_empty[r]);
+            }
+            if (i == my_tiles - 1) pdl_trigger();
+            bad = bad || *abort_flag != 0;
+            // epilogue: bf16 row segment of 128 columns (NaN once the CTA has aborted)
+            if (live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.y + (size_t)m * prm.ldy + n0);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float2 v = f2unpack(acc[4 * c + j]);
+                        if (bad) v.x = v.y = __int_as_float(0x7FC00000);
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(v.x, v.y);
+                        wv[j] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
+                    dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
             }
         }
     }
@@ -502,8 +619,10 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     prm.pb1 = pb1;
     prm.pb2 = pb2;
     prm.ldy = ldy;
-    const dim3 grid(N / BN, (M + BM - 1) / BM);
-    if (grid.y > 65535) return fail(PQ_ERR_SHAPE, "pq_gemm_tc: M = %d too large", M);
+    const long long ntiles = (long long)(N / BN) * ((M + BM - 1) / BM);
+    if (ntiles > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_gemm_tc: M = %d too large", M);
+    const int ctas = (int)(ntiles < sm_count ? ntiles : (sm_count > 0 ? sm_count : 1));
+    const dim3 grid(ctas);
     cudaError_t e = cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
