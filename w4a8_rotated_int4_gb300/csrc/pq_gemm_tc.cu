@@ -52,7 +52,7 @@ constexpr int BM = 256, BN = 128, BK = 128;    // BM = two M=128 MMA halves
 constexpr int kStages = 3;
 constexpr int kFoldWarps = 8;     // warps 0..7: warp w folds rows 128(w/4) + 32(w%4)..+31, all columns
 constexpr int kExpWarps = 4;      // warps 8..11
-constexpr int kTmaWarp = 12, kMmaWarp = 13;   // warps 14, 15 idle
+constexpr int kTmaWarp = 12, kMmaWarp = 13, kRowWarp = 14;   // warp 15 idle
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kFoldRegs = 216, kOtherRegs = 40;   // 256 * 216 + 256 * 40 = 65536
 constexpr uint32_t kABytes = BM * BK;
@@ -69,11 +69,15 @@ struct __align__(1024) Stage {
     uint32_t sz[BN];          // f16 (sc, zscale) per column
 };
 
-// fp32 column scales of one slab for the fold warps, in a ring of their own so
-// a stage is free as soon as its MMAs complete (the fold lags the MMA).
+// fp32 scales of one slab for the fold warps, in a ring of their own so a
+// stage is free as soon as its MMAs complete (the fold lags the MMA).  The
+// column part comes from the expansion warps; the row part is copied straight
+// from global memory by the row warp (cp.async), which runs up to a ring's
+// depth ahead, so no global-load latency reaches the fold warps.
 constexpr int kSzfRing = 4;
 struct __align__(16) SzfSlot {
-    float4 v[BN / 2];         // (sc[n], sc[n+1], zs8[n], zs8[n+1]) for even n
+    float4 v[BN / 2];         // (sc[n], sc[n+1], -zs8[n], -zs8[n+1]) for even n
+    float2 row[BM];           // (asg, rs) of tile row i (0 past M)
 };
 
 struct Ctrl {
@@ -82,7 +86,7 @@ struct Ctrl {
     uint64_t empty[kStages];
     uint64_t szf_full[kSzfRing];
     uint64_t szf_empty[kSzfRing];
-    uint64_t tmem_full[2];
+    uint64_t tmem_full[2][2];     // [m-half][accumulator buffer]
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
     int abort;
@@ -155,6 +159,18 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy (zero-fill when !valid; the source
+// is then not read) and the arrival on an mbarrier once all of this thread's
+// copies have landed (the arrival is part of the barrier's expected count).
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -214,17 +230,8 @@ __device__ __forceinline__ float2 f2unpack(uint64_t v) {
     return r;
 }
 // ---------------------------------------------------------------- fold pieces
-// Issue a 16-column TMEM load (no wait) / wait for it, carrying the registers
+// Wait for the thread's outstanding TMEM loads, carrying the registers
 // through the wait so their uses stay after it.
-__device__ __forceinline__ void tmem_issue16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
 __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
@@ -233,17 +240,17 @@ __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
-// One wait for two outstanding 16-column loads (tcgen05.wait::ld covers every
-// load the thread has issued), carrying all 32 registers through it.
-__device__ __forceinline__ void tmem_wait2x16(uint32_t (&a)[16], uint32_t (&b)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
-                   "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
-                   "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]),
-                   "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
-                   "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
-                 :
-                 : "memory");
+// 16x256b.x4 TMEM load (no wait): for repetition j (columns 8j..8j+7 of the
+// address), d[4j], d[4j+1] = lane base + g4, columns 8j + 2c4 + {0, 1};
+// d[4j+2], d[4j+3] = lane base + 8 + g4, same columns (g4 = lane / 4, c4 = lane % 4).
+__device__ __forceinline__ void tmem_issue256(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
 }
 
 // Packed ops, kept in program order (volatile) so each chunk's chains are
@@ -259,18 +266,28 @@ __device__ __forceinline__ uint64_t ffma2v(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-// acc[j] += asg * (sc * D - zs8 * rs) for the 8 column pairs of one chunk,
-// issued stage by stage across all 8 pairs (8 independent chains per stage).
-__device__ __forceinline__ void fold_chunk(const uint32_t (&d)[16], const ulonglong2 *zf, uint64_t *acc,
-                                           uint64_t sa2, uint64_t nr2) {
+// Fold one 16x256b.x4 load: four column pairs for two rows (lo: d[4j..4j+1],
+// hi: d[4j+2..4j+3]); acc += asg * (sc * D + (-zs8) * rs), stage by stage
+// (z[j].x = sc pair, z[j].y = -zs8 pair, nr = rs splat).
+__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const ulonglong2 (&z)[4], uint64_t *acc_lo,
+                                           uint64_t *acc_hi, uint64_t sa_lo, uint64_t nr_lo, uint64_t sa_hi,
+                                           uint64_t nr_hi) {
     uint64_t t[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        t[j] = fmul2v(f2pack(__uint_as_float(d[2 * j]), __uint_as_float(d[2 * j + 1])), zf[j].x);
+    for (int j = 0; j < 4; ++j) {
+        t[2 * j] = fmul2v(f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), z[j].x);
+        t[2 * j + 1] = fmul2v(f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), z[j].x);
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) t[j] = ffma2v(zf[j].y, nr2, t[j]);
+    for (int j = 0; j < 4; ++j) {
+        t[2 * j] = ffma2v(z[j].y, nr_lo, t[2 * j]);
+        t[2 * j + 1] = ffma2v(z[j].y, nr_hi, t[2 * j + 1]);
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = ffma2v(sa2, t[j], acc[j]);
+    for (int j = 0; j < 4; ++j) {
+        acc_lo[j] = ffma2v(sa_lo, t[2 * j], acc_lo[j]);
+        acc_hi[j] = ffma2v(sa_hi, t[2 * j + 1], acc_hi[j]);
+    }
 }
 
 // Tile i of this CTA: output-feature tile fastest, its partition from pb1/pb2.
@@ -310,11 +327,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_init(&ctl->empty[s], 1);            // the MMA commit
         }
         for (int r = 0; r < kSzfRing; ++r) {
-            mbar_init(&ctl->szf_full[r], kExpWarps);
+            mbar_init(&ctl->szf_full[r], kExpWarps + 32);   // + the row warp's cp.async arrivals
             mbar_init(&ctl->szf_empty[r], kFoldWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->tmem_full[b], 1);
+            mbar_init(&ctl->tmem_full[0][b], 1);
+            mbar_init(&ctl->tmem_full[1][b], 1);
             mbar_init(&ctl->tmem_empty[b], kFoldWarps);
         }
         ctl->abort = 0;
@@ -378,6 +396,28 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
             }
         }
+    } else if (warp == kRowWarp) {
+        // ------------------------------------------------ per-row scales
+        pdl_wait();        // asg and rs are the preceding prologue's output
+        for (int it = 0; it < total; ++it) {
+            const int r = it % kSzfRing, ruse = it / kSzfRing;
+            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag)) {
+                if (lane == 0) set_abort(ctl, prm.status, kStatusWaitEmpty);
+                break;
+            }
+            int n0, m0, p;
+            tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+            const size_t off = ((size_t)p * G + (size_t)(it % G)) * (size_t)M;
+#pragma unroll
+            for (int u = 0; u < BM / 32; ++u) {
+                const int i = lane + 32 * u, m = m0 + i;
+                const bool ok = m < M;     // rows past M are zero-filled
+                cp_async4(&szf[r].row[i].x, ok ? prm.asg + off + m : prm.asg, ok);
+                cp_async4(&szf[r].row[i].y, ok ? prm.rs + off + m : prm.rs, ok);
+            }
+            cp_async_arrive(&ctl->szf_full[r]);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -399,18 +439,22 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
                 const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
                 const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
+                // half 0, then half 1, each committed on its own so the two
+                // fold warp groups start half a slab apart
 #pragma unroll
-                for (int kk = 0; kk < BK / 32; ++kk) {   // +32 bytes along K inside the swizzle row
+                for (int kk = 0; kk < BK / 32; ++kk)   // +32 bytes along K inside the swizzle row
                     mma_f8(d0, ad0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kk > 0 ? 1u : 0u);
+                mma_commit(&ctl->tmem_full[0][b]);
+#pragma unroll
+                for (int kk = 0; kk < BK / 32; ++kk)
                     mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kk > 0 ? 1u : 0u);
-                }
                 mma_commit(&ctl->empty[s]);
-                mma_commit(&ctl->tmem_full[b]);
+                mma_commit(&ctl->tmem_full[1][b]);
                 committed = it + 1;
             }
             if (*abort_flag && committed > 0) {   // MMAs must finish before TMEM is freed
                 const int it = committed - 1;
-                if (!mbar_wait(&ctl->tmem_full[it & 1], (it >> 1) & 1) && prm.status)
+                if (!mbar_wait(&ctl->tmem_full[1][it & 1], (it >> 1) & 1) && prm.status)
                     atomicOr(prm.status, kStatusDrain);
             }
         }
@@ -430,11 +474,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 w0 = st.sz[2 * et];
                 w1 = st.sz[2 * et + 1];
             }
+            // all eight packed loads first (the stores below could alias them
+            // as far as the compiler knows), then expand and store
+            uint2 pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                pk[i] = *reinterpret_cast<const uint2 *>(st.bp + ((et >> 3) + 16 * i) * (BK / 2) + chunk * 8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = (et >> 3) + 16 * i;
-                const uint2 pk = *reinterpret_cast<const uint2 *>(st.bp + row * (BK / 2) + chunk * 8);
-                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = expand16(pk);
+                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = expand16(pk[i]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -447,7 +496,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             if (et < BN / 2) {
                 const float sc0 = f16lo(w0), sc1 = f16lo(w1);
-                szf[r].v[et] = make_float4(sc0, sc1, f16hi(w0) + 8.0f * sc0, f16hi(w1) + 8.0f * sc1);
+                szf[r].v[et] = make_float4(sc0, sc1, -(f16hi(w0) + 8.0f * sc0), -(f16hi(w1) + 8.0f * sc1));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->szf_full[r]);
@@ -455,87 +504,85 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     } else if (warp < kFoldWarps) {
         // ------------------------------------------------ fold warps
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFoldRegs));
+        // 16x256b TMEM loads: thread (g4, c4) of the warp holds rows
+        // 128h + 32q + 8i + g4 (i = 0..3) and column pairs 8J + 2c4 (J = 0..15),
+        // so each per-column scale load serves four rows.
         const int q = warp & 3, h = warp >> 2;
-        const int row = 128 * h + 32 * q + lane;
-        pdl_wait();        // asg and rs are the preceding prologue's output
+        const int g4 = lane >> 2, c4 = lane & 3;
+        const int row0 = 128 * h + 32 * q + g4;
+        pdl_wait();        // y may still be read by the preceding kernel
         bool bad = false;
         for (int i = 0; i < my_tiles; ++i) {
             int n0, m0, p;
             tile_coords(i, ntn, pb1, pb2, n0, m0, p);
-            const int m = m0 + row;
-            const bool live = m < M;
-            uint64_t acc[64];                 // column pairs (2c, 2c+1)
+            const int mb = m0 + row0;     // rows mb + 8 * ri
+            uint64_t acc[4][16];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) acc[c] = 0;
-            const float *asg_p = prm.asg + (size_t)p * G * M + m;
-            const float *rs_p = prm.rs + (size_t)p * G * M + m;
-            // per-row scales, loaded two slabs ahead of their use
-            float sa0 = 0.0f, r0s = 0.0f, sa1 = 0.0f, r1s = 0.0f;
-            if (live && !bad) {
-                sa0 = __ldg(asg_p);
-                r0s = __ldg(rs_p);
-                if (G > 1) {
-                    sa1 = __ldg(asg_p + (size_t)M);
-                    r1s = __ldg(rs_p + (size_t)M);
-                }
-            }
+            for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+                for (int J = 0; J < 16; ++J) acc[ri][J] = 0;
             for (int kb = 0; kb < G && !bad; ++kb) {
                 const int it = i * G + kb;
                 const int b = it & 1, tuse = it >> 1;
-                const uint64_t sa2 = f2pack(sa0, sa0), nr2 = f2pack(-r0s, -r0s);
-                sa0 = sa1;
-                r0s = r1s;
-                if (kb + 2 < G && live) {
-                    sa1 = __ldg(asg_p + (size_t)(kb + 2) * M);
-                    r1s = __ldg(rs_p + (size_t)(kb + 2) * M);
-                }
                 const int r = it % kSzfRing, ruse = it / kSzfRing;
                 if (!wait_or_abort(&ctl->szf_full[r], ruse & 1, abort_flag) ||
-                    !wait_or_abort(&ctl->tmem_full[b], tuse & 1, abort_flag)) {
+                    !wait_or_abort(&ctl->tmem_full[h][b], tuse & 1, abort_flag)) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     bad = true;
                     break;
                 }
                 tc_fence_after();
-                const ulonglong2 *zf = reinterpret_cast<const ulonglong2 *>(szf[r].v);
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + h * BN);
-                // eight 16-column chunks; the load of chunk rd+1 is in flight
-                // while chunk rd is folded
-                uint32_t rbuf[2][16];
-                tmem_issue16(taddr, rbuf[0]);
-                tmem_wait16(rbuf[0]);
+                // eight steps (32-column block cb, 16-lane half sh), one
+                // 16x256b.x4 load each; the load of step k+1 is in flight
+                // while step k is folded
+                uint32_t dbuf[2][16];
+                tmem_issue256(taddr, dbuf[0]);
+                uint64_t sa2[4], rs2[4];
 #pragma unroll
-                for (int rd = 0; rd < BN / 16; ++rd) {
-                    const int cur = rd & 1;
-                    if (rd + 1 < BN / 16) {
-                        tmem_issue16(taddr + 16 * (rd + 1), rbuf[cur ^ 1]);
-                    } else {   // every load of this buffer has completed
+                for (int ri = 0; ri < 4; ++ri) {
+                    const float2 v = szf[r].row[row0 + 8 * ri];
+                    sa2[ri] = f2pack(v.x, v.x);
+                    rs2[ri] = f2pack(v.y, v.y);
+                }
+                const ulonglong2 *zf = reinterpret_cast<const ulonglong2 *>(szf[r].v) + c4;
+                ulonglong2 z[4];
+                tmem_wait16(dbuf[0]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int cb = k >> 1, sh = k & 1, cur = k & 1;
+                    if (k + 1 < 8) {
+                        tmem_issue256(taddr + ((uint32_t)(16 * ((k + 1) & 1)) << 16) + 32 * ((k + 1) >> 1),
+                                      dbuf[cur ^ 1]);
+                    } else {       // every load of this buffer has completed
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&ctl->tmem_empty[b]);
                     }
-                    fold_chunk(rbuf[cur], zf + 8 * rd, acc + 8 * rd, sa2, nr2);
-                    if (rd + 1 < BN / 16) tmem_wait16(rbuf[cur ^ 1]);
+                    if (sh == 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) z[j] = zf[4 * (4 * cb + j)];
+                    }
+                    fold_block(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
+                               rs2[2 * sh], sa2[2 * sh + 1], rs2[2 * sh + 1]);
+                    if (k + 1 < 8) tmem_wait16(dbuf[cur ^ 1]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->szf_empty[r]);
             }
             if (i == my_tiles - 1) pdl_trigger();
             bad = bad || *abort_flag != 0;
-            // epilogue: bf16 row segment of 128 columns (NaN once the CTA has aborted)
-            if (live) {
-                uint4 *dst = reinterpret_cast<uint4 *>(prm.y + (size_t)m * prm.ldy + n0);
+            // epilogue: bf16 pairs (NaN once the CTA has aborted)
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t wv[4];
+            for (int ri = 0; ri < 4; ++ri) {
+                if (mb + 8 * ri >= M) continue;
+                uint32_t *dst = reinterpret_cast<uint32_t *>(prm.y + (size_t)(mb + 8 * ri) * prm.ldy + n0 + 2 * c4);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float2 v = f2unpack(acc[4 * c + j]);
-                        if (bad) v.x = v.y = __int_as_float(0x7FC00000);
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(v.x, v.y);
-                        wv[j] = *reinterpret_cast<const uint32_t *>(&v2);
-                    }
-                    dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                for (int J = 0; J < 16; ++J) {
+                    float2 v = f2unpack(acc[ri][J]);
+                    if (bad) v.x = v.y = __int_as_float(0x7FC00000);
+                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(v.x, v.y);
+                    dst[4 * J] = *reinterpret_cast<const uint32_t *>(&v2);
                 }
             }
         }
