@@ -126,6 +126,7 @@ class ClockSampler:
 class Workload:
     def __init__(self, pq, torch, name, M, dev):
         self.c, self.label = describe(name, M)
+        self.name = name if M is None else "%s:%d" % (name, M)
         c = self.c
         prob = pqgen.make_problem(**c)
         self.prob = prob
@@ -263,6 +264,33 @@ def e2e_workload(pq, torch, wl, steps, warmup, stream, dev):
     return e0.elapsed_time(e1) / steps, xh.numel() * 2, yh.numel() * 2
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the kernel on the workload, with the SHA-256 of the kernel's
+# source at capture time.  The figure is reported only while the source is
+# unchanged; otherwise traffic is null.
+NCU_TRAFFIC = {
+    ("pq_gemm_skinny", "decode:1"): dict(
+        bytes=47379968 + 2048, profile="profiles/pq_gemm_skinny_decode_gate_up_m1.md",
+        src="w4a8_rotated_int4_gb300/csrc/pq_gemm_skinny.cu",
+        sha256="426b5645f0fb6237a62cbfb0fc095d2169790ab0b211429bb432fac2eec9a396"),
+    ("pq_gemm_tc", "prefill"): dict(
+        bytes=74486784 + 41364736, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        src="w4a8_rotated_int4_gb300/csrc/pq_gemm_tc.cu",
+        sha256="fb8c22e9b78aff60dc2a4e3a5f1aae92c36e41de152d218c52462fa0f95b6f1f"),
+}
+
+
+def ncu_traffic(kernel, workload):
+    import hashlib
+    e = NCU_TRAFFIC.get((kernel, workload))
+    if e is None:
+        return None
+    with open(os.path.join(ROOT, e["src"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != e["sha256"]:
+            return None
+    return e["bytes"]
+
+
 def roofline(wl, r, peaks, traffic=None):
     if wl.gemm_kernel == "skinny":
         achieved = wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9
@@ -286,7 +314,9 @@ def summarize(wl, r, steps, peaks):
         "gemm_tflops": round(wl.flops / (r["gemm_ms"] * 1e-3) / 1e12, 2),
         "gemm_gbs": round(wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9, 1),
         "prologue_gbs": round(wl.pro_bytes / (r["pro_ms"] * 1e-3) / 1e9, 1),
-        "roofline": roofline(wl, r, peaks), "copies": wl.copies,
+        "roofline": roofline(wl, r, peaks, ncu_traffic(
+            "pq_gemm_skinny" if wl.gemm_kernel == "skinny" else "pq_gemm_tc", wl.name)),
+        "copies": wl.copies,
     }
 
 
