@@ -159,10 +159,10 @@ class Workload:
         pq.pq_rotate_quant(self.x[j], self.rec[j], self.cs[j], a=self.a[j], asg=self.asg[j],
                            rs=self.rs[j], stream=stream)
 
-    def gemm(self, pq, i, stream):
+    def gemm(self, pq, i, stream, fn=None):
         j = i % self.copies
-        pq.pq_gemm(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1, self.pb2,
-                   y=self.y[j], stream=stream)
+        (fn or pq.pq_gemm)(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1,
+                           self.pb2, y=self.y[j], stream=stream)
 
     def step(self, pq, i, stream):
         self.prologue(pq, i, stream)
@@ -228,7 +228,31 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
         b.record(stream)
         torch.cuda.synchronize()
         per[key] = a.elapsed_time(b) / (reps * C)
-    return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"])
+    paths = time_gemm_paths(pq, torch, wl, reps, stream) if wl.c["M"] <= 16 else {}
+    return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths)
+
+
+def time_gemm_paths(pq, torch, wl, reps, stream):
+    """GEMM-only time per launch (ms) of every kernel that accepts this M,
+    each from a graph of one launch per input copy, replayed `reps` times."""
+    M = wl.c["M"]
+    paths = [("tc", pq.pq_gemm_tc)]
+    if M <= pq.pq_gemm_skinny_max_m():
+        paths += [("skinny", pq.pq_gemm_skinny), ("tcn", pq.pq_gemm_tcn)]
+    out = {}
+    for name, fn in paths:
+        C = wl.copies
+        g = _capture(torch, lambda: [wl.gemm(pq, j, None, fn) for j in range(C)])
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out[name] = a.elapsed_time(b) / (reps * C)
+    return out
 
 
 class _Null:
@@ -317,6 +341,7 @@ def summarize(wl, r, steps, peaks):
         "roofline": roofline(wl, r, peaks, ncu_traffic(
             "pq_gemm_skinny" if wl.gemm_kernel == "skinny" else "pq_gemm_tc", wl.name)),
         "copies": wl.copies,
+        "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
     }
 
 
@@ -476,6 +501,7 @@ def main():
                    "l2": "%d rotating input copies (> 2x L2)" % wl.copies},
         "prologue_us": head["prologue_us"], "gemm_us": head["gemm_us"],
         "roofline": head["roofline"],
+        "gemm_us_by_kernel": head["gemm_us_by_kernel"],
         "e2e": None if e2e_ms is None else {
             "value": round(e2e_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "how": "public API per step: pinned H2D of x, "

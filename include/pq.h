@@ -30,12 +30,15 @@
  *     PQ_ERR_CUDA.  Faults inside a kernel surface at the caller's next
  *     synchronisation, as for any CUDA kernel.
  *   - Kernels are launched as programmatic dependents (programmatic stream
- *     serialization): pq_rotate_quant waits for the preceding kernel in the
- *     stream before it reads anything; pq_gemm may begin streaming `w` and
- *     `sz` (load-time tables) while the preceding kernel is still running if
- *     that kernel signals early completion -- as pq_rotate_quant does -- and
- *     waits for it before reading `a`, `asg`, `rs` or writing `y`.  So `w` and
- *     `sz` must not be written by the kernel issued right before pq_gemm.
+ *     serialization).  Each kernel may read its load-time tables while the
+ *     preceding kernel in the stream is still running, if that kernel signals
+ *     early completion (all kernels here do), and waits for the preceding
+ *     kernel before it reads anything else or writes anything:
+ *     pq_rotate_quant may read `rec` and `cs` early, then waits before reading
+ *     `x` and writing `a`, `asg`, `rs`; pq_gemm may stream `w` and `sz` early,
+ *     then waits before reading `a`, `asg`, `rs` or writing `y`.  So `rec` and
+ *     `cs` must not be written by the kernel issued right before
+ *     pq_rotate_quant, nor `w` and `sz` by the one right before pq_gemm.
  *     The relaxation survives CUDA-graph capture.
  *   - Device pointers must be 16-byte aligned unless stated otherwise.
  *   - Inputs (x, channel scales, angles, scales) are finite; results for
@@ -188,9 +191,12 @@ pq_status pq_gemm(const void *a, const float *asg, const float *rs, int M, int N
 int pq_gemm_skinny_max_m(void);
 
 /*
- * The two GEMM kernels behind pq_gemm, callable on their own (same arguments
- * and result).  pq_gemm_skinny accepts 1 <= M <= 16 (PQ_ERR_SHAPE otherwise);
- * pq_gemm_tc accepts any M >= 1.
+ * The GEMM kernels behind pq_gemm, callable on their own (same arguments and
+ * result).  pq_gemm_skinny (CUDA cores; weights streamed once, exact products
+ * accumulated in fp32) accepts 1 <= M <= 16; pq_gemm_tcn (tensor cores,
+ * operands swapped: 128 output features x up to 16 tokens per MMA, weights
+ * streamed once) accepts 1 <= M <= 16; pq_gemm_tc (tensor cores, 256-token x
+ * 128-feature tiles) accepts any M >= 1.  A larger M returns PQ_ERR_SHAPE.
  *
  * dev_status (device, 4-byte aligned, may be NULL): every wait inside the
  * kernels is bounded; a wait that gives up (never expected) ORs a nonzero
@@ -203,6 +209,9 @@ pq_status pq_gemm_skinny(const void *a, const float *asg, const float *rs, int M
 pq_status pq_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
                      int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
                      unsigned int *dev_status, void *stream);
+pq_status pq_gemm_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                      int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
+                      unsigned int *dev_status, void *stream);
 
 /*
  * The prologue's device e4m3 encoder applied to n fp32 values ([CVT]: NaN ->

@@ -161,6 +161,7 @@ def gemm_paths(pq, M):
     paths = [("tc", pq.pq_gemm_tc)]
     if M <= pq.pq_gemm_skinny_max_m():
         paths.append(("skinny", pq.pq_gemm_skinny))
+        paths.append(("tcn", pq.pq_gemm_tcn))
     return paths
 
 
@@ -173,7 +174,8 @@ def run_gemm(fn, a, asg, rs, L, pb1, pb2, M, N, ldy=None, fill=float("nan")):
     import ctypes as C
     import w4a8_rotated_int4_gb300 as m
     lib = m.lib()
-    name = "pq_gemm_tc" if fn is m.pq_gemm_tc else "pq_gemm_skinny"
+    name = {m.pq_gemm_tc: "pq_gemm_tc", m.pq_gemm_skinny: "pq_gemm_skinny",
+            m.pq_gemm_tcn: "pq_gemm_tcn"}[fn]
     P = a.shape[0]
     K = a.shape[2]
     st = getattr(lib, name)(C.c_void_p(a.data_ptr()), C.c_void_p(asg.data_ptr()),
@@ -333,6 +335,38 @@ def test_full_workload_sampled(pq, orc, name, M):
                                prob.pb2)
     yg = y.float().cpu().numpy()[ms, ns]
     assert_close(yg, y64, "%s M=%d" % (name, prob.M))
-    if prob.M <= pq.pq_gemm_skinny_max_m():      # the other path on the same inputs
-        y2 = pq.pq_gemm_tc(a, asg, rs, L.w_d, L.sz_d, prob.pb1, prob.pb2)
-        assert_close(y2.float().cpu().numpy()[ms, ns], y64, "tc %s M=%d" % (name, prob.M))
+    if prob.M <= pq.pq_gemm_skinny_max_m():      # the other paths on the same inputs
+        for tag, fn in (("tc", pq.pq_gemm_tc), ("skinny", pq.pq_gemm_skinny), ("tcn", pq.pq_gemm_tcn)):
+            y2 = fn(a, asg, rs, L.w_d, L.sz_d, prob.pb1, prob.pb2)
+            assert_close(y2.float().cpu().numpy()[ms, ns], y64, "%s %s M=%d" % (tag, name, prob.M))
+
+
+# ---------------------------------------------------------------- repeated launches
+@pytest.mark.parametrize("path", ["skinny", "tcn", "tc"])
+def test_gemm_repeated_graph_launches_status_clean(pq, orc, path):
+    """Many back-to-back launches chained by programmatic dependent launch,
+    replayed from a CUDA graph over rotating buffers: every bounded wait in
+    every launch must succeed (status word stays 0) and the last results must
+    still match the first ones bit for bit."""
+    M, K, N = 4, 5120, 17408
+    prob = pqgen.make_problem(M, K, N, seed=12)
+    L = Problem(pq, orc, prob, check_pack=False)
+    fn = {"skinny": pq.pq_gemm_skinny, "tcn": pq.pq_gemm_tcn, "tc": pq.pq_gemm_tc}[path]
+    C = 7
+    acts = [pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d) for _ in range(C)]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(C)]
+    st = torch.zeros((C, 1), dtype=torch.int32, device="cuda")
+    fn(*acts[0], L.w_d, L.sz_d, N, N, y=ys[0], dev_status=st[0])
+    torch.cuda.synchronize()
+    ref = ys[0].clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for j in range(C):
+            fn(*acts[j], L.w_d, L.sz_d, N, N, y=ys[j], dev_status=st[j])
+    reps = 300 if path != "tc" else 40
+    for _ in range(reps):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(st.abs().sum().item()) == 0, "a bounded wait gave up: %s" % st.flatten().tolist()
+    for j in range(C):
+        assert torch.equal(ys[j], ref), j

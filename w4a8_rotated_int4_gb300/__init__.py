@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libpq.so")
 EXPORTS = (
     "pq_abi_version", "pq_status_string", "pq_last_error", "pq_pack_sizes", "pq_pack",
     "pq_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny", "pq_gemm_tc",
+    "pq_gemm_tcn",
     "pq_e4m3_encode",
 )
 
@@ -68,7 +69,7 @@ def lib() -> C.CDLL:
     L.pq_gemm.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp]
     L.pq_gemm_skinny_max_m.restype = i32
     L.pq_gemm_skinny_max_m.argtypes = []
-    for name in ("pq_gemm_skinny", "pq_gemm_tc"):
+    for name in ("pq_gemm_skinny", "pq_gemm_tc", "pq_gemm_tcn"):
         f = getattr(L, name)
         f.restype = i32
         f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
@@ -206,6 +207,11 @@ def pq_gemm_skinny(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=Non
 
 def pq_gemm_tc(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
     return _gemm_path(lib().pq_gemm_tc, "pq_gemm_tc", a, asg, rs, w, sz, pb1, pb2, y,
+                      dev_status, stream)
+
+
+def pq_gemm_tcn(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    return _gemm_path(lib().pq_gemm_tcn, "pq_gemm_tcn", a, asg, rs, w, sz, pb1, pb2, y,
                       dev_status, stream)
 
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpq.so")
 
-SOURCES = ["pq_abi.cpp", "pq_rotate_quant.cu", "pq_gemm_skinny.cu", "pq_gemm_tc.cu"]
+SOURCES = ["pq_abi.cpp", "pq_rotate_quant.cu", "pq_gemm_skinny.cu", "pq_gemm_tc.cu", "pq_gemm_tcn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -313,6 +313,20 @@ extern "C" pq_status pq_gemm_tc(const void *a, const float *asg, const float *rs
     return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, sms);
 }
 
+extern "C" pq_status pq_gemm_tcn(const void *a, const float *asg, const float *rs, int M, int N,
+                                 int K, int P, int pb1, int pb2, const void *w, const void *sz,
+                                 void *y, int ldy, unsigned int *dev_status, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (M > kTcnMaxM) return fail(PQ_ERR_SHAPE, "pq_gemm_tcn: M = %d > %d", M, kTcnMaxM);
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream);
+}
+
 extern "C" pq_status pq_gemm(const void *a, const float *asg, const float *rs, int M, int N, int K,
                              int P, int pb1, int pb2, const void *w, const void *sz, void *y,
                              int ldy, void *stream) {

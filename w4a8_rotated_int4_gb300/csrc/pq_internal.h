@@ -38,6 +38,11 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
                          int P, int pb1, int pb2, const void *w, const void *sz, void *y,
                          int ldy, unsigned int *dev_status, void *stream, int sm_count);
 
+pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                          int P, int pb1, int pb2, const void *w, const void *sz, void *y,
+                          int ldy, unsigned int *dev_status, void *stream);
+
 constexpr int kSkinnyMaxM = 16;   // largest M the CUDA-core decode kernel accepts
+constexpr int kTcnMaxM = 16;      // largest M the narrow tensor-core kernel accepts
 
 }  // namespace pq

@@ -260,15 +260,16 @@ rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
     const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
     const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
     const bool live = m < M;
-    pdl_wait();        // x may be the previous kernel's output
     pdl_trigger();
 
-    // every global load first: x pair, channel-scale pair, the 8 records of pair t
-    const uint32_t xw = live ? __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m * ldx + 128 * g) + t) : 0u;
+    // the load-time tables first (channel-scale pair, the 8 records of pair t):
+    // they are read while the preceding kernel may still be running
     const uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs + (size_t)p * K + 128 * g) + t);
     uint2 r8[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
+    pdl_wait();        // x may be the previous kernel's output; a, asg, rs may still be read by it
+    const uint32_t xw = live ? __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m * ldx + 128 * g) + t) : 0u;
 
     v[tt][2 * t] = __fmul_rn(bf16lo(xw), half_to_float((uint16_t)(cw & 0xFFFF)));
     v[tt][2 * t + 1] = __fmul_rn(bf16hi(xw), half_to_float((uint16_t)(cw >> 16)));
