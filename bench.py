@@ -152,7 +152,13 @@ class Workload:
         self.y = [t.empty((M, N), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
         self.pb1, self.pb2 = prob.pb1, prob.pb2
         self.gemm_bytes, self.pro_bytes, self.flops = gemm_bytes, pro_bytes, flops
-        self.gemm_kernel = "skinny" if M_of(c) <= pq.pq_gemm_skinny_max_m() else "tcgen05"
+        sms = torch_sms(t)
+        if M_of(c) == 1 or (M_of(c) <= pq.pq_gemm_skinny_max_m() and 2 * (c["N"] // 128) < sms):
+            self.gemm_kernel = "skinny"          # the kernel pq_gemm dispatches to
+        elif M_of(c) <= pq.pq_gemm_skinny_max_m():
+            self.gemm_kernel = "tcn"
+        else:
+            self.gemm_kernel = "tcgen05"
 
     def prologue(self, pq, i, stream):
         j = i % self.copies
@@ -167,6 +173,10 @@ class Workload:
     def step(self, pq, i, stream):
         self.prologue(pq, i, stream)
         self.gemm(pq, i, stream)
+
+
+def torch_sms(torch):
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
 
 def M_of(c):
@@ -315,10 +325,13 @@ def ncu_traffic(kernel, workload):
     return e["bytes"]
 
 
+KERNEL_NAMES = {"skinny": "pq_gemm_skinny", "tcn": "pq_gemm_tcn", "tcgen05": "pq_gemm_tc"}
+
+
 def roofline(wl, r, peaks, traffic=None):
-    if wl.gemm_kernel == "skinny":
+    if wl.gemm_kernel in ("skinny", "tcn"):      # decode band: weights streamed once
         achieved = wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9
-        return {"kernel": "pq_gemm_skinny", "bound": "hbm", "achieved": round(achieved, 1),
+        return {"kernel": KERNEL_NAMES[wl.gemm_kernel], "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                 "peak_source": peaks["src"] + " (hbm_gbs)", "traffic": traffic}
     fp8_peak = 2.0 * peaks["bf16"]
@@ -338,8 +351,7 @@ def summarize(wl, r, steps, peaks):
         "gemm_tflops": round(wl.flops / (r["gemm_ms"] * 1e-3) / 1e12, 2),
         "gemm_gbs": round(wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9, 1),
         "prologue_gbs": round(wl.pro_bytes / (r["pro_ms"] * 1e-3) / 1e9, 1),
-        "roofline": roofline(wl, r, peaks, ncu_traffic(
-            "pq_gemm_skinny" if wl.gemm_kernel == "skinny" else "pq_gemm_tc", wl.name)),
+        "roofline": roofline(wl, r, peaks, ncu_traffic(KERNEL_NAMES[wl.gemm_kernel], wl.name)),
         "copies": wl.copies,
         "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
     }

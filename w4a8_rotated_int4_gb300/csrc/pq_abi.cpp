@@ -336,8 +336,16 @@ extern "C" pq_status pq_gemm(const void *a, const float *asg, const float *rs, i
     int sms = 0;
     st = check_device(&sms);
     if (st != PQ_OK) return st;
-    if (M <= kSkinnyMaxM)
+    // M = 1: the CUDA-core kernel streams the weights with the fewest instructions.
+    // 2 <= M <= 16: the narrow tensor-core kernel, when its 128-feature tiles cover
+    // at least half the SMs (it streams each tile from one SM); otherwise the
+    // CUDA-core kernel, which spreads 8-feature octets over every SM.
+    // M > 16: the prefill tensor-core kernel.
+    if (M <= kSkinnyMaxM) {
+        if (M >= 2 && M <= kTcnMaxM && 2 * (N / 128) >= sms)
+            return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream);
         return launch_gemm_skinny(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream,
                                   sms);
+    }
     return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, sms);
 }

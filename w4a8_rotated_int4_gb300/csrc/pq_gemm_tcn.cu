@@ -59,14 +59,17 @@ constexpr int kMmaWarp0 = 2, kMmaWarps = 4;               // warps 2..5, one per
 // expansion: kExpGroups groups of 4 warps, group e expands slabs it = e mod kExpGroups,
 // so that several slabs are expanded at once
 constexpr int kExpWarp0 = kMmaWarp0 + kMmaWarps, kExpWarps = 4, kExpGroups = 4;   // warps 6..21
-// fold warps 22..25: warp w reads TMEM lane quarter w % 4 (all four are covered)
-constexpr int kFoldWarp0 = kExpWarp0 + kExpWarps * kExpGroups, kFoldWarps = 4;
-constexpr int kThreads = (kFoldWarp0 + kFoldWarps) * 32;
+// fold: kFoldSets sets of 4 warps (warps 22..29), set f folds the slabs
+// it = f mod kFoldSets into accumulators of its own, summed at the end; warp w
+// reads TMEM lane quarter w % 4 (each set covers all four)
+constexpr int kFoldWarp0 = kExpWarp0 + kExpWarps * kExpGroups, kFoldWarps = 4, kFoldSets = 2;
+constexpr int kThreads = (kFoldWarp0 + kFoldWarps * kFoldSets) * 32;
 // An mbarrier parity wait cannot tell phase u+1 from phase u-1, so a waiter must
 // never wait for a barrier's next use before it has seen the previous one.  Each
 // stage and each scale slot is therefore always served by the same expand group
 // and the same MMA warp, which take their slabs in order.
 static_assert(kStages % kExpGroups == 0 && kStages % kMmaWarps == 0, "stage ownership");
+static_assert(kMmaWarps % kFoldSets == 0, "accumulator ownership");
 constexpr uint32_t kBxBytes = NN * BK;        // expanded weights, 128 rows x 128 B
 constexpr uint32_t kAaBytes = MT * BK;        // activations, 16 rows x 128 B
 constexpr uint32_t kBpBytes = NN * BK / 2;    // packed weights, 128 rows x 64 B
@@ -106,7 +109,8 @@ struct Ctrl {
 constexpr size_t kSmemBytes =
     kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot) + kRowRing * sizeof(RowSlot) + sizeof(Ctrl) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kSzfRing % kExpGroups == 0, "scale slot ownership");
+static_assert(kSzfRing % kExpGroups == 0 && kSzfRing % kFoldSets == 0 && kRowRing % kFoldSets == 0,
+              "scale slot ownership");
 
 struct TcnParams {
     const float *asg;
@@ -213,24 +217,27 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         // ------------------------------------------------ MMA issuers
         // full_b implies full_tma: the expand warps waited for the stage's
         // copies (activations included) before they arrived on full_b
+        // The whole warp runs the loop (so the descriptors stay warp-uniform)
+        // and one elected lane issues the MMAs and commits.
         const int b = warp - kMmaWarp0;
-        if (lane == 0) {
-            int committed = -1;
-            for (int it = b; it < G; it += kMmaWarps) {
-                const int s = it % kStages, use = it / kStages;
-                const int tuse = it / kMmaWarps;
-                if (!wait_or_abort(&ctl->full_b[s], use & 1, abort_flag)) {
-                    set_abort(ctl, prm.status, kStatusWaitFull);
-                    break;
-                }
-                if (tuse > 0 && !wait_or_abort(&ctl->tmem_empty[b], (tuse - 1) & 1, abort_flag)) {
-                    set_abort(ctl, prm.status, kStatusWaitTmem);
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t ad = desc_sw128(smem_u32(stg[s].bx));
-                const uint64_t bd = desc_sw128(smem_u32(stg[s].aa));
-                const uint32_t d = tmem + (uint32_t)(b * MT);
+        int committed = -1;
+        for (int it = b; it < G; it += kMmaWarps) {
+            const int s = it % kStages, use = it / kStages;
+            const int tuse = it / kMmaWarps;
+            // full_b, and the accumulator's release by the fold (its first use
+            // waits on nothing: the phase before the first reads as complete)
+            const bool ok = __all_sync(0xFFFFFFFFu,
+                                       wait3_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
+                                                      &ctl->full_b[s], use & 1, abort_flag));
+            if (!ok) {
+                if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull | kStatusWaitTmem);
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad = desc_sw128(smem_u32(stg[s].bx));
+            const uint64_t bd = desc_sw128(smem_u32(stg[s].aa));
+            const uint32_t d = tmem + (uint32_t)(b * MT);
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)   // +32 bytes along K inside the swizzle row
                     mma_f8(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdescN, kk > 0 ? 1u : 0u);
@@ -239,15 +246,16 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 // exits would land in the shared memory of the next CTA on this SM.
                 if (it + kStages < G) mma_commit(&ctl->empty[s]);
                 mma_commit(&ctl->tmem_full[b]);
-                committed = it;
             }
-            if (*abort_flag && committed >= 0) {   // MMAs and their arrivals must land before exit
-                if (!mbar_wait(&ctl->tmem_full[b], (committed / kMmaWarps) & 1) && prm.status)
-                    atomicOr(prm.status, kStatusDrain);
-                if (committed + kStages < G &&
-                    !mbar_wait(&ctl->empty[committed % kStages], (committed / kStages) & 1) && prm.status)
-                    atomicOr(prm.status, kStatusDrain);
-            }
+            __syncwarp();
+            committed = it;
+        }
+        if (*abort_flag && committed >= 0 && lane == 0) {   // MMAs and their arrivals must land before exit
+            if (!mbar_wait(&ctl->tmem_full[b], (committed / kMmaWarps) & 1) && prm.status)
+                atomicOr(prm.status, kStatusDrain);
+            if (committed + kStages < G &&
+                !mbar_wait(&ctl->empty[committed % kStages], (committed / kStages) & 1) && prm.status)
+                atomicOr(prm.status, kStatusDrain);
         }
     } else if (warp == kRowWarp) {
         // ------------------------------------------------ per-token scales
@@ -313,22 +321,22 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->szf_full[r]);
         }
-    } else if (warp >= kFoldWarp0 && warp < kFoldWarp0 + kFoldWarps) {
+    } else if (warp >= kFoldWarp0 && warp < kFoldWarp0 + kFoldWarps * kFoldSets) {
         // ------------------------------------------------ fold warps
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int n = 32 * q + lane;         // output feature within the tile
+        const int fs = (warp - kFoldWarp0) / kFoldWarps;
         pdl_wait();        // y may still be read by the preceding kernel
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
         bool bad = false;
-        for (int it = 0; it < G; ++it) {
+        for (int it = fs; it < G; it += kFoldSets) {
             const int b = it % kMmaWarps, tuse = it / kMmaWarps;
             const int r = it % kSzfRing, ruse = it / kSzfRing;
             const int rr = it % kRowRing, rruse = it / kRowRing;
-            if (!wait_or_abort(&ctl->row_full[rr], rruse & 1, abort_flag) ||
-                !wait_or_abort(&ctl->szf_full[r], ruse & 1, abort_flag) ||
-                !wait_or_abort(&ctl->tmem_full[b], tuse & 1, abort_flag)) {
+            if (!wait3_or_abort(&ctl->row_full[rr], rruse & 1, &ctl->szf_full[r], ruse & 1,
+                                &ctl->tmem_full[b], tuse & 1, abort_flag)) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 bad = true;
                 break;
@@ -355,13 +363,27 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 mbar_arrive(&ctl->row_empty[rr]);
             }
         }
-        bad = bad || *abort_flag != 0;
-        // epilogue: one bf16 per token (NaN once the CTA has aborted)
+        // the sets meet in shared memory (stage 0's expanded-weight buffer is
+        // free: every MMA has completed once each set has seen its last slab)
+        float *part = reinterpret_cast<float *>(stg[0].bx);      // [kFoldSets - 1][MT][NN]
+        if (fs > 0) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m < M) {
-                const float v = bad ? __int_as_float(0x7FC00000) : acc[m];
-                prm.y[(size_t)m * prm.ldy + n0 + n] = __float2bfloat16_rn(v);
+            for (int m = 0; m < MT; ++m) part[((fs - 1) * MT + m) * NN + n] = acc[m];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kFoldWarps * kFoldSets * 32) : "memory");
+        if (fs == 0) {
+            bad = bad || *abort_flag != 0;
+            for (int f = 1; f < kFoldSets; ++f) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m] += part[((f - 1) * MT + m) * NN + n];
+            }
+            // epilogue: one bf16 per token (NaN once the CTA has aborted)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {
+                    const float v = bad ? __int_as_float(0x7FC00000) : acc[m];
+                    prm.y[(size_t)m * prm.ldy + n0 + n] = __float2bfloat16_rn(v);
+                }
             }
         }
     }

@@ -55,7 +55,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 
 // kind::f8f6f4 instruction descriptor: D fp32 (bits 4-5 = 1), A and B e4m3
 // (type 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t idesc_f8(int m, int n) {
+__host__ __device__ constexpr uint32_t idesc_f8(int m, int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
@@ -66,6 +66,33 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
         : "memory");
+}
+
+// Non-blocking test of up to three mbarrier phases issued back to back, so
+// their shared-memory round trips overlap (acquire on success).  A null
+// barrier counts as complete.
+__device__ __forceinline__ uint32_t mbar_test3(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
+                                               uint64_t *b2, uint32_t p2) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred q0, q1, q2;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n"
+        "and.pred q0, q0, q1;\nand.pred q0, q0, q2;\nselp.u32 %0, 1, 0, q0;\n}"
+        : "=r"(r)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
+        : "memory");
+    return r;
+}
+
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n.reg .pred p;\n.reg .b32 r;\nelect.sync r|p, 0xffffffff;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -96,6 +123,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
+
+// Bounded wait for three phases: one overlapped test first, then each barrier
+// in turn (the common case, all three complete, costs one round trip).
+__device__ __forceinline__ bool wait3_or_abort(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
+                                               uint64_t *b2, uint32_t p2, volatile int *abort_flag) {
+    if (mbar_test3(b0, p0, b1, p1, b2, p2)) return true;
+    return wait_or_abort(b0, p0, abort_flag) && wait_or_abort(b1, p1, abort_flag) &&
+           wait_or_abort(b2, p2, abort_flag);
+}
+
 
 
 // e4m3 codes of 4 nibbles (selector bits 0..15): nibble c < 8 picks byte c of
