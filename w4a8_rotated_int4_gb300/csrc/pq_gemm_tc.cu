@@ -267,25 +267,29 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int committed = 0;
-            for (int it = 0; it < total; ++it) {
-                const int s = it % kStages, use = it / kStages;
-                const int b = it & 1, tuse = it >> 1;
-                if (!wait_or_abort(&ctl->full_tma[s], use & 1, abort_flag) ||
-                    !wait_or_abort(&ctl->full_b[s], use & 1, abort_flag)) {
-                    set_abort(ctl, prm.status, kStatusWaitFull);
-                    break;
-                }
-                if (tuse > 0 && !wait_or_abort(&ctl->tmem_empty[b], (tuse - 1) & 1, abort_flag)) {
-                    set_abort(ctl, prm.status, kStatusWaitTmem);
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t ad0 = desc_sw128(smem_u32(stg[s].a));
-                const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
-                const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
-                const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
+        // The whole warp runs the loop (so the descriptors stay warp-uniform)
+        // and one elected lane issues the MMAs and commits.  full_b implies
+        // full_tma: the expand warps waited for the stage's copies before they
+        // arrived on full_b.
+        int committed = 0;
+        for (int it = 0; it < total; ++it) {
+            const int s = it % kStages, use = it / kStages;
+            const int b = it & 1, tuse = it >> 1;
+            // the accumulator's first use waits on nothing: the phase before
+            // the first reads as complete
+            const bool ok = __all_sync(0xFFFFFFFFu,
+                                       wait3_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
+                                                      &ctl->full_b[s], use & 1, abort_flag));
+            if (!ok) {
+                if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull | kStatusWaitTmem);
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad0 = desc_sw128(smem_u32(stg[s].a));
+            const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
+            const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
+            const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
+            if (elect_one()) {
                 // half 0, then half 1, each committed on its own so the two
                 // fold warp groups start half a slab apart
 #pragma unroll
@@ -300,18 +304,19 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // exits would land in the shared memory of the next CTA on this SM.
                 if (it + kStages < total) mma_commit(&ctl->empty[s]);
                 mma_commit(&ctl->tmem_full[1][b]);
-                committed = it + 1;
             }
-            if (*abort_flag && committed > 0) {   // MMAs and their arrivals must land before exit
-                const int it = committed - 1;
-                if (!mbar_wait(&ctl->tmem_full[0][it & 1], (it >> 1) & 1) && prm.status)
-                    atomicOr(prm.status, kStatusDrain);
-                if (!mbar_wait(&ctl->tmem_full[1][it & 1], (it >> 1) & 1) && prm.status)
-                    atomicOr(prm.status, kStatusDrain);
-                if (it + kStages < total && !mbar_wait(&ctl->empty[it % kStages], (it / kStages) & 1) &&
-                    prm.status)
-                    atomicOr(prm.status, kStatusDrain);
-            }
+            __syncwarp();
+            committed = it + 1;
+        }
+        if (*abort_flag && committed > 0 && lane == 0) {   // MMAs and their arrivals must land before exit
+            const int it = committed - 1;
+            if (!mbar_wait(&ctl->tmem_full[0][it & 1], (it >> 1) & 1) && prm.status)
+                atomicOr(prm.status, kStatusDrain);
+            if (!mbar_wait(&ctl->tmem_full[1][it & 1], (it >> 1) & 1) && prm.status)
+                atomicOr(prm.status, kStatusDrain);
+            if (it + kStages < total && !mbar_wait(&ctl->empty[it % kStages], (it / kStages) & 1) &&
+                prm.status)
+                atomicOr(prm.status, kStatusDrain);
         }
     } else if (warp >= kFoldWarps && warp < kFoldWarps + kExpWarps) {
         // ------------------------------------------------ nibble expansion
@@ -380,8 +385,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int it = i * G + kb;
                 const int b = it & 1, tuse = it >> 1;
                 const int r = it % kSzfRing, ruse = it / kSzfRing;
-                if (!wait_or_abort(&ctl->szf_full[r], ruse & 1, abort_flag) ||
-                    !wait_or_abort(&ctl->tmem_full[h][b], tuse & 1, abort_flag)) {
+                if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
+                                    &ctl->szf_full[r], ruse & 1, abort_flag)) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     bad = true;
                     break;
