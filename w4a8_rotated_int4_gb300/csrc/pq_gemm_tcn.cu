@@ -69,13 +69,16 @@ constexpr int kThreads = (kFoldWarp0 + kFoldWarps * kFoldSets) * 32;
 // stage and each scale slot is therefore always served by the same expand group
 // and the same MMA warp, which take their slabs in order.
 static_assert(kStages % kExpGroups == 0 && kStages % kMmaWarps == 0, "stage ownership");
-static_assert(kMmaWarps % kFoldSets == 0, "accumulator ownership");
+// TMEM accumulators: slab it uses buffer it % kTmemBufs, issued by MMA warp
+// it % kMmaWarps and folded by set it % kFoldSets (each buffer keeps its owners)
+constexpr int kTmemBufs = 8;
+static_assert(kTmemBufs % kMmaWarps == 0 && kTmemBufs % kFoldSets == 0, "accumulator ownership");
 constexpr uint32_t kBxBytes = NN * BK;        // expanded weights, 128 rows x 128 B
 constexpr uint32_t kAaBytes = MT * BK;        // activations, 16 rows x 128 B
 constexpr uint32_t kBpBytes = NN * BK / 2;    // packed weights, 128 rows x 64 B
 constexpr uint32_t kSzBytes = NN * 4;
 constexpr uint32_t kTxBytes = kBpBytes + kAaBytes + kSzBytes;
-constexpr uint32_t kTmemCols = 64;            // kMmaWarps accumulators x 16 columns
+constexpr uint32_t kTmemCols = 128;           // 8 accumulators x 16 columns
 constexpr uint32_t kIdescN = idesc_f8(NN, MT);
 
 struct __align__(1024) Stage {
@@ -100,8 +103,8 @@ struct Ctrl {
     uint64_t szf_empty[kSzfRing];
     uint64_t row_full[kRowRing];
     uint64_t row_empty[kRowRing];
-    uint64_t tmem_full[kMmaWarps];
-    uint64_t tmem_empty[kMmaWarps];
+    uint64_t tmem_full[kTmemBufs];
+    uint64_t tmem_empty[kTmemBufs];
     uint32_t tmem_base;
     int abort;
 };
@@ -155,7 +158,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             mbar_init(&ctl->row_full[r], 32);               // the row warp's cp.async arrivals
             mbar_init(&ctl->row_empty[r], kFoldWarps);
         }
-        for (int b = 0; b < kMmaWarps; ++b) {
+        for (int b = 0; b < kTmemBufs; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
             mbar_init(&ctl->tmem_empty[b], kFoldWarps);
         }
@@ -219,11 +222,11 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         // copies (activations included) before they arrived on full_b
         // The whole warp runs the loop (so the descriptors stay warp-uniform)
         // and one elected lane issues the MMAs and commits.
-        const int b = warp - kMmaWarp0;
+        const int j = warp - kMmaWarp0;
         int committed = -1;
-        for (int it = b; it < G; it += kMmaWarps) {
+        for (int it = j; it < G; it += kMmaWarps) {
             const int s = it % kStages, use = it / kStages;
-            const int tuse = it / kMmaWarps;
+            const int b = it % kTmemBufs, tuse = it / kTmemBufs;
             // full_b, and the accumulator's release by the fold (its first use
             // waits on nothing: the phase before the first reads as complete)
             const bool ok = __all_sync(0xFFFFFFFFu,
@@ -251,7 +254,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             committed = it;
         }
         if (*abort_flag && committed >= 0 && lane == 0) {   // MMAs and their arrivals must land before exit
-            if (!mbar_wait(&ctl->tmem_full[b], (committed / kMmaWarps) & 1) && prm.status)
+            if (!mbar_wait(&ctl->tmem_full[committed % kTmemBufs], (committed / kTmemBufs) & 1) && prm.status)
                 atomicOr(prm.status, kStatusDrain);
             if (committed + kStages < G &&
                 !mbar_wait(&ctl->empty[committed % kStages], (committed / kStages) & 1) && prm.status)
@@ -332,7 +335,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
         bool bad = false;
         for (int it = fs; it < G; it += kFoldSets) {
-            const int b = it % kMmaWarps, tuse = it / kMmaWarps;
+            const int b = it % kTmemBufs, tuse = it / kTmemBufs;
             const int r = it % kSzfRing, ruse = it / kSzfRing;
             const int rr = it % kRowRing, rruse = it / kRowRing;
             if (!wait3_or_abort(&ctl->row_full[rr], rruse & 1, &ctl->szf_full[r], ruse & 1,
