@@ -308,9 +308,13 @@ NCU_TRAFFIC = {
         src="w4a8_rotated_int4_gb300/csrc/pq_gemm_skinny.cu",
         sha256="426b5645f0fb6237a62cbfb0fc095d2169790ab0b211429bb432fac2eec9a396"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=74486784 + 41364736, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        bytes=72338688 + 39974912, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
         src="w4a8_rotated_int4_gb300/csrc/pq_gemm_tc.cu",
-        sha256="fb8c22e9b78aff60dc2a4e3a5f1aae92c36e41de152d218c52462fa0f95b6f1f"),
+        sha256="dc07fd9e6f3ef14522a8bea3187da443b8aba022c0205ee7b5e3934326392312"),
+    ("pq_gemm_tcn", "decode:16"): dict(
+        bytes=47473408 + 256, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
+        src="w4a8_rotated_int4_gb300/csrc/pq_gemm_tcn.cu",
+        sha256="a6def0ed26f0281e978960564d0a85ce62bd9a102ae583ce1ad41deec4095cde"),
 }
 
 
