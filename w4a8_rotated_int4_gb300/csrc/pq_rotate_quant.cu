@@ -37,27 +37,32 @@ namespace {
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-    float f;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f) : "r"(addr) : "memory");
+__device__ __forceinline__ float2 lds_f32x2(uint32_t addr) {
+    float2 f;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(f.x), "=f"(f.y) : "r"(addr) : "memory");
     return f;
 }
-__device__ __forceinline__ void sts_f32(uint32_t addr, float f) {
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(f) : "memory");
+__device__ __forceinline__ void sts_f32x2(uint32_t addr, float2 f) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(f.x), "f"(f.y) : "memory");
 }
 
-constexpr int kTok = 32;              // tokens per CTA (lane = token)
-constexpr int kWarps = 4;             // warp w rotates pairs 16w..16w+15 of each layer
-constexpr int kThreads = kTok * kWarps;
+// Many tokens: lane l holds tokens 2l and 2l+1 of the CTA's 64 (adjacent, so
+// every shared-memory access moves both with one 8-byte instruction); warp w
+// rotates pairs 16w..16w+15 of every layer.
+constexpr int kTok = 64;              // tokens per CTA
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kXsStride = 65;         // words per staged x row (64 + 1 pad)
 constexpr int kCodeStride = 144;      // bytes per staged code row
 
 struct __align__(16) Smem {
-    float v[128][kTok];               // 16 KB, v[k][token]
-    uint32_t xs[kTok][kXsStride];     // x tile, two bf16 per word
-    float4 rec[8][64];                // records of (p, g): byte offsets of v[i], v[j]; cos; sin
+    float2 v[128][kTok / 2];          // 32 KB, v[k][token pair]: (token 2l, token 2l+1)
+    union {
+        uint32_t xs[kTok][kXsStride]; // x tile, two bf16 per word (before the layers)
+        uint8_t codes[kTok][kCodeStride];   // e4m3 codes (after them)
+    };
+    uint2 rec[8][64];                 // records of (p, g): byte offsets of v[i] | v[j] << 16; f16 cos | sin << 16
     float cs[128];
-    uint8_t codes[kTok][kCodeStride];
     float red_max[kWarps][kTok];
     int red_sum[kWarps][kTok];
 };
@@ -101,29 +106,30 @@ __device__ __forceinline__ void givens(float c, float s, float &vi, float &vj) {
     vj = nj;
 }
 
-// Many tokens: lane = token, warp w rotates pairs 16w..16w+15 of every layer.
 __global__ void __launch_bounds__(kThreads)
 rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P,
                     const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
                     uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
-    __shared__ Smem sm;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m0 = blockIdx.x * kTok, g = blockIdx.y, G = K >> 7;
     const float inv448 = __fdiv_rn(1.0f, 448.0f);
     pdl_wait();        // x may be the previous kernel's output
     pdl_trigger();
 
-    // x tile: issued together with the first partition's records and scales
-    uint4 xv[4];
+    // x tile (64 rows of 256 bytes): issued together with the records and scales
+    uint4 xv[8];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
+    for (int it = 0; it < 8; ++it) {
         const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
         xv[it] = make_uint4(0, 0, 0, 0);
         if (m0 + row < M)
             xv[it] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + row) * ldx + 128 * g) + q);
     }
 
-    for (int p = 0; p < P; ++p) {
+    {
+        const int p = blockIdx.z;      // one partition per CTA: partitions run side by side
         uint4 rv[2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
@@ -131,15 +137,13 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
             rv[it] = __ldg(reinterpret_cast<const uint4 *>(rec + ((size_t)(p * 8 + r) * G + g) * 64) + q);
         }
         const uint16_t csv = __ldg(cs + (size_t)p * K + 128 * g + tid);
-        if (p == 0) {
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
-                uint32_t *d = &sm.xs[row][4 * q];
-                d[0] = xv[it].x; d[1] = xv[it].y; d[2] = xv[it].z; d[3] = xv[it].w;
-            }
+        for (int it = 0; it < 8; ++it) {
+            const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
+            uint32_t *d = &sm.xs[row][4 * q];
+            d[0] = xv[it].x; d[1] = xv[it].y; d[2] = xv[it].z; d[3] = xv[it].w;
         }
-        // decoded records: shared-memory byte offsets of v[i][0], v[j][0]; cos, sin in fp32
+        // decoded records: shared-memory byte offsets of v[i][0], v[j][0]; f16 cos, sin
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
@@ -147,10 +151,7 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t i = w0[h] & 0xFF, j = (w0[h] >> 8) & 0xFF;
-                sm.rec[r][2 * q + h] = make_float4(__uint_as_float(i * (uint32_t)(kTok * 4)),
-                                                   __uint_as_float(j * (uint32_t)(kTok * 4)),
-                                                   half_to_float((uint16_t)(w1[h] & 0xFFFF)),
-                                                   half_to_float((uint16_t)(w1[h] >> 16)));
+                sm.rec[r][2 * q + h] = make_uint2(i * (uint32_t)(kTok * 4) | (j * (uint32_t)(kTok * 4)) << 16, w1[h]);
             }
         }
         sm.cs[tid] = half_to_float(csv);
@@ -160,95 +161,101 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
 #pragma unroll 4
         for (int q = 0; q < 16; ++q) {
             const int kw = 16 * warp + q;                 // word index: channels 2kw, 2kw+1
-            const uint32_t wv = sm.xs[lane][kw];
-            sm.v[2 * kw][lane] = __fmul_rn(bf16lo(wv), sm.cs[2 * kw]);
-            sm.v[2 * kw + 1][lane] = __fmul_rn(bf16hi(wv), sm.cs[2 * kw + 1]);
+            const uint32_t w0 = sm.xs[2 * lane][kw], w1 = sm.xs[2 * lane + 1][kw];
+            sm.v[2 * kw][lane] = make_float2(__fmul_rn(bf16lo(w0), sm.cs[2 * kw]),
+                                             __fmul_rn(bf16lo(w1), sm.cs[2 * kw]));
+            sm.v[2 * kw + 1][lane] = make_float2(__fmul_rn(bf16hi(w0), sm.cs[2 * kw + 1]),
+                                                 __fmul_rn(bf16hi(w1), sm.cs[2 * kw + 1]));
         }
         __syncthreads();
 
         // eight Givens layers; the pairs of one layer are disjoint, so a warp
-        // reads all 32 operands of its 16 pairs before writing any result
+        // reads all operands of a batch of pairs before writing any result
         const uint32_t vlane = smem_addr(&sm.v[0][lane]);
         for (int r = 0; r < 8; ++r) {
-            float vi[16], vj[16], cc[16], ss[16];
-            uint32_t ai[16], aj[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const float4 rr = sm.rec[r][16 * warp + q];
-                ai[q] = vlane + __float_as_uint(rr.x);
-                aj[q] = vlane + __float_as_uint(rr.y);
-                cc[q] = rr.z;
-                ss[q] = rr.w;
-                vi[q] = lds_f32(ai[q]);
-                vj[q] = lds_f32(aj[q]);
-            }
+            for (int half = 0; half < 2; ++half) {
+                float2 vi[8], vj[8];
+                float cc[8], ss[8];
+                uint32_t ai[8], aj[8];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                givens(cc[q], ss[q], vi[q], vj[q]);
-                sts_f32(ai[q], vi[q]);
-                sts_f32(aj[q], vj[q]);
+                for (int q = 0; q < 8; ++q) {
+                    const uint2 rr = sm.rec[r][16 * warp + 8 * half + q];
+                    ai[q] = vlane + (rr.x & 0xFFFFu);
+                    aj[q] = vlane + (rr.x >> 16);
+                    cc[q] = half_to_float((uint16_t)(rr.y & 0xFFFFu));
+                    ss[q] = half_to_float((uint16_t)(rr.y >> 16));
+                    vi[q] = lds_f32x2(ai[q]);
+                    vj[q] = lds_f32x2(aj[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    givens(cc[q], ss[q], vi[q].x, vj[q].x);
+                    givens(cc[q], ss[q], vi[q].y, vj[q].y);
+                    sts_f32x2(ai[q], vi[q]);
+                    sts_f32x2(aj[q], vj[q]);
+                }
             }
             __syncthreads();
         }
 
-        // quantise: warp w takes channels 32w..32w+31 of every token
-        float vals[32];
-        float amax = 0.0f;
+        // quantise: warp w takes channels 32w..32w+31 of both tokens of the lane
+        float2 vals[32];
+        float amax0 = 0.0f, amax1 = 0.0f;
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
             vals[q] = sm.v[32 * warp + q][lane];
-            amax = fmaxf(amax, fabsf(vals[q]));
+            amax0 = fmaxf(amax0, fabsf(vals[q].x));
+            amax1 = fmaxf(amax1, fabsf(vals[q].y));
         }
-        sm.red_max[warp][lane] = amax;
+        sm.red_max[warp][2 * lane] = amax0;
+        sm.red_max[warp][2 * lane + 1] = amax1;
         __syncthreads();
-        amax = fmaxf(fmaxf(sm.red_max[0][lane], sm.red_max[1][lane]),
-                     fmaxf(sm.red_max[2][lane], sm.red_max[3][lane]));
-        const float scale = __fmul_rn(amax, inv448);
-        uint32_t packed[8];
-        int sum512 = 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            uint32_t word = 0;
-            if (scale != 0.0f) {
-                const uint32_t c01 = e4m3x2(__fdiv_rn(vals[4 * q + 1], scale),
-                                            __fdiv_rn(vals[4 * q], scale));
-                const uint32_t c23 = e4m3x2(__fdiv_rn(vals[4 * q + 3], scale),
-                                            __fdiv_rn(vals[4 * q + 2], scale));
-                word = c01 | (c23 << 16);
+        for (int t = 0; t < 2; ++t) {
+            const int tok = 2 * lane + t;
+            const float amax = fmaxf(fmaxf(sm.red_max[0][tok], sm.red_max[1][tok]),
+                                     fmaxf(sm.red_max[2][tok], sm.red_max[3][tok]));
+            const float scale = __fmul_rn(amax, inv448);
+            uint32_t packed[8];
+            int sum512 = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint32_t word = 0;
+                if (scale != 0.0f) {
+                    const float e0 = t ? vals[4 * q].y : vals[4 * q].x, e1 = t ? vals[4 * q + 1].y : vals[4 * q + 1].x;
+                    const float e2 = t ? vals[4 * q + 2].y : vals[4 * q + 2].x, e3 = t ? vals[4 * q + 3].y : vals[4 * q + 3].x;
+                    const uint32_t c01 = e4m3x2(__fdiv_rn(e1, scale), __fdiv_rn(e0, scale));
+                    const uint32_t c23 = e4m3x2(__fdiv_rn(e3, scale), __fdiv_rn(e2, scale));
+                    word = c01 | (c23 << 16);
+                }
+                packed[q] = word;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) sum512 += e4m3_times512((word >> (8 * b)) & 0xFF);
             }
-            packed[q] = word;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) sum512 += e4m3_times512((word >> (8 * b)) & 0xFF);
+            uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[tok][32 * warp]);
+            cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            sm.red_sum[warp][tok] = sum512;
+            if (warp == 0 && m0 + tok < M) asg[((size_t)p * G + g) * M + m0 + tok] = scale;
         }
-        uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[lane][32 * warp]);
-        cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        sm.red_sum[warp][lane] = sum512;
         __syncthreads();
 
-        // stores: 128-byte code rows, then one scale and one row-sum per token
+        // stores: 128-byte code rows, then one row-sum per token
         for (int c = tid; c < kTok * 8; c += kThreads) {
             const int row = c >> 3, q = c & 7;
             if (m0 + row < M)
                 reinterpret_cast<uint4 *>(a + ((size_t)p * M + m0 + row) * K + 128 * g)[q] =
                     *reinterpret_cast<const uint4 *>(&sm.codes[row][16 * q]);
         }
-        if (m0 + lane < M) {
-            const size_t o = ((size_t)p * G + g) * M + m0 + lane;
-            if (warp == 0) asg[o] = scale;
-            if (warp == 1) {
-                const int s = sm.red_sum[0][lane] + sm.red_sum[1][lane] + sm.red_sum[2][lane] +
-                              sm.red_sum[3][lane];
-                rs[o] = __fmul_rn(__int2float_rn(s), 1.0f / 512.0f);
-            }
+        if (tid < kTok && m0 + tid < M) {
+            const size_t o = ((size_t)p * G + g) * M + m0 + tid;
+            const int s = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
+            rs[o] = __fmul_rn(__int2float_rn(s), 1.0f / 512.0f);
         }
-        __syncthreads();
     }
 }
 
-// Few tokens (decode): 64 threads per token, thread t owns pair t of every
-// layer (its 8 records live in registers) and channels 2t, 2t+1 for the
-// quantisation; grid.z runs the partitions side by side.
 template <int T>
 __global__ void __launch_bounds__(64 * T)
 rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
@@ -344,9 +351,13 @@ pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const
             e = launch_pdl(rotate_quant_small_kernel<4>, dim3((M + 3) / 4, K / 128, P), dim3(256), 0, st, xp,
                            M, K, ldx, rp, cp, ap, asg, rs);
     } else {
-        const dim3 grid((M + kTok - 1) / kTok, K / 128);
+        const dim3 grid((M + kTok - 1) / kTok, K / 128, P);
         if (grid.x > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_rotate_quant: M = %d too large", M);
-        e = launch_pdl(rotate_quant_kernel, grid, dim3(kThreads), 0, st, xp, M, K, ldx, P, rp, cp, ap, asg, rs);
+        e = cudaFuncSetAttribute(rotate_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(Smem));
+        if (e == cudaSuccess)
+            e = launch_pdl(rotate_quant_kernel, grid, dim3(kThreads), sizeof(Smem), st, xp, M, K, ldx, P, rp,
+                           cp, ap, asg, rs);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_quant launch: %s", cudaGetErrorString(e));
