@@ -364,30 +364,49 @@ def summarize(wl, r, steps, peaks):
 # ---------------------------------------------------------------- oracle timing
 class OracleSample:
     """The CPU oracle (as it stands) on a bounded sample of the workload: the
-    full prologue for all tokens and the fp64 GEMM for a slice of output
-    columns, scaled to all columns.  Inputs are generated and packed once."""
+    prologue for a slice of the tokens and the fp64 GEMM for a slice of the
+    output columns, both scaled to the whole workload.  The slices are sized
+    so one step takes about `step_budget_s`.  Inputs are generated and packed
+    once."""
 
-    def __init__(self, name, M=None, budget_s=10.0):
+    def __init__(self, name, M=None, step_budget_s=1.0):
         import oracle
         self.oracle = oracle
         c, self.label = describe(name, M)
         self.c = c
         self.prob = pqgen.make_problem(**c)
         self.tab = oracle.pack(self.prob)
-        N = c["N"]
-        self.ncols = 128
-        # size the column slice so one step's GEMM takes about budget_s / 4
+        N, Mt = c["N"], c["M"]
+        # token slice for the prologue: halve until it fits half the budget
+        self.mtok = Mt
+        while True:
+            t = self._time_prologue()
+            if t <= step_budget_s / 2 or self.mtok == 1:
+                break
+            self.mtok = max(1, self.mtok // 2)
+        self.a, self.asg, self.rs = self.oracle.rotate_quant(self.prob.x, self.prob.cs, self.tab["rec"])
+        # column slice for the GEMM (all tokens, codes from the full prologue)
+        self.ncols = 8
         while True:
             self._slice()
             t = self._gemm()
-            if t > budget_s / 4 or self.ncols >= N:
+            if t > step_budget_s / 4 or self.ncols >= N:
                 break
-            self.ncols = min(N, self.ncols * 4)
+            self.ncols = min(N, self.ncols * 2)
+        while self.ncols > 8 and t > step_budget_s / 2:
+            self.ncols //= 2
+            self._slice()
+            t = self._gemm()
+
+    def _time_prologue(self):
+        x = np.ascontiguousarray(self.prob.x[:self.mtok])
+        t0 = time.perf_counter()
+        self.oracle.rotate_quant(x, self.prob.cs, self.tab["rec"])
+        return time.perf_counter() - t0
 
     def _slice(self):
         self.codes = np.ascontiguousarray(self.tab["codes"][:, :self.ncols])
         self.sz = np.ascontiguousarray(self.tab["sz"][:, :self.ncols])
-        self.a, self.asg, self.rs = self.oracle.rotate_quant(self.prob.x, self.prob.cs, self.tab["rec"])
 
     def _gemm(self):
         pb = min(self.prob.pb1, self.ncols), min(self.prob.pb2, self.ncols)
@@ -396,15 +415,13 @@ class OracleSample:
         return time.perf_counter() - t0
 
     def step_us(self):
-        t0 = time.perf_counter()
-        self.a, self.asg, self.rs = self.oracle.rotate_quant(self.prob.x, self.prob.cs, self.tab["rec"])
-        t_pro = time.perf_counter() - t0
-        t_g = self._gemm()
-        return (t_pro + t_g * (self.c["N"] / self.ncols)) * 1e6
+        t_pro = self._time_prologue() * (self.c["M"] / self.mtok)
+        t_g = self._gemm() * (self.c["N"] / self.ncols)
+        return (t_pro + t_g) * 1e6
 
     def describe(self):
-        return ("prologue on all %d tokens + fp64 GEMM on %d of %d output columns per step, "
-                "scaled to all columns" % (self.c["M"], self.ncols, self.c["N"]))
+        return ("prologue on %d of %d tokens + fp64 GEMM on %d of %d output columns per step, "
+                "both scaled to the whole workload" % (self.mtok, self.c["M"], self.ncols, self.c["N"]))
 
     def cores(self):
         return self.oracle.num_threads()
@@ -447,7 +464,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        orc = OracleSample(name, M, budget_s=4.0)
+        # the whole --warmup W --steps K run stays near 90 s of host time
+        orc = OracleSample(name, M, step_budget_s=min(1.0, 90.0 / max(1, args.steps + args.warmup)))
         per_step = []
         for i in range(args.warmup + args.steps):
             us = orc.step_us()
@@ -528,7 +546,7 @@ def main():
         "peaks": peaks,
     }
     if not args.no_cpu_baseline:
-        orc = OracleSample(name, M)
+        orc = OracleSample(name, M, step_budget_s=4.0)
         us = float(np.mean([orc.step_us() for _ in range(3)]))
         line["cpu_baseline"] = {"value": round(us, 1), "unit": "us", "cores": orc.cores(),
                                 "kind": "oracle", "sample": orc.describe() + ", mean of 3"}
