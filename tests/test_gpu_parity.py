@@ -370,3 +370,23 @@ def test_gemm_repeated_graph_launches_status_clean(pq, orc, path):
     assert int(st.abs().sum().item()) == 0, "a bounded wait gave up: %s" % st.flatten().tolist()
     for j in range(C):
         assert torch.equal(ys[j], ref), j
+
+
+@pytest.mark.parametrize("K", [1152, 2176])
+@pytest.mark.parametrize("M", [1, 16])
+def test_gemm_tail_slabs_repeated(pq, orc, M, K):
+    """K/128 one past a multiple of the kernels' stage counts, so the last slab
+    reuses a stage while other warps finish: twenty launches per path must
+    all match the fp64 oracle and each other bit for bit."""
+    N = 512
+    prob = pqgen.make_problem(M, K, N, seed=13)
+    L = Problem(pq, orc, prob, check_pack=False)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    torch.cuda.synchronize()
+    y64 = orc.gemm_f64(a.cpu().numpy(), asg.cpu().numpy(), rs.cpu().numpy(), L.t["codes"], L.t["sz"], N, N)
+    for name, fn in gemm_paths(pq, M):
+        first = run_gemm(fn, a, asg, rs, L, N, N, M, N)
+        assert_close(first, y64, "%s M=%d K=%d" % (name, M, K))
+        for _ in range(20):
+            y = run_gemm(fn, a, asg, rs, L, N, N, M, N)
+            assert np.array_equal(y, first), name

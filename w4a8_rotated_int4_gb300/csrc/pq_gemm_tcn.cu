@@ -54,12 +54,14 @@ constexpr int kRowRing = 16;      // per-token scales, copied by the row warp (l
 // A single thread issues an MMA only every ~100 cycles, so four MMA warps
 // (one per SM sub-partition) take turns: warp j issues the slabs it = j mod 4
 // into TMEM accumulator j.
-constexpr int kTmaWarp = 0, kRowWarp = 1;
-constexpr int kMmaWarp0 = 2, kMmaWarps = 4;               // warps 2..5, one per sub-partition
+// TMA: issuing a tensor copy costs one thread ~120 cycles, so kTmaWarps
+// producers take the slabs in turn (warp t fills the stages s = t mod kTmaWarps)
+constexpr int kTmaWarps = 2, kRowWarp = kTmaWarps;
+constexpr int kMmaWarp0 = kRowWarp + 1, kMmaWarps = 4;    // warps 3..6, one per sub-partition
 // expansion: kExpGroups groups of 4 warps, group e expands slabs it = e mod kExpGroups,
 // so that several slabs are expanded at once
-constexpr int kExpWarp0 = kMmaWarp0 + kMmaWarps, kExpWarps = 4, kExpGroups = 4;   // warps 6..21
-// fold: kFoldSets sets of 4 warps (warps 22..29), set f folds the slabs
+constexpr int kExpWarp0 = kMmaWarp0 + kMmaWarps, kExpWarps = 4, kExpGroups = 4;   // warps 7..22
+// fold: kFoldSets sets of 4 warps (warps 23..30), set f folds the slabs
 // it = f mod kFoldSets into accumulators of its own, summed at the end; warp w
 // reads TMEM lane quarter w % 4 (each set covers all four)
 constexpr int kFoldWarp0 = kExpWarp0 + kExpWarps * kExpGroups, kFoldWarps = 4, kFoldSets = 2;
@@ -68,7 +70,8 @@ constexpr int kThreads = (kFoldWarp0 + kFoldWarps * kFoldSets) * 32;
 // never wait for a barrier's next use before it has seen the previous one.  Each
 // stage and each scale slot is therefore always served by the same expand group
 // and the same MMA warp, which take their slabs in order.
-static_assert(kStages % kExpGroups == 0 && kStages % kMmaWarps == 0, "stage ownership");
+static_assert(kStages % kExpGroups == 0 && kStages % kMmaWarps == 0 && kStages % kTmaWarps == 0,
+              "stage ownership");
 // TMEM accumulators: slab it uses buffer it % kTmemBufs, issued by MMA warp
 // it % kMmaWarps and folded by set it % kFoldSets (each buffer keeps its owners)
 constexpr int kTmemBufs = 8;
@@ -178,25 +181,28 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const uint32_t tmem = ctl->tmem_base;
     pdl_trigger();     // the next kernel may start its own load-time prefetch
 
-    if (warp == kTmaWarp) {
-        // ------------------------------------------------ TMA producer
+    if (warp < kTmaWarps) {
+        // ------------------------------------------------ TMA producers
         if (lane == 0) {
+            const int tw = warp;
             prefetch_map(&tmA);
             prefetch_map(&tmB);
             prefetch_map(&tmS);
             // first stages: weights and SZ (load-time tables) before the
             // preceding kernel has finished, activations after pdl_wait
             const int pre = G < kStages ? G : kStages;
-            for (int it = 0; it < pre; ++it) {
+            int last = -1;             // the last slab this producer issued
+            for (int it = tw; it < pre; it += kTmaWarps) {
                 mbar_arrive_expect_tx(&ctl->full_tma[it], kTxBytes);
                 tma_load_2d(stg[it].bp, &tmB, it * (BK / 2), n0, &ctl->full_tma[it]);
                 tma_load_2d(stg[it].sz, &tmS, 8 * it, n0 / 8, &ctl->full_tma[it]);
             }
             pdl_wait();
-            for (int it = 0; it < pre; ++it)
+            for (int it = tw; it < pre; it += kTmaWarps) {
                 tma_load_3d(stg[it].aa, &tmA, it * BK, 0, p, &ctl->full_tma[it]);
-            int issued = pre;
-            for (int it = pre; it < G; ++it) {
+                last = it;
+            }
+            for (int it = pre + tw; it < G; it += kTmaWarps) {   // pre is a multiple of kTmaWarps here
                 const int s = it % kStages, use = it / kStages;
                 if (!wait_or_abort(&ctl->empty[s], (use - 1) & 1, abort_flag)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
@@ -206,12 +212,11 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 tma_load_2d(stg[s].bp, &tmB, it * (BK / 2), n0, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].sz, &tmS, 8 * it, n0 / 8, &ctl->full_tma[s]);
                 tma_load_3d(stg[s].aa, &tmA, it * BK, 0, p, &ctl->full_tma[s]);
-                issued = it + 1;
+                last = it;
             }
-            if (*abort_flag) {   // let issued copies land before shared memory is released
-                for (int s = 0; s < kStages && s < issued; ++s) {
-                    const int last = (issued - 1 - s) / kStages;
-                    if (!mbar_wait(&ctl->full_tma[s], last & 1) && prm.status)
+            if (*abort_flag) {   // let this producer's copies land before shared memory is released
+                for (int it = last; it >= 0 && it > last - kStages; it -= kTmaWarps) {
+                    if (!mbar_wait(&ctl->full_tma[it % kStages], (it / kStages) & 1) && prm.status)
                         atomicOr(prm.status, kStatusDrain);
                 }
             }
@@ -366,9 +371,12 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 mbar_arrive(&ctl->row_empty[rr]);
             }
         }
-        // the sets meet in shared memory (stage 0's expanded-weight buffer is
-        // free: every MMA has completed once each set has seen its last slab)
+        // the sets meet in shared memory, in stage 0's expanded-weight buffer:
+        // it is free only once BOTH sets have seen their last slab (then every
+        // expansion and MMA has completed) -- a set that finishes first must
+        // not write while the other set's last slab may still be in stage 0
         float *part = reinterpret_cast<float *>(stg[0].bx);      // [kFoldSets - 1][MT][NN]
+        asm volatile("bar.sync 1, %0;" ::"n"(kFoldWarps * kFoldSets * 32) : "memory");
         if (fs > 0) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) part[((fs - 1) * MT + m) * NN + n] = acc[m];
