@@ -428,15 +428,30 @@ class OracleSample:
 
 
 # ---------------------------------------------------------------- main
-def dist_init():
+def dist_init(backend="nccl"):
+    """(rank, world size, torch.distributed or None).  Ranks are replicas:
+    the layer needs no exchange, so the only collectives are the barriers
+    around the timed region and the max of the per-rank times."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws <= 1:
         return 0, 1, None
     import torch.distributed as dist
     rank = int(os.environ.get("RANK", "0"))
-    backend = "nccl"
     dist.init_process_group(backend=backend)
     return rank, ws, dist
+
+
+def combine_ranks(total_ms, steps, ws, dist, device):
+    """The job's time for `steps` steps is the slowest rank's; the reported
+    value is that time per step divided by the number of replicas (each ran
+    `steps` steps, so the whole job finished ws * steps of them)."""
+    if dist:
+        import torch
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    step_us = total_ms * 1e3 / steps
+    return total_ms, step_us / ws
 
 
 def main():
@@ -499,13 +514,8 @@ def main():
     wl = Workload(pq, torch, name, M, dev)
     sampler = ClockSampler(local) if rank == 0 else None
     r = time_workload(pq, torch, wl, args.steps, args.warmup, stream, barrier, sampler)
-    total_ms = r["total_ms"]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = combine_ranks(r["total_ms"], args.steps, ws, dist, dev)
     step_us = total_ms * 1e3 / args.steps
-    value = step_us / ws            # whole-job time per step: ws replicas each ran `steps` steps
     e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else e2e_workload(
         pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, dev)
     head = summarize(wl, dict(r, total_ms=total_ms), args.steps, peaks)
