@@ -13,9 +13,19 @@
 // 8 kw + l/4) and keeps that slice of the MT activation rows in registers for
 // the whole launch (as f16 pairs; e4m3 converts to f16 exactly).  A producer
 // warp streams each octet's weight rows (8 x K/2 contiguous bytes) and its SZ
-// words (G x 32 contiguous bytes) into a 2..4-stage shared-memory ring with bulk copies
+// words (G x 32 contiguous bytes) into a shared-memory ring with bulk copies
 // (cp.async.bulk + mbarrier transaction counts), so the weight stream is
 // independent of register pressure.
+//
+// Consumer groups.  A CTA may hold up to three groups of nkw compute warps
+// that share its producer and its ring: octet i of the CTA's run goes to group
+// i mod ngrp and ring stage i mod S (S a multiple of ngrp, so a stage always
+// serves the same group and no waiter can fall two phases behind).  One CTA
+// per SM with three groups beats three one-group CTAs: the producer issues the
+// SM's octets in one order, they land in about that order, and the groups take
+// them round robin, so the SM's groups finish within about one octet of each
+// other (three separate CTAs on an SM were measured to finish up to 2.5 us
+// apart, the first one served taking its whole run ahead of the others).
 //
 // Arithmetic.  A weight nibble c is turned into an f16 *subnormal* whose bits
 // are the nibble (value c * 2^-24) by one AND per two nibbles -- no integer to
@@ -55,7 +65,7 @@ struct SkinnyParams {
     __nv_bfloat16 *y;
     unsigned int *status;
     int M, N, K, G, pb1, pb2, ldy;
-    int oct_per_cta, n_oct, nkw, stages;
+    int oct_per_cta, n_oct, nkw, ngrp, stages;
     uint32_t stage_bytes, w_bytes;
 };
 
@@ -108,10 +118,48 @@ __device__ __forceinline__ void split_step(const float (&in)[NC], float (&out)[N
     }
 }
 
+// The producer: lane 0 of the last warp streams the CTA's octets, in order,
+// into the S-stage ring: each octet's weight rows (8 x K/2 contiguous bytes)
+// and its SZ words (G x 32 contiguous bytes) with two bulk copies completing
+// on full[s]; a stage is refilled once its consumer group has released it on
+// empty[s].  (Weights and SZ words are load-time tables, not written by the
+// preceding kernel, so they stream before its completion.)
+__device__ __forceinline__ void produce_octets(const SkinnyParams &prm, uint8_t *smem, uint64_t *full,
+                                               uint64_t *empty, volatile int *abort_flag, int oct0,
+                                               int noct) {
+    const int S = prm.stages, K = prm.K, G = prm.G;
+    int issued = 0;
+    for (int i = 0, s = 0, use = 0; i < noct; ++i) {     // s = i mod S, use = i / S
+        if (i > 0 && ++s == S) {
+            s = 0;
+            ++use;
+        }
+        if (*abort_flag) break;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+            if (prm.status) atomicOr(prm.status, kStatusWaitEmpty);
+            *abort_flag = 1;
+            break;
+        }
+        uint8_t *st = smem + (size_t)s * prm.stage_bytes;
+        const int o = oct0 + i;
+        mbar_arrive_expect_tx(&full[s], prm.stage_bytes);
+        bulk_g2s(st, prm.w + (size_t)o * 8 * (K / 2), prm.w_bytes, &full[s]);
+        bulk_g2s(st + prm.w_bytes, prm.sz + (size_t)o * G * 8, 32u * (uint32_t)G, &full[s]);
+        issued = i + 1;
+    }
+    // on abort: let every copy already issued land before shared memory is released
+    if (*abort_flag) {
+        for (int s = 0; s < S && s < issued; ++s) {
+            const int last_use = (issued - 1 - s) / S;
+            if (!mbar_wait(&full[s], last_use & 1) && prm.status) atomicOr(prm.status, kStatusDrain);
+        }
+    }
+}
+
 template <int MT>
 __global__ void skinny_kernel(const SkinnyParams prm) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int nkw = prm.nkw, S = prm.stages;
+    const int nkw = prm.nkw, S = prm.stages, ngrp = prm.ngrp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * prm.stage_bytes);
     uint64_t *empty = full + S;
@@ -136,39 +184,11 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
     __syncthreads();
 
     pdl_trigger();
-    if (warp == nkw) {
-        // ---------------- producer warp ----------------
-        // (weights and SZ words are load-time tables, not written by the
-        // preceding kernel, so they stream before its completion)
-        int issued = 0;
-        if (lane == 0) {
-            for (int i = 0; i < noct; ++i) {
-                const int s = i % S, use = i / S;
-                if (*abort_flag) break;
-                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-                    if (prm.status) atomicOr(prm.status, kStatusWaitEmpty);
-                    *abort_flag = 1;
-                    break;
-                }
-                uint8_t *st = smem + (size_t)s * prm.stage_bytes;
-                const int o = oct0 + i;
-                mbar_arrive_expect_tx(&full[s], prm.stage_bytes);
-                bulk_g2s(st, prm.w + (size_t)o * 8 * (K / 2), prm.w_bytes, &full[s]);
-                bulk_g2s(st + prm.w_bytes, prm.sz + (size_t)o * G * 8, 32u * (uint32_t)G, &full[s]);
-                issued = i + 1;
-            }
-            // on abort: let every copy already issued land before shared memory is released
-            if (*abort_flag) {
-                for (int s = 0; s < S && s < issued; ++s) {
-                    const int last_use = (issued - 1 - s) / S;
-                    if (!mbar_wait(&full[s], last_use & 1) && prm.status)
-                        atomicOr(prm.status, kStatusDrain);
-                }
-            }
-        }
+    if (warp == ngrp * nkw) {
+        if (lane == 0) produce_octets(prm, smem, full, empty, abort_flag, oct0, noct);
     } else {
         // ---------------- compute warps ----------------
-        const int kw = warp;
+        const int grp = warp / nkw, kw = warp - grp * nkw;
         const int k0 = 1024 * kw + 32 * lane;
         const bool kvalid = k0 < K;
         const int g = kvalid ? (k0 >> 7) : 0;
@@ -177,8 +197,13 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
         // per row of this lane's group: 2^24 asg, asg * rs and 8 * asg * rs
         float asg24_r[MT], ar_r[MT], ar8_r[MT];
         int cur_p = -1;
-        for (int i = 0; i < noct; ++i) {
-            const int s = i % S, use = i / S;
+        // s = i mod S and use = i / S, stepped without a division (S is a
+        // multiple of ngrp, so s wraps back to grp)
+        for (int i = grp, s = grp, use = 0; i < noct; i += ngrp) {
+            if (i > grp && (s += ngrp) >= S) {
+                s -= S;
+                ++use;
+            }
             const int n0 = (oct0 + i) * 8;
             const int p = (n0 >= prm.pb1) + (n0 >= prm.pb2);
             if (p != cur_p) {
@@ -297,57 +322,68 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
     }
 }
 
-// Whether the MT-row instantiation fits the register file with nkw + 1 warps.
-template <int MT>
-bool fits_registers(int nkw) {
+using SkinnyFn = void (*)(SkinnyParams);
+
+// Registers per thread (allocation granule of 8) and the thread limit of a
+// kernel, or false if its attributes cannot be read.
+bool kernel_limits(SkinnyFn k, int *regs, int *max_threads) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, skinny_kernel<MT>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    const int regs = (fa.numRegs + 7) / 8 * 8;
-    return regs * 32 * (nkw + 1) <= 65536 && 32 * (nkw + 1) <= fa.maxThreadsPerBlock;
+    *regs = (fa.numRegs + 7) / 8 * 8;
+    *max_threads = fa.maxThreadsPerBlock;
+    return true;
 }
 
-template <int MT>
-pq_status launch_mt(SkinnyParams prm, int sm_count, cudaStream_t stream) {
-    const int threads = 32 * (prm.nkw + 1);
-    const int mtiles = (prm.M + MT - 1) / MT;
+// Whether kernel k fits the register file with `warps` warps.
+bool fits_registers(SkinnyFn k, int warps) {
+    int regs, max_threads;
+    if (!kernel_limits(k, &regs, &max_threads)) return false;
+    return regs * 32 * warps <= 65536 && 32 * warps <= max_threads;
+}
+
+// Launch kernel k (mt rows per M-tile) over the octet ring.  Three consumer
+// groups per SM (the more compute warps per SM, the more load latency is
+// hidden): preferably one CTA with three groups, else fewer groups per CTA
+// and more CTAs, each group with 2..4 ring stages; shared memory and
+// registers per SM are kept under their limits.  CTAs per M-tile: a whole
+// multiple of the SM count when there are enough octets, each with a balanced
+// octet range.
+pq_status launch_ring(SkinnyFn k, int mt, SkinnyParams prm, int sm_count, cudaStream_t stream) {
+    const int mtiles = (prm.M + mt - 1) / mt;
     const int sms = sm_count > 0 ? sm_count : 1;
-    // Up to three CTAs per SM (the more compute warps per SM, the more load
-    // latency is hidden), each with its own 2..4-stage ring; shared memory per
-    // SM is kept under kSmemBudget.  CTAs per M-tile: a whole multiple of the
-    // SM count when there are enough octets, each with a balanced octet range.
-    int per_sm = 3;
     auto smem_for = [&](int stages, int opc) {
         return (size_t)stages * prm.stage_bytes + 16 * (size_t)stages + 16 +
-               (size_t)prm.nkw * MT * opc * 8 * 4;
+               (size_t)prm.nkw * mt * opc * 8 * 4;
     };
-    for (;;) {
-        int ctas = sms * per_sm / mtiles;
-        if (ctas < 1) ctas = 1;
-        if (ctas > prm.n_oct) ctas = prm.n_oct;
-        const int opc = (prm.n_oct + ctas - 1) / ctas;
-        int stages = 4;
-        while (stages > 2 && smem_for(stages, opc) * per_sm > (size_t)kSmemBudget) --stages;
-        if (smem_for(stages, opc) * per_sm <= (size_t)kSmemBudget || per_sm == 1) {
-            if (smem_for(stages, opc) > (size_t)kSmemBudget)
-                return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d needs too much shared memory", prm.K);
-            prm.stages = stages;
+    for (int ngrp = 3; ngrp >= 1; --ngrp) {
+        const int warps = ngrp * prm.nkw + 1;
+        for (int per_sm = 3 / ngrp; per_sm >= 1; --per_sm) {
+            if (!fits_registers(k, warps * per_sm)) continue;
+            int ctas = sms * per_sm / mtiles;
+            if (ctas < 1) ctas = 1;
+            if (ctas > prm.n_oct) ctas = prm.n_oct;
+            const int opc = (prm.n_oct + ctas - 1) / ctas;
+            int spg = 4;
+            while (spg > 2 && smem_for(ngrp * spg, opc) * per_sm > (size_t)kSmemBudget) --spg;
+            const size_t smem = smem_for(ngrp * spg, opc);
+            if (smem * per_sm > (size_t)kSmemBudget) continue;
+            prm.ngrp = ngrp;
+            prm.stages = ngrp * spg;
             prm.oct_per_cta = opc;
             const dim3 grid(ctas, mtiles);
-            const size_t smem = smem_for(stages, opc);
-            cudaError_t e = cudaFuncSetAttribute(skinny_kernel<MT>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess)
                 return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            e = launch_pdl(skinny_kernel<MT>, grid, dim3(threads), smem, stream, prm);
+            e = launch_pdl(k, grid, dim3(32 * warps), smem, stream, prm);
             if (e == cudaSuccess) e = cudaGetLastError();
             if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
             return PQ_OK;
         }
-        --per_sm;
     }
+    return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d needs too much shared memory", prm.K);
 }
 
 }  // namespace
@@ -378,14 +414,15 @@ pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, i
     prm.stage_bytes = prm.w_bytes + 32u * (uint32_t)prm.G;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // rows per M-tile: the smallest power of two >= M (at most 8) whose
-    // instantiation fits the register file with this many k-warps
-    if (M == 1 && fits_registers<1>(prm.nkw)) return launch_mt<1>(prm, sm_count, st);
-    if (M <= 2 && fits_registers<2>(prm.nkw)) return launch_mt<2>(prm, sm_count, st);
-    if (M <= 4 && fits_registers<4>(prm.nkw)) return launch_mt<4>(prm, sm_count, st);
-    if (fits_registers<8>(prm.nkw)) return launch_mt<8>(prm, sm_count, st);
-    if (fits_registers<4>(prm.nkw)) return launch_mt<4>(prm, sm_count, st);
-    if (fits_registers<2>(prm.nkw)) return launch_mt<2>(prm, sm_count, st);
-    if (fits_registers<1>(prm.nkw)) return launch_mt<1>(prm, sm_count, st);
+    // instantiation fits the register file with one group of k-warps
+    const int w1 = prm.nkw + 1;
+    if (M == 1 && fits_registers(skinny_kernel<1>, w1)) return launch_ring(skinny_kernel<1>, 1, prm, sm_count, st);
+    if (M <= 2 && fits_registers(skinny_kernel<2>, w1)) return launch_ring(skinny_kernel<2>, 2, prm, sm_count, st);
+    if (M <= 4 && fits_registers(skinny_kernel<4>, w1)) return launch_ring(skinny_kernel<4>, 4, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<8>, w1)) return launch_ring(skinny_kernel<8>, 8, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<4>, w1)) return launch_ring(skinny_kernel<4>, 4, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<2>, w1)) return launch_ring(skinny_kernel<2>, 2, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<1>, w1)) return launch_ring(skinny_kernel<1>, 1, prm, sm_count, st);
     return fail(PQ_ERR_CUDA, "pq_gemm_skinny: no instantiation fits K = %d", K);
 }
 
