@@ -212,9 +212,10 @@ GEMM_SMALL = [  # M, K, N, P, pb
     (16, 1152, 512, 1, None), (7, 512, 384, 3, (128, 256)), (12, 384, 512, 2, (256, 512)),
     (129, 512, 256, 1, None), (200, 896, 384, 3, (128, 256)), (256, 1024, 512, 1, None),
     (33, 1152, 256, 1, None), (18, 8704, 128, 1, None),
-    # several octets per CTA of the decode kernel, consumer groups with
-    # unequal octet counts and partition switches inside a CTA's run
+    # several octets per CTA of the decode kernel and partition switches
+    # inside a CTA's run; M = 2 runs its three-group CTAs (unequal group loads)
     (1, 1152, 8448, 3, (2048, 4992)), (3, 640, 6016, 2, (2944, 6016)), (6, 384, 4096, 1, None),
+    (2, 5120, 8448, 2, (4096, 8448)),
 ]
 
 

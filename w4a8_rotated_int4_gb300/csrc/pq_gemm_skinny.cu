@@ -20,12 +20,17 @@
 // Consumer groups.  A CTA may hold up to three groups of nkw compute warps
 // that share its producer and its ring: octet i of the CTA's run goes to group
 // i mod ngrp and ring stage i mod S (S a multiple of ngrp, so a stage always
-// serves the same group and no waiter can fall two phases behind).  One CTA
-// per SM with three groups beats three one-group CTAs: the producer issues the
-// SM's octets in one order, they land in about that order, and the groups take
-// them round robin, so the SM's groups finish within about one octet of each
-// other (three separate CTAs on an SM were measured to finish up to 2.5 us
-// apart, the first one served taking its whole run ahead of the others).
+// serves the same group and no waiter can fall two phases behind).  The launch
+// prefers three one-group CTAs per SM and falls back to one CTA with three
+// groups.  Measured on decode gate_up (M = 1, K = 5120, N = 17408):
+//   - GEMM alone, back to back: the three-group CTA is faster, 11.0 vs
+//     11.6 us.  Its groups take the SM's octets round robin and finish within
+//     about one octet of each other.  Three separate CTAs on one SM finish up
+//     to 2.5 us apart, because the first one served runs its whole range ahead.
+//   - Decode step after the prologue: three separate CTAs are faster, 14.4 vs
+//     16.0 us.  As soon as the first of them exits, the next launch's CTA
+//     takes its place and prefetches weights during this launch's tail and
+//     the next prologue.  A whole-SM CTA leaves no such room.
 //
 // Arithmetic.  A weight nibble c is turned into an f16 *subnormal* whose bits
 // are the nibble (value c * 2^-24) by one AND per two nibbles -- no integer to
@@ -346,11 +351,11 @@ bool fits_registers(SkinnyFn k, int warps) {
 
 // Launch kernel k (mt rows per M-tile) over the octet ring.  Three consumer
 // groups per SM (the more compute warps per SM, the more load latency is
-// hidden): preferably one CTA with three groups, else fewer groups per CTA
-// and more CTAs, each group with 2..4 ring stages; shared memory and
-// registers per SM are kept under their limits.  CTAs per M-tile: a whole
-// multiple of the SM count when there are enough octets, each with a balanced
-// octet range.
+// hidden): preferably three one-group CTAs, else one CTA with three groups,
+// else fewer, each group with 2..4 ring stages; shared memory and registers
+// per SM are kept under their limits.  CTAs per M-tile: a whole multiple of
+// the SM count when there are enough octets, each with a balanced octet
+// range.
 pq_status launch_ring(SkinnyFn k, int mt, SkinnyParams prm, int sm_count, cudaStream_t stream) {
     const int mtiles = (prm.M + mt - 1) / mt;
     const int sms = sm_count > 0 ? sm_count : 1;
@@ -358,30 +363,31 @@ pq_status launch_ring(SkinnyFn k, int mt, SkinnyParams prm, int sm_count, cudaSt
         return (size_t)stages * prm.stage_bytes + 16 * (size_t)stages + 16 +
                (size_t)prm.nkw * mt * opc * 8 * 4;
     };
-    for (int ngrp = 3; ngrp >= 1; --ngrp) {
+    // (groups per CTA, CTAs per SM) in order of preference
+    constexpr int kConfigs[5][2] = {{1, 3}, {3, 1}, {1, 2}, {2, 1}, {1, 1}};
+    for (const auto &cfg : kConfigs) {
+        const int ngrp = cfg[0], per_sm = cfg[1];
         const int warps = ngrp * prm.nkw + 1;
-        for (int per_sm = 3 / ngrp; per_sm >= 1; --per_sm) {
-            if (!fits_registers(k, warps * per_sm)) continue;
-            int ctas = sms * per_sm / mtiles;
-            if (ctas < 1) ctas = 1;
-            if (ctas > prm.n_oct) ctas = prm.n_oct;
-            const int opc = (prm.n_oct + ctas - 1) / ctas;
-            int spg = 4;
-            while (spg > 2 && smem_for(ngrp * spg, opc) * per_sm > (size_t)kSmemBudget) --spg;
-            const size_t smem = smem_for(ngrp * spg, opc);
-            if (smem * per_sm > (size_t)kSmemBudget) continue;
-            prm.ngrp = ngrp;
-            prm.stages = ngrp * spg;
-            prm.oct_per_cta = opc;
-            const dim3 grid(ctas, mtiles);
-            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess)
-                return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            e = launch_pdl(k, grid, dim3(32 * warps), smem, stream, prm);
-            if (e == cudaSuccess) e = cudaGetLastError();
-            if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
-            return PQ_OK;
-        }
+        if (!fits_registers(k, warps * per_sm)) continue;
+        int ctas = sms * per_sm / mtiles;
+        if (ctas < 1) ctas = 1;
+        if (ctas > prm.n_oct) ctas = prm.n_oct;
+        const int opc = (prm.n_oct + ctas - 1) / ctas;
+        int spg = 4;
+        while (spg > 2 && smem_for(ngrp * spg, opc) * per_sm > (size_t)kSmemBudget) --spg;
+        const size_t smem = smem_for(ngrp * spg, opc);
+        if (smem * per_sm > (size_t)kSmemBudget) continue;
+        prm.ngrp = ngrp;
+        prm.stages = ngrp * spg;
+        prm.oct_per_cta = opc;
+        const dim3 grid(ctas, mtiles);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        e = launch_pdl(k, grid, dim3(32 * warps), smem, stream, prm);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "skinny launch: %s", cudaGetErrorString(e));
+        return PQ_OK;
     }
     return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d needs too much shared memory", prm.K);
 }
