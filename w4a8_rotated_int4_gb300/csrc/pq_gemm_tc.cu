@@ -14,9 +14,10 @@
 //                zero-filled past M), the packed weight tile w[n0:n0+128]
 //                [64kb:+64] and the slab's 128 SZ words (16 octets x 8 words
 //                of the [N/8][G][8] table) into stage s.
-//   expand warps turn each nibble c into the e4m3 code of c (0..15 are exact
-//                in e4m3) in the canonical K-major SWIZZLE_128B layout the MMA
-//                reads, and convert the SZ words to fp32 (sc, zscale + 8 sc).
+//   expand warps turn each nibble c into the e4m3 byte of value c * 2^-9 (the
+//                nibble alone in its byte) in the canonical K-major
+//                SWIZZLE_128B layout the MMA reads, and convert the SZ words
+//                to fp32 (2^9 sc, zscale + 8 sc).
 //   MMA warp     issues 2 x 4 tcgen05.mma m128n128k32 (kind::f8f6f4, fp32
 //                accumulate), one chain per half, into one of two TMEM
 //                accumulator sets, so the MMAs of slab kb+1 run while slab kb
@@ -356,7 +357,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             if (et < BN / 2) {
                 const float sc0 = f16lo(w0), sc1 = f16lo(w1);
-                szf[r].v[et] = make_float4(sc0, sc1, -(f16hi(w0) + 8.0f * sc0), -(f16hi(w1) + 8.0f * sc1));
+                // the MMA sums a * c * 2^-9 (expand16), so sc carries 2^9
+                szf[r].v[et] = make_float4(kNibbleScale * sc0, kNibbleScale * sc1, -(f16hi(w0) + 8.0f * sc0),
+                                           -(f16hi(w1) + 8.0f * sc1));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->szf_full[r]);

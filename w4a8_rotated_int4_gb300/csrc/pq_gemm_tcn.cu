@@ -16,9 +16,10 @@
 //   TMA warp     packed weights w[n0:+128][64g:+64], the group's SZ words and
 //                the activation tile a[p][0:16][128g:+128] (SWIZZLE_128B)
 //                into one of kStages stages.
-//   expand warps nibble c -> e4m3(c) in the canonical K-major SWIZZLE_128B
-//                layout (the MMA's A operand), and the SZ words -> fp32
-//                (sc, -(zscale + 8 sc)) into a ring slot of their own.
+//   expand warps nibble c -> the e4m3 byte of value c * 2^-9 (the nibble alone
+//                in its byte) in the canonical K-major SWIZZLE_128B layout
+//                (the MMA's A operand), and the SZ words -> fp32
+//                (2^9 sc, -(zscale + 8 sc)) into a ring slot of their own.
 //   row warp     cp.async of the group's per-token (asg, rs) into a deeper ring.
 //   MMA warps    4 x tcgen05.mma m128n16k32 (kind::f8f6f4, fp32 accumulate)
 //                into one of four 16-column TMEM accumulators (one per MMA warp).
@@ -323,8 +324,9 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             if (et < NN / 2) {
                 const float sc0 = f16lo(w0), sc1 = f16lo(w1);
                 // word j of the slab's SZ box is octet j / 8, column j % 8: column n = j
-                szf[r].col[2 * et] = make_float2(sc0, -(f16hi(w0) + 8.0f * sc0));
-                szf[r].col[2 * et + 1] = make_float2(sc1, -(f16hi(w1) + 8.0f * sc1));
+                // the MMA sums a * c * 2^-9 (expand16), so sc carries 2^9
+                szf[r].col[2 * et] = make_float2(kNibbleScale * sc0, -(f16hi(w0) + 8.0f * sc0));
+                szf[r].col[2 * et + 1] = make_float2(kNibbleScale * sc1, -(f16hi(w1) + 8.0f * sc1));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->szf_full[r]);

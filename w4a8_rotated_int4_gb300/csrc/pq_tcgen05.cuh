@@ -135,32 +135,32 @@ __device__ __forceinline__ bool wait3_or_abort(uint64_t *b0, uint32_t p0, uint64
 
 
 
-// e4m3 codes of 4 nibbles (selector bits 0..15): nibble c < 8 picks byte c of
-// the low table, c >= 8 picks byte c-8 of the high table; PRMT's sign mode
-// (selector bit 3) turns the other table's byte into 0x00 since every entry
-// has a clear sign bit.
-// (PTX prmt in its default mode honours the sign-replicate bit of each
-// selector nibble; the __byte_perm intrinsic only uses the low three bits.)
+// PTX prmt in its default mode (the __byte_perm intrinsic only uses the low
+// three bits of each selector nibble).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
 
-__device__ __forceinline__ uint32_t expand4(uint32_t sel, uint32_t sel_x8) {
-    constexpr uint32_t kLo0 = 0x44403800u, kLo1 = 0x4E4C4A48u;   // e4m3(0..7)
-    constexpr uint32_t kHi0 = 0x53525150u, kHi1 = 0x57565554u;   // e4m3(8..15)
-    return prmt(kLo0, kLo1, sel) | prmt(kHi0, kHi1, sel_x8);
-}
+// Sixteen packed nibbles (byte j: code of k = 2j in bits 0..3, k = 2j + 1 in
+// bits 4..7) -> sixteen e4m3 bytes in k order, each the e4m3 value c * 2^-9:
+// a byte holding a nibble c alone is exactly that e4m3 number (bit 3 is the
+// lowest exponent bit, so codes 0..7 are the subnormals m * 2^-9 and 8..15
+// the normals (1 + m/8) * 2^-6).  One AND gives the even-k nibbles, a shift
+// and an AND the odd-k ones, and two byte permutes interleave them back into
+// k order: 10 instructions per 16 weights.  The MMA result is therefore
+// 2^-9 * sum a * c; the fold multiplies its weight scale by 2^9.
+constexpr float kNibbleScale = 512.0f;
 
 __device__ __forceinline__ uint4 expand16(uint2 pk) {
-    const uint32_t x0 = pk.x, x1 = pk.y;
-    const uint32_t y0 = x0 ^ 0x88888888u, y1 = x1 ^ 0x88888888u;
+    const uint32_t lo0 = pk.x & 0x0F0F0F0Fu, hi0 = (pk.x >> 4) & 0x0F0F0F0Fu;
+    const uint32_t lo1 = pk.y & 0x0F0F0F0Fu, hi1 = (pk.y >> 4) & 0x0F0F0F0Fu;
     uint4 o;
-    o.x = expand4(x0, y0);
-    o.y = expand4(x0 >> 16, y0 >> 16);
-    o.z = expand4(x1, y1);
-    o.w = expand4(x1 >> 16, y1 >> 16);
+    o.x = prmt(lo0, hi0, 0x5140u);     // k 0, 1, 2, 3
+    o.y = prmt(lo0, hi0, 0x7362u);     // k 4, 5, 6, 7
+    o.z = prmt(lo1, hi1, 0x5140u);
+    o.w = prmt(lo1, hi1, 0x7362u);
     return o;
 }
 
