@@ -300,32 +300,40 @@ def e2e_workload(pq, torch, wl, steps, warmup, stream, dev):
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the kernel on the workload, with the SHA-256 of the kernel's
-# source at capture time.  The figure is reported only while the source is
-# unchanged; otherwise traffic is null.
+# sources (concatenated in the listed order) at capture time.  The figure is
+# reported only while those sources are unchanged; otherwise traffic is null.
+_CSRC = "w4a8_rotated_int4_gb300/csrc/"
 NCU_TRAFFIC = {
     ("pq_gemm_skinny", "decode:1"): dict(
-        bytes=47379968 + 2048, profile="profiles/pq_gemm_skinny_decode_gate_up_m1.md",
-        src="w4a8_rotated_int4_gb300/csrc/pq_gemm_skinny.cu",
-        sha256="426b5645f0fb6237a62cbfb0fc095d2169790ab0b211429bb432fac2eec9a396"),
+        bytes=47379968 + 0, profile="profiles/pq_gemm_skinny_decode_gate_up_m1.md",
+        src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
+        sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=72338688 + 39974912, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
-        src="w4a8_rotated_int4_gb300/csrc/pq_gemm_tc.cu",
-        sha256="dc07fd9e6f3ef14522a8bea3187da443b8aba022c0205ee7b5e3934326392312"),
+        bytes=73961984 + 41309696, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
+        sha256="ce0d46e8c0fc6a3015f059af2ef226199d1c63c80fd97b7c9a0143dc83b2c7e0"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47473408 + 256, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
-        src="w4a8_rotated_int4_gb300/csrc/pq_gemm_tcn.cu",
-        sha256="a6def0ed26f0281e978960564d0a85ce62bd9a102ae583ce1ad41deec4095cde"),
+        bytes=47468544 + 768, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
+        src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
+        sha256="d32fccfa38ae6671c70e584b8fbfa0cbf2d59e889b805d8957520b96514a4d6e"),
 }
 
 
-def ncu_traffic(kernel, workload):
+def sources_sha256(files):
     import hashlib
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()
+
+
+def ncu_traffic(kernel, workload):
     e = NCU_TRAFFIC.get((kernel, workload))
     if e is None:
         return None
-    with open(os.path.join(ROOT, e["src"]), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != e["sha256"]:
-            return None
+    if sources_sha256(e["src"]) != e["sha256"]:
+        return None
     return e["bytes"]
 
 
