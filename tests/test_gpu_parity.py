@@ -272,6 +272,30 @@ def test_gemm_zero_point_eight_gives_zero(pq, orc):
         assert float(np.max(mag)) > 1e-3
 
 
+@pytest.mark.parametrize("M", [300, 3])
+def test_gemm_zero_scale_groups(pq, orc, M):
+    """A group whose scale is 0 (either sign) dequantizes to -zscale whatever
+    its codes.  The packer never writes one with a nonzero zscale, so the SZ
+    table is edited by hand here; every path must still match the oracle
+    (the prefill kernel masks such codes and folds the zero point apart)."""
+    K, N = 512, 256
+    G = K // 128
+    prob = pqgen.make_problem(M, K, N, seed=21 + M)
+    L = Problem(pq, orc, prob)
+    rng = np.random.default_rng(5)
+    sz = L.t["sz"].copy()                                    # [G, N, 2] f16 bits
+    pick = rng.random((G, N)) < 0.15
+    zs = (rng.standard_normal((G, N)) * 0.02).astype(np.float16).view(np.uint16)
+    sz[..., 0][pick] = np.where(rng.random(int(pick.sum())) < 0.5, 0x0000, 0x8000)
+    sz[..., 1][pick] = zs[pick]
+    L.sz_d = dev_u16(np.ascontiguousarray(sz.reshape(G, N // 8, 8, 2).transpose(1, 0, 2, 3)))
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    y64 = orc.gemm_f64(a.cpu().numpy(), asg.cpu().numpy(), rs.cpu().numpy(), L.t["codes"], sz, N, N)
+    for name, fn in gemm_paths(pq, M):
+        y = run_gemm(fn, a, asg, rs, L, N, N, M, N)
+        assert_close(y, y64, "%s zero-scale groups M=%d" % (name, M))
+
+
 def test_gemm_merged_equals_sliced(pq, orc):
     """One P=3 launch == three P=1 launches on the column slices, bit for bit."""
     M, K, N = 40, 640, 512

@@ -14,20 +14,32 @@
 //                zero-filled past M), the packed weight tile w[n0:n0+128]
 //                [64kb:+64] and the slab's 128 SZ words (16 octets x 8 words
 //                of the [N/8][G][8] table) into stage s.
+//   row warps    copy the slab's per-row asg and rs (cp.async) into a ring
+//                slot of their own, up to the ring's depth ahead.
 //   expand warps turn each nibble c into the e4m3 byte of value c * 2^-9 (the
 //                nibble alone in its byte) in the canonical K-major
-//                SWIZZLE_128B layout the MMA reads, and convert the SZ words
-//                to fp32 (2^9 sc, zscale + 8 sc).
-//   MMA warp     issues 2 x 4 tcgen05.mma m128n128k32 (kind::f8f6f4, fp32
-//                accumulate), one chain per half, into one of two TMEM
-//                accumulator sets, so the MMAs of slab kb+1 run while slab kb
-//                is folded.
-//   fold warps   (one thread per row, 128 columns each) tcgen05.ld the slab's
-//                D' = sum_k dec(a) * c and fold it into fp32 registers with
-//                packed f32x2 operations:
-//                acc += asg * (sc * D' - (zscale + 8 sc) * rs), which equals
-//                asg * (sc * D - zscale * rs) with D the sum over (c - 8):
-//                D' = D + 8 * rs exactly, and zscale + 8 sc is exact in fp32.
+//                SWIZZLE_128B layout the MMA reads, and write the zero-point
+//                MMA's operands: per column zq = 2^-9 (zscale + 8 sc) / sc',
+//                per row -rs, each as three bf16 parts (below), plus the
+//                fold's column scale 2^9 sc'.  sc' = sc, or 1 where sc = 0,
+//                whose codes are masked to 0.
+//   MMA warp     per half: 4 tcgen05.mma m128n128k32 (kind::f8f6f4, fp32
+//                accumulate), then one m128n128k16 kind::f16 (bf16) MMA of the
+//                zero-point operands into the same accumulator, so TMEM holds
+//                D'' = 2^-9 (sum_k dec(a) c - rs * zq); two accumulator sets,
+//                so the MMAs of slab kb+1 run while slab kb is folded.
+//   fold warps   (one thread per row, 128 columns each) tcgen05.ld D'' and
+//                fold it into fp32 registers with packed f32x2 operations:
+//                acc += (asg * 2^9 sc') * D''.  That is
+//                asg * (sc * D' - (zscale + 8 sc) * rs) with D' = sum dec(a) c
+//                = D + 8 rs, D the sum over (c - 8): the zero point of the
+//                method, moved onto the tensor core (two fp32 operations per
+//                element and slab instead of three).
+// Zero-point operand precision: with rs = h + m + l and zq = zh + zm + zl
+// (bf16_split3, 24 significant bits each), k = 0..5 of the row operand carry
+// -(h, h, m, h, l, m) against (zh, zm, zh, zl, zh, zm) in the column operand:
+// every product of parts whose orders sum to <= 2, so the MMA adds -rs * zq
+// to about 2^-24 relative (products are exact, sums fp32).
 // The fold warpgroups raise their register budget (setmaxnreg) to hold the
 // 128 accumulators; the others lower theirs.
 // Epilogue: bf16 rows < M are stored; nothing else is written.
@@ -54,7 +66,7 @@ constexpr int BM = 256, BN = 128, BK = 128;    // BM = two M=128 MMA halves
 constexpr int kStages = 3;
 constexpr int kFoldWarps = 8;     // warps 0..7: warp w folds rows 128(w/4) + 32(w%4)..+31, all columns
 constexpr int kExpWarps = 4;      // warps 8..11
-constexpr int kTmaWarp = 12, kMmaWarp = 13, kRowWarp = 14;   // warp 15 idle
+constexpr int kTmaWarp = 12, kMmaWarp = 13, kRowWarp = 14;   // row warps 14 and 15: tile half 0, 1
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kFoldRegs = 216, kOtherRegs = 40;   // 256 * 216 + 256 * 40 = 65536
 constexpr uint32_t kABytes = BM * BK;
@@ -64,11 +76,19 @@ constexpr uint32_t kSzBytes = BN * 4;
 constexpr uint32_t kTxBytes = kABytes + kBpBytes + kSzBytes;
 constexpr uint32_t kTmemCols = 512;    // 2 buffers x 2 halves x 128 columns
 
+// The zero-point MMA's operands: K = 16 bf16 per row (only k = 0..2 are
+// nonzero), K-major without swizzle: core matrices of 8 rows x 16 bytes, the
+// k = 0..7 one at (row / 8) * 256 + (row % 8) * 16 and the k = 8..15 one
+// (always zero) 128 bytes after it.
+constexpr uint32_t kZLbo = 128, kZSbo = 256;
+constexpr uint32_t kZaBytes = BM * 32, kZbBytes = BN * 32;
+
 struct __align__(1024) Stage {
     uint8_t a[kABytes];       // 256 rows x 128 B, SWIZZLE_128B (TMA); half h at 16 KB * h
     uint8_t bx[kBxBytes];     // 128 rows x 128 B, SWIZZLE_128B (expand warps)
     uint8_t bp[kBpBytes];     // 128 rows x 64 B packed nibbles (TMA)
     uint32_t sz[BN];          // f16 (sc, zscale) per column
+    uint8_t zb[kZbBytes];     // zero-point operand per column (expand warps)
 };
 
 // fp32 scales of one slab for the fold warps, in a ring of their own so a
@@ -78,8 +98,10 @@ struct __align__(1024) Stage {
 // depth ahead, so no global-load latency reaches the fold warps.
 constexpr int kSzfRing = 4;
 struct __align__(16) SzfSlot {
-    float4 v[BN / 2];         // (sc[n], sc[n+1], -zs8[n], -zs8[n+1]) for even n
-    float2 row[BM];           // (asg, rs) of tile row i (0 past M)
+    float2 sc[BN / 2];        // (2^9 sc'[n], 2^9 sc'[n+1]) for even n (sc' = sc, or 1 where sc = 0)
+    float row[BM];            // asg of tile row i (0 past M)
+    float rsv[BM];            // rs of tile row i (0 past M), staging for za
+    uint8_t za[kZaBytes];     // zero-point operand per row (row warp)
 };
 
 struct Ctrl {
@@ -88,6 +110,7 @@ struct Ctrl {
     uint64_t empty[kStages];
     uint64_t szf_full[kSzfRing];
     uint64_t szf_empty[kSzfRing];
+    uint64_t rows_full[kSzfRing];   // the row warps' copies of a slab's asg and rs have landed
     uint64_t tmem_full[2][2];     // [m-half][accumulator buffer]
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
@@ -95,6 +118,7 @@ struct Ctrl {
 };
 
 constexpr size_t kSmemBytes = kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot) + sizeof(Ctrl) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct TcParams {
     const float *asg;
@@ -107,7 +131,8 @@ struct TcParams {
 
 // ---------------------------------------------------------------- PTX helpers
 using namespace tc;
-constexpr uint32_t kIdesc = idesc_f8(128, BN);   // one M=128 half x BN columns
+constexpr uint32_t kIdesc = idesc_f8(128, BN);     // one M=128 half x BN columns
+constexpr uint32_t kIdescZ = idesc_bf16(128, BN);  // the zero-point MMA of a half
 
 __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsigned int code) {
     if (status) atomicOr(status, code);
@@ -115,26 +140,18 @@ __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsig
 }
 
 // Fold one 16x256b.x4 load: four column pairs for two rows (lo: d[4j..4j+1],
-// hi: d[4j+2..4j+3]); acc += asg * (sc * D + (-zs8) * rs), stage by stage
-// (z[j].x = sc pair, z[j].y = -zs8 pair, nr = rs splat).
-__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const ulonglong2 (&z)[4], uint64_t *acc_lo,
-                                           uint64_t *acc_hi, uint64_t sa_lo, uint64_t nr_lo, uint64_t sa_hi,
-                                           uint64_t nr_hi) {
-    uint64_t t[8];
+// hi: d[4j+2..4j+3]).  The accumulator already holds D'' = D' - rs * zq (the
+// zero-point MMA), so acc += (asg * sc) * D'' with z[j] = the sc pair of
+// column pair j and sa = the row's asg splat: two packed operations per two
+// elements.
+__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64_t (&z)[4], uint64_t *acc_lo,
+                                           uint64_t *acc_hi, uint64_t sa_lo, uint64_t sa_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        t[2 * j] = fmul2v(f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), z[j].x);
-        t[2 * j + 1] = fmul2v(f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), z[j].x);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        t[2 * j] = ffma2v(z[j].y, nr_lo, t[2 * j]);
-        t[2 * j + 1] = ffma2v(z[j].y, nr_hi, t[2 * j + 1]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        acc_lo[j] = ffma2v(sa_lo, t[2 * j], acc_lo[j]);
-        acc_hi[j] = ffma2v(sa_hi, t[2 * j + 1], acc_hi[j]);
+        const uint64_t t_lo = fmul2v(sa_lo, z[j]), t_hi = fmul2v(sa_hi, z[j]);
+        acc_lo[j] = ffma2v(t_lo, f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), acc_lo[j]);
+        acc_hi[j] = ffma2v(t_hi, f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                           acc_hi[j]);
     }
 }
 
@@ -175,7 +192,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_init(&ctl->empty[s], 1);            // the MMA commit
         }
         for (int r = 0; r < kSzfRing; ++r) {
-            mbar_init(&ctl->szf_full[r], kExpWarps + 32);   // + the row warp's cp.async arrivals
+            mbar_init(&ctl->szf_full[r], kExpWarps);
+            mbar_init(&ctl->rows_full[r], 64);              // every lane of the two row warps (cp.async)
             mbar_init(&ctl->szf_empty[r], kFoldWarps);
         }
         for (int b = 0; b < 2; ++b) {
@@ -186,6 +204,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         ctl->abort = 0;
         fence_mbar_init();
     }
+    // the zero-point operands' k = 3..15 stay zero for the whole launch; the
+    // roles rewrite only k = 0..2 of each row
+    for (int s = 0; s < kStages; ++s)
+        for (uint32_t o = threadIdx.x * 16; o < kZbBytes; o += kThreads * 16)
+            *reinterpret_cast<uint4 *>(stg[s].zb + o) = make_uint4(0u, 0u, 0u, 0u);
+    for (int r = 0; r < kSzfRing; ++r)
+        for (uint32_t o = threadIdx.x * 16; o < kZaBytes; o += kThreads * 16)
+            *reinterpret_cast<uint4 *>(szf[r].za + o) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&ctl->tmem_base)),
@@ -244,8 +271,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
             }
         }
-    } else if (warp == kRowWarp) {
+    } else if (warp >= kRowWarp) {
         // ------------------------------------------------ per-row scales
+        // asg and rs of a slab's rows by cp.async into the slab's ring slot,
+        // up to a ring's depth ahead; the expansion warps turn rs into the
+        // zero-point MMA's row operand.  Row warp hw copies tile half hw.
+        const int row0 = (BM / 2) * (warp - kRowWarp);
         pdl_wait();        // asg and rs are the preceding prologue's output
         for (int it = 0; it < total; ++it) {
             const int r = it % kSzfRing, ruse = it / kSzfRing;
@@ -257,13 +288,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
             const size_t off = ((size_t)p * G + (size_t)(it % G)) * (size_t)M;
 #pragma unroll
-            for (int u = 0; u < BM / 32; ++u) {
-                const int i = lane + 32 * u, m = m0 + i;
+            for (int u = 0; u < BM / 64; ++u) {
+                const int i = row0 + lane + 32 * u, m = m0 + i;
                 const bool ok = m < M;     // rows past M are zero-filled
-                cp_async4(&szf[r].row[i].x, ok ? prm.asg + off + m : prm.asg, ok);
-                cp_async4(&szf[r].row[i].y, ok ? prm.rs + off + m : prm.rs, ok);
+                cp_async4(&szf[r].row[i], ok ? prm.asg + off + m : prm.asg, ok);
+                cp_async4(&szf[r].rsv[i], ok ? prm.rs + off + m : prm.rs, ok);
             }
-            cp_async_arrive(&ctl->szf_full[r]);
+            cp_async_arrive(&ctl->rows_full[r]);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
     } else if (warp == kMmaWarp) {
@@ -271,11 +302,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // The whole warp runs the loop (so the descriptors stay warp-uniform)
         // and one elected lane issues the MMAs and commits.  full_b implies
         // full_tma: the expand warps waited for the stage's copies before they
-        // arrived on full_b.
+        // arrived on full_b, after writing the zero-point operands.
         int committed = 0;
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages, use = it / kStages;
             const int b = it & 1, tuse = it >> 1;
+            const int r = it % kSzfRing;
             // the accumulator's first use waits on nothing: the phase before
             // the first reads as complete
             const bool ok = __all_sync(0xFFFFFFFFu,
@@ -289,17 +321,23 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint64_t ad0 = desc_sw128(smem_u32(stg[s].a));
             const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
             const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
+            const uint64_t za0 = desc_noswz(smem_u32(szf[r].za), kZLbo, kZSbo);
+            const uint64_t za1 = desc_noswz(smem_u32(szf[r].za + kZaBytes / 2), kZLbo, kZSbo);
+            const uint64_t zbd = desc_noswz(smem_u32(stg[s].zb), kZLbo, kZSbo);
             const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
             if (elect_one()) {
                 // half 0, then half 1, each committed on its own so the two
-                // fold warp groups start half a slab apart
+                // fold warp groups start half a slab apart; each half's chain
+                // ends with the zero-point MMA (bf16, K = 16)
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)   // +32 bytes along K inside the swizzle row
                     mma_f8(d0, ad0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
+                mma_bf16(d0, za0, zbd, kIdescZ, 1u);
                 mma_commit(&ctl->tmem_full[0][b]);
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)
                     mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
+                mma_bf16(d1, za1, zbd, kIdescZ, 1u);
                 // A stage that is never refilled gets no release: nothing would wait
                 // for that arrival, and an arrival still in flight when the CTA
                 // exits would land in the shared memory of the next CTA on this SM.
@@ -325,44 +363,73 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const int chunk = et & 7;
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages, use = it / kStages;
-            if (!wait_or_abort(&ctl->full_tma[s], use & 1, abort_flag)) {
+            const int r = it % kSzfRing, ruse = it / kSzfRing;
+            // the stage's copies, the ring slot free (its previous slab folded;
+            // the phase before the first reads as complete) and the slab's row
+            // copies landed; warp-uniform, so the warp stays converged for its
+            // votes and syncs
+            if (!__all_sync(0xFFFFFFFFu,
+                            wait3_or_abort(&ctl->full_tma[s], use & 1, &ctl->szf_empty[r], (ruse - 1) & 1,
+                                           &ctl->rows_full[r], ruse & 1, abort_flag))) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
             Stage &st = stg[s];
-            uint32_t w0 = 0, w1 = 0;
-            if (et < BN / 2) {            // read the SZ words now: the stage may be refilled after full_b
-                w0 = st.sz[2 * et];
-                w1 = st.sz[2 * et + 1];
-            }
+            const uint32_t wcol = st.sz[et];   // column et's SZ word, read before full_b frees the stage
             // all eight packed loads first (the stores below could alias them
             // as far as the compiler knows), then expand and store
             uint2 pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 pk[i] = *reinterpret_cast<const uint2 *>(st.bp + ((et >> 3) + 16 * i) * (BK / 2) + chunk * 8);
+            // A column with sc = 0 dequantizes to -zs whatever its codes, so its
+            // codes must not reach the MMA: the fold then scales it by 1 and
+            // the zero-point MMA alone gives -zs * rs.  Lane l checks row
+            // 4w + l % 4 + 16 (l / 4) of this warp's 32 rows.
+            const bool any_zero_sc = __any_sync(
+                0xFFFFFFFFu, (st.sz[4 * (et >> 5) + (lane & 3) + 16 * (lane >> 2)] & 0x7FFFu) == 0u);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = (et >> 3) + 16 * i;
-                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = expand16(pk[i]);
+                uint4 e = expand16(pk[i]);
+                if (any_zero_sc && (st.sz[row] & 0x7FFFu) == 0u) e = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
             }
+            // the zero-point MMA's column operand (zh, zm, zh, zl, zh, zm) in
+            // bf16 parts of zq = 2^-9 (zscale + 8 sc) / sc', sc' = sc, or 1 where
+            // sc = 0 (2^-9: the unit of the MMA's sum, see expand16); one
+            // column per thread.  zq only corrects, so a division to 2 ulp
+            // (about 2^-23) is accurate enough.
+            const float sc = f16lo(wcol);
+            const float sce = sc != 0.0f ? sc : 1.0f;
+            {
+                const float zq = __fdividef(f16hi(wcol) + 8.0f * sc, sce) * (1.0f / kNibbleScale);
+                uint32_t h, m, l;
+                bf16_split3(zq, h, m, l);
+                *reinterpret_cast<uint4 *>(st.zb + (et >> 3) * kZSbo + (et & 7) * 16) =
+                    make_uint4(h | (m << 16), h | (l << 16), h | (m << 16), 0u);
+            }
+            // the zero-point MMA's row operand for rows et and et + 128: with
+            // rs = h + m + l and zq = zh + zm + zl (bf16 parts, bf16_split3),
+            // k = 0..5 carry -(h, h, m, h, l, m) against (zh, zm, zh, zl, zh, zm),
+            // so the MMA adds -(every product of parts whose orders sum to
+            // <= 2) = -rs * zq to about 2^-24 relative
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = et + 128 * u;
+                uint32_t h, m, l;
+                bf16_split3(-szf[r].rsv[i], h, m, l);
+                *reinterpret_cast<uint4 *>(szf[r].za + (i >> 3) * kZSbo + (i & 7) * 16) =
+                    make_uint4(h | (h << 16), m | (h << 16), l | (m << 16), 0u);
+            }
+            // the MMA sums a * c * 2^-9 (expand16), so sc' carries 2^9
+            reinterpret_cast<float *>(szf[r].sc)[et] = kNibbleScale * sce;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->full_b[s]);
-            // fp32 scales for the fold, into the ring slot of this slab
-            const int r = it % kSzfRing, ruse = it / kSzfRing;
-            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag)) {
-                if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
-                break;
+            if (lane == 0) {
+                mbar_arrive(&ctl->full_b[s]);
+                mbar_arrive(&ctl->szf_full[r]);
             }
-            if (et < BN / 2) {
-                const float sc0 = f16lo(w0), sc1 = f16lo(w1);
-                // the MMA sums a * c * 2^-9 (expand16), so sc carries 2^9
-                szf[r].v[et] = make_float4(kNibbleScale * sc0, kNibbleScale * sc1, -(f16hi(w0) + 8.0f * sc0),
-                                           -(f16hi(w1) + 8.0f * sc1));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->szf_full[r]);
         }
     } else if (warp < kFoldWarps) {
         // ------------------------------------------------ fold warps
@@ -401,15 +468,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // while step k is folded
                 uint32_t dbuf[2][16];
                 tmem_issue256(taddr, dbuf[0]);
-                uint64_t sa2[4], rs2[4];
+                uint64_t sa2[4];
 #pragma unroll
                 for (int ri = 0; ri < 4; ++ri) {
-                    const float2 v = szf[r].row[row0 + 8 * ri];
-                    sa2[ri] = f2pack(v.x, v.x);
-                    rs2[ri] = f2pack(v.y, v.y);
+                    const float v = szf[r].row[row0 + 8 * ri];
+                    sa2[ri] = f2pack(v, v);
                 }
-                const ulonglong2 *zf = reinterpret_cast<const ulonglong2 *>(szf[r].v) + c4;
-                ulonglong2 z[4];
+                const uint64_t *zf = reinterpret_cast<const uint64_t *>(szf[r].sc) + c4;
+                uint64_t z[4];
                 tmem_wait16(dbuf[0]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -427,7 +493,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         for (int j = 0; j < 4; ++j) z[j] = zf[4 * (4 * cb + j)];
                     }
                     fold_block(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
-                               rs2[2 * sh], sa2[2 * sh + 1], rs2[2 * sh + 1]);
+                               sa2[2 * sh + 1]);
                     if (k + 1 < 8) tmem_wait16(dbuf[cur ^ 1]);
                 }
                 __syncwarp();

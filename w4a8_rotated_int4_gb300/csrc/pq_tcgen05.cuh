@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -66,6 +67,42 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
         : "memory");
+}
+
+// K-major operand without swizzle (layout type 0): 8-row x 16-byte core
+// matrices, lbo = byte distance between core matrices adjacent along K, sbo =
+// between core matrices adjacent along M/N; descriptor version 1.
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// kind::f16 instruction descriptor with bf16 A and B (type 1 at bits 7-9 and
+// 10-12), D fp32, both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accum) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+// x ~ hi + mid + lo, each the bf16 rounding (to nearest even) of what the
+// previous parts leave (those differences are exact in fp32), as raw bf16
+// bits: 24 significant bits between them.
+__device__ __forceinline__ void bf16_split3(float x, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const float r1 = __fsub_rn(x, __bfloat162float(h));
+    const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+    const float r2 = __fsub_rn(r1, __bfloat162float(m));
+    hi = __bfloat16_as_ushort(h);
+    mid = __bfloat16_as_ushort(m);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
 // Non-blocking test of up to three mbarrier phases issued back to back, so
