@@ -309,9 +309,9 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=73961984 + 41309696, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        bytes=73469952 + 40301824, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="ce0d46e8c0fc6a3015f059af2ef226199d1c63c80fd97b7c9a0143dc83b2c7e0"),
+        sha256="f428a3813b839e774e476dc474be35d494ce09ae446cf233e439db3c0f0fd33e"),
     ("pq_gemm_tcn", "decode:16"): dict(
         bytes=47468544 + 768, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
