@@ -49,6 +49,12 @@ def lib():
         L.orc_repack.argtypes = [i32, i32, vp, vp]
         L.orc_rotate_group_f32.argtypes = [vp, i32, i32, i32, vp]
         L.orc_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_bf16_from_float.restype = C.c_uint16
+        L.orc_bf16_from_float.argtypes = [C.c_float]
+        L.orc_row_sumsq.restype = C.c_float
+        L.orc_row_sumsq.argtypes = [i32, vp]
+        L.orc_add_rms_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, C.c_float, vp, vp,
+                                               vp, vp, vp, vp, vp]
         L.orc_gemm_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.orc_gemm_f64_sampled.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp]
@@ -194,6 +200,40 @@ def rotate_quant(x: np.ndarray, cs: np.ndarray, rec: np.ndarray, want_v: bool = 
     lib().orc_rotate_quant(M, K, ldx, P, _p(x), _p(cs), _p(rec), _p(a), _p(asg), _p(rs),
                            _p(v) if want_v else None)
     return (a, asg, rs, v) if want_v else (a, asg, rs)
+
+
+# ------------------------------------------------- fused producer (reading R10)
+def bf16_from_float(f: float) -> int:
+    return int(lib().orc_bf16_from_float(f))
+
+
+def row_sumsq(s: np.ndarray) -> np.float32:
+    """fp32 sum of squares of one row of bf16 values (reading R10 order)."""
+    s = _c(s, np.float32)
+    return np.float32(lib().orc_row_sumsq(s.shape[0], _p(s)))
+
+
+def add_rms_rotate_quant(x, res, gamma, eps, cs, rec):
+    """Residual add + Gemma RMSNorm + rotate + quant (reading R10).
+    x, res bf16 bits [M, ldx]; gamma bf16 bits [K]; eps float; cs f16 bits
+    [P, K].  Returns (res_out bf16 [M,K], h bf16 [M,K], a, asg, rs)."""
+    x = _c(x, np.uint16)
+    res = _c(res, np.uint16)
+    gamma = _c(gamma, np.uint16)
+    cs = _c(cs, np.uint16)
+    rec = _c(rec, np.uint8)
+    M, ldx = x.shape
+    assert res.shape == x.shape
+    P, K = cs.shape
+    G = K // 128
+    res_out = np.empty((M, K), dtype=np.uint16)
+    h = np.empty((M, K), dtype=np.uint16)
+    a = np.empty((P, M, K), dtype=np.uint8)
+    asg = np.empty((P, G, M), dtype=np.float32)
+    rs = np.empty((P, G, M), dtype=np.float32)
+    lib().orc_add_rms_rotate_quant(M, K, ldx, P, _p(x), _p(res), _p(gamma), float(eps), _p(cs),
+                                   _p(rec), _p(res_out), _p(h), _p(a), _p(asg), _p(rs))
+    return res_out, h, a, asg, rs
 
 
 # ---------------------------------------------------------------- GEMM

@@ -40,6 +40,20 @@
  *   R9 GEMM: y = sum_g asg * (sc * D - zscale * rs) with
  *      D = sum_{k in g} dec(A[k]) * (c[k] - 8), in fp64, using the f16 table
  *      values ("table-true").
+ *   R10 fused producer ([LOG] "2026-09-02/03: rotation stream (fused add +
+ *      RMSNorm + rotate + quant producers)": residual add + Gemma RMSNorm +
+ *      channel scale + rotation + per-group quant in one pass).  Per row:
+ *        s[k]  = bf16_RNE(fl32(x[k] + r[k]))          (the new residual)
+ *        ss    = sum over groups g, in order, in fp32, of the group's pairwise
+ *                sum of s[k]^2 (recursive halving: P(v[0:n]) =
+ *                fl32(P(v[0:n/2]) + P(v[n/2:n])), P of one element = s^2,
+ *                which is exact in fp32)
+ *        inv   = fl32(1 / fl32(sqrt(fl32(fl32(ss / K) + eps))))  (correctly
+ *                rounded sqrt and division)
+ *        h[k]  = bf16_RNE(fl32(fl32(s[k] * inv) * fl32(1 + gamma[k])))
+ *      then the pq_rotate_quant semantics on h.  The pages fix the op order
+ *      ("in vLLM's exact op order": s * rsqrt(mean(s^2) + eps) * (1 + w)) but
+ *      not the reduction order or the rsqrt rounding; these are the readings.
  */
 #include <math.h>
 #include <stdint.h>
@@ -334,6 +348,67 @@ void orc_rotate_quant(int M, int K, int ldx, int P, const uint16_t *x, const uin
                 if (v_out)
                     memcpy(v_out + ((size_t)p * M + m) * K + 128 * g, v, sizeof v);
             }
+}
+
+/* fp32 -> bf16 bit pattern, round to nearest, ties to even (finite input). */
+uint16_t orc_bf16_from_float(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+/* Pairwise sum of n = 2^j fp32 values (reading R10): the two halves' sums,
+ * added in fp32. */
+static float pairwise_f32(const float *v, int n)
+{
+    if (n == 1)
+        return v[0];
+    return f_add(pairwise_f32(v, n / 2), pairwise_f32(v + n / 2, n / 2));
+}
+
+/* Sum of squares of one bf16-valued row of K values (reading R10). */
+float orc_row_sumsq(int K, const float *s)
+{
+    float ss = 0.0f;
+    float sq[128];
+    for (int g = 0; g < K / 128; g++) {
+        for (int k = 0; k < 128; k++)
+            sq[k] = f_mul(s[128 * g + k], s[128 * g + k]);
+        ss = f_add(ss, pairwise_f32(sq, 128));
+    }
+    return ss;
+}
+
+/*
+ * Fused producer (reading R10).  x, res bf16 [M][ldx]; gamma bf16 [K]; the
+ * rest as orc_rotate_quant.  Writes res_out bf16 [M][K] (the new residual),
+ * h_out bf16 [M][K] (the normed rows) and the rotate_quant outputs of h.
+ */
+void orc_add_rms_rotate_quant(int M, int K, int ldx, int P, const uint16_t *x, const uint16_t *res,
+                              const uint16_t *gamma, float eps, const uint16_t *cs, const uint8_t *rec,
+                              uint16_t *res_out, uint16_t *h_out, uint8_t *a, float *asg, float *rs)
+{
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; m++) {
+        float *s = (float *)malloc(sizeof(float) * (size_t)K);
+        for (int k = 0; k < K; k++) {
+            uint16_t sb = orc_bf16_from_float(f_add(orc_bf16_to_float(x[(size_t)m * ldx + k]),
+                                                    orc_bf16_to_float(res[(size_t)m * ldx + k])));
+            res_out[(size_t)m * K + k] = sb;
+            s[k] = orc_bf16_to_float(sb);
+        }
+        float ss = orc_row_sumsq(K, s);
+        float var = f_div(ss, (float)K);
+        float inv = f_div(1.0f, sqrtf(f_add(var, eps)));
+        for (int k = 0; k < K; k++) {
+            float w1 = f_add(1.0f, orc_bf16_to_float(gamma[k]));
+            h_out[(size_t)m * K + k] = orc_bf16_from_float(f_mul(f_mul(s[k], inv), w1));
+        }
+        free(s);
+    }
+    orc_rotate_quant(M, K, K, P, h_out, cs, rec, a, asg, rs, NULL);
 }
 
 /* ------------------------------------------------------------------ */

@@ -1,0 +1,137 @@
+"""Pins of the oracle's fused producer (residual add + Gemma RMSNorm + rotate
++ quant) to things other than itself: torch's bfloat16 rounding and its
+rms_norm, exact sums, closed forms and exact scaling identities.
+
+Page: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", section
+"2026-09-02/03: rotation stream (fused add + RMSNorm + rotate + quant
+producers)": one producer does residual add + Gemma RMSNorm (vLLM's op order)
++ channel scale + rotation + per-group quant and returns (hs, residual, A,
+ASG, RS).  The summation order and the rsqrt rounding are readings (R10).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import pqgen
+
+torch = pytest.importorskip("torch")
+
+
+def bf16_bits(f32):
+    """torch's float32 -> bfloat16 rounding (RNE), as uint16 bits."""
+    t = torch.from_numpy(np.ascontiguousarray(f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f32(b):
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+def problem(M, K, P=1, seed=0, scale=1.0):
+    prob = pqgen.make_problem(M, K, 256, P=P, seed=seed)
+    rng = np.random.default_rng(seed + 100)
+    res = bf16_bits(rng.standard_normal((M, K)).astype(np.float32) * np.float32(scale))
+    gamma = bf16_bits(rng.standard_normal(K).astype(np.float32) * np.float32(0.2))
+    return prob, res, gamma
+
+
+def test_bf16_rounding_matches_torch(orc):
+    rng = np.random.default_rng(3)
+    f = np.concatenate([rng.standard_normal(4000).astype(np.float32) * 1000,
+                        # exact ties: 1 + 2^-8 (tie to 1), 1 + 3 * 2^-8 (tie to 1 + 2^-6)
+                        np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8)], np.float32)])
+    got = np.array([orc.bf16_from_float(float(v)) for v in f], dtype=np.uint16)
+    assert np.array_equal(got, bf16_bits(f))
+    assert got[-3] == 0x3F80 and got[-2] == 0x3F82 and got[-1] == 0xBF80
+
+
+def test_row_sumsq_exact_cases(orc):
+    # equal powers of two: every partial sum is exact, the total is K c^2
+    for K, c in ((128, 0.5), (5120, 2.0 ** -6), (896, 3.0)):
+        s = np.full(K, c, dtype=np.float32)
+        assert orc.row_sumsq(s) == np.float32(K * c * c)
+    # one nonzero entry per group: each group sum is that square, the total
+    # their sum in group order
+    s = np.zeros(512, np.float32)
+    s[[5, 200, 300, 511]] = [2.0, -3.0, 0.25, 1.0]
+    assert orc.row_sumsq(s) == np.float32(4 + 9 + 0.0625 + 1)
+
+
+def test_row_sumsq_within_pairwise_bound(orc):
+    rng = np.random.default_rng(4)
+    for K in (128, 1024, 5120):
+        s = bf16_to_f32(bf16_bits(rng.standard_normal(K).astype(np.float32)))
+        exact = math.fsum(float(v) * float(v) for v in s)
+        got = float(orc.row_sumsq(s))
+        # pairwise in a group: 7 roundings deep; then G sequential adds
+        depth = 7 + K // 128
+        assert abs(got - exact) <= depth * 2.0 ** -24 * exact * 1.01
+
+
+def test_residual_and_norm_match_torch(orc):
+    M, K = 6, 1024
+    prob, res, gamma = problem(M, K, seed=5)
+    t = orc.pack(prob)
+    eps = 1e-6
+    res_out, h, a, asg, rs = orc.add_rms_rotate_quant(prob.x, res, gamma, eps, prob.cs, t["rec"])
+    xs = torch.from_numpy(bf16_to_f32(prob.x)).to(torch.bfloat16)
+    rr = torch.from_numpy(bf16_to_f32(res)).to(torch.bfloat16)
+    s = xs + rr                                   # bf16 add: fp32 sum rounded once
+    assert np.array_equal(res_out, s.view(torch.int16).numpy().view(np.uint16))
+    w = 1.0 + torch.from_numpy(bf16_to_f32(gamma))
+    ref = torch.nn.functional.rms_norm(s.float(), (K,), w, eps)
+    # the same formula with another reduction order and rsqrt: within one
+    # bf16 step of the fp32 reference (plus a hair for the reference's own
+    # rounding)
+    got = torch.from_numpy(bf16_to_f32(h))
+    step = 2.0 ** -7 * ref.abs()
+    assert bool(((got - ref).abs() <= step * 1.01 + 1e-30).all())
+
+
+def test_quant_stage_is_rotate_quant_of_h(orc):
+    M, K, P = 4, 512, 3
+    prob, res, gamma = problem(M, K, P=P, seed=6)
+    t = orc.pack(prob)
+    res_out, h, a, asg, rs = orc.add_rms_rotate_quant(prob.x, res, gamma, 1e-5, prob.cs, t["rec"])
+    a2, asg2, rs2 = orc.rotate_quant(h, prob.cs, t["rec"])
+    assert np.array_equal(a, a2) and np.array_equal(asg, asg2) and np.array_equal(rs, rs2)
+
+
+def test_zero_rows_and_zero_weight(orc):
+    M, K = 3, 256
+    prob, res, gamma = problem(M, K, seed=7)
+    t = orc.pack(prob)
+    res0 = prob.x.copy() ^ np.uint16(0x8000)     # x + (-x) = 0 in every channel
+    _, h, a, asg, rs = orc.add_rms_rotate_quant(prob.x, res0, gamma, 1e-6, prob.cs, t["rec"])
+    assert not h.any() and not a.any() and not asg.any() and not rs.any()
+    # Gemma weight -1: (1 + w) = 0 zeroes every normed value
+    gneg = np.full(K, 0xBF80, dtype=np.uint16)   # bf16 -1.0
+    _, h, a, asg, rs = orc.add_rms_rotate_quant(prob.x, res, gneg, 1e-6, prob.cs, t["rec"])
+    assert not (h & 0x7FFF).any() and not a.any() and not asg.any()
+
+
+def test_scaling_by_two_leaves_h_unchanged(orc):
+    # with eps = 0: s -> 2s makes ss -> 4 ss, sqrt -> 2 sqrt, inv -> inv / 2
+    # exactly, so h is bit-identical; a dropped square or a missing 1/K breaks it
+    M, K = 4, 640
+    prob, res, gamma = problem(M, K, seed=8)
+    t = orc.pack(prob)
+    x2 = bf16_bits(bf16_to_f32(prob.x) * 2)
+    r2 = bf16_bits(bf16_to_f32(res) * 2)
+    o1 = orc.add_rms_rotate_quant(prob.x, res, gamma, 0.0, prob.cs, t["rec"])
+    o2 = orc.add_rms_rotate_quant(x2, r2, gamma, 0.0, prob.cs, t["rec"])
+    assert np.array_equal(o1[1], o2[1])
+    assert np.array_equal(bf16_to_f32(o2[0]), 2 * bf16_to_f32(o1[0]))
+
+
+def test_norm_of_constant_row_is_one(orc):
+    # s = c everywhere (power of two), gamma = 0, eps = 0: h = sign(c) exactly
+    M, K = 2, 384
+    prob, _, _ = problem(M, K, seed=9)
+    t = orc.pack(prob)
+    x = np.full((M, K), 0x3E80, dtype=np.uint16)       # 0.25
+    x[1] = 0xC100                                      # -8.0
+    zero = np.zeros((M, K), dtype=np.uint16)
+    _, h, _, _, _ = orc.add_rms_rotate_quant(x, zero, np.zeros(K, np.uint16), 0.0, prob.cs, t["rec"])
+    assert (h[0] == 0x3F80).all() and (h[1] == 0xBF80).all()
