@@ -162,6 +162,41 @@ pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P, const voi
                           const void *cs, void *a, float *asg, float *rs, void *stream);
 
 /*
+ * Fused producer ([LOG] "2026-09-02/03: rotation stream (fused add + RMSNorm
+ * + rotate + quant producers)"): residual add + Gemma RMSNorm + the
+ * pq_rotate_quant steps, for every row m < M:
+ *   s[k]  = bf16(fl(x[m][k] + residual[m][k]))          -> residual_out
+ *   ss    = sum of s[k]^2: within each 128-group the pairwise sum by
+ *           recursive halving (fp32), then the group sums added in group
+ *           order (fp32)
+ *   inv   = fl(1 / fl(sqrt(fl(fl(ss / K) + eps))))      (IEEE sqrt, divide)
+ *   h[k]  = bf16(fl(fl(s[k] * inv) * fl(1 + gamma[k])))  -> h
+ *   then a, asg, rs = pq_rotate_quant of h (all P partitions).
+ * Every step is a separately rounded IEEE operation, so the outputs are
+ * bit-identical to a CPU evaluation in that order.  M <= 16 runs one fused
+ * launch (each CTA recomputes its row's norm); larger M runs a norm kernel
+ * and then pq_rotate_quant's kernel on h.
+ *
+ *   x, residual    bf16 [M][ldx] (device), ldx >= K, ldx a multiple of 8
+ *   gamma          bf16 [K] (device): the RMSNorm weight, applied as (1 + gamma)
+ *   eps            >= 0 and finite; a row of zeros needs eps > 0
+ *   rec, cs        as for pq_rotate_quant
+ *   residual_out   bf16 [M][K] (device, written); must not overlap x or
+ *                  residual (other CTAs still read the whole input rows)
+ *   h              bf16 [M][K] (device, written): the normed rows
+ *   a, asg, rs     as written by pq_rotate_quant
+ * Programmatic dependent launch: gamma, rec and cs may be read before the
+ * preceding kernel completes; x and residual are read after it.
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE (M < 1, K not a positive multiple of 128,
+ * ldx < K, eps negative or not finite, residual_out overlapping an input),
+ * PQ_ERR_ALIGN, PQ_ERR_PARTITION, PQ_ERR_ARCH, PQ_ERR_CUDA.
+ */
+pq_status pq_add_rms_rotate_quant(const void *x, const void *residual, const void *gamma, float eps,
+                                  int M, int K, int ldx, int P, const void *rec, const void *cs,
+                                  void *residual_out, void *h, void *a, float *asg, float *rs,
+                                  void *stream);
+
+/*
  * uint4 x e4m3 group GEMM ([D1], [D2], [D4]):
  *   p(n)   = (n >= pb1) + (n >= pb2)
  *   D      = sum_{k in g} dec(a[p(n)][m][k]) * (c[k][n] - 8)

@@ -140,6 +140,30 @@ def test_rotate_quant_argument_checks(L, case, status):
     assert L.pq_rotate_quant(*[args[k] for k in order], None) == status
 
 
+X2, R2, O2, H2 = (C.c_void_p(0x300000), C.c_void_p(0x400000), C.c_void_p(0x500000),
+                  C.c_void_p(0x600000))
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(x=None), 1), (dict(gamma=None), 1), (dict(res_out=None), 1), (dict(h=None), 1),
+    (dict(M=0), 2), (dict(K=100), 2), (dict(ldx=128, K=256), 2),
+    (dict(eps=-1e-6), 2), (dict(eps=float("nan")), 2), (dict(eps=float("inf")), 2),
+    # the outputs may not overlap the inputs (other CTAs still read whole rows)
+    (dict(res_out=R2), 2), (dict(res_out=C.c_void_p(0x300000 + 512)), 2), (dict(h=X2), 2),
+    (dict(P=0), 5), (dict(P=4), 5), (dict(x=C.c_void_p(0x300008)), 3), (dict(ldx=260), 3),
+    (dict(gamma=C.c_void_p(0x100004)), 3), (dict(asg=C.c_void_p(0x200001)), 3),
+])
+@cpu_only
+def test_add_rms_rotate_quant_argument_checks(L, case, status):
+    args = dict(x=X2, res=R2, gamma=A, eps=1e-6, M=4, K=256, ldx=256, P=1, rec=A, cs=A, res_out=O2, h=H2,
+                a=A, asg=S, rs=S)
+    args.update(case)
+    order = ["x", "res", "gamma", "eps", "M", "K", "ldx", "P", "rec", "cs", "res_out", "h", "a", "asg", "rs"]
+    vals = [args[k] for k in order]
+    assert L.pq_add_rms_rotate_quant(*vals, None) == status
+    assert L.pq_last_error()
+
+
 def test_device_calls_without_gpu_report_arch(L):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -147,6 +171,7 @@ def test_device_calls_without_gpu_report_arch(L):
     vals = [A, S, S, 4, 256, 256, 1, 256, 256, A, A, A, 256]
     assert L.pq_gemm(*vals, None) == 6
     assert L.pq_rotate_quant(A, 4, 256, 256, 1, A, A, A, S, S, None) == 6
+    assert L.pq_add_rms_rotate_quant(X2, R2, A, 1e-6, 4, 256, 256, 1, A, A, O2, H2, A, S, S, None) == 6
     assert L.pq_e4m3_encode(S, A, 16, None) == 6
     with pytest.raises(pq.PQError) as e:
         pq._check(6, "probe")

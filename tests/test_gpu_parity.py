@@ -156,6 +156,66 @@ def test_prologue_strided_x(pq, orc):
     assert np.array_equal(asg.cpu().numpy(), asg_o) and np.array_equal(rs.cpu().numpy(), rs_o)
 
 
+# ---------------------------------------------------------------- fused producer
+def producer_inputs(M, K, ldx, seed):
+    """Residual rows and a Gemma weight for the fused producer (bf16 bits)."""
+    rng = np.random.default_rng(seed + 1000)
+    r = rng.standard_normal((M, ldx)).astype(np.float32) * np.float32(0.7)
+    res = torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w = rng.standard_normal(K).astype(np.float32) * np.float32(0.2)
+    gamma = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return res, gamma
+
+
+PRODUCER_CASES = [  # M, K, P, ldx pad
+    (1, 5120, 1, 0), (2, 1024, 3, 0), (3, 896, 2, 64), (4, 256, 1, 0), (16, 5120, 1, 0),
+    (17, 640, 3, 0), (100, 1152, 1, 64), (7, 16384, 1, 0),
+]
+
+
+@pytest.mark.parametrize("M,K,P,pad", PRODUCER_CASES)
+def test_add_rms_rotate_quant_bit_exact(pq, orc, M, K, P, pad):
+    N = 384 if P == 3 else 256
+    pb = (128, 256) if P == 3 else ((128, 256) if P == 2 else None)
+    prob = pqgen.make_problem(M, K, N, P=P, seed=M + K + P, pb=pb)
+    ldx = K + pad
+    xw = np.full((M, ldx), 0x7FC0, dtype=np.uint16)        # NaN padding must never be read
+    xw[:, :K] = prob.x
+    res, gamma = producer_inputs(M, K, ldx, M * 7 + K)
+    res[:, K:] = 0x7FC0
+    rec = orc.records(prob.pairs, prob.theta)
+    G = K // 128
+    bufs, (a, asg, rs), gpad = canary_outputs(P, M, K, G)
+    ro, h, a, asg, rs = pq.pq_add_rms_rotate_quant(
+        dev_u16(xw).view(torch.bfloat16), dev_u16(res).view(torch.bfloat16), dev_u16(gamma).view(torch.bfloat16),
+        1e-6, torch.from_numpy(rec).cuda(), dev_u16(prob.cs), a=a, asg=asg, rs=rs)
+    torch.cuda.synchronize()
+    ro_o, h_o, a_o, asg_o, rs_o = orc.add_rms_rotate_quant(xw, res, gamma, 1e-6, prob.cs, rec)
+    u16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(u16(ro), ro_o), "residual differs"
+    assert np.array_equal(u16(h), h_o), "normed rows differ at %s" % (np.argwhere(u16(h) != h_o)[:3].tolist(),)
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    assert np.array_equal(asg.cpu().numpy().view(np.uint32), asg_o.view(np.uint32))
+    assert np.array_equal(rs.cpu().numpy().view(np.uint32), rs_o.view(np.uint32))
+    check_guards(bufs, gpad)
+
+
+def test_add_rms_rotate_quant_feeds_the_gemm(pq, orc):
+    """The producer's outputs are a valid pq_gemm input: the layer matches the
+    oracle's GEMM of the oracle's producer outputs."""
+    M, K, N = 1, 5120, 1024
+    prob = pqgen.make_problem(M, K, N, seed=77)
+    L = Problem(pq, orc, prob)
+    res, gamma = producer_inputs(M, K, K, 77)
+    _, _, a, asg, rs = pq.pq_add_rms_rotate_quant(
+        L.x_d, dev_u16(res).view(torch.bfloat16), dev_u16(gamma).view(torch.bfloat16), 1e-6, L.rec_d, L.cs_d)
+    y = pq.pq_gemm(a, asg, rs, L.w_d, L.sz_d)
+    torch.cuda.synchronize()
+    _, _, a_o, asg_o, rs_o = orc.add_rms_rotate_quant(prob.x, res, gamma, 1e-6, prob.cs, L.t["rec"])
+    y64 = orc.gemm_f64(a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], N, N)
+    assert_close(y.float().cpu().numpy(), y64, "producer -> pq_gemm")
+
+
 # ---------------------------------------------------------------- GEMM helpers
 def gemm_paths(pq, M):
     paths = [("tc", pq.pq_gemm_tc)]

@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(_HERE, "libpq.so")
 # Every symbol include/pq.h declares.
 EXPORTS = (
     "pq_abi_version", "pq_status_string", "pq_last_error", "pq_pack_sizes", "pq_pack",
-    "pq_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny", "pq_gemm_tc",
+    "pq_rotate_quant", "pq_add_rms_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny",
+    "pq_gemm_tc",
     "pq_gemm_tcn",
     "pq_e4m3_encode",
 )
@@ -65,6 +66,8 @@ def lib() -> C.CDLL:
     L.pq_pack.argtypes = [i32, i32, i32] + [vp] * 8
     L.pq_rotate_quant.restype = i32
     L.pq_rotate_quant.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.pq_add_rms_rotate_quant.restype = i32
+    L.pq_add_rms_rotate_quant.argtypes = [vp, vp, vp, C.c_float, i32, i32, i32, i32] + [vp] * 8
     L.pq_gemm.restype = i32
     L.pq_gemm.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp]
     L.pq_gemm_skinny_max_m.restype = i32
@@ -171,6 +174,36 @@ def pq_rotate_quant(x, rec, cs, a=None, asg=None, rs=None, stream=None):
     _check(lib().pq_rotate_quant(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(a),
                                  _dptr(asg), _dptr(rs), _stream(stream)), "pq_rotate_quant")
     return a, asg, rs
+
+
+def pq_add_rms_rotate_quant(x, residual, gamma, eps, rec, cs, residual_out=None, h=None, a=None,
+                            asg=None, rs=None, stream=None):
+    """Residual add + Gemma RMSNorm + rotate + quant in one call.
+    x, residual bf16 [M, ldx>=K] (CUDA, same strides), gamma bf16 [K], eps
+    float, rec and cs as for pq_rotate_quant.  Returns (residual_out bf16
+    [M,K], h bf16 [M,K], a uint8 [P,M,K], asg f32 [P,G,M], rs f32 [P,G,M])."""
+    torch = _torch()
+    M, ldx = x.shape
+    if tuple(residual.shape) != (M, ldx) or residual.stride(0) != x.stride(0):
+        raise PQError("residual must have x's shape and row stride")
+    P, K = cs.shape
+    G = K // 128
+    dev = x.device
+    if residual_out is None:
+        residual_out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if h is None:
+        h = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if a is None:
+        a = torch.empty((P, M, K), dtype=torch.uint8, device=dev)
+    if asg is None:
+        asg = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    if rs is None:
+        rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _check(lib().pq_add_rms_rotate_quant(_dptr(x), _dptr(residual), _dptr(gamma), C.c_float(eps), M, K,
+                                         x.stride(0), P, _dptr(rec), _dptr(cs), _dptr(residual_out),
+                                         _dptr(h), _dptr(a), _dptr(asg), _dptr(rs), _stream(stream)),
+           "pq_add_rms_rotate_quant")
+    return residual_out, h, a, asg, rs
 
 
 def _gemm_args(a, asg, rs, w, sz, pb1, pb2, y):

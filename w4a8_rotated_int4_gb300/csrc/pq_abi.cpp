@@ -272,6 +272,39 @@ extern "C" pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P
     return launch_rotate_quant(x, M, K, ldx, P, rec, cs, a, asg, rs, stream);
 }
 
+// Whether [a, a + na) and [b, b + nb) share a byte.
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+extern "C" pq_status pq_add_rms_rotate_quant(const void *x, const void *residual, const void *gamma, float eps,
+                                             int M, int K, int ldx, int P, const void *rec, const void *cs,
+                                             void *residual_out, void *h, void *a, float *asg, float *rs,
+                                             void *stream) {
+    clear_error();
+    if (!x || !residual || !gamma || !rec || !cs || !residual_out || !h || !a || !asg || !rs)
+        return fail(PQ_ERR_NULL, "NULL buffer");
+    if (M < 1 || K < 128 || K % 128 || ldx < K)
+        return fail(PQ_ERR_SHAPE, "M = %d, K = %d, ldx = %d", M, K, ldx);
+    if ((long long)M * ldx > (1ll << 40)) return fail(PQ_ERR_SHAPE, "sizes too large");
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return fail(PQ_ERR_SHAPE, "eps must be finite and >= 0");
+    if (P < 1 || P > PQ_MAX_PARTITIONS) return fail(PQ_ERR_PARTITION, "P = %d outside 1..3", P);
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(gamma, 16) || !aligned(rec, 16) ||
+        !aligned(cs, 16) || !aligned(residual_out, 16) || !aligned(h, 16) || !aligned(a, 16) ||
+        !aligned(asg, 4) || !aligned(rs, 4) || ldx % 8)
+        return fail(PQ_ERR_ALIGN, "x, residual, gamma, rec, cs, residual_out, h, a need 16-byte "
+                    "alignment, asg/rs 4-byte, ldx a multiple of 8");
+    const size_t in_bytes = ((size_t)(M - 1) * ldx + K) * 2, out_bytes = (size_t)M * K * 2;
+    if (overlaps(residual_out, out_bytes, x, in_bytes) || overlaps(residual_out, out_bytes, residual, in_bytes) ||
+        overlaps(h, out_bytes, x, in_bytes) || overlaps(h, out_bytes, residual, in_bytes))
+        return fail(PQ_ERR_SHAPE, "residual_out and h must not overlap x or residual");
+    pq_status st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    return launch_add_rms_rotate_quant(x, residual, gamma, eps, M, K, ldx, P, rec, cs, residual_out, h, a, asg,
+                                       rs, stream);
+}
+
 extern "C" pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream) {
     clear_error();
     if (!in || !out) return fail(PQ_ERR_NULL, "NULL buffer");

@@ -24,6 +24,7 @@
 // Decode band (M <= 16): 64 threads per token, thread t owns pair t of every
 // layer and keeps its 8 records in registers; one CTA per (token block, group,
 // partition), so at M = 1 the whole prologue is one short dependent chain.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -256,31 +257,17 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
     }
 }
 
+// The decode-band tail shared by the small kernels: token tt's 128 scaled
+// values of group g are in v[tt] (written by all 64 threads of the token, then
+// __syncthreads); eight Givens layers through shared memory, amax, the e4m3
+// codes and the exact row-sum, stored for partition p.
 template <int T>
-__global__ void __launch_bounds__(64 * T)
-rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
-                          const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
-                          uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
-    __shared__ float v[T][128];
-    __shared__ float red_max[T][2];
-    __shared__ int red_sum[T][2];
-    const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
-    const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
-    const bool live = m < M;
-    pdl_trigger();
-
-    // the load-time tables first (channel-scale pair, the 8 records of pair t):
-    // they are read while the preceding kernel may still be running
-    const uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs + (size_t)p * K + 128 * g) + t);
-    uint2 r8[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
-    pdl_wait();        // x may be the previous kernel's output; a, asg, rs may still be read by it
-    const uint32_t xw = live ? __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m * ldx + 128 * g) + t) : 0u;
-
-    v[tt][2 * t] = __fmul_rn(bf16lo(xw), half_to_float((uint16_t)(cw & 0xFFFF)));
-    v[tt][2 * t + 1] = __fmul_rn(bf16hi(xw), half_to_float((uint16_t)(cw >> 16)));
-    __syncthreads();
+__device__ __forceinline__ void small_rotate_quant_tail(float (&v)[T][128], float (&red_max)[T][2],
+                                                        int (&red_sum)[T][2], const uint2 (&r8)[8], int tt,
+                                                        int t, int lane, int half, int m, int g, int p,
+                                                        int M, int K, bool live, uint8_t *__restrict__ a,
+                                                        float *__restrict__ asg, float *__restrict__ rs) {
+    const int G = K >> 7;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int i = r8[r].x & 0xFF, j = (r8[r].x >> 8) & 0xFF;
@@ -313,6 +300,182 @@ rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
             asg[o] = scale;
             rs[o] = __fmul_rn(__int2float_rn(red_sum[tt][0] + red_sum[tt][1]), 1.0f / 512.0f);
         }
+    }
+}
+
+template <int T>
+__global__ void __launch_bounds__(64 * T)
+rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
+                          const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
+                          uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
+    __shared__ float v[T][128];
+    __shared__ float red_max[T][2];
+    __shared__ int red_sum[T][2];
+    const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
+    const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
+    const bool live = m < M;
+    pdl_trigger();
+
+    // the load-time tables first (channel-scale pair, the 8 records of pair t):
+    // they are read while the preceding kernel may still be running
+    const uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs + (size_t)p * K + 128 * g) + t);
+    uint2 r8[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
+    pdl_wait();        // x may be the previous kernel's output; a, asg, rs may still be read by it
+    const uint32_t xw = live ? __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m * ldx + 128 * g) + t) : 0u;
+
+    v[tt][2 * t] = __fmul_rn(bf16lo(xw), half_to_float((uint16_t)(cw & 0xFFFF)));
+    v[tt][2 * t + 1] = __fmul_rn(bf16hi(xw), half_to_float((uint16_t)(cw >> 16)));
+    __syncthreads();
+    small_rotate_quant_tail<T>(v, red_max, red_sum, r8, tt, t, lane, half, m, g, p, M, K, live, a, asg, rs);
+}
+
+// ---------------------------------------------------------------------------
+// Fused producer: residual add + Gemma RMSNorm + channel scale + rotation +
+// per-group quant ("2026-09-02/03: rotation stream (fused add + RMSNorm +
+// rotate + quant producers)").  Per row:
+//   s = bf16(x + r)  (the new residual);  ss = sum of s^2 (order below);
+//   inv = 1 / sqrt(ss / K + eps)  (correctly rounded sqrt and division);
+//   h = bf16((s * inv) * (1 + gamma));  then the pq_rotate_quant steps on h.
+// Order of ss: thread t of a row's 64 holds channels 2t, 2t+1 of each
+// 128-group; the group's sum is the lane's pair sum, the xor tree over the
+// warp (channels 64 half .. +63) and warp 0's + warp 1's -- the pairwise sum
+// by recursive halving -- and the row adds the group sums in group order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_round(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
+
+__device__ __forceinline__ uint32_t bf16_pack2(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// s of the two channels of a lane, from the x and residual words
+__device__ __forceinline__ float2 residual_add(uint32_t xw, uint32_t rw) {
+    return make_float2(bf16_round(__fadd_rn(bf16lo(xw), bf16lo(rw))),
+                       bf16_round(__fadd_rn(bf16hi(xw), bf16hi(rw))));
+}
+
+// Group sums of s^2 of one row into gs[half * G + g] (one value per warp and
+// group); also returns the x and residual words of group g_keep.
+__device__ __forceinline__ void row_group_sumsq(const uint16_t *__restrict__ xrow,
+                                                const uint16_t *__restrict__ rrow, int G, int t, int lane,
+                                                int half, bool live, float *gs, int g_keep, uint32_t &xk,
+                                                uint32_t &rk) {
+    for (int g0 = 0; g0 < G; g0 += 8) {
+        uint32_t xw[8], rw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int gg = g0 + j;
+            xw[j] = rw[j] = 0u;
+            if (live && gg < G) {
+                xw[j] = __ldg(reinterpret_cast<const uint32_t *>(xrow + 128 * gg) + t);
+                rw[j] = __ldg(reinterpret_cast<const uint32_t *>(rrow + 128 * gg) + t);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int gg = g0 + j;
+            if (gg < G) {
+                const float2 s = residual_add(xw[j], rw[j]);
+                float q = __fadd_rn(__fmul_rn(s.x, s.x), __fmul_rn(s.y, s.y));
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, o));
+                if (lane == 0) gs[half * G + gg] = q;
+                if (gg == g_keep) {
+                    xk = xw[j];
+                    rk = rw[j];
+                }
+            }
+        }
+    }
+}
+
+// 1 / sqrt(ss / K + eps) of a row from its group sums (one thread)
+__device__ __forceinline__ float row_inv_rms(const float *gs, int G, int K, float eps) {
+    float ss = 0.0f;
+    for (int gg = 0; gg < G; ++gg) ss = __fadd_rn(ss, __fadd_rn(gs[gg], gs[G + gg]));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+}
+
+// Decode band: one CTA per (token block, group, partition) as the small
+// kernel, each recomputing the whole row's norm (the row is read from L2);
+// partition 0 writes the new residual and h of its group.
+template <int T>
+__global__ void __launch_bounds__(64 * T)
+add_rms_rotate_quant_small_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ res, int M,
+                                  int K, int ldx, const uint16_t *__restrict__ gamma, float eps,
+                                  const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
+                                  uint16_t *__restrict__ res_out, uint16_t *__restrict__ h_out,
+                                  uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
+    extern __shared__ float gss[];       // [T][2][G] group sums
+    __shared__ float v[T][128];
+    __shared__ float red_max[T][2];
+    __shared__ int red_sum[T][2];
+    __shared__ float inv_s[T];
+    const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
+    const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
+    const bool live = m < M;
+    pdl_trigger();
+
+    // load-time tables first: channel scales, records, Gemma weights
+    const uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs + (size_t)p * K + 128 * g) + t);
+    const uint32_t gw = __ldg(reinterpret_cast<const uint32_t *>(gamma + 128 * g) + t);
+    uint2 r8[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
+    pdl_wait();        // x and res may be the previous kernel's output
+
+    uint32_t xk = 0u, rk = 0u;
+    float *gs = gss + tt * 2 * G;
+    row_group_sumsq(x + (size_t)m * ldx, res + (size_t)m * ldx, G, t, lane, half, live, gs, g, xk, rk);
+    __syncthreads();
+    if (t == 0) inv_s[tt] = row_inv_rms(gs, G, K, eps);
+    __syncthreads();
+    const float inv = inv_s[tt];
+    const float2 s = residual_add(xk, rk);
+    const float h0 = bf16_round(__fmul_rn(__fmul_rn(s.x, inv), __fadd_rn(1.0f, bf16lo(gw))));
+    const float h1 = bf16_round(__fmul_rn(__fmul_rn(s.y, inv), __fadd_rn(1.0f, bf16hi(gw))));
+    if (live && p == 0) {
+        reinterpret_cast<uint32_t *>(res_out + (size_t)m * K + 128 * g)[t] = bf16_pack2(s.x, s.y);
+        reinterpret_cast<uint32_t *>(h_out + (size_t)m * K + 128 * g)[t] = bf16_pack2(h0, h1);
+    }
+    v[tt][2 * t] = __fmul_rn(h0, half_to_float((uint16_t)(cw & 0xFFFF)));
+    v[tt][2 * t + 1] = __fmul_rn(h1, half_to_float((uint16_t)(cw >> 16)));
+    __syncthreads();
+    small_rotate_quant_tail<T>(v, red_max, red_sum, r8, tt, t, lane, half, m, g, p, M, K, live, a, asg, rs);
+}
+
+// Above the decode band: the norm alone, four rows per CTA (64 threads per
+// row), writing the new residual and h; pq_rotate_quant's kernel follows.
+__global__ void __launch_bounds__(256)
+add_rms_norm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ res, int M, int K, int ldx,
+                    const uint16_t *__restrict__ gamma, float eps, uint16_t *__restrict__ res_out,
+                    uint16_t *__restrict__ h_out) {
+    extern __shared__ float gss[];       // [4][2][G]
+    __shared__ float inv_s[4];
+    const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
+    const int m = blockIdx.x * 4 + tt, G = K >> 7;
+    const bool live = m < M;
+    pdl_wait();        // x and res may be the previous kernel's output
+    pdl_trigger();
+    uint32_t xk = 0u, rk = 0u;
+    float *gs = gss + tt * 2 * G;
+    const uint16_t *xrow = x + (size_t)m * ldx, *rrow = res + (size_t)m * ldx;
+    row_group_sumsq(xrow, rrow, G, t, lane, half, live, gs, -1, xk, rk);
+    __syncthreads();
+    if (t == 0) inv_s[tt] = row_inv_rms(gs, G, K, eps);
+    __syncthreads();
+    if (!live) return;
+    const float inv = inv_s[tt];
+    for (int gg = 0; gg < G; ++gg) {
+        const float2 s = residual_add(__ldg(reinterpret_cast<const uint32_t *>(xrow + 128 * gg) + t),
+                                      __ldg(reinterpret_cast<const uint32_t *>(rrow + 128 * gg) + t));
+        const uint32_t gw = __ldg(reinterpret_cast<const uint32_t *>(gamma + 128 * gg) + t);
+        const float h0 = __fmul_rn(__fmul_rn(s.x, inv), __fadd_rn(1.0f, bf16lo(gw)));
+        const float h1 = __fmul_rn(__fmul_rn(s.y, inv), __fadd_rn(1.0f, bf16hi(gw)));
+        reinterpret_cast<uint32_t *>(res_out + (size_t)m * K + 128 * gg)[t] = bf16_pack2(s.x, s.y);
+        reinterpret_cast<uint32_t *>(h_out + (size_t)m * K + 128 * gg)[t] = bf16_pack2(h0, h1);
     }
 }
 
@@ -362,6 +525,58 @@ pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_quant launch: %s", cudaGetErrorString(e));
     return PQ_OK;
+}
+
+pq_status launch_add_rms_rotate_quant(const void *x, const void *res, const void *gamma, float eps, int M,
+                                      int K, int ldx, int P, const void *rec, const void *cs, void *res_out,
+                                      void *h, void *a, float *asg, float *rs, void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t *xp = static_cast<const uint16_t *>(x), *rp = static_cast<const uint16_t *>(res);
+    const uint16_t *gp = static_cast<const uint16_t *>(gamma), *cp = static_cast<const uint16_t *>(cs);
+    const uint2 *recp = static_cast<const uint2 *>(rec);
+    uint16_t *rop = static_cast<uint16_t *>(res_out), *hp = static_cast<uint16_t *>(h);
+    uint8_t *ap = static_cast<uint8_t *>(a);
+    const int G = K / 128;
+    if (G > 65535) return fail(PQ_ERR_SHAPE, "pq_add_rms_rotate_quant: K = %d too large", K);
+    cudaError_t e;
+    if (M <= 16) {
+        // decode band: one fused launch
+        const int T = M == 1 ? 1 : (M == 2 ? 2 : 4);
+        const size_t smem = (size_t)T * 2 * G * sizeof(float);
+        const dim3 grid((M + T - 1) / T, G, P), block(64 * T);
+        if (T == 1) {
+            e = cudaFuncSetAttribute(add_rms_rotate_quant_small_kernel<1>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e == cudaSuccess)
+                e = launch_pdl(add_rms_rotate_quant_small_kernel<1>, grid, block, smem, st, xp, rp, M, K, ldx, gp,
+                               eps, recp, cp, rop, hp, ap, asg, rs);
+        } else if (T == 2) {
+            e = cudaFuncSetAttribute(add_rms_rotate_quant_small_kernel<2>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e == cudaSuccess)
+                e = launch_pdl(add_rms_rotate_quant_small_kernel<2>, grid, block, smem, st, xp, rp, M, K, ldx, gp,
+                               eps, recp, cp, rop, hp, ap, asg, rs);
+        } else {
+            e = cudaFuncSetAttribute(add_rms_rotate_quant_small_kernel<4>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e == cudaSuccess)
+                e = launch_pdl(add_rms_rotate_quant_small_kernel<4>, grid, block, smem, st, xp, rp, M, K, ldx, gp,
+                               eps, recp, cp, rop, hp, ap, asg, rs);
+        }
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "add_rms_rotate_quant launch: %s", cudaGetErrorString(e));
+        return PQ_OK;
+    }
+    // above it: the norm, then the prologue on h (chained by programmatic
+    // dependent launch; the prologue waits for the norm before reading h)
+    const size_t smem = (size_t)4 * 2 * G * sizeof(float);
+    e = cudaFuncSetAttribute(add_rms_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = launch_pdl(add_rms_norm_kernel, dim3((M + 3) / 4), dim3(256), smem, st, xp, rp, M, K, ldx, gp, eps, rop,
+                       hp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "add_rms_norm launch: %s", cudaGetErrorString(e));
+    return launch_rotate_quant(h, M, K, K, P, rec, cs, a, asg, rs, stream);
 }
 
 pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream) {
