@@ -44,10 +44,11 @@
  *      RMSNorm + rotate + quant producers)": residual add + Gemma RMSNorm +
  *      channel scale + rotation + per-group quant in one pass).  Per row:
  *        s[k]  = bf16_RNE(fl32(x[k] + r[k]))          (the new residual)
- *        ss    = sum over groups g, in order, in fp32, of the group's pairwise
- *                sum of s[k]^2 (recursive halving: P(v[0:n]) =
- *                fl32(P(v[0:n/2]) + P(v[n/2:n])), P of one element = s^2,
- *                which is exact in fp32)
+ *        ss    = pairwise sum (recursive halving: P(v[0:n]) =
+ *                fl32(P(v[0:n/2]) + P(v[n/2:n]))) of the 64 lane sums
+ *                S[t] = sum over groups g, in order, in fp32, of
+ *                fl32(s[128g+2t]^2 + s[128g+2t+1]^2)  (each square is
+ *                exact in fp32)
  *        inv   = fl32(1 / fl32(sqrt(fl32(fl32(ss / K) + eps))))  (correctly
  *                rounded sqrt and division)
  *        h[k]  = bf16_RNE(fl32(fl32(s[k] * inv) * fl32(1 + gamma[k])))
@@ -368,17 +369,21 @@ static float pairwise_f32(const float *v, int n)
     return f_add(pairwise_f32(v, n / 2), pairwise_f32(v + n / 2, n / 2));
 }
 
-/* Sum of squares of one bf16-valued row of K values (reading R10). */
+/* Sum of squares of one bf16-valued row of K values (reading R10): lane t
+ * of 64 sums its channel pair (2t, 2t+1) over the groups in order, then
+ * the 64 lane sums are added pairwise. */
 float orc_row_sumsq(int K, const float *s)
 {
-    float ss = 0.0f;
-    float sq[128];
-    for (int g = 0; g < K / 128; g++) {
-        for (int k = 0; k < 128; k++)
-            sq[k] = f_mul(s[128 * g + k], s[128 * g + k]);
-        ss = f_add(ss, pairwise_f32(sq, 128));
+    float lane[64];
+    for (int t = 0; t < 64; t++) {
+        float acc = 0.0f;
+        for (int g = 0; g < K / 128; g++) {
+            const float a = s[128 * g + 2 * t], b = s[128 * g + 2 * t + 1];
+            acc = f_add(acc, f_add(f_mul(a, a), f_mul(b, b)));
+        }
+        lane[t] = acc;
     }
-    return ss;
+    return pairwise_f32(lane, 64);
 }
 
 /*

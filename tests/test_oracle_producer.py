@@ -51,8 +51,7 @@ def test_row_sumsq_exact_cases(orc):
     for K, c in ((128, 0.5), (5120, 2.0 ** -6), (896, 3.0)):
         s = np.full(K, c, dtype=np.float32)
         assert orc.row_sumsq(s) == np.float32(K * c * c)
-    # one nonzero entry per group: each group sum is that square, the total
-    # their sum in group order
+    # a few nonzero entries: every partial sum is exact
     s = np.zeros(512, np.float32)
     s[[5, 200, 300, 511]] = [2.0, -3.0, 0.25, 1.0]
     assert orc.row_sumsq(s) == np.float32(4 + 9 + 0.0625 + 1)
@@ -64,8 +63,8 @@ def test_row_sumsq_within_pairwise_bound(orc):
         s = bf16_to_f32(bf16_bits(rng.standard_normal(K).astype(np.float32)))
         exact = math.fsum(float(v) * float(v) for v in s)
         got = float(orc.row_sumsq(s))
-        # pairwise in a group: 7 roundings deep; then G sequential adds
-        depth = 7 + K // 128
+        # per lane: G sequential adds of pair sums; then 6 pairwise levels
+        depth = K // 128 + 1 + 6
         assert abs(got - exact) <= depth * 2.0 ** -24 * exact * 1.01
 
 
