@@ -165,6 +165,32 @@ class Workload:
         pq.pq_rotate_quant(self.x[j], self.rec[j], self.cs[j], a=self.a[j], asg=self.asg[j],
                            rs=self.rs[j], stream=stream)
 
+    def producer_buffers(self, torch, dev):
+        """Inputs and outputs of the fused producer (residual add + RMSNorm +
+        rotate + quant), one set per input copy, allocated on first use."""
+        if getattr(self, "res", None) is not None:
+            return
+        c, t = self.c, torch
+        M, K = c["M"], c["K"]
+        rng = np.random.default_rng(17)
+        r = t.from_numpy(rng.standard_normal((M, K)).astype(np.float32) * np.float32(0.7)).to(t.bfloat16)
+        g = t.from_numpy(rng.standard_normal(K).astype(np.float32) * np.float32(0.2)).to(t.bfloat16)
+        self.res = [r.to(dev) for _ in range(self.copies)]
+        self.gamma = [g.to(dev) for _ in range(self.copies)]
+        self.res_out = [t.empty((M, K), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
+        self.h = [t.empty((M, K), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
+        P, G = c["P"], K // 128
+        # bytes the producer must move: x, residual, gamma, cs, records in;
+        # new residual, normed rows, codes, scales and row-sums out
+        self.prod_bytes = 2 * M * K * 2 + K * 2 + P * K * 2 + P * 8 * G * 64 * 8 + \
+            2 * M * K * 2 + P * M * K + 2 * P * G * M * 4
+
+    def producer(self, pq, i, stream):
+        j = i % self.copies
+        pq.pq_add_rms_rotate_quant(self.x[j], self.res[j], self.gamma[j], 1e-6, self.rec[j], self.cs[j],
+                                   residual_out=self.res_out[j], h=self.h[j], a=self.a[j], asg=self.asg[j],
+                                   rs=self.rs[j], stream=stream)
+
     def gemm(self, pq, i, stream, fn=None):
         j = i % self.copies
         (fn or pq.pq_gemm)(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1,
@@ -238,8 +264,24 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
         b.record(stream)
         torch.cuda.synchronize()
         per[key] = a.elapsed_time(b) / (reps * C)
+    # the fused producer (residual add + RMSNorm + rotate + quant) on its own
+    wl.producer_buffers(torch, wl.x[0].device)
+    for j in range(C):
+        wl.producer(pq, j, None)
+    torch.cuda.synchronize()
+    g_prod = _capture(torch, lambda: [wl.producer(pq, j, None) for j in range(C)])
+    g_prod.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g_prod.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    per["prod"] = a.elapsed_time(b) / (reps * C)
     paths = time_gemm_paths(pq, torch, wl, reps, stream) if wl.c["M"] <= 16 else {}
-    return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths)
+    return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths,
+                prod_ms=per["prod"])
 
 
 def time_gemm_paths(pq, torch, wl, reps, stream):
@@ -363,6 +405,9 @@ def summarize(wl, r, steps, peaks):
         "gemm_tflops": round(wl.flops / (r["gemm_ms"] * 1e-3) / 1e12, 2),
         "gemm_gbs": round(wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9, 1),
         "prologue_gbs": round(wl.pro_bytes / (r["pro_ms"] * 1e-3) / 1e9, 1),
+        # the fused producer (residual add + RMSNorm + rotate + quant) alone
+        "producer_us": round(r["prod_ms"] * 1e3, 3),
+        "producer_gbs": round(wl.prod_bytes / (r["prod_ms"] * 1e-3) / 1e9, 1),
         "roofline": roofline(wl, r, peaks, ncu_traffic(KERNEL_NAMES[wl.gemm_kernel], wl.name)),
         "copies": wl.copies,
         "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
@@ -552,6 +597,7 @@ def main():
                    "P": wl.c["P"], "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "%d rotating input copies (> 2x L2)" % wl.copies},
         "prologue_us": head["prologue_us"], "gemm_us": head["gemm_us"],
+        "producer_us": head["producer_us"],
         "roofline": head["roofline"],
         "gemm_us_by_kernel": head["gemm_us_by_kernel"],
         "e2e": None if e2e_ms is None else {

@@ -166,9 +166,9 @@ pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P, const voi
  * + rotate + quant producers)"): residual add + Gemma RMSNorm + the
  * pq_rotate_quant steps, for every row m < M:
  *   s[k]  = bf16(fl(x[m][k] + residual[m][k]))          -> residual_out
- *   ss    = sum of s[k]^2: within each 128-group the pairwise sum by
- *           recursive halving (fp32), then the group sums added in group
- *           order (fp32)
+ *   ss    = sum of s[k]^2: lane t of 64 sums fl(s^2 + s'^2) of its channel
+ *           pair (128g+2t, 128g+2t+1) over the groups in order (fp32), then
+ *           the 64 lane sums are added pairwise by recursive halving (fp32)
  *   inv   = fl(1 / fl(sqrt(fl(fl(ss / K) + eps))))      (IEEE sqrt, divide)
  *   h[k]  = bf16(fl(fl(s[k] * inv) * fl(1 + gamma[k])))  -> h
  *   then a, asg, rs = pq_rotate_quant of h (all P partitions).

@@ -339,9 +339,9 @@ rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
 //   inv = 1 / sqrt(ss / K + eps)  (correctly rounded sqrt and division);
 //   h = bf16((s * inv) * (1 + gamma));  then the pq_rotate_quant steps on h.
 // Order of ss: thread t of a row's 64 holds channels 2t, 2t+1 of each
-// 128-group; the group's sum is the lane's pair sum, the xor tree over the
-// warp (channels 64 half .. +63) and warp 0's + warp 1's -- the pairwise sum
-// by recursive halving -- and the row adds the group sums in group order.
+// 128-group and sums fl(s^2 + s'^2) over the groups in order (its lane sum);
+// the 64 lane sums are added pairwise by recursive halving: the xor tree over
+// each warp, then warp 0's + warp 1's.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_round(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
 
@@ -356,46 +356,51 @@ __device__ __forceinline__ float2 residual_add(uint32_t xw, uint32_t rw) {
                        bf16_round(__fadd_rn(bf16hi(xw), bf16hi(rw))));
 }
 
-// Group sums of s^2 of one row into gs[half * G + g] (one value per warp and
-// group); also returns the x and residual words of group g_keep.
-__device__ __forceinline__ void row_group_sumsq(const uint16_t *__restrict__ xrow,
-                                                const uint16_t *__restrict__ rrow, int G, int t, int lane,
-                                                int half, bool live, float *gs, int g_keep, uint32_t &xk,
-                                                uint32_t &rk) {
-    for (int g0 = 0; g0 < G; g0 += 8) {
-        uint32_t xw[8], rw[8];
+// This lane's sum over the groups, in order, of fl(s^2 + s'^2) for its
+// channel pair, with x and residual words read through rd(gg) -> (xw, rw).
+template <class Read>
+__device__ __forceinline__ float lane_sumsq(int G, Read rd) {
+    float acc = 0.0f;
+    int gg = 0;
+    for (; gg + 8 <= G; gg += 8) {
+        uint2 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = rd(gg + j);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int gg = g0 + j;
-            xw[j] = rw[j] = 0u;
-            if (live && gg < G) {
-                xw[j] = __ldg(reinterpret_cast<const uint32_t *>(xrow + 128 * gg) + t);
-                rw[j] = __ldg(reinterpret_cast<const uint32_t *>(rrow + 128 * gg) + t);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int gg = g0 + j;
-            if (gg < G) {
-                const float2 s = residual_add(xw[j], rw[j]);
-                float q = __fadd_rn(__fmul_rn(s.x, s.x), __fmul_rn(s.y, s.y));
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, o));
-                if (lane == 0) gs[half * G + gg] = q;
-                if (gg == g_keep) {
-                    xk = xw[j];
-                    rk = rw[j];
-                }
-            }
+            const float2 s = residual_add(w[j].x, w[j].y);
+            acc = __fadd_rn(acc, __fadd_rn(__fmul_rn(s.x, s.x), __fmul_rn(s.y, s.y)));
         }
     }
+    for (; gg < G; ++gg) {
+        const uint2 w = rd(gg);
+        const float2 s = residual_add(w.x, w.y);
+        acc = __fadd_rn(acc, __fadd_rn(__fmul_rn(s.x, s.x), __fmul_rn(s.y, s.y)));
+    }
+    return acc;
 }
 
-// 1 / sqrt(ss / K + eps) of a row from its group sums (one thread)
-__device__ __forceinline__ float row_inv_rms(const float *gs, int G, int K, float eps) {
-    float ss = 0.0f;
-    for (int gg = 0; gg < G; ++gg) ss = __fadd_rn(ss, __fadd_rn(gs[gg], gs[G + gg]));
+// The pairwise sum of the row's 64 lane sums: the xor tree over the warp
+// (every lane ends with the warp's sum), written to wsum[half]; after a
+// __syncthreads, row_inv_rms adds warp 0's and warp 1's.
+__device__ __forceinline__ void warp_pairwise(float acc, int lane, int half, float *wsum) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+    if (lane == 0) wsum[half] = acc;
+}
+
+// 1 / sqrt(ss / K + eps) from the two warps' sums
+__device__ __forceinline__ float row_inv_rms(const float *wsum, int K, float eps) {
+    const float ss = __fadd_rn(wsum[0], wsum[1]);
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+}
+
+// 16-byte asynchronous global -> shared copy, zero-filled when !valid (the
+// source is then not read)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
 }
 
 // Decode band: one CTA per (token block, group, partition) as the small
@@ -408,14 +413,17 @@ add_rms_rotate_quant_small_kernel(const uint16_t *__restrict__ x, const uint16_t
                                   const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
                                   uint16_t *__restrict__ res_out, uint16_t *__restrict__ h_out,
                                   uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
-    extern __shared__ float gss[];       // [T][2][G] group sums
+    // dynamic shared memory: each token's x row and residual row [T][2][K]
+    // (bf16), staged with one wave of copies
+    extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ float v[T][128];
     __shared__ float red_max[T][2];
     __shared__ int red_sum[T][2];
-    __shared__ float inv_s[T];
+    __shared__ float wsum[T][2];
     const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
     const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = K >> 7;
     const bool live = m < M;
+    uint16_t *rows = reinterpret_cast<uint16_t *>(dsm);
     pdl_trigger();
 
     // load-time tables first: channel scales, records, Gemma weights
@@ -426,13 +434,22 @@ add_rms_rotate_quant_small_kernel(const uint16_t *__restrict__ x, const uint16_t
     for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
     pdl_wait();        // x and res may be the previous kernel's output
 
-    uint32_t xk = 0u, rk = 0u;
-    float *gs = gss + tt * 2 * G;
-    row_group_sumsq(x + (size_t)m * ldx, res + (size_t)m * ldx, G, t, lane, half, live, gs, g, xk, rk);
+    uint16_t *xs = rows + (size_t)tt * 2 * K, *rsm = xs + K;
+    {
+        const uint16_t *xrow = x + (size_t)m * ldx, *rrow = res + (size_t)m * ldx;
+        for (int c = t; c < K / 8; c += 64) {      // 16-byte chunks of 8 values
+            cp_async16(xs + 8 * c, live ? xrow + 8 * c : x, live);
+            cp_async16(rsm + 8 * c, live ? rrow + 8 * c : res, live);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
     __syncthreads();
-    if (t == 0) inv_s[tt] = row_inv_rms(gs, G, K, eps);
+    const uint32_t *xs32 = reinterpret_cast<const uint32_t *>(xs), *rs32 = reinterpret_cast<const uint32_t *>(rsm);
+    warp_pairwise(lane_sumsq(G, [&](int gg) { return make_uint2(xs32[64 * gg + t], rs32[64 * gg + t]); }), lane,
+                  half, wsum[tt]);
+    const uint32_t xk = xs32[64 * g + t], rk = rs32[64 * g + t];
     __syncthreads();
-    const float inv = inv_s[tt];
+    const float inv = row_inv_rms(wsum[tt], K, eps);
     const float2 s = residual_add(xk, rk);
     const float h0 = bf16_round(__fmul_rn(__fmul_rn(s.x, inv), __fadd_rn(1.0f, bf16lo(gw))));
     const float h1 = bf16_round(__fmul_rn(__fmul_rn(s.y, inv), __fadd_rn(1.0f, bf16hi(gw))));
@@ -452,22 +469,21 @@ __global__ void __launch_bounds__(256)
 add_rms_norm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ res, int M, int K, int ldx,
                     const uint16_t *__restrict__ gamma, float eps, uint16_t *__restrict__ res_out,
                     uint16_t *__restrict__ h_out) {
-    extern __shared__ float gss[];       // [4][2][G]
-    __shared__ float inv_s[4];
+    __shared__ float wsum[4][2];
     const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
     const int m = blockIdx.x * 4 + tt, G = K >> 7;
     const bool live = m < M;
     pdl_wait();        // x and res may be the previous kernel's output
     pdl_trigger();
-    uint32_t xk = 0u, rk = 0u;
-    float *gs = gss + tt * 2 * G;
     const uint16_t *xrow = x + (size_t)m * ldx, *rrow = res + (size_t)m * ldx;
-    row_group_sumsq(xrow, rrow, G, t, lane, half, live, gs, -1, xk, rk);
-    __syncthreads();
-    if (t == 0) inv_s[tt] = row_inv_rms(gs, G, K, eps);
+    const uint32_t *x32 = reinterpret_cast<const uint32_t *>(xrow), *r32 = reinterpret_cast<const uint32_t *>(rrow);
+    warp_pairwise(lane_sumsq(G, [&](int gg) {
+                      return live ? make_uint2(__ldg(x32 + 64 * gg + t), __ldg(r32 + 64 * gg + t)) : make_uint2(0u, 0u);
+                  }),
+                  lane, half, wsum[tt]);
     __syncthreads();
     if (!live) return;
-    const float inv = inv_s[tt];
+    const float inv = row_inv_rms(wsum[tt], K, eps);
     for (int gg = 0; gg < G; ++gg) {
         const float2 s = residual_add(__ldg(reinterpret_cast<const uint32_t *>(xrow + 128 * gg) + t),
                                       __ldg(reinterpret_cast<const uint32_t *>(rrow + 128 * gg) + t));
@@ -539,10 +555,12 @@ pq_status launch_add_rms_rotate_quant(const void *x, const void *res, const void
     const int G = K / 128;
     if (G > 65535) return fail(PQ_ERR_SHAPE, "pq_add_rms_rotate_quant: K = %d too large", K);
     cudaError_t e;
-    if (M <= 16) {
+    const int Tsmall = M == 1 ? 1 : (M == 2 ? 2 : 4);
+    const size_t small_smem = (size_t)Tsmall * 2 * K * 2;
+    if (M <= 16 && small_smem <= 160 * 1024) {
         // decode band: one fused launch
         const int T = M == 1 ? 1 : (M == 2 ? 2 : 4);
-        const size_t smem = (size_t)T * 2 * G * sizeof(float);
+        const size_t smem = (size_t)T * 2 * K * 2;
         const dim3 grid((M + T - 1) / T, G, P), block(64 * T);
         if (T == 1) {
             e = cudaFuncSetAttribute(add_rms_rotate_quant_small_kernel<1>,
@@ -569,11 +587,7 @@ pq_status launch_add_rms_rotate_quant(const void *x, const void *res, const void
     }
     // above it: the norm, then the prologue on h (chained by programmatic
     // dependent launch; the prologue waits for the norm before reading h)
-    const size_t smem = (size_t)4 * 2 * G * sizeof(float);
-    e = cudaFuncSetAttribute(add_rms_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-        e = launch_pdl(add_rms_norm_kernel, dim3((M + 3) / 4), dim3(256), smem, st, xp, rp, M, K, ldx, gp, eps, rop,
-                       hp);
+    e = launch_pdl(add_rms_norm_kernel, dim3((M + 3) / 4), dim3(256), 0, st, xp, rp, M, K, ldx, gp, eps, rop, hp);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "add_rms_norm launch: %s", cudaGetErrorString(e));
     return launch_rotate_quant(h, M, K, K, P, rec, cs, a, asg, rs, stream);
