@@ -202,19 +202,19 @@ def rotate_quant(x: np.ndarray, cs: np.ndarray, rec: np.ndarray, want_v: bool = 
     return (a, asg, rs, v) if want_v else (a, asg, rs)
 
 
-# ------------------------------------------------- fused producer (reading R10)
+# ------------------------------------------------- fused producer (reading R16)
 def bf16_from_float(f: float) -> int:
     return int(lib().orc_bf16_from_float(f))
 
 
 def row_sumsq(s: np.ndarray) -> np.float32:
-    """fp32 sum of squares of one row of bf16 values (reading R10 order)."""
+    """fp32 sum of squares of one row of bf16 values (reading R16 order)."""
     s = _c(s, np.float32)
     return np.float32(lib().orc_row_sumsq(s.shape[0], _p(s)))
 
 
 def add_rms_rotate_quant(x, res, gamma, eps, cs, rec):
-    """Residual add + Gemma RMSNorm + rotate + quant (reading R10).
+    """Residual add + Gemma RMSNorm + rotate + quant (reading R16).
     x, res bf16 bits [M, ldx]; gamma bf16 bits [K]; eps float; cs f16 bits
     [P, K].  Returns (res_out bf16 [M,K], h bf16 [M,K], a, asg, rs)."""
     x = _c(x, np.uint16)

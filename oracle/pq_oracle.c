@@ -40,7 +40,7 @@
  *   R9 GEMM: y = sum_g asg * (sc * D - zscale * rs) with
  *      D = sum_{k in g} dec(A[k]) * (c[k] - 8), in fp64, using the f16 table
  *      values ("table-true").
- *   R10 fused producer ([LOG] "2026-09-02/03: rotation stream (fused add +
+ *   R16 fused producer ([LOG] "2026-09-02/03: rotation stream (fused add +
  *      RMSNorm + rotate + quant producers)": residual add + Gemma RMSNorm +
  *      channel scale + rotation + per-group quant in one pass).  Per row:
  *        s[k]  = bf16_RNE(fl32(x[k] + r[k]))          (the new residual)
@@ -360,7 +360,7 @@ uint16_t orc_bf16_from_float(float f)
     return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
 }
 
-/* Pairwise sum of n = 2^j fp32 values (reading R10): the two halves' sums,
+/* Pairwise sum of n = 2^j fp32 values (reading R16): the two halves' sums,
  * added in fp32. */
 static float pairwise_f32(const float *v, int n)
 {
@@ -369,7 +369,7 @@ static float pairwise_f32(const float *v, int n)
     return f_add(pairwise_f32(v, n / 2), pairwise_f32(v + n / 2, n / 2));
 }
 
-/* Sum of squares of one bf16-valued row of K values (reading R10): lane t
+/* Sum of squares of one bf16-valued row of K values (reading R16): lane t
  * of 64 sums its channel pair (2t, 2t+1) over the groups in order, then
  * the 64 lane sums are added pairwise. */
 float orc_row_sumsq(int K, const float *s)
@@ -387,7 +387,7 @@ float orc_row_sumsq(int K, const float *s)
 }
 
 /*
- * Fused producer (reading R10).  x, res bf16 [M][ldx]; gamma bf16 [K]; the
+ * Fused producer (reading R16).  x, res bf16 [M][ldx]; gamma bf16 [K]; the
  * rest as orc_rotate_quant.  Writes res_out bf16 [M][K] (the new residual),
  * h_out bf16 [M][K] (the normed rows) and the rotate_quant outputs of h.
  */

@@ -6,7 +6,7 @@ Page: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", section
 "2026-09-02/03: rotation stream (fused add + RMSNorm + rotate + quant
 producers)": one producer does residual add + Gemma RMSNorm (vLLM's op order)
 + channel scale + rotation + per-group quant and returns (hs, residual, A,
-ASG, RS).  The summation order and the rsqrt rounding are readings (R10).
+ASG, RS).  The summation order and the rsqrt rounding are readings (R16).
 """
 import math
 
