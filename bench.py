@@ -355,9 +355,9 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
         sha256="f428a3813b839e774e476dc474be35d494ce09ae446cf233e439db3c0f0fd33e"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47468544 + 768, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
+        bytes=47469568 + 0, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="d32fccfa38ae6671c70e584b8fbfa0cbf2d59e889b805d8957520b96514a4d6e"),
+        sha256="0d5ace53fa4ba86815ab1be091a380b093aac698c16677376cf9599502fea61a"),
 }
 
 
