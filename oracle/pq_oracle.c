@@ -20,7 +20,7 @@
  *   [CVT]  same page, section "2026-09-15: hardware e4m3 convert in the
  *          producers" (NaN -> 0, -0 -> +0, clamp +-448, then RNE convert).
  *
- * Readings of points the pages leave open (each also listed in the design doc):
+ * Readings of points the pages leave open:
  *   R1 pairs: entries 2t and 2t+1 of a layer's 128-group form pair t, and the
  *      angle of pair t is theta[layer][64*g + t].
  *   R2 rotation: x_i' = c*x_i + s*x_j, x_j' = -s*x_i + c*x_j, layers 0..7,
