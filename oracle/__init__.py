@@ -55,6 +55,11 @@ def lib():
         L.orc_row_sumsq.argtypes = [i32, vp]
         L.orc_add_rms_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, C.c_float, vp, vp,
                                                vp, vp, vp, vp, vp]
+        L.orc_exp32.restype = C.c_float
+        L.orc_exp32.argtypes = [C.c_float]
+        L.orc_silu_mul.restype = C.c_uint16
+        L.orc_silu_mul.argtypes = [C.c_uint16, C.c_uint16]
+        L.orc_silu_mul_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.orc_gemm_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.orc_gemm_f64_sampled.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp]
@@ -234,6 +239,34 @@ def add_rms_rotate_quant(x, res, gamma, eps, cs, rec):
     lib().orc_add_rms_rotate_quant(M, K, ldx, P, _p(x), _p(res), _p(gamma), float(eps), _p(cs),
                                    _p(rec), _p(res_out), _p(h), _p(a), _p(asg), _p(rs))
     return res_out, h, a, asg, rs
+
+
+# ------------------------------------------------- silu-mul producer (reading R17)
+def exp32(x: float) -> float:
+    return float(lib().orc_exp32(x))
+
+
+def silu_mul(g: int, u: int) -> int:
+    """bf16 bits of bf16(bf16(silu(g)) * u) for bf16 bits g, u."""
+    return int(lib().orc_silu_mul(g, u))
+
+
+def silu_mul_rotate_quant(y, cs, rec):
+    """y bf16 bits [M, ldy] with gate in [0, I) and up in [I, 2I), I = K of
+    cs.  Returns (act bf16 [M,I], a, asg, rs)."""
+    y = _c(y, np.uint16)
+    cs = _c(cs, np.uint16)
+    rec = _c(rec, np.uint8)
+    M, ldy = y.shape
+    P, I = cs.shape
+    assert ldy >= 2 * I
+    G = I // 128
+    act = np.empty((M, I), dtype=np.uint16)
+    a = np.empty((P, M, I), dtype=np.uint8)
+    asg = np.empty((P, G, M), dtype=np.float32)
+    rs = np.empty((P, G, M), dtype=np.float32)
+    lib().orc_silu_mul_rotate_quant(M, I, ldy, P, _p(y), _p(cs), _p(rec), _p(act), _p(a), _p(asg), _p(rs))
+    return act, a, asg, rs
 
 
 # ---------------------------------------------------------------- GEMM

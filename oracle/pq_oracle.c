@@ -55,6 +55,20 @@
  *      then the pq_rotate_quant semantics on h.  The pages fix the op order
  *      ("in vLLM's exact op order": s * rsqrt(mean(s^2) + eps) * (1 + w)) but
  *      not the reduction order or the rsqrt rounding; these are the readings.
+ *   R17 silu-mul producer ([LOG] "2026-09-03: rotation stream 2 (silu-mul,
+ *      ...)": "MODE 0 silu(g)*u (bf16-rounded silu, bf16 product)" + the
+ *      rotate_quant body).  The merged gate/up output y holds g in columns
+ *      [0, I) and u in [I, 2I).  Per element:
+ *        e   = exp32(-g)        (below)
+ *        sg  = bf16_RNE(fl32(g / fl32(1 + e)))
+ *        act = bf16_RNE(fl32(sg * u))
+ *      then the pq_rotate_quant semantics on act (K = I).  exp32 is fixed
+ *      here so that both implementations give the same bits: Cody-Waite
+ *      reduction n = rint(x * log2(e)), r = fl(fl(x - n*LN2_HI) - n*LN2_LO)
+ *      (LN2_HI = 0.693145751953125 has 13 trailing zero bits, so n*LN2_HI is
+ *      exact for |n| <= 2^13), the Taylor polynomial of exp of degree 6 in
+ *      Horner form with separately rounded steps, and an exact scaling by
+ *      2^n (x < -103 gives 0, x > 88 gives +inf).
  */
 #include <math.h>
 #include <stdint.h>
@@ -414,6 +428,51 @@ void orc_add_rms_rotate_quant(int M, int K, int ldx, int P, const uint16_t *x, c
         free(s);
     }
     orc_rotate_quant(M, K, K, P, h_out, cs, rec, a, asg, rs, NULL);
+}
+
+/* exp(x) in fp32 by the fixed sequence of reading R17. */
+float orc_exp32(float x)
+{
+    if (x > 88.0f)
+        return INFINITY;
+    if (x < -103.0f)
+        return 0.0f;
+    const float log2e = 1.44269502f, ln2_hi = 0.693145751953125f, ln2_lo = 1.42860677e-06f;
+    const float n = rintf(f_mul(x, log2e));
+    const float r = f_sub(f_sub(x, f_mul(n, ln2_hi)), f_mul(n, ln2_lo));
+    /* 1 + r(1 + r(1/2 + r(1/6 + r(1/24 + r(1/120 + r/720))))) */
+    float p = f_mul(r, 1.0f / 720.0f);
+    p = f_mul(r, f_add(1.0f / 120.0f, p));
+    p = f_mul(r, f_add(1.0f / 24.0f, p));
+    p = f_mul(r, f_add(1.0f / 6.0f, p));
+    p = f_mul(r, f_add(0.5f, p));
+    p = f_mul(r, f_add(1.0f, p));
+    p = f_add(1.0f, p);
+    return ldexpf(p, (int)n);
+}
+
+/* silu(g) * u of one element as bf16 bits (reading R17). */
+uint16_t orc_silu_mul(uint16_t g, uint16_t u)
+{
+    const float gf = orc_bf16_to_float(g);
+    const float e = orc_exp32(-gf);
+    const float sg = orc_bf16_to_float(orc_bf16_from_float(f_div(gf, f_add(1.0f, e))));
+    return orc_bf16_from_float(f_mul(sg, orc_bf16_to_float(u)));
+}
+
+/*
+ * silu-mul producer (reading R17).  y bf16 [M][ldy] with the gate in
+ * columns [0, I) and up in [I, 2I); writes act_out bf16 [M][I] and the
+ * rotate_quant outputs of act (K = I).
+ */
+void orc_silu_mul_rotate_quant(int M, int I, int ldy, int P, const uint16_t *y, const uint16_t *cs,
+                               const uint8_t *rec, uint16_t *act_out, uint8_t *a, float *asg, float *rs)
+{
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; m++)
+        for (int k = 0; k < I; k++)
+            act_out[(size_t)m * I + k] = orc_silu_mul(y[(size_t)m * ldy + k], y[(size_t)m * ldy + I + k]);
+    orc_rotate_quant(M, I, I, P, act_out, cs, rec, a, asg, rs, NULL);
 }
 
 /* ------------------------------------------------------------------ */

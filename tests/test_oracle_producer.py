@@ -134,3 +134,51 @@ def test_norm_of_constant_row_is_one(orc):
     zero = np.zeros((M, K), dtype=np.uint16)
     _, h, _, _, _ = orc.add_rms_rotate_quant(x, zero, np.zeros(K, np.uint16), 0.0, prob.cs, t["rec"])
     assert (h[0] == 0x3F80).all() and (h[1] == 0xBF80).all()
+
+
+# ---------------------------------------------------------------- silu-mul producer
+# Page: same log, "2026-09-03: rotation stream 2 (silu-mul, GDN gated norm,
+# attention gate fused with rotate+quant)": MODE 0 is silu(g)*u with a
+# bf16-rounded silu and a bf16 product, then the rotate_quant body.  The exp
+# routine is a reading (R17) fixed so both implementations agree bit for bit.
+def test_exp32_accuracy(orc):
+    xs = np.concatenate([np.linspace(-87.0, 88.0, 20001), [0.0, -1e-8, 1e-8, 0.5, -0.5, 1.0]])
+    for x in xs:
+        x = float(np.float32(x))
+        got, ref = orc.exp32(x), math.exp(x)
+        assert abs(got - ref) <= 2.0 ** -22 * ref, (x, got, ref)
+    assert orc.exp32(0.0) == 1.0
+    assert orc.exp32(89.0) == math.inf and orc.exp32(-104.0) == 0.0
+
+
+def test_silu_mul_matches_torch(orc):
+    rng = np.random.default_rng(11)
+    g = bf16_bits(np.concatenate([rng.standard_normal(3000).astype(np.float32) * 4,
+                                  np.array([0.0, 50.0, -100.0, 1.0, -1.0], np.float32)]))
+    u = bf16_bits(rng.standard_normal(g.size).astype(np.float32) * 2)
+    got = np.array([orc.silu_mul(int(a), int(b)) for a, b in zip(g, u)], dtype=np.uint16)
+    gt = torch.from_numpy(bf16_to_f32(g)).to(torch.bfloat16)
+    ut = torch.from_numpy(bf16_to_f32(u)).to(torch.bfloat16)
+    ref = (torch.nn.functional.silu(gt.float()).to(torch.bfloat16) * ut).float().numpy()
+    gotf = bf16_to_f32(got)
+    # another exp can move the bf16 silu by one step, and the product by one more
+    assert np.all(np.abs(gotf - ref) <= 2.0 ** -6 * np.abs(ref) + 1e-37)
+    assert np.mean(gotf == ref) > 0.99
+    # special values: silu(0) = 0; silu(50) = 50 exactly; silu(-100) = -0
+    assert gotf[-5] == 0.0
+    assert gotf[-4] == bf16_to_f32(bf16_bits(np.float32(50.0) * bf16_to_f32(u[-4:-3])))[0]
+    assert gotf[-3] == 0.0
+
+
+def test_silu_mul_quant_stage_is_rotate_quant(orc):
+    M, I, P = 3, 384, 2
+    prob = pqgen.make_problem(M, I, 256, P=P, seed=12, pb=(128, 256))
+    t = orc.pack(prob)
+    rng = np.random.default_rng(13)
+    y = bf16_bits(rng.standard_normal((M, 2 * I + 64)).astype(np.float32) * 3)
+    act, a, asg, rs = orc.silu_mul_rotate_quant(y, prob.cs, t["rec"])
+    expect = np.array([[orc.silu_mul(int(y[m, k]), int(y[m, I + k])) for k in range(I)] for m in range(M)],
+                      dtype=np.uint16)
+    assert np.array_equal(act, expect)
+    a2, asg2, rs2 = orc.rotate_quant(act, prob.cs, t["rec"])
+    assert np.array_equal(a, a2) and np.array_equal(asg, asg2) and np.array_equal(rs, rs2)
