@@ -179,6 +179,10 @@ class Workload:
         self.gamma = [g.to(dev) for _ in range(self.copies)]
         self.res_out = [t.empty((M, K), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
         self.h = [t.empty((M, K), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
+        # the silu-mul producer's merged gate/up input, for I = K
+        yv = rng.standard_normal((M, 2 * K)).astype(np.float32) * np.float32(3.0)
+        self.ygu = [t.from_numpy(yv).to(t.bfloat16).to(dev) for _ in range(self.copies)]
+        self.act = [t.empty((M, K), dtype=t.bfloat16, device=dev) for _ in range(self.copies)]
         P, G = c["P"], K // 128
         # bytes the producer must move: x, residual, gamma, cs, records in;
         # new residual, normed rows, codes, scales and row-sums out
@@ -190,6 +194,11 @@ class Workload:
         pq.pq_add_rms_rotate_quant(self.x[j], self.res[j], self.gamma[j], 1e-6, self.rec[j], self.cs[j],
                                    residual_out=self.res_out[j], h=self.h[j], a=self.a[j], asg=self.asg[j],
                                    rs=self.rs[j], stream=stream)
+
+    def silu_producer(self, pq, i, stream):
+        j = i % self.copies
+        pq.pq_silu_mul_rotate_quant(self.ygu[j], self.rec[j], self.cs[j], act=self.act[j], a=self.a[j],
+                                    asg=self.asg[j], rs=self.rs[j], stream=stream)
 
     def gemm(self, pq, i, stream, fn=None):
         j = i % self.copies
@@ -279,9 +288,22 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
     b.record(stream)
     torch.cuda.synchronize()
     per["prod"] = a.elapsed_time(b) / (reps * C)
+    # the silu-mul producer on its own
+    for j in range(C):
+        wl.silu_producer(pq, j, None)
+    torch.cuda.synchronize()
+    g_silu = _capture(torch, lambda: [wl.silu_producer(pq, j, None) for j in range(C)])
+    g_silu.replay()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        g_silu.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    per["silu"] = a.elapsed_time(b) / (reps * C)
     paths = time_gemm_paths(pq, torch, wl, reps, stream) if wl.c["M"] <= 16 else {}
     return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths,
-                prod_ms=per["prod"])
+                prod_ms=per["prod"], silu_ms=per["silu"])
 
 
 def time_gemm_paths(pq, torch, wl, reps, stream):
@@ -408,6 +430,8 @@ def summarize(wl, r, steps, peaks):
         # the fused producer (residual add + RMSNorm + rotate + quant) alone
         "producer_us": round(r["prod_ms"] * 1e3, 3),
         "producer_gbs": round(wl.prod_bytes / (r["prod_ms"] * 1e-3) / 1e9, 1),
+        # the silu-mul producer (silu(gate) * up + rotate + quant, I = K) alone
+        "silu_producer_us": round(r["silu_ms"] * 1e3, 3),
         "roofline": roofline(wl, r, peaks, ncu_traffic(KERNEL_NAMES[wl.gemm_kernel], wl.name)),
         "copies": wl.copies,
         "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
@@ -597,7 +621,7 @@ def main():
                    "P": wl.c["P"], "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "%d rotating input copies (> 2x L2)" % wl.copies},
         "prologue_us": head["prologue_us"], "gemm_us": head["gemm_us"],
-        "producer_us": head["producer_us"],
+        "producer_us": head["producer_us"], "silu_producer_us": head["silu_producer_us"],
         "roofline": head["roofline"],
         "gemm_us_by_kernel": head["gemm_us_by_kernel"],
         "e2e": None if e2e_ms is None else {

@@ -197,6 +197,37 @@ pq_status pq_add_rms_rotate_quant(const void *x, const void *residual, const voi
                                   void *stream);
 
 /*
+ * silu-mul producer ([LOG] "2026-09-03: rotation stream 2 (silu-mul, GDN
+ * gated norm, attention gate fused with rotate+quant)", MODE 0): for every
+ * row m < M and channel k < I of the merged gate/up output y (gate g in
+ * columns [0, I), up u in [I, 2I)):
+ *   e      = exp32(-g)   -- a fixed fp32 sequence: n = rint(fl(x log2 e)),
+ *            r = fl(fl(x - n ln2_hi) - n ln2_lo) with ln2_hi =
+ *            0.693145751953125, ln2_lo = 1.42860677e-06, the degree-6 Taylor
+ *            polynomial of exp in Horner form, exact scaling by 2^n; x > 88
+ *            gives +inf, x < -103 gives 0
+ *   act[k] = bf16(fl(bf16(fl(g / fl(1 + e))) * u))
+ *   then a, asg, rs = pq_rotate_quant of act with K = I.
+ * Every step is a separately rounded IEEE operation, so the outputs are
+ * bit-identical to a CPU evaluation in that order.  M <= 16 runs one launch;
+ * larger M runs an elementwise kernel and then pq_rotate_quant's kernel.
+ *
+ *   y        bf16 [M][ldy] (device), ldy >= 2*I, ldy a multiple of 8
+ *   I        the down projection's K: a positive multiple of 128
+ *   rec, cs  as for pq_rotate_quant, for K = I
+ *   act      bf16 [M][I] (device, written); must not overlap y
+ *   a, asg, rs  as written by pq_rotate_quant
+ * Programmatic dependent launch: rec and cs may be read before the preceding
+ * kernel completes; y is read after it.
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE (M < 1, I not a positive multiple of
+ * 128, ldy < 2*I, act overlapping y), PQ_ERR_ALIGN, PQ_ERR_PARTITION,
+ * PQ_ERR_ARCH, PQ_ERR_CUDA.
+ */
+pq_status pq_silu_mul_rotate_quant(const void *y, int M, int I, int ldy, int P, const void *rec,
+                                   const void *cs, void *act, void *a, float *asg, float *rs,
+                                   void *stream);
+
+/*
  * uint4 x e4m3 group GEMM ([D1], [D2], [D4]):
  *   p(n)   = (n >= pb1) + (n >= pb2)
  *   D      = sum_{k in g} dec(a[p(n)][m][k]) * (c[k][n] - 8)

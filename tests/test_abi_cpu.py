@@ -164,6 +164,21 @@ def test_add_rms_rotate_quant_argument_checks(L, case, status):
     assert L.pq_last_error()
 
 
+@pytest.mark.parametrize("case,status", [
+    (dict(y=None), 1), (dict(act=None), 1), (dict(M=0), 2), (dict(I=100), 2), (dict(ldy=256 + 128), 2),
+    (dict(act=C.c_void_p(0x300000 + 1024)), 2),          # act overlapping y
+    (dict(P=0), 5), (dict(P=4), 5), (dict(y=C.c_void_p(0x300008)), 3), (dict(ldy=516), 3),
+    (dict(rs=C.c_void_p(0x200002)), 3),
+])
+@cpu_only
+def test_silu_mul_rotate_quant_argument_checks(L, case, status):
+    args = dict(y=X2, M=4, I=256, ldy=512, P=1, rec=A, cs=A, act=O2, a=A, asg=S, rs=S)
+    args.update(case)
+    order = ["y", "M", "I", "ldy", "P", "rec", "cs", "act", "a", "asg", "rs"]
+    assert L.pq_silu_mul_rotate_quant(*[args[k] for k in order], None) == status
+    assert L.pq_last_error()
+
+
 def test_device_calls_without_gpu_report_arch(L):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -172,6 +187,7 @@ def test_device_calls_without_gpu_report_arch(L):
     assert L.pq_gemm(*vals, None) == 6
     assert L.pq_rotate_quant(A, 4, 256, 256, 1, A, A, A, S, S, None) == 6
     assert L.pq_add_rms_rotate_quant(X2, R2, A, 1e-6, 4, 256, 256, 1, A, A, O2, H2, A, S, S, None) == 6
+    assert L.pq_silu_mul_rotate_quant(X2, 4, 256, 512, 1, A, A, O2, A, S, S, None) == 6
     assert L.pq_e4m3_encode(S, A, 16, None) == 6
     with pytest.raises(pq.PQError) as e:
         pq._check(6, "probe")

@@ -216,6 +216,63 @@ def test_add_rms_rotate_quant_feeds_the_gemm(pq, orc):
     assert_close(y.float().cpu().numpy(), y64, "producer -> pq_gemm")
 
 
+SILU_CASES = [  # M, I, P, ldy pad
+    (1, 8704, 1, 0), (2, 384, 3, 64), (5, 1024, 2, 0), (16, 256, 1, 0), (17, 640, 1, 128), (300, 1152, 3, 0),
+]
+
+
+@pytest.mark.parametrize("M,I,P,pad", SILU_CASES)
+def test_silu_mul_rotate_quant_bit_exact(pq, orc, M, I, P, pad):
+    N = 384 if P == 3 else 256
+    pb = (128, 256) if P in (2, 3) else None
+    prob = pqgen.make_problem(M, I, N, P=P, seed=M + I + 3 * P, pb=pb)
+    rng = np.random.default_rng(M * 5 + I)
+    ldy = 2 * I + pad
+    yv = rng.standard_normal((M, ldy)).astype(np.float32) * np.float32(3.0)
+    y = torch.from_numpy(yv).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    y[:, 2 * I:] = 0x7FC0                                    # padding must never be read
+    rec = orc.records(prob.pairs, prob.theta)
+    G = I // 128
+    bufs, (a, asg, rs), gpad = canary_outputs(P, M, I, G)
+    act, a, asg, rs = pq.pq_silu_mul_rotate_quant(dev_u16(y).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+                                                  dev_u16(prob.cs), a=a, asg=asg, rs=rs)
+    torch.cuda.synchronize()
+    act_o, a_o, asg_o, rs_o = orc.silu_mul_rotate_quant(y, prob.cs, rec)
+    got = act.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, act_o), "act differs at %s" % (np.argwhere(got != act_o)[:3].tolist(),)
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    assert np.array_equal(asg.cpu().numpy().view(np.uint32), asg_o.view(np.uint32))
+    assert np.array_equal(rs.cpu().numpy().view(np.uint32), rs_o.view(np.uint32))
+    check_guards(bufs, gpad)
+
+
+def test_mlp_chain_matches_oracle(pq, orc):
+    """norm producer -> gate_up GEMM -> silu-mul producer -> down GEMM at
+    decode, against the oracle's chain (each GEMM to its 2e-3 gate; the
+    producers' inputs are the GPU's own GEMM outputs, so the comparison of
+    the down projection is against the oracle run on those)."""
+    M, K, I = 2, 1024, 512
+    up = pqgen.make_problem(M, K, 2 * I, seed=31)
+    down = pqgen.make_problem(M, I, K, seed=32)
+    Lu, Ld = Problem(pq, orc, up), Problem(pq, orc, down)
+    res, gamma = producer_inputs(M, K, K, 31)
+    _, _, a1, s1, r1 = pq.pq_add_rms_rotate_quant(Lu.x_d, dev_u16(res).view(torch.bfloat16),
+                                                  dev_u16(gamma).view(torch.bfloat16), 1e-6, Lu.rec_d, Lu.cs_d)
+    y1 = pq.pq_gemm(a1, s1, r1, Lu.w_d, Lu.sz_d)
+    act, a2, s2, r2 = pq.pq_silu_mul_rotate_quant(y1, Ld.rec_d, Ld.cs_d)
+    y2 = pq.pq_gemm(a2, s2, r2, Ld.w_d, Ld.sz_d)
+    torch.cuda.synchronize()
+    _, _, a1o, s1o, r1o = orc.add_rms_rotate_quant(up.x, res, gamma, 1e-6, up.cs, Lu.t["rec"])
+    assert np.array_equal(a1.cpu().numpy(), a1o)
+    y1_64 = orc.gemm_f64(a1o, s1o, r1o, Lu.t["codes"], Lu.t["sz"], 2 * I, 2 * I)
+    assert_close(y1.float().cpu().numpy(), y1_64, "gate_up")
+    y1_bits = y1.view(torch.int16).cpu().numpy().view(np.uint16)
+    act_o, a2o, s2o, r2o = orc.silu_mul_rotate_quant(y1_bits, down.cs, Ld.t["rec"])
+    assert np.array_equal(act.view(torch.int16).cpu().numpy().view(np.uint16), act_o)
+    y2_64 = orc.gemm_f64(a2o, s2o, r2o, Ld.t["codes"], Ld.t["sz"], K, K)
+    assert_close(y2.float().cpu().numpy(), y2_64, "down")
+
+
 # ---------------------------------------------------------------- GEMM helpers
 def gemm_paths(pq, M):
     paths = [("tc", pq.pq_gemm_tc)]

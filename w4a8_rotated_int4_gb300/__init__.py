@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libpq.so")
 # Every symbol include/pq.h declares.
 EXPORTS = (
     "pq_abi_version", "pq_status_string", "pq_last_error", "pq_pack_sizes", "pq_pack",
-    "pq_rotate_quant", "pq_add_rms_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny",
+    "pq_rotate_quant", "pq_add_rms_rotate_quant", "pq_silu_mul_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny",
     "pq_gemm_tc",
     "pq_gemm_tcn",
     "pq_e4m3_encode",
@@ -68,6 +68,8 @@ def lib() -> C.CDLL:
     L.pq_rotate_quant.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     L.pq_add_rms_rotate_quant.restype = i32
     L.pq_add_rms_rotate_quant.argtypes = [vp, vp, vp, C.c_float, i32, i32, i32, i32] + [vp] * 8
+    L.pq_silu_mul_rotate_quant.restype = i32
+    L.pq_silu_mul_rotate_quant.argtypes = [vp, i32, i32, i32, i32] + [vp] * 7
     L.pq_gemm.restype = i32
     L.pq_gemm.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp]
     L.pq_gemm_skinny_max_m.restype = i32
@@ -204,6 +206,30 @@ def pq_add_rms_rotate_quant(x, residual, gamma, eps, rec, cs, residual_out=None,
                                          _dptr(h), _dptr(a), _dptr(asg), _dptr(rs), _stream(stream)),
            "pq_add_rms_rotate_quant")
     return residual_out, h, a, asg, rs
+
+
+def pq_silu_mul_rotate_quant(y, rec, cs, act=None, a=None, asg=None, rs=None, stream=None):
+    """silu(gate) * up + rotate + quant.  y bf16 [M, ldy >= 2I] (CUDA): the
+    merged gate/up output, gate in columns [0, I) and up in [I, 2I); rec and
+    cs for the down projection (cs f16 [P, I]).  Returns (act bf16 [M, I],
+    a uint8 [P, M, I], asg f32 [P, G, M], rs f32 [P, G, M])."""
+    torch = _torch()
+    M, ldy = y.shape
+    P, I = cs.shape
+    G = I // 128
+    dev = y.device
+    if act is None:
+        act = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+    if a is None:
+        a = torch.empty((P, M, I), dtype=torch.uint8, device=dev)
+    if asg is None:
+        asg = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    if rs is None:
+        rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _check(lib().pq_silu_mul_rotate_quant(_dptr(y), M, I, y.stride(0), P, _dptr(rec), _dptr(cs), _dptr(act),
+                                          _dptr(a), _dptr(asg), _dptr(rs), _stream(stream)),
+           "pq_silu_mul_rotate_quant")
+    return act, a, asg, rs
 
 
 def _gemm_args(a, asg, rs, w, sz, pb1, pb2, y):

@@ -305,6 +305,26 @@ extern "C" pq_status pq_add_rms_rotate_quant(const void *x, const void *residual
                                        rs, stream);
 }
 
+extern "C" pq_status pq_silu_mul_rotate_quant(const void *y, int M, int I, int ldy, int P, const void *rec,
+                                              const void *cs, void *act, void *a, float *asg, float *rs,
+                                              void *stream) {
+    clear_error();
+    if (!y || !rec || !cs || !act || !a || !asg || !rs) return fail(PQ_ERR_NULL, "NULL buffer");
+    if (M < 1 || I < 128 || I % 128 || ldy < 2 * I)
+        return fail(PQ_ERR_SHAPE, "M = %d, I = %d, ldy = %d", M, I, ldy);
+    if ((long long)M * ldy > (1ll << 40)) return fail(PQ_ERR_SHAPE, "sizes too large");
+    if (P < 1 || P > PQ_MAX_PARTITIONS) return fail(PQ_ERR_PARTITION, "P = %d outside 1..3", P);
+    if (!aligned(y, 16) || !aligned(rec, 16) || !aligned(cs, 16) || !aligned(act, 16) || !aligned(a, 16) ||
+        !aligned(asg, 4) || !aligned(rs, 4) || ldy % 8)
+        return fail(PQ_ERR_ALIGN, "y, rec, cs, act, a need 16-byte alignment, asg/rs 4-byte, ldy a "
+                    "multiple of 8");
+    if (overlaps(act, (size_t)M * I * 2, y, ((size_t)(M - 1) * ldy + 2 * I) * 2))
+        return fail(PQ_ERR_SHAPE, "act must not overlap y");
+    pq_status st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    return launch_silu_mul_rotate_quant(y, M, I, ldy, P, rec, cs, act, a, asg, rs, stream);
+}
+
 extern "C" pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream) {
     clear_error();
     if (!in || !out) return fail(PQ_ERR_NULL, "NULL buffer");

@@ -30,6 +30,8 @@ pq_status check_gemm_args(const void *a, const float *asg, const float *rs, int 
 pq_status launch_add_rms_rotate_quant(const void *x, const void *res, const void *gamma, float eps, int M,
                                       int K, int ldx, int P, const void *rec, const void *cs, void *res_out,
                                       void *h, void *a, float *asg, float *rs, void *stream);
+pq_status launch_silu_mul_rotate_quant(const void *y, int M, int I, int ldy, int P, const void *rec,
+                                       const void *cs, void *act, void *a, float *asg, float *rs, void *stream);
 pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
                               const void *cs, void *a, float *asg, float *rs, void *stream);
 pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream);

@@ -495,6 +495,88 @@ add_rms_norm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
     }
 }
 
+// ---------------------------------------------------------------------------
+// silu-mul producer ("2026-09-03: rotation stream 2 (silu-mul, GDN gated norm,
+// attention gate fused with rotate+quant)", MODE 0): the merged gate/up
+// output y holds g in columns [0, I) and u in [I, 2I);
+//   act = bf16(bf16(g / (1 + exp(-g))) * u),  then the pq_rotate_quant steps
+// on act (K = I).  exp is the fixed sequence below, so the result is the
+// same bits on any IEEE fp32 machine that follows it.
+// ---------------------------------------------------------------------------
+
+// exp(x) in fp32: Cody-Waite reduction n = rint(x log2 e),
+// r = (x - n ln2_hi) - n ln2_lo (ln2_hi has 13 trailing zero bits, so n ln2_hi
+// is exact), the degree-6 Taylor polynomial of exp in Horner form and an
+// exact scaling by 2^n; x > 88 gives +inf and x < -103 gives 0.  Every step
+// is a separately rounded IEEE operation.
+__device__ __forceinline__ float exp32_fixed(float x) {
+    if (x > 88.0f) return __int_as_float(0x7F800000);
+    if (x < -103.0f) return 0.0f;
+    const float n = rintf(__fmul_rn(x, 1.44269502f));
+    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0.693145751953125f)), __fmul_rn(n, 1.42860677e-06f));
+    float q = __fmul_rn(r, 1.0f / 720.0f);
+    q = __fmul_rn(r, __fadd_rn(1.0f / 120.0f, q));
+    q = __fmul_rn(r, __fadd_rn(1.0f / 24.0f, q));
+    q = __fmul_rn(r, __fadd_rn(1.0f / 6.0f, q));
+    q = __fmul_rn(r, __fadd_rn(0.5f, q));
+    q = __fmul_rn(r, __fadd_rn(1.0f, q));
+    q = __fadd_rn(1.0f, q);
+    return ldexpf(q, (int)n);
+}
+
+__device__ __forceinline__ float silu_mul1(float g, float u) {
+    const float sg = bf16_round(__fdiv_rn(g, __fadd_rn(1.0f, exp32_fixed(-g))));
+    return bf16_round(__fmul_rn(sg, u));
+}
+
+// Decode band: the small prologue's grid; partition 0 also writes act.
+template <int T>
+__global__ void __launch_bounds__(64 * T)
+silu_mul_rotate_quant_small_kernel(const uint16_t *__restrict__ y, int M, int I, int ldy,
+                                   const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
+                                   uint16_t *__restrict__ act_out, uint8_t *__restrict__ a,
+                                   float *__restrict__ asg, float *__restrict__ rs) {
+    __shared__ float v[T][128];
+    __shared__ float red_max[T][2];
+    __shared__ int red_sum[T][2];
+    const int tid = threadIdx.x, tt = tid >> 6, t = tid & 63, lane = tid & 31, half = (tid >> 5) & 1;
+    const int m = blockIdx.x * T + tt, g = blockIdx.y, p = blockIdx.z, G = I >> 7;
+    const bool live = m < M;
+    pdl_trigger();
+    const uint32_t cw = __ldg(reinterpret_cast<const uint32_t *>(cs + (size_t)p * I + 128 * g) + t);
+    uint2 r8[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) r8[r] = __ldg(rec + ((size_t)(p * 8 + r) * G + g) * 64 + t);
+    pdl_wait();        // y may be the previous kernel's output
+    const uint16_t *yrow = y + (size_t)m * ldy;
+    const uint32_t gw = live ? __ldg(reinterpret_cast<const uint32_t *>(yrow + 128 * g) + t) : 0u;
+    const uint32_t uw = live ? __ldg(reinterpret_cast<const uint32_t *>(yrow + I + 128 * g) + t) : 0u;
+    const float a0 = silu_mul1(bf16lo(gw), bf16lo(uw)), a1 = silu_mul1(bf16hi(gw), bf16hi(uw));
+    if (live && p == 0) reinterpret_cast<uint32_t *>(act_out + (size_t)m * I + 128 * g)[t] = bf16_pack2(a0, a1);
+    v[tt][2 * t] = __fmul_rn(a0, half_to_float((uint16_t)(cw & 0xFFFF)));
+    v[tt][2 * t + 1] = __fmul_rn(a1, half_to_float((uint16_t)(cw >> 16)));
+    __syncthreads();
+    small_rotate_quant_tail<T>(v, red_max, red_sum, r8, tt, t, lane, half, m, g, p, M, I, live, a, asg, rs);
+}
+
+// Above the band: act elementwise, two channels per thread; blockIdx.x
+// walks a row's channel pairs, blockIdx.y the rows.  pq_rotate_quant's
+// kernel on act follows.
+__global__ void __launch_bounds__(256)
+silu_mul_kernel(const uint16_t *__restrict__ y, int M, int I, int ldy, uint16_t *__restrict__ act_out) {
+    pdl_wait();        // y may be the previous kernel's output
+    pdl_trigger();
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;   // channel pair
+    if (c >= I / 2) return;
+    for (int m = blockIdx.y; m < M; m += gridDim.y) {
+        const uint16_t *yrow = y + (size_t)m * ldy;
+        const uint32_t gw = __ldg(reinterpret_cast<const uint32_t *>(yrow) + c);
+        const uint32_t uw = __ldg(reinterpret_cast<const uint32_t *>(yrow + I) + c);
+        reinterpret_cast<uint32_t *>(act_out + (size_t)m * I)[c] =
+            bf16_pack2(silu_mul1(bf16lo(gw), bf16lo(uw)), silu_mul1(bf16hi(gw), bf16hi(uw)));
+    }
+}
+
 __global__ void e4m3_encode_kernel(const float *__restrict__ in, uint8_t *__restrict__ out,
                                    size_t n) {
     const size_t stride = (size_t)gridDim.x * blockDim.x * 2;
@@ -591,6 +673,38 @@ pq_status launch_add_rms_rotate_quant(const void *x, const void *res, const void
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "add_rms_norm launch: %s", cudaGetErrorString(e));
     return launch_rotate_quant(h, M, K, K, P, rec, cs, a, asg, rs, stream);
+}
+
+pq_status launch_silu_mul_rotate_quant(const void *y, int M, int I, int ldy, int P, const void *rec,
+                                       const void *cs, void *act, void *a, float *asg, float *rs,
+                                       void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t *yp = static_cast<const uint16_t *>(y), *cp = static_cast<const uint16_t *>(cs);
+    const uint2 *recp = static_cast<const uint2 *>(rec);
+    uint16_t *actp = static_cast<uint16_t *>(act);
+    uint8_t *ap = static_cast<uint8_t *>(a);
+    const int G = I / 128;
+    if (G > 65535) return fail(PQ_ERR_SHAPE, "pq_silu_mul_rotate_quant: I = %d too large", I);
+    cudaError_t e;
+    if (M <= 16) {
+        if (M == 1)
+            e = launch_pdl(silu_mul_rotate_quant_small_kernel<1>, dim3(1, G, P), dim3(64), 0, st, yp, M, I, ldy,
+                           recp, cp, actp, ap, asg, rs);
+        else if (M == 2)
+            e = launch_pdl(silu_mul_rotate_quant_small_kernel<2>, dim3(1, G, P), dim3(128), 0, st, yp, M, I, ldy,
+                           recp, cp, actp, ap, asg, rs);
+        else
+            e = launch_pdl(silu_mul_rotate_quant_small_kernel<4>, dim3((M + 3) / 4, G, P), dim3(256), 0, st, yp, M,
+                           I, ldy, recp, cp, actp, ap, asg, rs);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "silu_mul_rotate_quant launch: %s", cudaGetErrorString(e));
+        return PQ_OK;
+    }
+    const dim3 grid((unsigned)((I / 2 + 255) / 256), (unsigned)(M < 65535 ? M : 65535));
+    e = launch_pdl(silu_mul_kernel, grid, dim3(256), 0, st, yp, M, I, ldy, actp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "silu_mul launch: %s", cudaGetErrorString(e));
+    return launch_rotate_quant(act, M, I, I, P, rec, cs, a, asg, rs, stream);
 }
 
 pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream) {
