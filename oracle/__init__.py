@@ -60,6 +60,10 @@ def lib():
         L.orc_silu_mul.restype = C.c_uint16
         L.orc_silu_mul.argtypes = [C.c_uint16, C.c_uint16]
         L.orc_silu_mul_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_rotate_tokquant.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_gemm_ptok_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.orc_gemm_ptok_f64_sampled.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32,
+                                                vp, vp, vp, vp, vp, vp]
         L.orc_gemm_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.orc_gemm_f64_sampled.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp]
@@ -267,6 +271,45 @@ def silu_mul_rotate_quant(y, cs, rec):
     rs = np.empty((P, G, M), dtype=np.float32)
     lib().orc_silu_mul_rotate_quant(M, I, ldy, P, _p(y), _p(cs), _p(rec), _p(act), _p(a), _p(asg), _p(rs))
     return act, a, asg, rs
+
+
+# ------------------------------------------------- per-token scales (reading R18)
+def rotate_tokquant(x, cs, rec):
+    """(xr bf16 [P,M,K], a e4m3 [P,M,K], As f32 [P,M], rs f32 [P,G,M])."""
+    x = _c(x, np.uint16)
+    cs = _c(cs, np.uint16)
+    rec = _c(rec, np.uint8)
+    M, ldx = x.shape
+    P, K = cs.shape
+    G = K // 128
+    xr = np.empty((P, M, K), dtype=np.uint16)
+    a = np.empty((P, M, K), dtype=np.uint8)
+    As = np.empty((P, M), dtype=np.float32)
+    rs = np.empty((P, G, M), dtype=np.float32)
+    lib().orc_rotate_tokquant(M, K, ldx, P, _p(x), _p(cs), _p(rec), _p(xr), _p(a), _p(As), _p(rs))
+    return xr, a, As, rs
+
+
+def gemm_ptok_f64(a, As, rs, codes, sz, pb1, pb2) -> np.ndarray:
+    a = _c(a, np.uint8); As = _c(As, np.float32); rs = _c(rs, np.float32)
+    codes = _c(codes, np.uint8); sz = _c(sz, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_gemm_ptok_f64(M, N, K, pb1, pb2, _p(a), _p(As), _p(rs), _p(codes), _p(sz), _p(y))
+    return y
+
+
+def gemm_ptok_f64_sampled(ms, ns, a, As, rs, codes, sz, pb1, pb2) -> np.ndarray:
+    ms = _c(ms, np.int32); ns = _c(ns, np.int32)
+    a = _c(a, np.uint8); As = _c(As, np.float32); rs = _c(rs, np.float32)
+    codes = _c(codes, np.uint8); sz = _c(sz, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty(len(ms), dtype=np.float64)
+    lib().orc_gemm_ptok_f64_sampled(len(ms), _p(ms), _p(ns), M, N, K, pb1, pb2, _p(a), _p(As), _p(rs),
+                                    _p(codes), _p(sz), _p(y))
+    return y
 
 
 # ---------------------------------------------------------------- GEMM

@@ -69,6 +69,17 @@
  *      exact for |n| <= 2^13), the Taylor polynomial of exp of degree 6 in
  *      Horner form with separately rounded steps, and an exact scaling by
  *      2^n (x < -103 gives 0, x > 88 gives +inf).
+ *   R18 per-token activation scales ([LOG] "PER-TOKEN PREFILL (v3, BUILT)":
+ *      pass A rotates into a bf16 scratch with group amaxes, pass C takes
+ *      As = max_g asg, encodes and forms plain row-sums; the PTOK GEMM folds
+ *      without the activation scale and applies As in the epilogue).  Per
+ *      row and partition:
+ *        v      = the pq_rotate_quant rotation of x * cs (fp32)
+ *        xr[k]  = bf16_RNE(v[k])                      (the scratch row)
+ *        asg_g  = fl32(max_{k in g} |xr[k]| * fl32(1/448));  As = max_g asg_g
+ *        a[k]   = e4m3(fl32(xr[k] / As)) (R6 rules; all 0x00 when As == 0)
+ *        rs_g   = fl32(exact sum of the decoded codes of group g)
+ *      GEMM: y = As * sum_g (sc * D - zscale * rs_g), in fp64 as R9.
  */
 #include <math.h>
 #include <stdint.h>
@@ -475,6 +486,53 @@ void orc_silu_mul_rotate_quant(int M, int I, int ldy, int P, const uint16_t *y, 
     orc_rotate_quant(M, I, I, P, act_out, cs, rec, a, asg, rs, NULL);
 }
 
+/*
+ * Per-token prologue (reading R18).  Outputs: xr bf16 [P][M][K] (the scratch
+ * row), a e4m3 [P][M][K], As f32 [P][M], rs f32 [P][G][M].
+ */
+void orc_rotate_tokquant(int M, int K, int ldx, int P, const uint16_t *x, const uint16_t *cs,
+                         const uint8_t *rec, uint16_t *xr, uint8_t *a, float *As, float *rs)
+{
+    int G = K / 128;
+    float c448 = inv448();
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int p = 0; p < P; p++)
+        for (int m = 0; m < M; m++) {
+            uint16_t *xrow = xr + ((size_t)p * M + m) * K;
+            float as = 0.0f;
+            for (int g = 0; g < G; g++) {
+                float v[128];
+                for (int k = 0; k < 128; k++)
+                    v[k] = f_mul(orc_bf16_to_float(x[(size_t)m * ldx + 128 * g + k]),
+                                 (float)orc_f16_to_double(cs[(size_t)p * K + 128 * g + k]));
+                orc_rotate_group_f32(rec, G, p, g, v);
+                float amax = 0.0f;
+                for (int k = 0; k < 128; k++) {
+                    xrow[128 * g + k] = orc_bf16_from_float(v[k]);
+                    float q = fabsf(orc_bf16_to_float(xrow[128 * g + k]));
+                    if (q > amax)
+                        amax = q;
+                }
+                float sg = f_mul(amax, c448);
+                if (sg > as)
+                    as = sg;
+            }
+            As[(size_t)p * M + m] = as;
+            uint8_t *arow = a + ((size_t)p * M + m) * K;
+            for (int g = 0; g < G; g++) {
+                int64_t sum512 = 0;
+                for (int k = 0; k < 128; k++) {
+                    uint8_t code = 0;
+                    if (as != 0.0f)
+                        code = orc_e4m3_encode(f_div(orc_bf16_to_float(xrow[128 * g + k]), as));
+                    arow[128 * g + k] = code;
+                    sum512 += (int64_t)llround(orc_e4m3_decode(code) * 512.0);
+                }
+                rs[((size_t)p * G + g) * M + m] = (float)((double)sum512 / 512.0);
+            }
+        }
+}
+
 /* ------------------------------------------------------------------ */
 /* GEMM in fp64                                                        */
 /* ------------------------------------------------------------------ */
@@ -517,6 +575,54 @@ void orc_gemm_f64(int M, int N, int K, int pb1, int pb2, const uint8_t *a, const
 }
 
 /* Sampled GEMM: y[i] = element (ms[i], ns[i]). */
+/* PTOK GEMM (reading R18): y[m][n] = As[p][m] * sum_g (sc * D - zscale * rs),
+ * fp64, table-true as R9.  As f32 [P][M]. */
+void orc_gemm_ptok_f64(int M, int N, int K, int pb1, int pb2, const uint8_t *a, const float *As,
+                       const float *rs, const uint8_t *codes, const uint16_t *sz, double *y)
+{
+    int G = K / 128, P = 1 + (pb1 < N) + (pb2 < N);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            int p = part_of(n, pb1, pb2);
+            const uint8_t *arow = a + ((size_t)p * M + m) * K;
+            double acc = 0.0;
+            for (int g = 0; g < G; g++) {
+                double D = 0.0;
+                for (int k = 128 * g; k < 128 * (g + 1); k++)
+                    D += orc_e4m3_decode(arow[k]) * ((double)codes[(size_t)k * N + n] - 8.0);
+                double sc = orc_f16_to_double(sz[((size_t)g * N + n) * 2]);
+                double zs = orc_f16_to_double(sz[((size_t)g * N + n) * 2 + 1]);
+                acc += sc * D - zs * (double)rs[((size_t)p * G + g) * M + m];
+            }
+            y[(size_t)m * N + n] = (double)As[(size_t)p * M + m] * acc;
+        }
+    (void)P;
+}
+
+/* the PTOK GEMM at sampled (m, n) pairs */
+void orc_gemm_ptok_f64_sampled(int count, const int *ms, const int *ns, int M, int N, int K, int pb1, int pb2,
+                               const uint8_t *a, const float *As, const float *rs, const uint8_t *codes,
+                               const uint16_t *sz, double *y)
+{
+    int G = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < count; i++) {
+        int m = ms[i], n = ns[i], p = part_of(n, pb1, pb2);
+        const uint8_t *arow = a + ((size_t)p * M + m) * K;
+        double acc = 0.0;
+        for (int g = 0; g < G; g++) {
+            double D = 0.0;
+            for (int k = 128 * g; k < 128 * (g + 1); k++)
+                D += orc_e4m3_decode(arow[k]) * ((double)codes[(size_t)k * N + n] - 8.0);
+            double sc = orc_f16_to_double(sz[((size_t)g * N + n) * 2]);
+            double zs = orc_f16_to_double(sz[((size_t)g * N + n) * 2 + 1]);
+            acc += sc * D - zs * (double)rs[((size_t)p * G + g) * M + m];
+        }
+        y[i] = (double)As[(size_t)p * M + m] * acc;
+    }
+}
+
 void orc_gemm_f64_sampled(int count, const int *ms, const int *ns, int M, int N, int K,
                           int pb1, int pb2, const uint8_t *a, const float *asg, const float *rs,
                           const uint8_t *codes, const uint16_t *sz, double *y)

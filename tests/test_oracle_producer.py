@@ -182,3 +182,47 @@ def test_silu_mul_quant_stage_is_rotate_quant(orc):
     assert np.array_equal(act, expect)
     a2, asg2, rs2 = orc.rotate_quant(act, prob.cs, t["rec"])
     assert np.array_equal(a, a2) and np.array_equal(asg, asg2) and np.array_equal(rs, rs2)
+
+
+# ---------------------------------------------------------------- per-token scales
+# Page: same log, "PER-TOKEN PREFILL (v3, BUILT)": pass A rotates into a bf16
+# scratch with group amaxes, pass C takes As = max_g asg, encodes and forms
+# plain row-sums, and the PTOK GEMM applies As in the epilogue (reading R18).
+def test_tokquant_steps_match_independent_pieces(orc):
+    M, K, P = 5, 640, 2
+    prob = pqgen.make_problem(M, K, 256, P=P, seed=14, pb=(128, 256))
+    t = orc.pack(prob)
+    xr, a, As, rs = orc.rotate_tokquant(prob.x, prob.cs, t["rec"])
+    # the rotation is the per-group prologue's (pinned on its own)
+    _, _, _, v = orc.rotate_quant(prob.x, prob.cs, t["rec"], want_v=True)
+    assert np.array_equal(xr, bf16_bits(v))
+    xrf = bf16_to_f32(xr)
+    G = K // 128
+    amax = np.abs(xrf.reshape(P, M, G, 128)).max(axis=3)
+    asg = (amax * np.float32(np.float32(1.0) / np.float32(448.0))).astype(np.float32)
+    assert np.array_equal(As, asg.max(axis=2))
+    # codes: the pinned encoder on fl32(xr / As); row-sums: exact sums of the decoded codes
+    q = (xrf / As[:, :, None]).astype(np.float32)
+    enc = np.array([orc.e4m3_encode(float(v)) for v in q.ravel()], dtype=np.uint8).reshape(q.shape)
+    assert np.array_equal(a, enc)
+    dec = orc.e4m3_decode_table()[a.astype(np.int64)]
+    exact = dec.reshape(P, M, G, 128).sum(axis=3)
+    assert np.array_equal(rs, np.transpose(exact, (0, 2, 1)).astype(np.float32))
+
+
+def test_ptok_gemm_is_the_group_gemm_with_one_scale(orc):
+    # with asg[g] = As for every group the per-group GEMM (pinned) is the same
+    # sum; only the fp64 association differs
+    M, K, N, P = 4, 512, 384, 3
+    prob = pqgen.make_problem(M, K, N, P=P, seed=15, pb=(128, 256))
+    t = orc.pack(prob)
+    _, a, As, rs = orc.rotate_tokquant(prob.x, prob.cs, t["rec"])
+    G = K // 128
+    asg = np.repeat(As[:, None, :], G, axis=1).astype(np.float32)
+    y1 = orc.gemm_ptok_f64(a, As, rs, t["codes"], t["sz"], 128, 256)
+    y2 = orc.gemm_f64(a, asg, rs, t["codes"], t["sz"], 128, 256)
+    assert np.allclose(y1, y2, rtol=1e-12, atol=1e-12 * np.abs(y2).max())
+    ms = np.array([0, 3, 1], np.int32)
+    ns = np.array([5, 200, 383], np.int32)
+    ys = orc.gemm_ptok_f64_sampled(ms, ns, a, As, rs, t["codes"], t["sz"], 128, 256)
+    assert np.array_equal(ys, y1[ms, ns])
