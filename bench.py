@@ -200,6 +200,25 @@ class Workload:
         pq.pq_silu_mul_rotate_quant(self.ygu[j], self.rec[j], self.cs[j], act=self.act[j], a=self.a[j],
                                     asg=self.asg[j], rs=self.rs[j], stream=stream)
 
+    def ptok_buffers(self, torch, dev):
+        """The per-token path's bf16 rotated rows and token scales, one set per
+        input copy, allocated on first use."""
+        if getattr(self, "xr", None) is not None:
+            return
+        P, M, K = self.c["P"], self.c["M"], self.c["K"]
+        self.xr = [torch.empty((P, M, K), dtype=torch.bfloat16, device=dev) for _ in range(self.copies)]
+        self.As = [torch.empty((P, M), dtype=torch.float32, device=dev) for _ in range(self.copies)]
+
+    def ptok_prologue(self, pq, i, stream):
+        j = i % self.copies
+        pq.pq_rotate_tokquant(self.x[j], self.rec[j], self.cs[j], xr=self.xr[j], a=self.a[j], As=self.As[j],
+                              rs=self.rs[j], stream=stream)
+
+    def ptok_gemm(self, pq, i, stream):
+        j = i % self.copies
+        pq.pq_gemm_ptok(self.a[j], self.As[j], self.rs[j], self.w[j], self.sz[j], self.pb1, self.pb2,
+                        y=self.y[j], stream=stream)
+
     def gemm(self, pq, i, stream, fn=None):
         j = i % self.copies
         (fn or pq.pq_gemm)(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1,
@@ -273,37 +292,37 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
         b.record(stream)
         torch.cuda.synchronize()
         per[key] = a.elapsed_time(b) / (reps * C)
+
+    def time_each(call):
+        """ms per call of call(pq, j, None), from a graph of one call per copy"""
+        for j in range(C):
+            call(pq, j, None)
+        torch.cuda.synchronize()
+        g = _capture(torch, lambda: [call(pq, j, None) for j in range(C)])
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * C)
+
     # the fused producer (residual add + RMSNorm + rotate + quant) on its own
     wl.producer_buffers(torch, wl.x[0].device)
-    for j in range(C):
-        wl.producer(pq, j, None)
-    torch.cuda.synchronize()
-    g_prod = _capture(torch, lambda: [wl.producer(pq, j, None) for j in range(C)])
-    g_prod.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        g_prod.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    per["prod"] = a.elapsed_time(b) / (reps * C)
+    per["prod"] = time_each(wl.producer)
     # the silu-mul producer on its own
-    for j in range(C):
-        wl.silu_producer(pq, j, None)
-    torch.cuda.synchronize()
-    g_silu = _capture(torch, lambda: [wl.silu_producer(pq, j, None) for j in range(C)])
-    g_silu.replay()
-    torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(reps):
-        g_silu.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    per["silu"] = a.elapsed_time(b) / (reps * C)
+    per["silu"] = time_each(wl.silu_producer)
     paths = time_gemm_paths(pq, torch, wl, reps, stream) if wl.c["M"] <= 16 else {}
-    return dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths,
-                prod_ms=per["prod"], silu_ms=per["silu"])
+    out = dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths,
+               prod_ms=per["prod"], silu_ms=per["silu"])
+    if wl.c["M"] > 16:
+        # the per-token activation-scale path: its two-pass prologue, then its GEMM
+        wl.ptok_buffers(torch, wl.x[0].device)
+        out["ptok_pro_ms"] = time_each(wl.ptok_prologue)
+        out["ptok_gemm_ms"] = time_each(wl.ptok_gemm)
+    return out
 
 
 def time_gemm_paths(pq, torch, wl, reps, stream):
@@ -433,6 +452,12 @@ def summarize(wl, r, steps, peaks):
         # the silu-mul producer (silu(gate) * up + rotate + quant, I = K) alone
         "silu_producer_us": round(r["silu_ms"] * 1e3, 3),
         "roofline": roofline(wl, r, peaks, ncu_traffic(KERNEL_NAMES[wl.gemm_kernel], wl.name)),
+        # per-token activation scales (M > 16): prologue (two passes) and GEMM
+        "ptok": ({"prologue_us": round(r["ptok_pro_ms"] * 1e3, 3), "gemm_us": round(r["ptok_gemm_ms"] * 1e3, 3),
+                  "gemm_tflops": round(wl.flops / (r["ptok_gemm_ms"] * 1e-3) / 1e12, 2),
+                  "gemm_frac_fp8": round(wl.flops / (r["ptok_gemm_ms"] * 1e-3) / 1e12 / (2 * peaks["bf16"]), 4),
+                  "step_us": round((r["ptok_pro_ms"] + r["ptok_gemm_ms"]) * 1e3, 3)}
+                 if "ptok_pro_ms" in r else None),
         "copies": wl.copies,
         "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
     }

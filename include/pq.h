@@ -16,6 +16,8 @@
  *   [Gates]    section "Gates passed" (scale = amax * (1/448.f), rows past M
  *              untouched, bf16-floor GEMM tolerance)
  *   [CVT]      section "2026-09-15: hardware e4m3 convert in the producers"
+ *   [PTOK]     section "Numbers", the per-token prefill item (pass A, pass C,
+ *              the PTOK GEMM with As in the epilogue)
  *
  * Conventions for every call:
  *   - Sizes are element counts.  G = K / 128.  "f16" = IEEE binary16,
@@ -278,6 +280,46 @@ pq_status pq_gemm_tc(const void *a, const float *asg, const float *rs, int M, in
 pq_status pq_gemm_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K,
                       int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
                       unsigned int *dev_status, void *stream);
+
+/*
+ * Per-token activation scales, prologue ([PTOK] pass A and pass C).  For
+ * every partition p, row m < M:
+ *   v     = the pq_rotate_quant rotation of x[m] * cs[p] (fp32, same steps)
+ *   xr[k] = bf16(v[k])                        (round to nearest even)
+ *   asg_g = fl(max_{k in g} |xr[k]| * fl(1/448))  for every group g
+ *   As    = max_g asg_g
+ *   a[k]  = e4m3(fl(xr[k] / As))              (all 0 when As == 0; [CVT])
+ *   rs_g  = sum_{k in g} dec(a[k])            (exact, then rounded to fp32)
+ * Two launches: pass A writes xr and the group scales (into rs); pass C reads
+ * them back and writes a, As and the row-sums over them.  Every step is a
+ * separately rounded IEEE operation, so the outputs are bit-identical to a CPU
+ * evaluation in that order.
+ *
+ *   x, rec, cs  as for pq_rotate_quant
+ *   xr          bf16 [P][M][K] (device, written): the rotated rows, the
+ *               scratch between the passes; must not overlap x
+ *   a           e4m3 [P][M][K] (device, written)
+ *   As          fp32 [P][M] (device, written; 4-byte aligned)
+ *   rs          fp32 [P][G][M] (device, written; 4-byte aligned): plain
+ *               row-sums, no activation scale in them
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE (M < 1, K not a positive multiple of 128,
+ * ldx < K, xr overlapping x), PQ_ERR_ALIGN, PQ_ERR_PARTITION, PQ_ERR_ARCH,
+ * PQ_ERR_CUDA.
+ */
+pq_status pq_rotate_tokquant(const void *x, int M, int K, int ldx, int P, const void *rec,
+                             const void *cs, void *xr, void *a, float *As, float *rs, void *stream);
+
+/*
+ * The GEMM on per-token scales ([PTOK] "PTOK GEMM"):
+ *   y[m][n] = bf16( As[p][m] * sum_g (sc[g][n] * D - zs[g][n] * rs[p][g][m]) )
+ * with p, D, sc, zs as for pq_gemm and a, As, rs from pq_rotate_tokquant.
+ * The tcgen05 prefill kernel with the group fold reduced to one fp32 multiply-
+ * add per element and slab and As applied once in the epilogue; any M >= 1.
+ * Arguments, dev_status and errors as for pq_gemm_tc.
+ */
+pq_status pq_gemm_ptok(const void *a, const float *As, const float *rs, int M, int N, int K, int P,
+                       int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
+                       unsigned int *dev_status, void *stream);
 
 /*
  * The prologue's device e4m3 encoder applied to n fp32 values ([CVT]: NaN ->

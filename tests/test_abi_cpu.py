@@ -117,6 +117,7 @@ def test_gemm_argument_checks(L, case, status):
     assert L.pq_gemm(*vals, None) == status
     assert L.pq_gemm_tc(*vals, None, None) == status
     assert L.pq_gemm_skinny(*vals, None, None) == status
+    assert L.pq_gemm_ptok(*vals, None, None) == status
     assert L.pq_last_error()
 
 
@@ -179,6 +180,21 @@ def test_silu_mul_rotate_quant_argument_checks(L, case, status):
     assert L.pq_last_error()
 
 
+@pytest.mark.parametrize("case,status", [
+    (dict(x=None), 1), (dict(xr=None), 1), (dict(As=None), 1), (dict(M=0), 2), (dict(K=100), 2),
+    (dict(ldx=128, K=256), 2), (dict(xr=C.c_void_p(0x300000 + 1024)), 2),     # xr overlapping x
+    (dict(P=0), 5), (dict(P=4), 5), (dict(x=C.c_void_p(0x300008)), 3), (dict(xr=C.c_void_p(0x500008)), 3),
+    (dict(ldx=260), 3), (dict(As=C.c_void_p(0x200002)), 3),
+])
+@cpu_only
+def test_rotate_tokquant_argument_checks(L, case, status):
+    args = dict(x=X2, M=4, K=256, ldx=256, P=1, rec=A, cs=A, xr=O2, a=A, As=S, rs=S)
+    args.update(case)
+    order = ["x", "M", "K", "ldx", "P", "rec", "cs", "xr", "a", "As", "rs"]
+    assert L.pq_rotate_tokquant(*[args[k] for k in order], None) == status
+    assert L.pq_last_error()
+
+
 def test_device_calls_without_gpu_report_arch(L):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -188,6 +204,8 @@ def test_device_calls_without_gpu_report_arch(L):
     assert L.pq_rotate_quant(A, 4, 256, 256, 1, A, A, A, S, S, None) == 6
     assert L.pq_add_rms_rotate_quant(X2, R2, A, 1e-6, 4, 256, 256, 1, A, A, O2, H2, A, S, S, None) == 6
     assert L.pq_silu_mul_rotate_quant(X2, 4, 256, 512, 1, A, A, O2, A, S, S, None) == 6
+    assert L.pq_rotate_tokquant(X2, 4, 256, 256, 1, A, A, O2, A, S, S, None) == 6
+    assert L.pq_gemm_ptok(*vals, None, None) == 6
     assert L.pq_e4m3_encode(S, A, 16, None) == 6
     with pytest.raises(pq.PQError) as e:
         pq._check(6, "probe")

@@ -292,7 +292,7 @@ def run_gemm(fn, a, asg, rs, L, pb1, pb2, M, N, ldy=None, fill=float("nan")):
     import w4a8_rotated_int4_gb300 as m
     lib = m.lib()
     name = {m.pq_gemm_tc: "pq_gemm_tc", m.pq_gemm_skinny: "pq_gemm_skinny",
-            m.pq_gemm_tcn: "pq_gemm_tcn"}[fn]
+            m.pq_gemm_tcn: "pq_gemm_tcn", m.pq_gemm_ptok: "pq_gemm_ptok"}[fn]
     P = a.shape[0]
     K = a.shape[2]
     st = getattr(lib, name)(C.c_void_p(a.data_ptr()), C.c_void_p(asg.data_ptr()),
@@ -484,6 +484,107 @@ def test_full_workload_sampled(pq, orc, name, M):
         for tag, fn in (("tc", pq.pq_gemm_tc), ("skinny", pq.pq_gemm_skinny), ("tcn", pq.pq_gemm_tcn)):
             y2 = fn(a, asg, rs, L.w_d, L.sz_d, prob.pb1, prob.pb2)
             assert_close(y2.float().cpu().numpy()[ms, ns], y64, "%s %s M=%d" % (tag, name, prob.M))
+
+
+# ---------------------------------------------------------------- per-token scales
+TOKQUANT_CASES = [  # M, K, P, pb, zero rows, generator knobs
+    (4, 256, 1, None, (), {}),
+    (1, 5120, 1, None, (), dict(outlier_frac=0.01)),
+    (5, 1152, 1, None, (2,), {}),
+    (64, 384, 3, (128, 256), (), {}),
+    (65, 640, 2, (256, 384), (0, 64), {}),
+    (333, 1024, 1, None, (), dict(x_mode="sparse", theta_range=1e-4)),
+    (2048, 5120, 1, None, (7,), {}),
+    (512, 5120, 3, (6144, 7168), (), {}),
+]
+
+
+def tokquant_problem(M, K, P, pb, zero_rows, knobs, N=None, seed=None):
+    N = N or (384 if P == 3 else 128 * P)
+    if pb is not None and pb[1] >= N:
+        N = pb[1] + 128 if P == 3 else pb[1]
+    prob = pqgen.make_problem(M, K, N, P=P, pb=pb, seed=seed if seed is not None else M + K, **knobs)
+    x = prob.x.copy()
+    for r in zero_rows:
+        x[r] = 0
+    return prob, x
+
+
+@pytest.mark.parametrize("M,K,P,pb,zero_rows,knobs", TOKQUANT_CASES,
+                         ids=["M%d-K%d-P%d" % c[:3] for c in TOKQUANT_CASES])
+def test_rotate_tokquant_bit_exact(pq, orc, M, K, P, pb, zero_rows, knobs):
+    """Per-token prologue: the bf16 rotated rows, codes, token scales and
+    plain row-sums bit-identical to the oracle; nothing outside them written."""
+    prob, x = tokquant_problem(M, K, P, pb, zero_rows, knobs)
+    G = K // 128
+    rec = orc.records(prob.pairs, prob.theta)
+    pad = 64
+    xr_buf = torch.full((P * M * K + 2 * pad,), -1, dtype=torch.int16, device="cuda")
+    as_buf = torch.full((P * M + 2 * pad,), float("nan"), dtype=torch.float32, device="cuda")
+    bufs, (a, _, rs), _ = canary_outputs(P, M, K, G, pad)
+    xr = xr_buf[pad:pad + P * M * K].view(P, M, K).view(torch.bfloat16)
+    As = as_buf[pad:pad + P * M].view(P, M)
+    pq.pq_rotate_tokquant(dev_u16(x).view(torch.bfloat16), torch.from_numpy(rec).cuda(), dev_u16(prob.cs),
+                          xr=xr, a=a, As=As, rs=rs)
+    torch.cuda.synchronize()
+    xr_o, a_o, As_o, rs_o = orc.rotate_tokquant(x, prob.cs, rec)
+    xr_g = xr.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(xr_g, xr_o), "xr differs at %s" % (np.argwhere(xr_g != xr_o)[:3].tolist(),)
+    a_g = a.cpu().numpy()
+    assert np.array_equal(a_g, a_o), "codes differ at %s" % (np.argwhere(a_g != a_o)[:3].tolist(),)
+    assert np.array_equal(As.cpu().numpy().view(np.uint32), As_o.view(np.uint32))
+    assert np.array_equal(rs.cpu().numpy().view(np.uint32), rs_o.view(np.uint32))
+    a_buf, r_buf = bufs[0].cpu(), bufs[2].cpu()
+    assert bool((a_buf[:pad] == CANARY).all()) and bool((a_buf[-pad:] == CANARY).all())
+    assert bool(torch.isnan(r_buf[:pad]).all()) and bool(torch.isnan(r_buf[-pad:]).all())
+    xb, ab = xr_buf.cpu(), as_buf.cpu()
+    assert bool((xb[:pad] == -1).all()) and bool((xb[-pad:] == -1).all())
+    assert bool(torch.isnan(ab[:pad]).all()) and bool(torch.isnan(ab[-pad:]).all())
+    for r in zero_rows:
+        assert (As_o[:, r] == 0).all() and (a_o[:, r] == 0).all()
+    if knobs.get("x_mode") == "sparse":
+        sub = ((a_o & 0x78) == 0) & ((a_o & 7) != 0)
+        assert sub.mean() > 0.3
+
+
+PTOK_GEMM = [  # M, K, N, P, pb
+    (1, 1024, 256, 1, None), (7, 512, 384, 3, (128, 256)), (129, 512, 256, 1, None),
+    (200, 896, 384, 3, (128, 256)), (256, 1024, 512, 1, None), (300, 1152, 384, 2, (256, 384)),
+    (33, 8704, 128, 1, None),
+]
+
+
+@pytest.mark.parametrize("M,K,N,P,pb", PTOK_GEMM)
+def test_gemm_ptok_vs_oracle(pq, orc, M, K, N, P, pb):
+    prob = pqgen.make_problem(M, K, N, P=P, pb=pb, seed=M * 5 + K + N)
+    x = prob.x.copy()
+    x[M // 2] = 0                                  # a token with As = 0
+    L = Problem(pq, orc, prob)
+    _, a, As, rs = pq.pq_rotate_tokquant(dev_u16(x).view(torch.bfloat16), L.rec_d, L.cs_d)
+    _, a_o, As_o, rs_o = orc.rotate_tokquant(x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    y64 = orc.gemm_ptok_f64(a_o, As_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
+    y = run_gemm(pq.pq_gemm_ptok, a, As, rs, L, prob.pb1, prob.pb2, M, N, ldy=N + 64)
+    assert (y[M // 2] == 0).all()
+    assert_close(y, y64, "ptok M=%d K=%d N=%d P=%d" % (M, K, N, P))
+
+
+@pytest.mark.parametrize("name", ["prefill", "down", "qkv"])
+def test_ptok_full_workload_sampled(pq, orc, name):
+    """At the benchmarked sizes: the per-token prologue bit-exact (full), the
+    per-token GEMM on 3000 sampled outputs against the fp64 oracle."""
+    prob = pqgen.config_problem(name)
+    L = Problem(pq, orc, prob, check_pack=(name != "down"))
+    xr, a, As, rs = pq.pq_rotate_tokquant(L.x_d, L.rec_d, L.cs_d)
+    y = pq.pq_gemm_ptok(a, As, rs, L.w_d, L.sz_d, prob.pb1, prob.pb2)
+    torch.cuda.synchronize()
+    xr_o, a_o, As_o, rs_o = orc.rotate_tokquant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(xr.view(torch.int16).cpu().numpy().view(np.uint16), xr_o)
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    assert np.array_equal(As.cpu().numpy(), As_o) and np.array_equal(rs.cpu().numpy(), rs_o)
+    ms, ns = _samples(prob.M, prob.N, prob.pb1, prob.pb2, 3000, 13)
+    y64 = orc.gemm_ptok_f64_sampled(ms, ns, a_o, As_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
+    assert_close(y.float().cpu().numpy()[ms, ns], y64, "ptok %s M=%d" % (name, prob.M))
 
 
 # ---------------------------------------------------------------- repeated launches

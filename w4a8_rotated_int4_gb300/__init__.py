@@ -26,6 +26,7 @@ EXPORTS = (
     "pq_rotate_quant", "pq_add_rms_rotate_quant", "pq_silu_mul_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny",
     "pq_gemm_tc",
     "pq_gemm_tcn",
+    "pq_rotate_tokquant", "pq_gemm_ptok",
     "pq_e4m3_encode",
 )
 
@@ -78,6 +79,10 @@ def lib() -> C.CDLL:
         f = getattr(L, name)
         f.restype = i32
         f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
+    L.pq_rotate_tokquant.restype = i32
+    L.pq_rotate_tokquant.argtypes = [vp, i32, i32, i32, i32] + [vp] * 7
+    L.pq_gemm_ptok.restype = i32
+    L.pq_gemm_ptok.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
     L.pq_e4m3_encode.restype = i32
     L.pq_e4m3_encode.argtypes = [vp, vp, st, vp]
     _lib = L
@@ -271,6 +276,34 @@ def pq_gemm_tc(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, s
 
 def pq_gemm_tcn(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
     return _gemm_path(lib().pq_gemm_tcn, "pq_gemm_tcn", a, asg, rs, w, sz, pb1, pb2, y,
+                      dev_status, stream)
+
+
+def pq_rotate_tokquant(x, rec, cs, xr=None, a=None, As=None, rs=None, stream=None):
+    """Per-token prologue: x bf16 [M, ldx>=K] (CUDA), rec, cs as for
+    pq_rotate_quant.  Returns (xr bf16 [P,M,K] rotated rows, a uint8 [P,M,K]
+    e4m3 codes, As f32 [P,M] token scales, rs f32 [P,G,M] plain row-sums)."""
+    torch = _torch()
+    M, ldx = x.shape
+    P, K = cs.shape
+    G = K // 128
+    dev = x.device
+    if xr is None:
+        xr = torch.empty((P, M, K), dtype=torch.bfloat16, device=dev)
+    if a is None:
+        a = torch.empty((P, M, K), dtype=torch.uint8, device=dev)
+    if As is None:
+        As = torch.empty((P, M), dtype=torch.float32, device=dev)
+    if rs is None:
+        rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _check(lib().pq_rotate_tokquant(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(xr), _dptr(a),
+                                    _dptr(As), _dptr(rs), _stream(stream)), "pq_rotate_tokquant")
+    return xr, a, As, rs
+
+
+def pq_gemm_ptok(a, As, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    """y bf16 [M, N] from the per-token prologue's outputs (As in the epilogue)."""
+    return _gemm_path(lib().pq_gemm_ptok, "pq_gemm_ptok", a, As, rs, w, sz, pb1, pb2, y,
                       dev_status, stream)
 
 

@@ -325,6 +325,38 @@ extern "C" pq_status pq_silu_mul_rotate_quant(const void *y, int M, int I, int l
     return launch_silu_mul_rotate_quant(y, M, I, ldy, P, rec, cs, act, a, asg, rs, stream);
 }
 
+extern "C" pq_status pq_rotate_tokquant(const void *x, int M, int K, int ldx, int P, const void *rec,
+                                        const void *cs, void *xr, void *a, float *As, float *rs, void *stream) {
+    clear_error();
+    if (!x || !rec || !cs || !xr || !a || !As || !rs) return fail(PQ_ERR_NULL, "NULL buffer");
+    if (M < 1 || K < 128 || K % 128 || ldx < K)
+        return fail(PQ_ERR_SHAPE, "M = %d, K = %d, ldx = %d", M, K, ldx);
+    if ((long long)M * ldx > (1ll << 40)) return fail(PQ_ERR_SHAPE, "sizes too large");
+    if (P < 1 || P > PQ_MAX_PARTITIONS) return fail(PQ_ERR_PARTITION, "P = %d outside 1..3", P);
+    if (!aligned(x, 16) || !aligned(rec, 16) || !aligned(cs, 16) || !aligned(xr, 16) || !aligned(a, 16) ||
+        !aligned(As, 4) || !aligned(rs, 4) || ldx % 8)
+        return fail(PQ_ERR_ALIGN, "x, rec, cs, xr, a need 16-byte alignment, As/rs 4-byte, ldx a "
+                    "multiple of 8");
+    if (overlaps(xr, (size_t)P * M * K * 2, x, ((size_t)(M - 1) * ldx + K) * 2))
+        return fail(PQ_ERR_SHAPE, "xr must not overlap x");
+    pq_status st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    return launch_rotate_tokquant(x, M, K, ldx, P, rec, cs, xr, a, As, rs, stream);
+}
+
+extern "C" pq_status pq_gemm_ptok(const void *a, const float *As, const float *rs, int M, int N, int K,
+                                  int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
+                                  unsigned int *dev_status, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, As, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    return launch_gemm_tc(a, As, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, sms, true);
+}
+
 extern "C" pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream) {
     clear_error();
     if (!in || !out) return fail(PQ_ERR_NULL, "NULL buffer");

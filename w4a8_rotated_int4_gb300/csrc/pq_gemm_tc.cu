@@ -43,6 +43,10 @@
 // The fold warpgroups raise their register budget (setmaxnreg) to hold the
 // 128 accumulators; the others lower theirs.
 // Epilogue: bf16 rows < M are stored; nothing else is written.
+// Per-token mode (the "Numbers" section's PTOK GEMM: one activation scale As
+// per token and partition, plain row-sums): the row warps copy rs only, the
+// fold is acc += (2^9 sc') * D'' (one packed operation per two elements) and
+// the epilogue multiplies each row by its As.
 //
 // Every wait is bounded (%globaltimer); a wait that gives up marks the CTA as
 // aborted, lets in-flight copies and MMAs finish, frees TMEM, fills its tile
@@ -121,7 +125,7 @@ constexpr size_t kSmemBytes = kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlo
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct TcParams {
-    const float *asg;
+    const float *asg;         // asg [P][G][M]; per-token: As [P][M]
     const float *rs;
     const uint32_t *sz;
     __nv_bfloat16 *y;
@@ -155,6 +159,19 @@ __device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64
     }
 }
 
+// The per-token fold: the accumulator holds D'' and the token scale is
+// applied in the epilogue, so acc += (2^9 sc') * D'': one packed operation
+// per two elements.
+__device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const uint64_t (&z)[4], uint64_t *acc_lo,
+                                               uint64_t *acc_hi) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        acc_lo[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), acc_lo[j]);
+        acc_hi[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                           acc_hi[j]);
+    }
+}
+
 // Tile i of this CTA: output-feature tile fastest, its partition from pb1/pb2.
 __device__ __forceinline__ void tile_coords(int i, int ntn, int pb1, int pb2, int &n0, int &m0, int &p) {
     const int t = (int)blockIdx.x + i * (int)gridDim.x;
@@ -168,6 +185,7 @@ __device__ __forceinline__ void tile_coords(int i, int ntn, int pb1, int pb2, in
 // tile fastest, so the CTAs running at once share activation rows and the
 // weight tiles stay L2-resident).  All pipelines run continuously across tile
 // boundaries; slab counter it = (tile index) * G + kb.
+template <bool kTok>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmS, const TcParams prm) {
@@ -291,7 +309,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             for (int u = 0; u < BM / 64; ++u) {
                 const int i = row0 + lane + 32 * u, m = m0 + i;
                 const bool ok = m < M;     // rows past M are zero-filled
-                cp_async4(&szf[r].row[i], ok ? prm.asg + off + m : prm.asg, ok);
+                if constexpr (!kTok) cp_async4(&szf[r].row[i], ok ? prm.asg + off + m : prm.asg, ok);
                 cp_async4(&szf[r].rsv[i], ok ? prm.rs + off + m : prm.rs, ok);
             }
             cp_async_arrive(&ctl->rows_full[r]);
@@ -469,10 +487,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 uint32_t dbuf[2][16];
                 tmem_issue256(taddr, dbuf[0]);
                 uint64_t sa2[4];
+                if constexpr (!kTok) {
 #pragma unroll
-                for (int ri = 0; ri < 4; ++ri) {
-                    const float v = szf[r].row[row0 + 8 * ri];
-                    sa2[ri] = f2pack(v, v);
+                    for (int ri = 0; ri < 4; ++ri) {
+                        const float v = szf[r].row[row0 + 8 * ri];
+                        sa2[ri] = f2pack(v, v);
+                    }
                 }
                 const uint64_t *zf = reinterpret_cast<const uint64_t *>(szf[r].sc) + c4;
                 uint64_t z[4];
@@ -492,8 +512,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                         for (int j = 0; j < 4; ++j) z[j] = zf[4 * (4 * cb + j)];
                     }
-                    fold_block(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
-                               sa2[2 * sh + 1]);
+                    if constexpr (kTok)
+                        fold_block_tok(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb);
+                    else
+                        fold_block(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
+                                   sa2[2 * sh + 1]);
                     if (k + 1 < 8) tmem_wait16(dbuf[cur ^ 1]);
                 }
                 __syncwarp();
@@ -501,14 +524,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             if (i == my_tiles - 1) pdl_trigger();
             bad = bad || *abort_flag != 0;
-            // epilogue: bf16 pairs (NaN once the CTA has aborted)
+            // epilogue: bf16 pairs (NaN once the CTA has aborted); per-token:
+            // times the row's As first
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri) {
                 if (mb + 8 * ri >= M) continue;
                 uint32_t *dst = reinterpret_cast<uint32_t *>(prm.y + (size_t)(mb + 8 * ri) * prm.ldy + n0 + 2 * c4);
+                float as = 1.0f;
+                if constexpr (kTok) as = __ldg(prm.asg + (size_t)p * M + mb + 8 * ri);
 #pragma unroll
                 for (int J = 0; J < 16; ++J) {
                     float2 v = f2unpack(acc[ri][J]);
+                    if constexpr (kTok) {
+                        v.x *= as;
+                        v.y *= as;
+                    }
                     if (bad) v.x = v.y = __int_as_float(0x7FC00000);
                     const __nv_bfloat162 v2 = __floats2bfloat162_rn(v.x, v.y);
                     dst[4 * J] = *reinterpret_cast<const uint32_t *>(&v2);
@@ -530,7 +560,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
                          int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
-                         unsigned int *dev_status, void *stream, int sm_count) {
+                         unsigned int *dev_status, void *stream, int sm_count, bool per_token) {
     (void)sm_count;
     auto enc = encode_fn();
     if (!enc) return fail(PQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -585,11 +615,11 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     if (ntiles > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_gemm_tc: M = %d too large", M);
     const int ctas = (int)(ntiles < sm_count ? ntiles : (sm_count > 0 ? sm_count : 1));
     const dim3 grid(ctas);
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kern = per_token ? tc_kernel<true> : tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    e = launch_pdl(tc_kernel, grid, dim3(kThreads), kSmemBytes, static_cast<cudaStream_t>(stream), tmA, tmB,
-                   tmS, prm);
+    e = launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, static_cast<cudaStream_t>(stream), tmA, tmB, tmS,
+                   prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "tc launch: %s", cudaGetErrorString(e));
     return PQ_OK;

@@ -71,6 +71,13 @@ struct __align__(16) Smem {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+__device__ __forceinline__ float bf16_round(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
+
+__device__ __forceinline__ uint32_t bf16_pack2(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
 __device__ __forceinline__ float half_to_float(uint16_t h) {
     float f;
     asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
@@ -107,10 +114,16 @@ __device__ __forceinline__ void givens(float c, float s, float &vi, float &vj) {
     vj = nj;
 }
 
+// kRot = false: the per-group quantisation (codes, asg, rs).
+// kRot = true: pass A of the per-token path -- the rotated rows rounded to
+// bf16 into xr [P][M][K] and each group's scale fl(max |xr| * fl(1/448)) into
+// asg (the token-quant pass reads them back); a and rs are not touched.
+template <bool kRot>
 __global__ void __launch_bounds__(kThreads)
 rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P,
                     const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
-                    uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs) {
+                    uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs,
+                    uint16_t *__restrict__ xr) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -203,57 +216,86 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
         // quantise: warp w takes channels 32w..32w+31 of both tokens of the lane
         float2 vals[32];
         float amax0 = 0.0f, amax1 = 0.0f;
+        if constexpr (kRot) {
+            // bf16 rows straight to xr (64 contiguous bytes per token and
+            // warp); amax over the rounded values
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            vals[q] = sm.v[32 * warp + q][lane];
-            amax0 = fmaxf(amax0, fabsf(vals[q].x));
-            amax1 = fmaxf(amax1, fabsf(vals[q].y));
-        }
-        sm.red_max[warp][2 * lane] = amax0;
-        sm.red_max[warp][2 * lane + 1] = amax1;
-        __syncthreads();
+            for (int t = 0; t < 2; ++t) {
+                uint32_t pk[16];
+                float am = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int tok = 2 * lane + t;
-            const float amax = fmaxf(fmaxf(sm.red_max[0][tok], sm.red_max[1][tok]),
-                                     fmaxf(sm.red_max[2][tok], sm.red_max[3][tok]));
-            const float scale = __fmul_rn(amax, inv448);
-            uint32_t packed[8];
-            int sum512 = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t word = 0;
-                if (scale != 0.0f) {
-                    const float e0 = t ? vals[4 * q].y : vals[4 * q].x, e1 = t ? vals[4 * q + 1].y : vals[4 * q + 1].x;
-                    const float e2 = t ? vals[4 * q + 2].y : vals[4 * q + 2].x, e3 = t ? vals[4 * q + 3].y : vals[4 * q + 3].x;
-                    const uint32_t c01 = e4m3x2(__fdiv_rn(e1, scale), __fdiv_rn(e0, scale));
-                    const uint32_t c23 = e4m3x2(__fdiv_rn(e3, scale), __fdiv_rn(e2, scale));
-                    word = c01 | (c23 << 16);
+                for (int q = 0; q < 16; ++q) {
+                    const float2 lo = sm.v[32 * warp + 2 * q][lane], hi = sm.v[32 * warp + 2 * q + 1][lane];
+                    pk[q] = bf16_pack2(t ? lo.y : lo.x, t ? hi.y : hi.x);
+                    am = fmaxf(am, fmaxf(fabsf(bf16lo(pk[q])), fabsf(bf16hi(pk[q]))));
                 }
-                packed[q] = word;
+                const int tok = 2 * lane + t;
+                sm.red_max[warp][tok] = am;
+                if (m0 + tok < M) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(xr + ((size_t)p * M + m0 + tok) * K + 128 * g + 32 * warp);
 #pragma unroll
-                for (int b = 0; b < 4; ++b) sum512 += e4m3_times512((word >> (8 * b)) & 0xFF);
+                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
             }
-            uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[tok][32 * warp]);
-            cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            sm.red_sum[warp][tok] = sum512;
-            if (warp == 0 && m0 + tok < M) asg[((size_t)p * G + g) * M + m0 + tok] = scale;
-        }
-        __syncthreads();
+            __syncthreads();
+            if (tid < kTok && m0 + tid < M) {
+                const float amax = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
+                                         fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
+                asg[((size_t)p * G + g) * M + m0 + tid] = __fmul_rn(amax, inv448);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                vals[q] = sm.v[32 * warp + q][lane];
+                amax0 = fmaxf(amax0, fabsf(vals[q].x));
+                amax1 = fmaxf(amax1, fabsf(vals[q].y));
+            }
+            sm.red_max[warp][2 * lane] = amax0;
+            sm.red_max[warp][2 * lane + 1] = amax1;
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int tok = 2 * lane + t;
+                const float amax = fmaxf(fmaxf(sm.red_max[0][tok], sm.red_max[1][tok]),
+                                         fmaxf(sm.red_max[2][tok], sm.red_max[3][tok]));
+                const float scale = __fmul_rn(amax, inv448);
+                uint32_t packed[8];
+                int sum512 = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t word = 0;
+                    if (scale != 0.0f) {
+                        const float e0 = t ? vals[4 * q].y : vals[4 * q].x, e1 = t ? vals[4 * q + 1].y : vals[4 * q + 1].x;
+                        const float e2 = t ? vals[4 * q + 2].y : vals[4 * q + 2].x, e3 = t ? vals[4 * q + 3].y : vals[4 * q + 3].x;
+                        const uint32_t c01 = e4m3x2(__fdiv_rn(e1, scale), __fdiv_rn(e0, scale));
+                        const uint32_t c23 = e4m3x2(__fdiv_rn(e3, scale), __fdiv_rn(e2, scale));
+                        word = c01 | (c23 << 16);
+                    }
+                    packed[q] = word;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) sum512 += e4m3_times512((word >> (8 * b)) & 0xFF);
+                }
+                uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[tok][32 * warp]);
+                cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                sm.red_sum[warp][tok] = sum512;
+                if (warp == 0 && m0 + tok < M) asg[((size_t)p * G + g) * M + m0 + tok] = scale;
+            }
+            __syncthreads();
 
-        // stores: 128-byte code rows, then one row-sum per token
-        for (int c = tid; c < kTok * 8; c += kThreads) {
-            const int row = c >> 3, q = c & 7;
-            if (m0 + row < M)
-                reinterpret_cast<uint4 *>(a + ((size_t)p * M + m0 + row) * K + 128 * g)[q] =
-                    *reinterpret_cast<const uint4 *>(&sm.codes[row][16 * q]);
-        }
-        if (tid < kTok && m0 + tid < M) {
-            const size_t o = ((size_t)p * G + g) * M + m0 + tid;
-            const int s = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
-            rs[o] = __fmul_rn(__int2float_rn(s), 1.0f / 512.0f);
-        }
+            // stores: 128-byte code rows, then one row-sum per token
+            for (int c = tid; c < kTok * 8; c += kThreads) {
+                const int row = c >> 3, q = c & 7;
+                if (m0 + row < M)
+                    reinterpret_cast<uint4 *>(a + ((size_t)p * M + m0 + row) * K + 128 * g)[q] =
+                        *reinterpret_cast<const uint4 *>(&sm.codes[row][16 * q]);
+            }
+            if (tid < kTok && m0 + tid < M) {
+                const size_t o = ((size_t)p * G + g) * M + m0 + tid;
+                const int s = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
+                rs[o] = __fmul_rn(__int2float_rn(s), 1.0f / 512.0f);
+            }
+        }  // !kRot
     }
 }
 
@@ -343,12 +385,6 @@ rotate_quant_small_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
 // the 64 lane sums are added pairwise by recursive halving: the xor tree over
 // each warp, then warp 0's + warp 1's.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float bf16_round(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
-
-__device__ __forceinline__ uint32_t bf16_pack2(float lo, float hi) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-}
 
 // s of the two channels of a lane, from the x and residual words
 __device__ __forceinline__ float2 residual_add(uint32_t xw, uint32_t rw) {
@@ -589,6 +625,60 @@ __global__ void e4m3_encode_kernel(const float *__restrict__ in, uint8_t *__rest
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pass C of the per-token path ("Prefill ladder" notes: per-token prefill,
+// pass C): for every row, As = max over the groups of pass A's group scales,
+// a = e4m3(fl(xr / As)) (all 0 when As = 0), and per group the exact sum of
+// what the codes decode to (plain row-sums: the token scale is applied in the
+// GEMM's epilogue).  One warp per token row; lane l takes the 8 channels
+// 8 (l & 15) .. +7 of group g0 + (l >> 4), two groups per step.  gsc and rs
+// may be the same buffer: a warp reads all of its row's group scales before
+// it writes that row's row-sums, and no other warp touches the row.
+// ---------------------------------------------------------------------------
+constexpr int kTqWarps = 8;
+
+__device__ __forceinline__ uint32_t e4m3x4_scaled(uint2 w, float as) {
+    return e4m3x2(__fdiv_rn(bf16hi(w.x), as), __fdiv_rn(bf16lo(w.x), as)) |
+           (e4m3x2(__fdiv_rn(bf16hi(w.y), as), __fdiv_rn(bf16lo(w.y), as)) << 16);
+}
+
+__global__ void __launch_bounds__(32 * kTqWarps)
+token_quant_kernel(const uint16_t *__restrict__ xr, int M, int K, const float *gsc, uint8_t *__restrict__ a,
+                   float *__restrict__ As, float *rs) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int m = blockIdx.x * kTqWarps + warp, p = blockIdx.y, G = K >> 7;
+    pdl_wait();        // xr and the group scales are the preceding pass's output
+    pdl_trigger();
+    if (m >= M) return;
+    float as = 0.0f;
+    for (int g = lane; g < G; g += 32) as = fmaxf(as, gsc[((size_t)p * G + g) * M + m]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) as = fmaxf(as, __shfl_xor_sync(0xFFFFFFFFu, as, o));
+    if (lane == 0) As[(size_t)p * M + m] = as;
+    const uint16_t *row = xr + ((size_t)p * M + m) * K;
+    uint8_t *arow = a + ((size_t)p * M + m) * K;
+    for (int g0 = 0; g0 < G; g0 += 2) {
+        const int g = g0 + (lane >> 4), c = 128 * g + 8 * (lane & 15);
+        int sum512 = 0;
+        if (g < G) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row + c));
+            uint32_t lo = 0, hi = 0;
+            if (as != 0.0f) {
+                lo = e4m3x4_scaled(make_uint2(v.x, v.y), as);
+                hi = e4m3x4_scaled(make_uint2(v.z, v.w), as);
+            }
+            *reinterpret_cast<uint2 *>(arow + c) = make_uint2(lo, hi);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                sum512 += e4m3_times512((lo >> (8 * b)) & 0xFF) + e4m3_times512((hi >> (8 * b)) & 0xFF);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sum512 += __shfl_xor_sync(0xFFFFFFFFu, sum512, o);
+        if ((lane & 15) == 0 && g < G)
+            rs[((size_t)p * G + g) * M + m] = __fmul_rn(__int2float_rn(sum512), 1.0f / 512.0f);
+    }
+}
+
 }  // namespace
 
 pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
@@ -614,14 +704,37 @@ pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const
     } else {
         const dim3 grid((M + kTok - 1) / kTok, K / 128, P);
         if (grid.x > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_rotate_quant: M = %d too large", M);
-        e = cudaFuncSetAttribute(rotate_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(rotate_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(Smem));
         if (e == cudaSuccess)
-            e = launch_pdl(rotate_quant_kernel, grid, dim3(kThreads), sizeof(Smem), st, xp, M, K, ldx, P, rp,
-                           cp, ap, asg, rs);
+            e = launch_pdl(rotate_quant_kernel<false>, grid, dim3(kThreads), sizeof(Smem), st, xp, M, K, ldx, P,
+                           rp, cp, ap, asg, rs, (uint16_t *)nullptr);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_quant launch: %s", cudaGetErrorString(e));
+    return PQ_OK;
+}
+
+pq_status launch_rotate_tokquant(const void *x, int M, int K, int ldx, int P, const void *rec, const void *cs,
+                                 void *xr, void *a, float *As, float *rs, void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint16_t *xrp = static_cast<uint16_t *>(xr);
+    if (K / 128 > 65535) return fail(PQ_ERR_SHAPE, "pq_rotate_tokquant: K = %d too large", K);
+    // pass A: rotation into xr, group scales into rs
+    const dim3 grid((M + kTok - 1) / kTok, K / 128, P);
+    cudaError_t e = cudaFuncSetAttribute(rotate_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(Smem));
+    if (e == cudaSuccess)
+        e = launch_pdl(rotate_quant_kernel<true>, grid, dim3(kThreads), sizeof(Smem), st,
+                       static_cast<const uint16_t *>(x), M, K, ldx, P, static_cast<const uint2 *>(rec),
+                       static_cast<const uint16_t *>(cs), (uint8_t *)nullptr, rs, (float *)nullptr, xrp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_tokquant pass A launch: %s", cudaGetErrorString(e));
+    // pass C: token scale, codes, row-sums
+    e = launch_pdl(token_quant_kernel, dim3((M + kTqWarps - 1) / kTqWarps, P), dim3(32 * kTqWarps), 0, st,
+                   (const uint16_t *)xrp, M, K, (const float *)rs, static_cast<uint8_t *>(a), As, rs);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_tokquant pass C launch: %s", cudaGetErrorString(e));
     return PQ_OK;
 }
 
