@@ -47,6 +47,13 @@ def lib():
         L.orc_records.argtypes = [i32, i32, vp, vp, vp]
         L.orc_sz.argtypes = [i32, i32, vp, vp, vp]
         L.orc_repack.argtypes = [i32, i32, vp, vp]
+        L.orc_unpack_plane.argtypes = [i32, i32, vp, vp]
+        L.orc_codes5.argtypes = [i32, i32, vp, vp, vp]
+        L.orc_sz5.argtypes = [i32, i32, vp, vp, vp, vp]
+        L.orc_repack5.argtypes = [i32, i32, vp, vp, vp, vp]
+        L.orc_gemm5_f64.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.orc_gemm5_f64_sampled.argtypes = [i32, vp, vp, i32, i32, i32, i32, i32,
+                                            vp, vp, vp, vp, vp, vp]
         L.orc_rotate_group_f32.argtypes = [vp, i32, i32, i32, vp]
         L.orc_rotate_quant.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.orc_bf16_from_float.restype = C.c_uint16
@@ -183,6 +190,78 @@ def repack(qweight: np.ndarray) -> np.ndarray:
     out = np.empty((N8 * 8, K // 2), dtype=np.uint8)
     lib().orc_repack(K, N8 * 8, _p(qweight), _p(out))
     return out
+
+
+# ---------------------------------------------------------------- int5 weights
+def unpack_plane(plane: np.ndarray, N: int) -> np.ndarray:
+    """Fifth-bit plane int32 [rows, N/32] -> bits uint8 [rows, N]."""
+    plane = _c(plane, np.int32)
+    out = np.empty((plane.shape[0], N), dtype=np.uint8)
+    lib().orc_unpack_plane(plane.shape[0], N, _p(plane), _p(out))
+    return out
+
+
+def codes5(lo: np.ndarray, hi: np.ndarray, N: int) -> np.ndarray:
+    """5-bit codes uint8 [rows, N] from the nibble words and the plane."""
+    lo = _c(lo, np.int32)
+    hi = _c(hi, np.int32)
+    out = np.empty((lo.shape[0], N), dtype=np.uint8)
+    lib().orc_codes5(lo.shape[0], N, _p(lo), _p(hi), _p(out))
+    return out
+
+
+def sz5_table(scales: np.ndarray, qzeros: np.ndarray, qzeros_hi: np.ndarray) -> np.ndarray:
+    """SZ table of int5 weights [G, N, 2] f16 (scale, scale*(zp-16))."""
+    scales = _c(scales, np.uint16)
+    qzeros = _c(qzeros, np.int32)
+    qzeros_hi = _c(qzeros_hi, np.int32)
+    G, N = scales.shape
+    out = np.empty((G, N, 2), dtype=np.uint16)
+    lib().orc_sz5(G, N, _p(scales), _p(qzeros), _p(qzeros_hi), _p(out))
+    return out
+
+
+def repack5(qweight: np.ndarray, qweight_hi: np.ndarray):
+    """Kernel layouts (w [N, K/2] low nibbles, whi [N, K/8] fifth bits)."""
+    qweight = _c(qweight, np.int32)
+    qweight_hi = _c(qweight_hi, np.int32)
+    K, N8 = qweight.shape
+    N = N8 * 8
+    w = np.empty((N, K // 2), dtype=np.uint8)
+    whi = np.empty((N, K // 8), dtype=np.uint8)
+    lib().orc_repack5(K, N, _p(qweight), _p(qweight_hi), _p(w), _p(whi))
+    return w, whi
+
+
+def gemm5_f64(a, asg, rs, codes, sz, pb1, pb2) -> np.ndarray:
+    a = _c(a, np.uint8); asg = _c(asg, np.float32); rs = _c(rs, np.float32)
+    codes = _c(codes, np.uint8); sz = _c(sz, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_gemm5_f64(M, N, K, pb1, pb2, _p(a), _p(asg), _p(rs), _p(codes), _p(sz), _p(y))
+    return y
+
+
+def gemm5_f64_sampled(ms, ns, a, asg, rs, codes, sz, pb1, pb2) -> np.ndarray:
+    ms = _c(ms, np.int32); ns = _c(ns, np.int32)
+    a = _c(a, np.uint8); asg = _c(asg, np.float32); rs = _c(rs, np.float32)
+    codes = _c(codes, np.uint8); sz = _c(sz, np.uint16)
+    P, M, K = a.shape
+    N = codes.shape[1]
+    y = np.empty(len(ms), dtype=np.float64)
+    lib().orc_gemm5_f64_sampled(len(ms), _p(ms), _p(ns), M, N, K, pb1, pb2, _p(a), _p(asg), _p(rs),
+                                _p(codes), _p(sz), _p(y))
+    return y
+
+
+def pack5(prob) -> dict:
+    """Oracle's own load-time tables for a generated int5 problem."""
+    sz = sz5_table(prob["scales"], prob["qzeros"], prob["qzeros_hi"])
+    w, whi = repack5(prob["qweight"], prob["qweight_hi"])
+    return dict(rec=records(prob["pairs"], prob["theta"]), sz=sz, sz_kernel=sz_kernel_layout(sz),
+                w=w, whi=whi, codes=codes5(prob["qweight"], prob["qweight_hi"], prob["N"]),
+                zp=codes5(prob["qzeros"], prob["qzeros_hi"], prob["N"]))
 
 
 # ---------------------------------------------------------------- prologue

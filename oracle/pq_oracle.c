@@ -80,6 +80,15 @@
  *        a[k]   = e4m3(fl32(xr[k] / As)) (R6 rules; all 0x00 when As == 0)
  *        rs_g   = fl32(exact sum of the decoded codes of group g)
  *      GEMM: y = As * sum_g (sc * D - zscale * rs_g), in fp64 as R9.
+ *   R19 int5 weights ([LOG] "2026-09-10: int5 W5A8 ParoQuant": 5-bit codes,
+ *      low nibbles in the int4 AWQ words, the fifth bit in [K, N/32] int32
+ *      planes; (c - 16) runs -16..15, every value exact in e4m3).  Readings:
+ *      bit j of plane word [r][w] is the fifth bit of column 32w + j (plain
+ *      bit order; the pages give no permutation for the planes); the zero
+ *      point's plane qzeros_hi is [G, N/32] (one row per group, as qzeros);
+ *      c = nibble + 16 * bit, zp likewise; zscale = f16_RNE(fl32(sc *
+ *      (zp - 16))) (exact product); the GEMM is R9 with
+ *      D = sum_{k in g} dec(A[k]) * (c[k] - 16).
  */
 #include <math.h>
 #include <stdint.h>
@@ -225,6 +234,27 @@ void orc_unpack_awq(int rows, int N, const int32_t *packed, uint8_t *out)
         }
 }
 
+/* R19: fifth-bit plane int32 [rows, N/32] -> bits uint8 [rows, N] (0/1). */
+void orc_unpack_plane(int rows, int N, const int32_t *plane, uint8_t *out)
+{
+    for (int r = 0; r < rows; r++)
+        for (int n = 0; n < N; n++) {
+            uint32_t w = (uint32_t)plane[(size_t)r * (N / 32) + n / 32];
+            out[(size_t)r * N + n] = (uint8_t)((w >> (n % 32)) & 1u);
+        }
+}
+
+/* R19: 5-bit codes [rows, N] (0..31) from the nibble words and the plane. */
+void orc_codes5(int rows, int N, const int32_t *lo, const int32_t *hi, uint8_t *out)
+{
+    uint8_t *bit = (uint8_t *)malloc((size_t)rows * N);
+    orc_unpack_awq(rows, N, lo, out);
+    orc_unpack_plane(rows, N, hi, bit);
+    for (size_t i = 0; i < (size_t)rows * N; i++)
+        out[i] = (uint8_t)(out[i] + 16 * bit[i]);
+    free(bit);
+}
+
 /* ------------------------------------------------------------------ */
 /* load-time tables                                                    */
 /* ------------------------------------------------------------------ */
@@ -288,6 +318,22 @@ void orc_sz(int G, int N, const uint16_t *scales, const int32_t *qzeros, uint16_
     free(zp);
 }
 
+/* R19: SZ table of int5 weights, zscale = f16(sc * (zp - 16)). */
+void orc_sz5(int G, int N, const uint16_t *scales, const int32_t *qzeros, const int32_t *qzeros_hi,
+             uint16_t *sz)
+{
+    uint8_t *zp = (uint8_t *)malloc((size_t)G * N);
+    orc_codes5(G, N, qzeros, qzeros_hi, zp);
+    for (int g = 0; g < G; g++)
+        for (int n = 0; n < N; n++) {
+            uint16_t sc = scales[(size_t)g * N + n];
+            float prod = f_mul((float)orc_f16_to_double(sc), (float)(zp[(size_t)g * N + n] - 16));
+            sz[((size_t)g * N + n) * 2 + 0] = sc;
+            sz[((size_t)g * N + n) * 2 + 1] = orc_f16_from_double((double)prod);
+        }
+    free(zp);
+}
+
 /* Kernel weight layout w[n][k/2]: low nibble = code at even k, high = odd k. */
 void orc_repack(int K, int N, const int32_t *qweight, uint8_t *w)
 {
@@ -298,6 +344,23 @@ void orc_repack(int K, int N, const int32_t *qweight, uint8_t *w)
             w[(size_t)n * (K / 2) + k / 2] =
                 (uint8_t)(c[(size_t)k * N + n] | (c[(size_t)(k + 1) * N + n] << 4));
     free(c);
+}
+
+/* Kernel layouts of int5 weights: the low nibbles as orc_repack, and the
+ * fifth bits whi[n][k/8], bit k % 8 of byte k / 8 = the fifth bit of (k, n). */
+void orc_repack5(int K, int N, const int32_t *qweight, const int32_t *qweight_hi, uint8_t *w, uint8_t *whi)
+{
+    orc_repack(K, N, qweight, w);
+    uint8_t *bit = (uint8_t *)malloc((size_t)K * N);
+    orc_unpack_plane(K, N, qweight_hi, bit);
+    for (int n = 0; n < N; n++)
+        for (int k = 0; k < K; k += 8) {
+            uint8_t b = 0;
+            for (int j = 0; j < 8; j++)
+                b |= (uint8_t)(bit[(size_t)(k + j) * N + n] << j);
+            whi[(size_t)n * (K / 8) + k / 8] = b;
+        }
+    free(bit);
 }
 
 /* ------------------------------------------------------------------ */
@@ -539,10 +602,11 @@ void orc_rotate_tokquant(int M, int K, int ldx, int P, const uint16_t *x, const 
 
 static int part_of(int n, int pb1, int pb2) { return (n >= pb1) + (n >= pb2); }
 
-/* one output element, table-true (reading R9) */
-static double gemm_elem(int m, int n, int M, int N, int K, int pb1, int pb2,
-                        const uint8_t *a, const float *asg, const float *rs,
-                        const uint8_t *codes, const uint16_t *sz)
+/* one output element, table-true (reading R9); off = 8 for int4 codes,
+ * 16 for int5 (R19) */
+static double gemm_elem_off(int m, int n, int M, int N, int K, int pb1, int pb2,
+                            const uint8_t *a, const float *asg, const float *rs,
+                            const uint8_t *codes, const uint16_t *sz, int off)
 {
     int G = K / 128;
     int p = part_of(n, pb1, pb2);
@@ -551,7 +615,7 @@ static double gemm_elem(int m, int n, int M, int N, int K, int pb1, int pb2,
     for (int g = 0; g < G; g++) {
         double D = 0.0;             /* exact: products and sums are multiples of 2^-9 below 2^53 */
         for (int k = 128 * g; k < 128 * g + 128; k++)
-            D += orc_e4m3_decode(arow[k]) * (double)((int)codes[(size_t)k * N + n] - 8);
+            D += orc_e4m3_decode(arow[k]) * (double)((int)codes[(size_t)k * N + n] - off);
         double sc = orc_f16_to_double(sz[((size_t)g * N + n) * 2 + 0]);
         double zs = orc_f16_to_double(sz[((size_t)g * N + n) * 2 + 1]);
         double s = asg[((size_t)p * G + g) * M + m];
@@ -559,6 +623,32 @@ static double gemm_elem(int m, int n, int M, int N, int K, int pb1, int pb2,
         y += s * (sc * D - zs * r);
     }
     return y;
+}
+
+static double gemm_elem(int m, int n, int M, int N, int K, int pb1, int pb2,
+                        const uint8_t *a, const float *asg, const float *rs,
+                        const uint8_t *codes, const uint16_t *sz)
+{
+    return gemm_elem_off(m, n, M, N, K, pb1, pb2, a, asg, rs, codes, sz, 8);
+}
+
+/* R19: the GEMM of int5 codes (0..31) with their SZ table, full and sampled. */
+void orc_gemm5_f64(int M, int N, int K, int pb1, int pb2, const uint8_t *a, const float *asg,
+                   const float *rs, const uint8_t *codes, const uint16_t *sz, double *y)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++)
+            y[(size_t)m * N + n] = gemm_elem_off(m, n, M, N, K, pb1, pb2, a, asg, rs, codes, sz, 16);
+}
+
+void orc_gemm5_f64_sampled(int count, const int *ms, const int *ns, int M, int N, int K,
+                           int pb1, int pb2, const uint8_t *a, const float *asg, const float *rs,
+                           const uint8_t *codes, const uint16_t *sz, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < count; i++)
+        y[i] = gemm_elem_off(ms[i], ns[i], M, N, K, pb1, pb2, a, asg, rs, codes, sz, 16);
 }
 
 /*

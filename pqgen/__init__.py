@@ -12,6 +12,12 @@ gfx1201 -- engineering log", section "Format"):
 * ``theta``    f16 ``[P, 8, K/2]`` Givens angles (uint16 bit patterns)
 * ``cs``       f16 ``[P, K]`` channel scales, stored pre-inverted (uint16 bits)
 
+With ``bits=5`` (int5 weights, "2026-09-10: int5 W5A8 ParoQuant"): ``qweight``
+and ``qzeros`` hold the low nibbles, and ``qweight_hi`` int32 ``[K, N/32]`` and
+``qzeros_hi`` int32 ``[K/128, N/32]`` the fifth bits, 32 columns per word.
+Every nibble and every fifth bit is an independent uniform draw, so the codes
+are uniform 0..31 and the zero points uniform 0..31.
+
 It holds none of the method's arithmetic: no rotation, no quantisation, no
 unpacking.  Every nibble of ``qweight`` is an independent uniform code 0..15
 and every nibble of ``qzeros`` an independent uniform zero point 2..14, so the
@@ -34,6 +40,7 @@ __all__ = [
 TENSOR_IDS = {
     "x": 1, "qweight": 2, "qzeros": 3, "scales": 4, "pairs": 5, "theta": 6,
     "cs": 7, "outliers": 8, "codes": 9, "asg": 10, "sparse": 11,
+    "qweight_hi": 12, "qzeros_hi": 13, "qzeros5": 14,
 }
 
 # The five workloads: (M, K, N, P, partition boundaries, extra knobs).
@@ -86,7 +93,7 @@ class Problem(dict):
 
 def make_problem(M: int, K: int, N: int, P: int = 1, seed: int = 0,
                  pb=None, outlier_frac: float = 0.0, x_sigma: float = 1.0,
-                 x_mode: str = "normal", theta_range: float = 0.5) -> Problem:
+                 x_mode: str = "normal", theta_range: float = 0.5, bits: int = 4) -> Problem:
     """Generate one synthetic linear layer and its input activations.
 
     x_mode: "normal"  -- x ~ N(0, x_sigma^2)
@@ -97,6 +104,8 @@ def make_problem(M: int, K: int, N: int, P: int = 1, seed: int = 0,
     """
     if K % 128 or N % 128:
         raise ValueError("K and N must be multiples of 128")
+    if bits not in (4, 5):
+        raise ValueError("bits must be 4 or 5")
     G = K // 128
     # activations, drawn and rounded to bf16 in row blocks (same stream as one draw)
     r = _rng(seed, "x")
@@ -128,7 +137,10 @@ def make_problem(M: int, K: int, N: int, P: int = 1, seed: int = 0,
     # eight independent uniform codes 0..15 per word == one uniform 32-bit word
     qweight = _rng(seed, "qweight").integers(0, 1 << 32, size=(K, N // 8),
                                              dtype=np.uint64).astype(np.uint32).view(np.int32)
-    qzeros = _nibble_words(_rng(seed, "qzeros"), (G, N // 8), 2, 14)
+    if bits == 4:
+        qzeros = _nibble_words(_rng(seed, "qzeros"), (G, N // 8), 2, 14)
+    else:
+        qzeros = _nibble_words(_rng(seed, "qzeros5"), (G, N // 8), 0, 15)
     scales = f16_bits(_rng(seed, "scales").uniform(0.002, 0.02, size=(G, N)))
     # rotations, one per partition
     pairs = np.empty((P, 8, K), dtype=np.int16)
@@ -147,9 +159,16 @@ def make_problem(M: int, K: int, N: int, P: int = 1, seed: int = 0,
         if pb is None:
             third = (N // 3) // 128 * 128
             pb = (third, 2 * third)
-    return Problem(M=M, K=K, N=N, P=P, G=G, seed=seed, pb1=int(pb[0]), pb2=int(pb[1]),
+    prob = Problem(M=M, K=K, N=N, P=P, G=G, seed=seed, pb1=int(pb[0]), pb2=int(pb[1]),
                    x=x, qweight=qweight, qzeros=qzeros, scales=scales,
-                   pairs=pairs, theta=theta, cs=cs)
+                   pairs=pairs, theta=theta, cs=cs, bits=bits)
+    if bits == 5:
+        def plane(name, rows):
+            return _rng(seed, name).integers(0, 1 << 32, size=(rows, N // 32),
+                                             dtype=np.uint64).astype(np.uint32).view(np.int32)
+        prob["qweight_hi"] = plane("qweight_hi", K)
+        prob["qzeros_hi"] = plane("qzeros_hi", G)
+    return prob
 
 
 def config_problem(name: str, M: int | None = None, **over) -> Problem:
