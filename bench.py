@@ -219,6 +219,25 @@ class Workload:
         pq.pq_gemm_ptok(self.a[j], self.As[j], self.rs[j], self.w[j], self.sz[j], self.pb1, self.pb2,
                         y=self.y[j], stream=stream)
 
+    def int5_buffers(self, pq, torch, dev):
+        """The same layer with int5 weights (same seed: the same activations
+        and rotations), packed by pq_pack5, one set per input copy."""
+        if getattr(self, "w5", None) is not None:
+            return
+        p5 = pqgen.make_problem(**self.c, bits=5)
+        _, sz, w, whi = pq.pq_pack5(p5.qweight, p5.qzeros, p5.qweight_hi, p5.qzeros_hi, p5.scales, p5.pairs,
+                                    p5.theta)
+        u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+        self.w5 = [torch.from_numpy(w).to(dev) for _ in range(self.copies)]
+        self.whi5 = [torch.from_numpy(whi).to(dev) for _ in range(self.copies)]
+        self.sz5 = [u16(sz) for _ in range(self.copies)]
+        self.gemm5_bytes = self.gemm_bytes + whi.nbytes
+
+    def gemm5(self, pq, i, stream):
+        j = i % self.copies
+        pq.pq_gemm5(self.a[j], self.asg[j], self.rs[j], self.w5[j], self.whi5[j], self.sz5[j], self.pb1, self.pb2,
+                    y=self.y[j], stream=stream)
+
     def gemm(self, pq, i, stream, fn=None):
         j = i % self.copies
         (fn or pq.pq_gemm)(self.a[j], self.asg[j], self.rs[j], self.w[j], self.sz[j], self.pb1,
@@ -317,6 +336,9 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
     paths = time_gemm_paths(pq, torch, wl, reps, stream) if wl.c["M"] <= 16 else {}
     out = dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths,
                prod_ms=per["prod"], silu_ms=per["silu"])
+    # the same GEMM on int5 weights
+    wl.int5_buffers(pq, torch, wl.x[0].device)
+    out["int5_gemm_ms"] = time_each(wl.gemm5)
     if wl.c["M"] > 16:
         # the per-token activation-scale path: its two-pass prologue, then its GEMM
         wl.ptok_buffers(torch, wl.x[0].device)
@@ -458,6 +480,11 @@ def summarize(wl, r, steps, peaks):
                   "gemm_frac_fp8": round(wl.flops / (r["ptok_gemm_ms"] * 1e-3) / 1e12 / (2 * peaks["bf16"]), 4),
                   "step_us": round((r["ptok_pro_ms"] + r["ptok_gemm_ms"]) * 1e3, 3)}
                  if "ptok_pro_ms" in r else None),
+        # int5 weights (W5A8): the GEMM alone, bytes incl. the fifth-bit planes
+        "int5": {"gemm_us": round(r["int5_gemm_ms"] * 1e3, 3),
+                 "gemm_gbs": round(wl.gemm5_bytes / (r["int5_gemm_ms"] * 1e-3) / 1e9, 1),
+                 "gemm_tflops": round(wl.flops / (r["int5_gemm_ms"] * 1e-3) / 1e12, 2),
+                 "vs_int4_time": round(r["int5_gemm_ms"] / r["gemm_ms"], 3)},
         "copies": wl.copies,
         "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
     }

@@ -18,6 +18,9 @@
  *   [CVT]      section "2026-09-15: hardware e4m3 convert in the producers"
  *   [PTOK]     section "Numbers", the per-token prefill item (pass A, pass C,
  *              the PTOK GEMM with As in the epilogue)
+ *   [INT5]     section "2026-09-10: int5 W5A8 ParoQuant" (5-bit codes: low
+ *              nibbles in the int4 words, the fifth bit in bit planes;
+ *              c - 16 exact in e4m3)
  *
  * Conventions for every call:
  *   - Sizes are element counts.  G = K / 128.  "f16" = IEEE binary16,
@@ -131,6 +134,25 @@ pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_t *sz_bytes
 pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
                   const uint16_t *scales, const int16_t *pairs, const uint16_t *theta,
                   void *rec, void *sz, void *w);
+
+/*
+ * Host packer for int5 weights ([INT5]).  As pq_pack, plus the fifth bits:
+ *   qweight, qzeros  the low nibbles of the 5-bit codes and zero points, in
+ *                    pq_pack's AWQ packing
+ *   qweight_hi       int32 [K][N/32]: bit j of word w = the fifth bit of the
+ *                    code of column 32w + j
+ *   qzeros_hi        int32 [G][N/32]: the zero points' fifth bits, same order
+ * so c = nibble + 16 * bit and zp likewise (0..31).  Outputs:
+ *   rec, w   as pq_pack (w holds the low nibbles)
+ *   sz       as pq_pack with zscale = f16(sc * (zp - 16))
+ *   whi      [N][K/8] bytes (N * K / 8): bit k % 8 of byte k / 8 of row n is
+ *            the fifth bit of c[k][n]
+ * Errors: as pq_pack.
+ */
+pq_status pq_pack5(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
+                   const int32_t *qweight_hi, const int32_t *qzeros_hi, const uint16_t *scales,
+                   const int16_t *pairs, const uint16_t *theta, void *rec, void *sz, void *w,
+                   void *whi);
 
 /* ------------------------------------------------------------------------ */
 /* Per forward (device)                                                     */
@@ -320,6 +342,30 @@ pq_status pq_rotate_tokquant(const void *x, int M, int K, int ldx, int P, const 
 pq_status pq_gemm_ptok(const void *a, const float *As, const float *rs, int M, int N, int K, int P,
                        int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
                        unsigned int *dev_status, void *stream);
+
+/*
+ * uint4 x e4m3 group GEMM on int5 weights ([INT5]): pq_gemm's result with
+ *   D = sum_{k in g} dec(a[p(n)][m][k]) * (c[k][n] - 16),  c in 0..31,
+ *   y[m][n] = bf16( sum_g asg[p][g][m] * (sc[g][n] * D - zs[g][n] * rs[p][g][m]) )
+ * and (sc, zs) from pq_pack5's SZ table.  The tensor cores take (c - 16) * 2^-9
+ * itself, exact in e4m3.  Tolerance and arguments as pq_gemm, plus
+ *   w, whi, sz  device copies of pq_pack5's outputs (whi 16-byte aligned)
+ * pq_gemm5 dispatches: M <= 16 with at least half the SMs covered by the
+ * 128-feature tiles runs the narrow tensor-core kernel (pq_gemm5_tcn), anything
+ * else the prefill tensor-core kernel (pq_gemm5_tc).  pq_gemm5_tcn accepts
+ * 1 <= M <= 16.  dev_status as for pq_gemm_tc.
+ * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE, PQ_ERR_ALIGN, PQ_ERR_PARTITION,
+ * PQ_ERR_ARCH, PQ_ERR_CUDA.
+ */
+pq_status pq_gemm5(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
+                   int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y, int ldy,
+                   void *stream);
+pq_status pq_gemm5_tc(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
+                      int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y,
+                      int ldy, unsigned int *dev_status, void *stream);
+pq_status pq_gemm5_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
+                       int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y,
+                       int ldy, unsigned int *dev_status, void *stream);
 
 /*
  * The prologue's device e4m3 encoder applied to n fp32 values ([CVT]: NaN ->

@@ -51,6 +51,22 @@ def test_pack_byte_equal_to_oracle(L, orc, shape):
     assert np.array_equal(w, t["w"])
 
 
+@pytest.mark.parametrize("shape", [(256, 128, 1), (640, 384, 3), (5120, 1024, 2)])
+def test_pack5_byte_equal_to_oracle(L, orc, shape):
+    """int5 packer: records, SZ (zp - 16), low nibbles and fifth-bit planes."""
+    K, N, P = shape
+    prob = pqgen.make_problem(2, K, N, P=P, seed=K + N + P + 5, bits=5)
+    rec, sz, w, whi = pq.pq_pack5(prob.qweight, prob.qzeros, prob.qweight_hi, prob.qzeros_hi, prob.scales,
+                                  prob.pairs, prob.theta)
+    t = orc.pack5(prob)
+    assert np.array_equal(rec, t["rec"])
+    assert np.array_equal(sz, t["sz_kernel"])
+    assert np.array_equal(w, t["w"])
+    assert np.array_equal(whi, t["whi"])
+    nul = C.c_void_p(0)
+    assert L.pq_pack5(K, N, P, *([nul] * 11)) == 1
+
+
 def test_pack_special_angles_and_scales(L, orc):
     """Angles and scales at the edges of f16: zero, subnormal, large, negative."""
     prob = pqgen.make_problem(1, 256, 256, seed=3)
@@ -118,6 +134,9 @@ def test_gemm_argument_checks(L, case, status):
     assert L.pq_gemm_tc(*vals, None, None) == status
     assert L.pq_gemm_skinny(*vals, None, None) == status
     assert L.pq_gemm_ptok(*vals, None, None) == status
+    v5 = vals[:10] + [A] + vals[10:]             # whi after w
+    assert L.pq_gemm5(*v5, None) == status
+    assert L.pq_gemm5_tc(*v5, None, None) == status
     assert L.pq_last_error()
 
 
@@ -206,6 +225,9 @@ def test_device_calls_without_gpu_report_arch(L):
     assert L.pq_silu_mul_rotate_quant(X2, 4, 256, 512, 1, A, A, O2, A, S, S, None) == 6
     assert L.pq_rotate_tokquant(X2, 4, 256, 256, 1, A, A, O2, A, S, S, None) == 6
     assert L.pq_gemm_ptok(*vals, None, None) == 6
+    v5 = vals[:10] + [A] + vals[10:]
+    assert L.pq_gemm5(*v5, None) == 6 and L.pq_gemm5_tcn(*v5, None, None) == 6
+    assert L.pq_gemm5(*(vals[:10] + [None] + vals[10:]), None) == 1
     assert L.pq_e4m3_encode(S, A, 16, None) == 6
     with pytest.raises(pq.PQError) as e:
         pq._check(6, "probe")

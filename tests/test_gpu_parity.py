@@ -587,6 +587,134 @@ def test_ptok_full_workload_sampled(pq, orc, name):
     assert_close(y.float().cpu().numpy()[ms, ns], y64, "ptok %s M=%d" % (name, prob.M))
 
 
+# ---------------------------------------------------------------- int5 weights
+class Problem5:
+    """A generated int5 layer: device tables from pq_pack5, host tables from
+    the oracle's packer (checked byte-equal)."""
+
+    def __init__(self, pq, orc, prob, check_pack=True):
+        self.prob = prob
+        self.rec, self.sz, self.w, self.whi = pq.pq_pack5(prob.qweight, prob.qzeros, prob.qweight_hi,
+                                                          prob.qzeros_hi, prob.scales, prob.pairs, prob.theta)
+        self.t = orc.pack5(prob)
+        if check_pack:
+            assert np.array_equal(self.rec, self.t["rec"])
+            assert np.array_equal(self.sz, self.t["sz_kernel"])
+            assert np.array_equal(self.w, self.t["w"])
+            assert np.array_equal(self.whi, self.t["whi"])
+        self.rec_d = torch.from_numpy(self.rec).cuda()
+        self.sz_d = dev_u16(self.sz)
+        self.w_d = torch.from_numpy(self.w).cuda()
+        self.whi_d = torch.from_numpy(self.whi).cuda()
+        self.cs_d = dev_u16(prob.cs)
+        self.x_d = dev_u16(prob.x).view(torch.bfloat16)
+
+
+def run_gemm5(name, a, asg, rs, L, pb1, pb2, M, N, ldy=None):
+    """pq_gemm5_tc / pq_gemm5_tcn through the C ABI into a NaN-filled strided y."""
+    import ctypes as C
+    import w4a8_rotated_int4_gb300 as m
+    ldy = ldy or N
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ybuf = torch.full((M + 3, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
+    P, K = a.shape[0], a.shape[2]
+    st = getattr(m.lib(), name)(C.c_void_p(a.data_ptr()), C.c_void_p(asg.data_ptr()), C.c_void_p(rs.data_ptr()),
+                                M, N, K, P, pb1, pb2, C.c_void_p(L.w_d.data_ptr()), C.c_void_p(L.whi_d.data_ptr()),
+                                C.c_void_p(L.sz_d.data_ptr()), C.c_void_p(ybuf.data_ptr()), ldy,
+                                C.c_void_p(status.data_ptr()), C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    m._check(st, name)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %d" % int(status.item())
+    yb = ybuf.float().cpu().numpy()
+    assert np.isnan(yb[M:]).all()
+    if ldy > N:
+        assert np.isnan(yb[:M, N:]).all()
+    return yb[:M, :N]
+
+
+def gemm5_paths(M):
+    return ["pq_gemm5_tc"] + (["pq_gemm5_tcn"] if M <= 16 else [])
+
+
+INT5_SMALL = [  # M, K, N, P, pb
+    (1, 1024, 256, 1, None), (4, 256, 128, 1, None), (16, 1152, 512, 1, None), (7, 512, 384, 3, (128, 256)),
+    (12, 384, 512, 2, (256, 512)), (129, 512, 256, 1, None), (200, 896, 384, 3, (128, 256)),
+    (256, 1024, 512, 1, None), (33, 8704, 128, 1, None), (3, 5120, 1024, 1, None),
+]
+
+
+@pytest.mark.parametrize("M,K,N,P,pb", INT5_SMALL)
+def test_gemm5_vs_oracle(pq, orc, M, K, N, P, pb):
+    prob = pqgen.make_problem(M, K, N, P=P, pb=pb, seed=M * 3 + K + N, bits=5)
+    L = Problem5(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    y64 = orc.gemm5_f64(a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
+    for name in gemm5_paths(M):
+        y = run_gemm5(name, a, asg, rs, L, prob.pb1, prob.pb2, M, N, ldy=N + 64)
+        assert_close(y, y64, "%s M=%d K=%d N=%d P=%d" % (name, M, K, N, P))
+    y = pq.pq_gemm5(a, asg, rs, L.w_d, L.whi_d, L.sz_d, prob.pb1, prob.pb2)
+    assert_close(y.float().cpu().numpy(), y64, "pq_gemm5 M=%d" % M)
+
+
+@pytest.mark.parametrize("M", [300, 3])
+def test_gemm5_zero_scale_groups(pq, orc, M):
+    """int5 columns whose scale is 0 dequantize to -zscale (set by hand here)."""
+    K, N = 512, 256
+    G = K // 128
+    prob = pqgen.make_problem(M, K, N, seed=41 + M, bits=5)
+    L = Problem5(pq, orc, prob)
+    rng = np.random.default_rng(7)
+    sz = L.t["sz"].copy()
+    pick = rng.random((G, N)) < 0.15
+    zs = (rng.standard_normal((G, N)) * 0.02).astype(np.float16).view(np.uint16)
+    sz[..., 0][pick] = np.where(rng.random(int(pick.sum())) < 0.5, 0x0000, 0x8000)
+    sz[..., 1][pick] = zs[pick]
+    L.sz_d = dev_u16(np.ascontiguousarray(sz.reshape(G, N // 8, 8, 2).transpose(1, 0, 2, 3)))
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    y64 = orc.gemm5_f64(a.cpu().numpy(), asg.cpu().numpy(), rs.cpu().numpy(), L.t["codes"], sz, N, N)
+    for name in gemm5_paths(M):
+        assert_close(run_gemm5(name, a, asg, rs, L, N, N, M, N), y64, "%s zero-scale M=%d" % (name, M))
+
+
+def test_gemm5_all_fifth_bits_equal_int4(pq, orc):
+    """With every fifth bit set, int5 codes and zero points are the int4 ones
+    plus 16: the same layer.  The two SZ tables round zscale to f16 from
+    different products (sc * zp vs sc * (zp - 8)), so the int5 and int4
+    oracles agree to that rounding only; the GPU is held to the int5 one."""
+    M, K, N = 16, 512, 256
+    prob = pqgen.make_problem(M, K, N, seed=3)
+    p5 = pqgen.Problem(dict(prob))
+    p5["qweight_hi"] = np.full((K, N // 32), -1, dtype=np.int32)
+    p5["qzeros_hi"] = np.full((K // 128, N // 32), -1, dtype=np.int32)
+    L4, L5 = Problem(pq, orc, prob), Problem5(pq, orc, p5)
+    assert np.array_equal(L4.w, L5.w) and (L5.whi == 0xFF).all()
+    a, asg, rs = pq.pq_rotate_quant(L4.x_d, L4.rec_d, L4.cs_d)
+    a_h, s_h, r_h = a.cpu().numpy(), asg.cpu().numpy(), rs.cpu().numpy()
+    y4 = orc.gemm_f64(a_h, s_h, r_h, L4.t["codes"], L4.t["sz"], N, N)
+    y64 = orc.gemm5_f64(a_h, s_h, r_h, L5.t["codes"], L5.t["sz"], N, N)
+    assert orc.rel_err(y64, y4) < 1e-3
+    for name in ("pq_gemm5_tc", "pq_gemm5_tcn"):
+        assert_close(run_gemm5(name, a, asg, rs, L5, N, N, M, N), y64, name)
+
+
+@pytest.mark.parametrize("name,M", [("decode", 1), ("decode", 16), ("prefill", None), ("qkv", None)])
+def test_gemm5_full_workload_sampled(pq, orc, name, M):
+    """int5 weights at the benchmarked sizes: 3000 sampled outputs against the
+    fp64 oracle (packer checked byte-equal)."""
+    prob = pqgen.config_problem(name, M=M, bits=5)
+    L = Problem5(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    y = pq.pq_gemm5(a, asg, rs, L.w_d, L.whi_d, L.sz_d, prob.pb1, prob.pb2)
+    torch.cuda.synchronize()
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    ms, ns = _samples(prob.M, prob.N, prob.pb1, prob.pb2, 3000, 17)
+    y64 = orc.gemm5_f64_sampled(ms, ns, a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
+    assert_close(y.float().cpu().numpy()[ms, ns], y64, "int5 %s M=%d" % (name, prob.M))
+
+
 # ---------------------------------------------------------------- repeated launches
 @pytest.mark.parametrize("path", ["skinny", "tcn", "tc"])
 def test_gemm_repeated_graph_launches_status_clean(pq, orc, path):

@@ -27,6 +27,7 @@ EXPORTS = (
     "pq_gemm_tc",
     "pq_gemm_tcn",
     "pq_rotate_tokquant", "pq_gemm_ptok",
+    "pq_pack5", "pq_gemm5", "pq_gemm5_tc", "pq_gemm5_tcn",
     "pq_e4m3_encode",
 )
 
@@ -83,6 +84,14 @@ def lib() -> C.CDLL:
     L.pq_rotate_tokquant.argtypes = [vp, i32, i32, i32, i32] + [vp] * 7
     L.pq_gemm_ptok.restype = i32
     L.pq_gemm_ptok.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
+    L.pq_pack5.restype = i32
+    L.pq_pack5.argtypes = [i32, i32, i32] + [vp] * 11
+    L.pq_gemm5.restype = i32
+    L.pq_gemm5.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, vp, i32, vp]
+    for name in ("pq_gemm5_tc", "pq_gemm5_tcn"):
+        f = getattr(L, name)
+        f.restype = i32
+        f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, vp, i32, vp, vp]
     L.pq_e4m3_encode.restype = i32
     L.pq_e4m3_encode.argtypes = [vp, vp, st, vp]
     _lib = L
@@ -142,6 +151,35 @@ def pq_pack(qweight: np.ndarray, qzeros: np.ndarray, scales: np.ndarray, pairs: 
                          _np_ptr(pairs), _np_ptr(theta), _np_ptr(rec), _np_ptr(sz), _np_ptr(w)),
            "pq_pack")
     return rec, sz, w
+
+
+def pq_pack5(qweight, qzeros, qweight_hi, qzeros_hi, scales, pairs, theta):
+    """Host packer for int5 weights: pq_pack's inputs plus the fifth-bit planes
+    qweight_hi int32 [K, N/32] and qzeros_hi int32 [G, N/32].  Returns
+    (rec, sz, w, whi uint8 [N, K/8])."""
+    qweight = np.ascontiguousarray(qweight, dtype=np.int32)
+    qzeros = np.ascontiguousarray(qzeros, dtype=np.int32)
+    qweight_hi = np.ascontiguousarray(qweight_hi, dtype=np.int32)
+    qzeros_hi = np.ascontiguousarray(qzeros_hi, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int16)
+    theta = np.ascontiguousarray(theta, dtype=np.uint16)
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    if pairs.ndim == 2:
+        pairs = pairs[None]
+        theta = theta[None]
+    P = pairs.shape[0]
+    G = K // 128
+    if qweight_hi.shape != (K, N // 32) or qzeros_hi.shape != (G, N // 32):
+        raise PQError("pq_pack5: fifth-bit planes must be [K, N/32] and [G, N/32]")
+    rec = np.empty((P, 8, G, 64, 8), dtype=np.uint8)
+    sz = np.empty((N // 8, G, 8, 2), dtype=np.uint16)
+    w = np.empty((N, K // 2), dtype=np.uint8)
+    whi = np.empty((N, K // 8), dtype=np.uint8)
+    _check(lib().pq_pack5(K, N, P, _np_ptr(qweight), _np_ptr(qzeros), _np_ptr(qweight_hi), _np_ptr(qzeros_hi),
+                          _np_ptr(scales), _np_ptr(pairs), _np_ptr(theta), _np_ptr(rec), _np_ptr(sz),
+                          _np_ptr(w), _np_ptr(whi)), "pq_pack5")
+    return rec, sz, w, whi
 
 
 # ---------------------------------------------------------------- device calls
@@ -305,6 +343,32 @@ def pq_gemm_ptok(a, As, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, 
     """y bf16 [M, N] from the per-token prologue's outputs (As in the epilogue)."""
     return _gemm_path(lib().pq_gemm_ptok, "pq_gemm_ptok", a, As, rs, w, sz, pb1, pb2, y,
                       dev_status, stream)
+
+
+def pq_gemm5(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, stream=None):
+    """y bf16 [M, N]: the group GEMM on int5 weights (pq_pack5's w, whi, sz)."""
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
+    _check(lib().pq_gemm5(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w), _dptr(whi),
+                          _dptr(sz), _dptr(y), y.stride(0), _stream(stream)), "pq_gemm5")
+    return y
+
+
+def _gemm5_path(fn, name, a, asg, rs, w, whi, sz, pb1, pb2, y, dev_status, stream):
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
+    st = _dptr(dev_status) if dev_status is not None else None
+    _check(fn(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w), _dptr(whi), _dptr(sz),
+              _dptr(y), y.stride(0), st, _stream(stream)), name)
+    return y
+
+
+def pq_gemm5_tc(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    return _gemm5_path(lib().pq_gemm5_tc, "pq_gemm5_tc", a, asg, rs, w, whi, sz, pb1, pb2, y, dev_status,
+                       stream)
+
+
+def pq_gemm5_tcn(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    return _gemm5_path(lib().pq_gemm5_tcn, "pq_gemm5_tcn", a, asg, rs, w, whi, sz, pb1, pb2, y, dev_status,
+                       stream)
 
 
 def pq_e4m3_encode(x, out=None, stream=None):

@@ -178,15 +178,17 @@ extern "C" pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_
     return PQ_OK;
 }
 
-extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
-                             const uint16_t *scales, const int16_t *pairs, const uint16_t *theta,
-                             void *rec, void *sz, void *w) {
-    clear_error();
-    if (!qweight || !qzeros || !scales || !pairs || !theta || !rec || !sz || !w)
-        return fail(PQ_ERR_NULL, "pq_pack: NULL pointer");
+// Both packers: int4 (qweight_hi == NULL) or int5 (the fifth-bit planes
+// qweight_hi [K][N/32], qzeros_hi [G][N/32], column 32w + j in bit j).
+static pq_status pack_layer(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
+                            const int32_t *qweight_hi, const int32_t *qzeros_hi, const uint16_t *scales,
+                            const int16_t *pairs, const uint16_t *theta, void *rec, void *sz, void *w,
+                            void *whi) {
     pq_status st = pq_pack_sizes(K, N, P, nullptr, nullptr, nullptr);
     if (st != PQ_OK) return st;
-    const int G = K / 128, W8 = N / 8;
+    const int G = K / 128, W8 = N / 8, W32 = N / 32;
+    const bool int5 = qweight_hi != nullptr;
+    const int offset = int5 ? 16 : 8;       // the code's midpoint: c - 8 (int4), c - 16 (int5)
 
     // pairs: every (p, layer, group) row a permutation of 0..127
     for (int row = 0; row < P * 8 * G; ++row) {
@@ -221,8 +223,8 @@ extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const 
                 o[7] = (uint8_t)(s >> 8);
             }
 
-    // SZ table: (sc, f16(sc * (zp - 8))), the product exact in fp32, one word
-    // per (column, group) at [n/8][g][n%8]
+    // SZ table: (sc, f16(sc * (zp - offset))), the product exact in fp32, one
+    // word per (column, group) at [n/8][g][n%8]
     uint32_t *so = static_cast<uint32_t *>(sz);
     for (int g = 0; g < G; ++g)
         for (int w8 = 0; w8 < W8; ++w8) {
@@ -230,9 +232,10 @@ extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const 
             for (int s = 0; s < 8; ++s) {
                 const int j = kAwqOrder[s];
                 const int n = 8 * w8 + j;
-                const int zp = (int)((zw >> (4 * s)) & 15u);
+                int zp = (int)((zw >> (4 * s)) & 15u);
+                if (int5) zp += 16 * (int)(((uint32_t)qzeros_hi[(size_t)g * W32 + n / 32] >> (n % 32)) & 1u);
                 const uint16_t sc = scales[(size_t)g * N + n];
-                const float prod = (float)half_value(sc) * (float)(zp - 8);
+                const float prod = (float)half_value(sc) * (float)(zp - offset);
                 so[((size_t)w8 * G + g) * 8 + j] = (uint32_t)sc | ((uint32_t)half_bits_rne((double)prod) << 16);
             }
         }
@@ -251,7 +254,39 @@ extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const 
             }
         }
     }
+
+    // int5: fifth bits whi[n][k/8], bit k % 8 of byte k / 8
+    if (int5) {
+        uint8_t *ho = static_cast<uint8_t *>(whi);
+        for (int k = 0; k < K; k += 8)
+            for (int n = 0; n < N; ++n) {
+                uint32_t b = 0;
+                for (int j = 0; j < 8; ++j)
+                    b |= (((uint32_t)qweight_hi[(size_t)(k + j) * W32 + n / 32] >> (n % 32)) & 1u) << j;
+                ho[(size_t)n * (K / 8) + k / 8] = (uint8_t)b;
+            }
+    }
     return PQ_OK;
+}
+
+extern "C" pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
+                             const uint16_t *scales, const int16_t *pairs, const uint16_t *theta,
+                             void *rec, void *sz, void *w) {
+    clear_error();
+    if (!qweight || !qzeros || !scales || !pairs || !theta || !rec || !sz || !w)
+        return fail(PQ_ERR_NULL, "pq_pack: NULL pointer");
+    return pack_layer(K, N, P, qweight, qzeros, nullptr, nullptr, scales, pairs, theta, rec, sz, w, nullptr);
+}
+
+extern "C" pq_status pq_pack5(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,
+                              const int32_t *qweight_hi, const int32_t *qzeros_hi, const uint16_t *scales,
+                              const int16_t *pairs, const uint16_t *theta, void *rec, void *sz, void *w,
+                              void *whi) {
+    clear_error();
+    if (!qweight || !qzeros || !qweight_hi || !qzeros_hi || !scales || !pairs || !theta || !rec || !sz || !w ||
+        !whi)
+        return fail(PQ_ERR_NULL, "pq_pack5: NULL pointer");
+    return pack_layer(K, N, P, qweight, qzeros, qweight_hi, qzeros_hi, scales, pairs, theta, rec, sz, w, whi);
 }
 
 extern "C" pq_status pq_rotate_quant(const void *x, int M, int K, int ldx, int P, const void *rec,
@@ -410,6 +445,54 @@ extern "C" pq_status pq_gemm_tcn(const void *a, const float *asg, const float *r
     st = check_device(&sms);
     if (st != PQ_OK) return st;
     return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream);
+}
+
+extern "C" pq_status pq_gemm5_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                                 int P, int pb1, int pb2, const void *w, const void *whi, const void *sz,
+                                 void *y, int ldy, unsigned int *dev_status, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (!whi) return fail(PQ_ERR_NULL, "NULL whi");
+    if (!aligned(whi, 16)) return fail(PQ_ERR_ALIGN, "whi needs 16-byte alignment");
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, sms, false, whi);
+}
+
+extern "C" pq_status pq_gemm5_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                                  int P, int pb1, int pb2, const void *w, const void *whi, const void *sz,
+                                  void *y, int ldy, unsigned int *dev_status, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (!whi) return fail(PQ_ERR_NULL, "NULL whi");
+    if (!aligned(whi, 16)) return fail(PQ_ERR_ALIGN, "whi needs 16-byte alignment");
+    if (M > kTcnMaxM) return fail(PQ_ERR_SHAPE, "pq_gemm5_tcn: M = %d > %d", M, kTcnMaxM);
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, whi);
+}
+
+extern "C" pq_status pq_gemm5(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
+                              int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y,
+                              int ldy, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (!whi) return fail(PQ_ERR_NULL, "NULL whi");
+    if (!aligned(whi, 16)) return fail(PQ_ERR_ALIGN, "whi needs 16-byte alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    // M <= 16: the narrow tensor-core kernel when its 128-feature tiles cover at
+    // least half the SMs; otherwise (and for M > 16) the prefill kernel
+    if (M <= kTcnMaxM && 2 * (N / 128) >= sms)
+        return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, whi);
+    return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, sms, false, whi);
 }
 
 extern "C" pq_status pq_gemm(const void *a, const float *asg, const float *rs, int M, int N, int K,

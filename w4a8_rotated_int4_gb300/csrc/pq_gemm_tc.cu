@@ -87,20 +87,28 @@ constexpr uint32_t kTmemCols = 512;    // 2 buffers x 2 halves x 128 columns
 constexpr uint32_t kZLbo = 128, kZSbo = 256;
 constexpr uint32_t kZaBytes = BM * 32, kZbBytes = BN * 32;
 
-struct __align__(1024) Stage {
+// int5 weights: the fifth bits of the slab, 128 rows x 16 B (one bit per k)
+constexpr uint32_t kBhBytes = BN * BK / 8;
+
+template <int kBits>
+struct __align__(1024) StageT {
     uint8_t a[kABytes];       // 256 rows x 128 B, SWIZZLE_128B (TMA); half h at 16 KB * h
     uint8_t bx[kBxBytes];     // 128 rows x 128 B, SWIZZLE_128B (expand warps)
     uint8_t bp[kBpBytes];     // 128 rows x 64 B packed nibbles (TMA)
     uint32_t sz[BN];          // f16 (sc, zscale) per column
     uint8_t zb[kZbBytes];     // zero-point operand per column (expand warps)
+    uint8_t bh[kBits == 5 ? kBhBytes : 16];   // int5: fifth-bit planes (TMA)
 };
 
 // fp32 scales of one slab for the fold warps, in a ring of their own so a
 // stage is free as soon as its MMAs complete (the fold lags the MMA).  The
 // column part comes from the expansion warps; the row part is copied straight
 // from global memory by the row warp (cp.async), which runs up to a ring's
-// depth ahead, so no global-load latency reaches the fold warps.
-constexpr int kSzfRing = 4;
+// depth ahead, so no global-load latency reaches the fold warps.  int5 keeps
+// three slots (its stages carry the fifth-bit tiles).
+constexpr int kSzfRingMax = 4;
+template <int kBits>
+constexpr int kSzfRingOf = kBits == 5 ? 3 : 4;
 struct __align__(16) SzfSlot {
     float2 sc[BN / 2];        // (2^9 sc'[n], 2^9 sc'[n+1]) for even n (sc' = sc, or 1 where sc = 0)
     float row[BM];            // asg of tile row i (0 past M)
@@ -112,17 +120,20 @@ struct Ctrl {
     uint64_t full_tma[kStages];
     uint64_t full_b[kStages];
     uint64_t empty[kStages];
-    uint64_t szf_full[kSzfRing];
-    uint64_t szf_empty[kSzfRing];
-    uint64_t rows_full[kSzfRing];   // the row warps' copies of a slab's asg and rs have landed
+    uint64_t szf_full[kSzfRingMax];
+    uint64_t szf_empty[kSzfRingMax];
+    uint64_t rows_full[kSzfRingMax];   // the row warps' copies of a slab's asg and rs have landed
     uint64_t tmem_full[2][2];     // [m-half][accumulator buffer]
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemBytes = kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot) + sizeof(Ctrl) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+template <int kBits>
+constexpr size_t smem_bytes() {
+    return kStages * sizeof(StageT<kBits>) + kSzfRingOf<kBits> * sizeof(SzfSlot) + sizeof(Ctrl) + 1024;
+}
+static_assert(smem_bytes<4>() <= 232448 && smem_bytes<5>() <= 232448, "shared memory per CTA");
 
 struct TcParams {
     const float *asg;         // asg [P][G][M]; per-token: As [P][M]
@@ -185,10 +196,14 @@ __device__ __forceinline__ void tile_coords(int i, int ntn, int pb1, int pb2, in
 // tile fastest, so the CTAs running at once share activation rows and the
 // weight tiles stay L2-resident).  All pipelines run continuously across tile
 // boundaries; slab counter it = (tile index) * G + kb.
-template <bool kTok>
+template <bool kTok, int kBits>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-          const __grid_constant__ CUtensorMap tmS, const TcParams prm) {
+          const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmH,
+          const TcParams prm) {
+    using Stage = StageT<kBits>;
+    constexpr int kSzfRing = kSzfRingOf<kBits>;
+    constexpr uint32_t kTx = kTxBytes + (kBits == 5 ? kBhBytes : 0u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Stage *stg = reinterpret_cast<Stage *>(base);
@@ -250,6 +265,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             prefetch_map(&tmA);
             prefetch_map(&tmB);
             prefetch_map(&tmS);
+            if constexpr (kBits == 5) prefetch_map(&tmH);
             int n0, m0, p;
             // first stages: weights and SZ (load-time tables) before the
             // preceding kernel has finished, activations after pdl_wait
@@ -257,9 +273,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             for (int it = 0; it < pre; ++it) {
                 tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
                 const int kb = it % G;
-                mbar_arrive_expect_tx(&ctl->full_tma[it], kTxBytes);
+                mbar_arrive_expect_tx(&ctl->full_tma[it], kTx);
                 tma_load_2d(stg[it].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[it]);
                 tma_load_2d(stg[it].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[it]);
+                if constexpr (kBits == 5) tma_load_2d(stg[it].bh, &tmH, kb * (BK / 8), n0, &ctl->full_tma[it]);
             }
             pdl_wait();
             for (int it = 0; it < pre; ++it) {
@@ -275,10 +292,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
                 const int kb = it % G;
-                mbar_arrive_expect_tx(&ctl->full_tma[s], kTxBytes);
+                mbar_arrive_expect_tx(&ctl->full_tma[s], kTx);
                 tma_load_3d(stg[s].a, &tmA, kb * BK, m0, p, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[s]);
+                if constexpr (kBits == 5) tma_load_2d(stg[s].bh, &tmH, kb * (BK / 8), n0, &ctl->full_tma[s]);
                 issued = it + 1;
             }
             if (*abort_flag) {   // let issued copies land before shared memory is released
@@ -397,9 +415,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // all eight packed loads first (the stores below could alias them
             // as far as the compiler knows), then expand and store
             uint2 pk[8];
+            uint32_t hb[8];           // int5: the fifth bits of the same 16 k (bit i = k 16 chunk + i)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
                 pk[i] = *reinterpret_cast<const uint2 *>(st.bp + ((et >> 3) + 16 * i) * (BK / 2) + chunk * 8);
+                if constexpr (kBits == 5)
+                    hb[i] = *reinterpret_cast<const uint16_t *>(st.bh + ((et >> 3) + 16 * i) * (BK / 8) + chunk * 2);
+            }
             // A column with sc = 0 dequantizes to -zs whatever its codes, so its
             // codes must not reach the MMA: the fold then scales it by 1 and
             // the zero-point MMA alone gives -zs * rs.  Lane l checks row
@@ -409,7 +431,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = (et >> 3) + 16 * i;
-                uint4 e = expand16(pk[i]);
+                uint4 e;
+                if constexpr (kBits == 5)
+                    e = expand16_int5(pk[i], hb[i]);
+                else
+                    e = expand16(pk[i]);
                 if (any_zero_sc && (st.sz[row] & 0x7FFFu) == 0u) e = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
             }
@@ -417,11 +443,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // bf16 parts of zq = 2^-9 (zscale + 8 sc) / sc', sc' = sc, or 1 where
             // sc = 0 (2^-9: the unit of the MMA's sum, see expand16); one
             // column per thread.  zq only corrects, so a division to 2 ulp
-            // (about 2^-23) is accurate enough.
+            // (about 2^-23) is accurate enough.  int5 feeds c - 16 itself
+            // (expand16_int5), so its zq is 2^-9 zscale / sc'.
             const float sc = f16lo(wcol);
             const float sce = sc != 0.0f ? sc : 1.0f;
             {
-                const float zq = __fdividef(f16hi(wcol) + 8.0f * sc, sce) * (1.0f / kNibbleScale);
+                const float zoff = kBits == 5 ? f16hi(wcol) : f16hi(wcol) + 8.0f * sc;
+                const float zq = __fdividef(zoff, sce) * (1.0f / kNibbleScale);
                 uint32_t h, m, l;
                 bf16_split3(zq, h, m, l);
                 *reinterpret_cast<uint4 *>(st.zb + (et >> 3) * kZSbo + (et & 7) * 16) =
@@ -560,8 +588,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
 pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
                          int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
-                         unsigned int *dev_status, void *stream, int sm_count, bool per_token) {
+                         unsigned int *dev_status, void *stream, int sm_count, bool per_token,
+                         const void *whi) {
     (void)sm_count;
+    const bool int5 = whi != nullptr;
     auto enc = encode_fn();
     if (!enc) return fail(PQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     CUtensorMap tmA, tmB, tmS;
@@ -599,6 +629,19 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(PQ_ERR_CUDA, "tensor map for sz: CUresult %d", (int)r);
     }
+    CUtensorMap tmH = tmB;        // int4: never read
+    if (int5) {
+        // fifth-bit planes [N][K/8] bytes: box = one slab (16 B) of 128 rows
+        const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(K / 8)};
+        const cuuint32_t box[2] = {BK / 8, BN};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUresult r = enc(&tmH, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(whi), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PQ_ERR_CUDA, "tensor map for whi: CUresult %d", (int)r);
+    }
     TcParams prm{};
     prm.asg = asg;
     prm.rs = rs;
@@ -615,10 +658,12 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     if (ntiles > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_gemm_tc: M = %d too large", M);
     const int ctas = (int)(ntiles < sm_count ? ntiles : (sm_count > 0 ? sm_count : 1));
     const dim3 grid(ctas);
-    auto kern = per_token ? tc_kernel<true> : tc_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kern = int5 ? (per_token ? tc_kernel<true, 5> : tc_kernel<false, 5>)
+                     : (per_token ? tc_kernel<true, 4> : tc_kernel<false, 4>);
+    const size_t smem = int5 ? smem_bytes<5>() : smem_bytes<4>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    e = launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, static_cast<cudaStream_t>(stream), tmA, tmB, tmS,
+    e = launch_pdl(kern, grid, dim3(kThreads), smem, static_cast<cudaStream_t>(stream), tmA, tmB, tmS, tmH,
                    prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "tc launch: %s", cudaGetErrorString(e));

@@ -49,7 +49,10 @@ using namespace tc;
 constexpr int NN = 128;           // output features per CTA (the MMA's M)
 constexpr int MT = 16;            // token columns (the MMA's N)
 constexpr int BK = 128;           // one scale group per slab
-constexpr int kStages = 8;
+// stages: 8 for int4; int5 stages also carry the fifth-bit tiles, so 4 fit
+constexpr int kStagesMax = 8;
+template <int kBits>
+constexpr int kStagesOf = kBits == 5 ? 4 : 8;
 constexpr int kSzfRing = 4;       // column scales, written by the expand warps (slot = group)
 constexpr int kRowRing = 16;      // per-token scales, copied by the row warp (latency of global loads)
 // A single thread issues an MMA only every ~100 cycles, so four MMA warps
@@ -71,7 +74,9 @@ constexpr int kThreads = (kFoldWarp0 + kFoldWarps * kFoldSets) * 32;
 // never wait for a barrier's next use before it has seen the previous one.  Each
 // stage and each scale slot is therefore always served by the same expand group
 // and the same MMA warp, which take their slabs in order.
-static_assert(kStages % kExpGroups == 0 && kStages % kMmaWarps == 0 && kStages % kTmaWarps == 0,
+static_assert(kStagesOf<4> % kExpGroups == 0 && kStagesOf<4> % kMmaWarps == 0 &&
+                  kStagesOf<4> % kTmaWarps == 0 && kStagesOf<5> % kExpGroups == 0 &&
+                  kStagesOf<5> % kMmaWarps == 0 && kStagesOf<5> % kTmaWarps == 0,
               "stage ownership");
 // TMEM accumulators: slab it uses buffer it % kTmemBufs, issued by MMA warp
 // it % kMmaWarps and folded by set it % kFoldSets (each buffer keeps its owners)
@@ -85,11 +90,15 @@ constexpr uint32_t kTxBytes = kBpBytes + kAaBytes + kSzBytes;
 constexpr uint32_t kTmemCols = 128;           // 8 accumulators x 16 columns
 constexpr uint32_t kIdescN = idesc_f8(NN, MT);
 
-struct __align__(1024) Stage {
+constexpr uint32_t kBhBytes = NN * BK / 8;    // int5: fifth bits, 128 rows x 16 B
+
+template <int kBits>
+struct __align__(1024) StageT {
     uint8_t bx[kBxBytes];     // SWIZZLE_128B, written by the expand warps
     uint8_t aa[kAaBytes];     // SWIZZLE_128B, written by the TMA
     uint8_t bp[kBpBytes];
     uint32_t sz[NN];
+    uint8_t bh[kBits == 5 ? kBhBytes : 16];   // int5: fifth-bit planes (TMA)
 };
 
 struct __align__(16) SzfSlot {
@@ -100,9 +109,9 @@ struct __align__(16) RowSlot {
 };
 
 struct Ctrl {
-    uint64_t full_tma[kStages];
-    uint64_t full_b[kStages];
-    uint64_t empty[kStages];
+    uint64_t full_tma[kStagesMax];
+    uint64_t full_b[kStagesMax];
+    uint64_t empty[kStagesMax];
     uint64_t szf_full[kSzfRing];
     uint64_t szf_empty[kSzfRing];
     uint64_t row_full[kRowRing];
@@ -113,9 +122,12 @@ struct Ctrl {
     int abort;
 };
 
-constexpr size_t kSmemBytes =
-    kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot) + kRowRing * sizeof(RowSlot) + sizeof(Ctrl) + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+template <int kBits>
+constexpr size_t smem_bytes() {
+    return kStagesOf<kBits> * sizeof(StageT<kBits>) + kSzfRing * sizeof(SzfSlot) + kRowRing * sizeof(RowSlot) +
+           sizeof(Ctrl) + 1024;
+}
+static_assert(smem_bytes<4>() <= 227 * 1024 && smem_bytes<5>() <= 227 * 1024, "shared memory budget");
 static_assert(kSzfRing % kExpGroups == 0 && kSzfRing % kFoldSets == 0 && kRowRing % kFoldSets == 0,
               "scale slot ownership");
 
@@ -132,9 +144,14 @@ __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsig
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+template <int kBits>
 __global__ void __launch_bounds__(kThreads, 1)
 tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-           const __grid_constant__ CUtensorMap tmS, const TcnParams prm) {
+           const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmH,
+           const TcnParams prm) {
+    using Stage = StageT<kBits>;
+    constexpr int kStages = kStagesOf<kBits>;
+    constexpr uint32_t kTx = kTxBytes + (kBits == 5 ? kBhBytes : 0u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Stage *stg = reinterpret_cast<Stage *>(base);
@@ -189,14 +206,16 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             prefetch_map(&tmA);
             prefetch_map(&tmB);
             prefetch_map(&tmS);
+            if constexpr (kBits == 5) prefetch_map(&tmH);
             // first stages: weights and SZ (load-time tables) before the
             // preceding kernel has finished, activations after pdl_wait
             const int pre = G < kStages ? G : kStages;
             int last = -1;             // the last slab this producer issued
             for (int it = tw; it < pre; it += kTmaWarps) {
-                mbar_arrive_expect_tx(&ctl->full_tma[it], kTxBytes);
+                mbar_arrive_expect_tx(&ctl->full_tma[it], kTx);
                 tma_load_2d(stg[it].bp, &tmB, it * (BK / 2), n0, &ctl->full_tma[it]);
                 tma_load_2d(stg[it].sz, &tmS, 8 * it, n0 / 8, &ctl->full_tma[it]);
+                if constexpr (kBits == 5) tma_load_2d(stg[it].bh, &tmH, it * (BK / 8), n0, &ctl->full_tma[it]);
             }
             pdl_wait();
             for (int it = tw; it < pre; it += kTmaWarps) {
@@ -209,9 +228,10 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
-                mbar_arrive_expect_tx(&ctl->full_tma[s], kTxBytes);
+                mbar_arrive_expect_tx(&ctl->full_tma[s], kTx);
                 tma_load_2d(stg[s].bp, &tmB, it * (BK / 2), n0, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].sz, &tmS, 8 * it, n0 / 8, &ctl->full_tma[s]);
+                if constexpr (kBits == 5) tma_load_2d(stg[s].bh, &tmH, it * (BK / 8), n0, &ctl->full_tma[s]);
                 tma_load_3d(stg[s].aa, &tmA, it * BK, 0, p, &ctl->full_tma[s]);
                 last = it;
             }
@@ -304,13 +324,22 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             // all eight packed loads first (the stores below could alias them
             // as far as the compiler knows), then expand and store
             uint2 pk[8];
+            uint32_t hb[8];           // int5: the fifth bits of the same 16 k
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
                 pk[i] = *reinterpret_cast<const uint2 *>(st.bp + ((et >> 3) + 16 * i) * (BK / 2) + chunk * 8);
+                if constexpr (kBits == 5)
+                    hb[i] = *reinterpret_cast<const uint16_t *>(st.bh + ((et >> 3) + 16 * i) * (BK / 8) + chunk * 2);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = (et >> 3) + 16 * i;
-                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = expand16(pk[i]);
+                uint4 e;
+                if constexpr (kBits == 5)
+                    e = expand16_int5(pk[i], hb[i]);
+                else
+                    e = expand16(pk[i]);
+                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -324,9 +353,11 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             if (et < NN / 2) {
                 const float sc0 = f16lo(w0), sc1 = f16lo(w1);
                 // word j of the slab's SZ box is octet j / 8, column j % 8: column n = j
-                // the MMA sums a * c * 2^-9 (expand16), so sc carries 2^9
-                szf[r].col[2 * et] = make_float2(kNibbleScale * sc0, -(f16hi(w0) + 8.0f * sc0));
-                szf[r].col[2 * et + 1] = make_float2(kNibbleScale * sc1, -(f16hi(w1) + 8.0f * sc1));
+                // the MMA sums a * c * 2^-9 (expand16), so sc carries 2^9; int5
+                // feeds c - 16 itself (expand16_int5), so its correction is zscale
+                const float o8 = kBits == 5 ? 0.0f : 8.0f;
+                szf[r].col[2 * et] = make_float2(kNibbleScale * sc0, -(f16hi(w0) + o8 * sc0));
+                szf[r].col[2 * et + 1] = make_float2(kNibbleScale * sc1, -(f16hi(w1) + o8 * sc1));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->szf_full[r]);
@@ -413,8 +444,9 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
 pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K,
                           int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
-                          unsigned int *dev_status, void *stream) {
+                          unsigned int *dev_status, void *stream, const void *whi) {
     if (M > MT) return fail(PQ_ERR_SHAPE, "pq_gemm_tcn: M = %d > %d", M, MT);
+    const bool int5 = whi != nullptr;
     auto enc = encode_fn();
     if (!enc) return fail(PQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     CUtensorMap tmA, tmB, tmS;
@@ -453,6 +485,19 @@ pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int 
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(PQ_ERR_CUDA, "tensor map for sz: CUresult %d", (int)r);
     }
+    CUtensorMap tmH = tmB;        // int4: never read
+    if (int5) {
+        // fifth-bit planes [N][K/8] bytes: box = one slab (16 B) of 128 rows
+        const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(K / 8)};
+        const cuuint32_t box[2] = {BK / 8, NN};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUresult r = enc(&tmH, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(whi), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PQ_ERR_CUDA, "tensor map for whi: CUresult %d", (int)r);
+    }
     TcnParams prm{};
     prm.asg = asg;
     prm.rs = rs;
@@ -464,11 +509,12 @@ pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int 
     prm.pb1 = pb1;
     prm.pb2 = pb2;
     prm.ldy = ldy;
-    cudaError_t e = cudaFuncSetAttribute(tcn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kern = int5 ? tcn_kernel<5> : tcn_kernel<4>;
+    const size_t smem = int5 ? smem_bytes<5>() : smem_bytes<4>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    e = launch_pdl(tcn_kernel, dim3(N / NN), dim3(kThreads), kSmemBytes, static_cast<cudaStream_t>(stream),
-                   tmA, tmB, tmS, prm);
+    e = launch_pdl(kern, dim3(N / NN), dim3(kThreads), smem, static_cast<cudaStream_t>(stream), tmA, tmB, tmS,
+                   tmH, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "tcn launch: %s", cudaGetErrorString(e));
     return PQ_OK;

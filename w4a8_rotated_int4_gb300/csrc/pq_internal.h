@@ -44,11 +44,11 @@ pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, i
 pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
                          int P, int pb1, int pb2, const void *w, const void *sz, void *y,
                          int ldy, unsigned int *dev_status, void *stream, int sm_count,
-                         bool per_token = false);
+                         bool per_token = false, const void *whi = nullptr);
 
 pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K,
                           int P, int pb1, int pb2, const void *w, const void *sz, void *y,
-                          int ldy, unsigned int *dev_status, void *stream);
+                          int ldy, unsigned int *dev_status, void *stream, const void *whi = nullptr);
 
 constexpr int kSkinnyMaxM = 16;   // largest M the CUDA-core decode kernel accepts
 constexpr int kTcnMaxM = 16;      // largest M the narrow tensor-core kernel accepts

@@ -201,6 +201,40 @@ __device__ __forceinline__ uint4 expand16(uint2 pk) {
     return o;
 }
 
+// 0xFF in byte j where bit 2j of b is set (j = 0..3), else 0x00.  The
+// multiply places bit 2j at bit 8j + 7 (shifts 7, 13, 19, 25); the other
+// partial products land on bits 9, 11, 13 (twice), 17, 19 (twice), 21, 25
+// (twice), 27 and 29, whose carries stop at the even bits 14, 20 and 26 that no
+// product reaches, so bits 7, 15, 23 and 31 hold exactly b0, b2, b4, b6.
+// The byte permute then replicates each byte's top bit over the byte.
+__device__ __forceinline__ uint32_t even_bit_mask(uint32_t b) {
+    return prmt((b & 0x55u) * 0x02082080u, 0u, 0xBA98u);
+}
+
+// int5 weights: sixteen packed low nibbles plus their sixteen fifth bits
+// (bit i of hb = the fifth bit of k = i) -> sixteen e4m3 bytes of value
+// (c - 16) * 2^-9, c = nibble + 16 * bit, in k order.  Fifth bit 1: c - 16 is
+// the nibble itself, the byte of expand16.  Fifth bit 0: c - 16 = -(16 -
+// nibble) with 16 - nibble in 1..16, and that magnitude alone in a byte is
+// again its own e4m3 value times 2^-9 (16 -> 0x10 = 2^-5), so the byte is
+// 0x80 | (16 - nibble) = 0x90 - nibble (no borrow leaves a byte).  The
+// selection runs on the even-k and odd-k nibble words before the interleave.
+__device__ __forceinline__ uint4 expand16_int5(uint2 pk, uint32_t hb) {
+    uint32_t nib[4] = {pk.x & 0x0F0F0F0Fu, (pk.x >> 4) & 0x0F0F0F0Fu, pk.y & 0x0F0F0F0Fu,
+                       (pk.y >> 4) & 0x0F0F0F0Fu};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {     // q: k = 8 (q / 2) + (q % 2) + 2j in byte j
+        const uint32_t m = even_bit_mask(hb >> (8 * (q >> 1) + (q & 1)));
+        nib[q] = (nib[q] & m) | ((0x90909090u - nib[q]) & ~m);
+    }
+    uint4 o;
+    o.x = prmt(nib[0], nib[1], 0x5140u);
+    o.y = prmt(nib[0], nib[1], 0x7362u);
+    o.z = prmt(nib[2], nib[3], 0x5140u);
+    o.w = prmt(nib[2], nib[3], 0x7362u);
+    return o;
+}
+
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFF))); }
 __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
