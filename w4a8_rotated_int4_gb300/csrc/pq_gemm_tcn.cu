@@ -49,10 +49,7 @@ using namespace tc;
 constexpr int NN = 128;           // output features per CTA (the MMA's M)
 constexpr int MT = 16;            // token columns (the MMA's N)
 constexpr int BK = 128;           // one scale group per slab
-// stages: 8 for int4; int5 stages also carry the fifth-bit tiles, so 4 fit
-constexpr int kStagesMax = 8;
-template <int kBits>
-constexpr int kStagesOf = kBits == 5 ? 4 : 8;
+constexpr int kStages = 8;
 constexpr int kSzfRing = 4;       // column scales, written by the expand warps (slot = group)
 constexpr int kRowRing = 16;      // per-token scales, copied by the row warp (latency of global loads)
 // A single thread issues an MMA only every ~100 cycles, so four MMA warps
@@ -74,9 +71,7 @@ constexpr int kThreads = (kFoldWarp0 + kFoldWarps * kFoldSets) * 32;
 // never wait for a barrier's next use before it has seen the previous one.  Each
 // stage and each scale slot is therefore always served by the same expand group
 // and the same MMA warp, which take their slabs in order.
-static_assert(kStagesOf<4> % kExpGroups == 0 && kStagesOf<4> % kMmaWarps == 0 &&
-                  kStagesOf<4> % kTmaWarps == 0 && kStagesOf<5> % kExpGroups == 0 &&
-                  kStagesOf<5> % kMmaWarps == 0 && kStagesOf<5> % kTmaWarps == 0,
+static_assert(kStages % kExpGroups == 0 && kStages % kMmaWarps == 0 && kStages % kTmaWarps == 0,
               "stage ownership");
 // TMEM accumulators: slab it uses buffer it % kTmemBufs, issued by MMA warp
 // it % kMmaWarps and folded by set it % kFoldSets (each buffer keeps its owners)
@@ -98,7 +93,19 @@ struct __align__(1024) StageT {
     uint8_t aa[kAaBytes];     // SWIZZLE_128B, written by the TMA
     uint8_t bp[kBpBytes];
     uint32_t sz[NN];
-    uint8_t bh[kBits == 5 ? kBhBytes : 16];   // int5: fifth-bit planes (TMA)
+};
+// int5 stages add the fifth-bit tile; to keep eight stages the packed nibbles
+// share their bytes with the expanded tile (the expansion group reads all of
+// them, meets on bp_read, then writes the tile over them).
+template <>
+struct __align__(1024) StageT<5> {
+    union {
+        uint8_t bx[kBxBytes];
+        uint8_t bp[kBpBytes];
+    };
+    uint8_t aa[kAaBytes];
+    uint32_t sz[NN];
+    uint8_t bh[kBhBytes];     // fifth bits, 128 rows x 16 B (TMA)
 };
 
 struct __align__(16) SzfSlot {
@@ -109,9 +116,10 @@ struct __align__(16) RowSlot {
 };
 
 struct Ctrl {
-    uint64_t full_tma[kStagesMax];
-    uint64_t full_b[kStagesMax];
-    uint64_t empty[kStagesMax];
+    uint64_t full_tma[kStages];
+    uint64_t full_b[kStages];
+    uint64_t empty[kStages];
+    uint64_t bp_read[kStages];   // int5: the group's packed loads are done
     uint64_t szf_full[kSzfRing];
     uint64_t szf_empty[kSzfRing];
     uint64_t row_full[kRowRing];
@@ -124,7 +132,7 @@ struct Ctrl {
 
 template <int kBits>
 constexpr size_t smem_bytes() {
-    return kStagesOf<kBits> * sizeof(StageT<kBits>) + kSzfRing * sizeof(SzfSlot) + kRowRing * sizeof(RowSlot) +
+    return kStages * sizeof(StageT<kBits>) + kSzfRing * sizeof(SzfSlot) + kRowRing * sizeof(RowSlot) +
            sizeof(Ctrl) + 1024;
 }
 static_assert(smem_bytes<4>() <= 227 * 1024 && smem_bytes<5>() <= 227 * 1024, "shared memory budget");
@@ -150,7 +158,6 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
            const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmH,
            const TcnParams prm) {
     using Stage = StageT<kBits>;
-    constexpr int kStages = kStagesOf<kBits>;
     constexpr uint32_t kTx = kTxBytes + (kBits == 5 ? kBhBytes : 0u);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -170,6 +177,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             mbar_init(&ctl->full_tma[s], 1);
             mbar_init(&ctl->full_b[s], kExpWarps);
             mbar_init(&ctl->empty[s], 1);            // the MMA commit
+            mbar_init(&ctl->bp_read[s], kExpWarps);
         }
         for (int r = 0; r < kSzfRing; ++r) {
             mbar_init(&ctl->szf_full[r], kExpWarps);
@@ -330,6 +338,18 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 pk[i] = *reinterpret_cast<const uint2 *>(st.bp + ((et >> 3) + 16 * i) * (BK / 2) + chunk * 8);
                 if constexpr (kBits == 5)
                     hb[i] = *reinterpret_cast<const uint16_t *>(st.bh + ((et >> 3) + 16 * i) * (BK / 8) + chunk * 2);
+            }
+            if constexpr (kBits == 5) {
+                // bp and bx share bytes: every warp of the group has its packed
+                // words in registers before any warp overwrites them.  A stage's
+                // next use needs the MMA of this one, which needs all four
+                // warps past this wait, so the parity never aliases.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->bp_read[s]);
+                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->bp_read[s], use & 1, abort_flag))) {
+                    if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
+                    break;
+                }
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
