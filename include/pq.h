@@ -312,7 +312,7 @@ pq_status pq_gemm_tcn(const void *a, const float *asg, const float *rs, int M, i
  *   As    = max_g asg_g
  *   a[k]  = e4m3(fl(xr[k] / As))              (all 0 when As == 0; [CVT])
  *   rs_g  = sum_{k in g} dec(a[k])            (exact, then rounded to fp32)
- * Two launches: pass A writes xr and the group scales (into rs); pass C reads
+Two launches: pass A writes xr and the group scales (into rs); pass C reads
  * them back and writes a, As and the row-sums over them.  Every step is a
  * separately rounded IEEE operation, so the outputs are bit-identical to a CPU
  * evaluation in that order.

@@ -143,6 +143,30 @@ def test_prologue_bit_exact(pq, orc, name, over):
         assert sub.mean() > 0.5
 
 
+def test_prologue_tiny_and_huge_scales(pq, orc):
+    """Groups whose scale falls below 2^-60 (the kernels then divide with the
+    IEEE divide) or sits near it, and huge values, in both quantisers (the
+    many-token prologue and the per-token pass C): bit-exact either way."""
+    M, K = 40, 512
+    prob = pqgen.make_problem(M, K, 128, seed=77)
+    xf = (prob.x.astype(np.uint32) << 16).view(np.float32).copy()
+    for r, f in zip(range(0, M, 4), (1e-16, 3e-17, 1e-18, 1e-22, 1e-30, 1e-36, 1e30, 4e35, 1e-17, 2e-17)):
+        xf[r] *= np.float32(f)
+    x = pqgen.to_bf16_bits(xf)
+    rec = orc.records(prob.pairs, prob.theta)
+    xd, rd, cd = dev_u16(x).view(torch.bfloat16), torch.from_numpy(rec).cuda(), dev_u16(prob.cs)
+    a, asg, rs = pq.pq_rotate_quant(xd, rd, cd)
+    _, a2, As, rs2 = pq.pq_rotate_tokquant(xd, rd, cd)
+    torch.cuda.synchronize()
+    a_o, asg_o, rs_o = orc.rotate_quant(x, prob.cs, rec)
+    _, a2_o, As_o, rs2_o = orc.rotate_tokquant(x, prob.cs, rec)
+    assert (asg_o[asg_o > 0] < 2.0 ** -60).any() and (asg_o >= 2.0 ** -60).any()
+    assert np.array_equal(a.cpu().numpy(), a_o) and np.array_equal(rs.cpu().numpy(), rs_o)
+    assert np.array_equal(asg.cpu().numpy(), asg_o)
+    assert np.array_equal(a2.cpu().numpy(), a2_o) and np.array_equal(rs2.cpu().numpy(), rs2_o)
+    assert np.array_equal(As.cpu().numpy(), As_o)
+
+
 def test_prologue_strided_x(pq, orc):
     """ldx > K: only the first K columns of each row are read."""
     prob = pqgen.make_problem(37, 384, 128, seed=21)
@@ -545,6 +569,22 @@ def test_rotate_tokquant_bit_exact(pq, orc, M, K, P, pb, zero_rows, knobs):
     if knobs.get("x_mode") == "sparse":
         sub = ((a_o & 0x78) == 0) & ((a_o & 7) != 0)
         assert sub.mean() > 0.3
+
+
+def test_rotate_tokquant_long_rows(pq, orc):
+    """928 groups per row (K = 118784): the token scale spans more groups than
+    a CTA of pass C has threads."""
+    M, K = 3, 118784
+    prob = pqgen.make_problem(M, K, 128, seed=K + M)
+    rec = orc.records(prob.pairs, prob.theta)
+    xr, a, As, rs = pq.pq_rotate_tokquant(dev_u16(prob.x).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+                                          dev_u16(prob.cs))
+    torch.cuda.synchronize()
+    xr_o, a_o, As_o, rs_o = orc.rotate_tokquant(prob.x, prob.cs, rec)
+    assert np.array_equal(xr.view(torch.int16).cpu().numpy().view(np.uint16), xr_o)
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    assert np.array_equal(As.cpu().numpy().view(np.uint32), As_o.view(np.uint32))
+    assert np.array_equal(rs.cpu().numpy().view(np.uint32), rs_o.view(np.uint32))
 
 
 PTOK_GEMM = [  # M, K, N, P, pb

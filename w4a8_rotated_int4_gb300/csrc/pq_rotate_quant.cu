@@ -98,6 +98,31 @@ __device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {
     return c;
 }
 
+// Correctly rounded a / b from y = RN(1/b) with multiply-adds only, after
+// Markstein's theorem (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990): if q
+// is within one ulp of a / b and y within half an ulp of 1 / b, then
+// RN(q + (a - b q) y), with the residual exact in one fused multiply-add, is
+// RN(a / b).  q0 = RN(a y) can be off by up to 1.5 ulp, so a first correction
+// makes it faithful and a second one exact.  This holds while no step
+// underflows or overflows: the callers keep b within [2^-60, 2^60]
+// (quot_ok) and |a / b| <= 448; where |a / b| is below ~2^-100 the last bit
+// may differ, and the e4m3 encoder maps every such value to 0 either way.
+// Checked against IEEE division on 5 * 10^8 pairs including halfway cases.
+// Used where one scale serves a whole CTA (the per-token pass C); in the
+// per-group quantisers, where each lane has its own scale, the IEEE divide
+// measured faster.
+__device__ __forceinline__ bool quot_ok(float b) { return b >= 0x1p-60f && b <= 0x1p60f; }
+__device__ __forceinline__ float quot_rn(float a, float b, float y) {
+    const float q0 = __fmul_rn(a, y);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, b, a), y, q0);
+    return __fmaf_rn(__fmaf_rn(-q1, b, a), y, q1);
+}
+// a / b rounded to nearest: quot_rn where it is exact, else the IEEE divide
+__device__ __forceinline__ float div_scale(float a, float b, float y, bool ok) {
+    return ok ? quot_rn(a, b, y) : __fdiv_rn(a, b);
+}
+
 // dec(code) * 2^9 as an integer (exact; |value| <= 448 * 512)
 __device__ __forceinline__ int e4m3_times512(uint32_t c) {
     const int e = (c >> 3) & 15, m = c & 7;
@@ -626,56 +651,62 @@ __global__ void e4m3_encode_kernel(const float *__restrict__ in, uint8_t *__rest
 }
 
 // ---------------------------------------------------------------------------
-// Pass C of the per-token path ("Prefill ladder" notes: per-token prefill,
-// pass C): for every row, As = max over the groups of pass A's group scales,
+// Pass C of the per-token path ("Numbers", the per-token prefill item, pass
+// C): for every row, As = max over the groups of pass A's group scales,
 // a = e4m3(fl(xr / As)) (all 0 when As = 0), and per group the exact sum of
 // what the codes decode to (plain row-sums: the token scale is applied in the
-// GEMM's epilogue).  One warp per token row; lane l takes the 8 channels
-// 8 (l & 15) .. +7 of group g0 + (l >> 4), two groups per step.  gsc and rs
-// may be the same buffer: a warp reads all of its row's group scales before
-// it writes that row's row-sums, and no other warp touches the row.
+// GEMM's epilogue).  One CTA of 128 threads per (row, partition): thread t
+// takes the 8 channels of chunk c8 = c0 + t, so the 16 lanes of a half-warp
+// hold one group.  gsc and rs may be the same buffer: the CTA reads all of its
+// row's group scales before the barrier and writes the row-sums after it, and
+// no other CTA touches the row.
 // ---------------------------------------------------------------------------
-constexpr int kTqWarps = 8;
+constexpr int kTqThreads = 128;
 
-__device__ __forceinline__ uint32_t e4m3x4_scaled(uint2 w, float as) {
-    return e4m3x2(__fdiv_rn(bf16hi(w.x), as), __fdiv_rn(bf16lo(w.x), as)) |
-           (e4m3x2(__fdiv_rn(bf16hi(w.y), as), __fdiv_rn(bf16lo(w.y), as)) << 16);
+__device__ __forceinline__ uint32_t e4m3x4_scaled(uint2 w, float as, float rcp, bool ok) {
+    return e4m3x2(div_scale(bf16hi(w.x), as, rcp, ok), div_scale(bf16lo(w.x), as, rcp, ok)) |
+           (e4m3x2(div_scale(bf16hi(w.y), as, rcp, ok), div_scale(bf16lo(w.y), as, rcp, ok)) << 16);
 }
 
-__global__ void __launch_bounds__(32 * kTqWarps)
+__global__ void __launch_bounds__(kTqThreads)
 token_quant_kernel(const uint16_t *__restrict__ xr, int M, int K, const float *gsc, uint8_t *__restrict__ a,
                    float *__restrict__ As, float *rs) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int m = blockIdx.x * kTqWarps + warp, p = blockIdx.y, G = K >> 7;
+    __shared__ float wmax[kTqThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int m = blockIdx.x, p = blockIdx.y, G = K >> 7;
     pdl_wait();        // xr and the group scales are the preceding pass's output
     pdl_trigger();
-    if (m >= M) return;
     float as = 0.0f;
-    for (int g = lane; g < G; g += 32) as = fmaxf(as, gsc[((size_t)p * G + g) * M + m]);
+    for (int g = t; g < G; g += kTqThreads) as = fmaxf(as, gsc[((size_t)p * G + g) * M + m]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) as = fmaxf(as, __shfl_xor_sync(0xFFFFFFFFu, as, o));
-    if (lane == 0) As[(size_t)p * M + m] = as;
+    if (lane == 0) wmax[warp] = as;
+    __syncthreads();   // every group scale of the row has been read
+    as = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    if (t == 0) As[(size_t)p * M + m] = as;
+    const bool ok = quot_ok(as);
+    const float rcp = __frcp_rn(as);
     const uint16_t *row = xr + ((size_t)p * M + m) * K;
     uint8_t *arow = a + ((size_t)p * M + m) * K;
-    for (int g0 = 0; g0 < G; g0 += 2) {
-        const int g = g0 + (lane >> 4), c = 128 * g + 8 * (lane & 15);
+    for (int c0 = 0; c0 < 16 * G; c0 += kTqThreads) {
+        const int c8 = c0 + t, g = c8 >> 4;
+        const bool valid = c8 < 16 * G;
         int sum512 = 0;
-        if (g < G) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row + c));
+        if (valid) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row) + c8);
             uint32_t lo = 0, hi = 0;
             if (as != 0.0f) {
-                lo = e4m3x4_scaled(make_uint2(v.x, v.y), as);
-                hi = e4m3x4_scaled(make_uint2(v.z, v.w), as);
+                lo = e4m3x4_scaled(make_uint2(v.x, v.y), as, rcp, ok);
+                hi = e4m3x4_scaled(make_uint2(v.z, v.w), as, rcp, ok);
             }
-            *reinterpret_cast<uint2 *>(arow + c) = make_uint2(lo, hi);
+            reinterpret_cast<uint2 *>(arow)[c8] = make_uint2(lo, hi);
 #pragma unroll
             for (int b = 0; b < 4; ++b)
                 sum512 += e4m3_times512((lo >> (8 * b)) & 0xFF) + e4m3_times512((hi >> (8 * b)) & 0xFF);
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) sum512 += __shfl_xor_sync(0xFFFFFFFFu, sum512, o);
-        if ((lane & 15) == 0 && g < G)
-            rs[((size_t)p * G + g) * M + m] = __fmul_rn(__int2float_rn(sum512), 1.0f / 512.0f);
+        if ((lane & 15) == 0 && valid) rs[((size_t)p * G + g) * M + m] = __fmul_rn(__int2float_rn(sum512), 1.0f / 512.0f);
     }
 }
 
@@ -731,7 +762,7 @@ pq_status launch_rotate_tokquant(const void *x, int M, int K, int ldx, int P, co
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_tokquant pass A launch: %s", cudaGetErrorString(e));
     // pass C: token scale, codes, row-sums
-    e = launch_pdl(token_quant_kernel, dim3((M + kTqWarps - 1) / kTqWarps, P), dim3(32 * kTqWarps), 0, st,
+    e = launch_pdl(token_quant_kernel, dim3(M, P), dim3(kTqThreads), 0, st,
                    (const uint16_t *)xrp, M, K, (const float *)rs, static_cast<uint8_t *>(a), As, rs);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "rotate_tokquant pass C launch: %s", cudaGetErrorString(e));
