@@ -414,13 +414,13 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=73469952 + 40301824, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        bytes=70999552 + 41818624, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="f428a3813b839e774e476dc474be35d494ce09ae446cf233e439db3c0f0fd33e"),
+        sha256="4c2810280826855a442f5cf46d9e9724eeee14d8f36bb3568f79cc19cc001203"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47469568 + 0, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
+        bytes=47468032 + 1024, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="0d5ace53fa4ba86815ab1be091a380b093aac698c16677376cf9599502fea61a"),
+        sha256="ab71aa5286337e7dda8c7d9ce3fbc5b94507a8a6571a7b9e4ef684983cd3428b"),
 }
 
 
