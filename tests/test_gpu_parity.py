@@ -437,6 +437,28 @@ def test_gemm_zero_scale_groups(pq, orc, M):
         assert_close(y, y64, "%s zero-scale groups M=%d" % (name, M))
 
 
+@pytest.mark.parametrize("M,K,N", [(512, 256, 10240), (300, 384, 10240)])
+def test_gemm_tc_split_last_round(pq, orc, M, K, N):
+    """160 tiles on 152 CTAs: the last 8 tiles run as 16 half items (128 rows
+    each; at M = 300 one half of each lies past M).  Every output of the
+    per-group, per-token and int5 prefill kernels against the oracle."""
+    prob = pqgen.make_problem(M, K, N, P=2, pb=(N // 2, N), seed=M + K)
+    L = Problem(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    y64 = orc.gemm_f64(a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], N // 2, N)
+    assert_close(run_gemm(pq.pq_gemm_tc, a, asg, rs, L, N // 2, N, M, N), y64, "tc split")
+    _, a_t, As, rs_t = pq.pq_rotate_tokquant(L.x_d, L.rec_d, L.cs_d)
+    _, a_to, As_o, rs_to = orc.rotate_tokquant(prob.x, prob.cs, L.t["rec"])
+    y64t = orc.gemm_ptok_f64(a_to, As_o, rs_to, L.t["codes"], L.t["sz"], N // 2, N)
+    assert_close(run_gemm(pq.pq_gemm_ptok, a_t, As, rs_t, L, N // 2, N, M, N), y64t, "ptok split")
+    p5 = pqgen.make_problem(M, K, N, P=2, pb=(N // 2, N), seed=M + K, bits=5)
+    L5 = Problem5(pq, orc, p5)
+    y64_5 = orc.gemm5_f64(a_o, asg_o, rs_o, L5.t["codes"], L5.t["sz"], N // 2, N)
+    assert_close(run_gemm5("pq_gemm5_tc", a, asg, rs, L5, N // 2, N, M, N), y64_5, "int5 split")
+
+
 def test_gemm_merged_equals_sliced(pq, orc):
     """One P=3 launch == three P=1 launches on the column slices, bit for bit."""
     M, K, N = 40, 640, 512

@@ -183,11 +183,43 @@ __device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const ui
     }
 }
 
-// Tile i of this CTA: output-feature tile fastest, its partition from pb1/pb2.
-__device__ __forceinline__ void tile_coords(int i, int ntn, int pb1, int pb2, int &n0, int &m0, int &p) {
-    const int t = (int)blockIdx.x + i * (int)gridDim.x;
-    n0 = (t % ntn) * BN;
-    m0 = (t / ntn) * BM;
+// Work items.  Tiles are numbered output-feature tile fastest; CTA c takes
+// items c, c + gridDim.x, ...  When the last round would hold at most half
+// the grid (rem = ntiles % gridDim.x <= gridDim.x / 2), its rem tiles become
+// 2 rem half items of 128 rows each, so that round takes about half as long.
+// A half item uses the M = 128 MMA half 0 and the fold warps of half 0; half
+// 1's MMAs are not issued and its fold warps only keep the barriers in step.
+// kSplit = false (the per-token kernel, where it measured slower) keeps whole
+// tiles throughout.
+template <bool kSplit>
+__device__ __forceinline__ bool split_round(int ntiles) {
+    const int C = (int)gridDim.x, rem = ntiles % C;
+    return kSplit && rem > 0 && 2 * rem <= C;
+}
+template <bool kSplit>
+__device__ __forceinline__ int item_count(int ntiles) {
+    return split_round<kSplit>(ntiles) ? ntiles + ntiles % (int)gridDim.x : ntiles;
+}
+// Whether item i of this CTA is a half item (see tile_coords).
+template <bool kSplit>
+__device__ __forceinline__ bool is_half_item(int i, int ntiles) {
+    return split_round<kSplit>(ntiles) && (int)blockIdx.x + i * (int)gridDim.x >= ntiles - ntiles % (int)gridDim.x;
+}
+// Item i of this CTA: n0, m0 (the item's first row), partition p, and
+// half_item (true for a 128-row half item).
+template <bool kSplit>
+__device__ __forceinline__ void tile_coords(int i, int ntn, int ntiles, int pb1, int pb2, int &n0, int &m0,
+                                            int &p, bool &half_item) {
+    const int C = (int)gridDim.x, t = (int)blockIdx.x + i * C;
+    const int rem = ntiles % C, nfull = ntiles - rem;
+    int tile = t, hsel = 0;
+    half_item = split_round<kSplit>(ntiles) && t >= nfull;
+    if (half_item) {
+        tile = nfull + ((t - nfull) >> 1);
+        hsel = (t - nfull) & 1;
+    }
+    n0 = (tile % ntn) * BN;
+    m0 = (tile / ntn) * BM + hsel * (BM / 2);
     p = (n0 >= pb1) + (n0 >= pb2);
 }
 
@@ -214,7 +246,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = prm.M, G = prm.K / BK;
     const int ntn = prm.N / BN, ntiles = ntn * ((M + BM - 1) / BM);
-    const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nitems = item_count<!kTok>(ntiles);
+    const int my_tiles = (int)blockIdx.x < nitems ? (nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total = my_tiles * G;
     const int pb1 = prm.pb1, pb2 = prm.pb2;
 
@@ -267,11 +300,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             prefetch_map(&tmS);
             if constexpr (kBits == 5) prefetch_map(&tmH);
             int n0, m0, p;
+            bool half_item;
             // first stages: weights and SZ (load-time tables) before the
             // preceding kernel has finished, activations after pdl_wait
             const int pre = total < kStages ? total : kStages;
             for (int it = 0; it < pre; ++it) {
-                tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+                tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
                 const int kb = it % G;
                 mbar_arrive_expect_tx(&ctl->full_tma[it], kTx);
                 tma_load_2d(stg[it].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[it]);
@@ -280,7 +314,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             pdl_wait();
             for (int it = 0; it < pre; ++it) {
-                tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+                tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
                 tma_load_3d(stg[it].a, &tmA, (it % G) * BK, m0, p, &ctl->full_tma[it]);
             }
             int issued = pre;
@@ -290,7 +324,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
-                tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+                tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
                 const int kb = it % G;
                 mbar_arrive_expect_tx(&ctl->full_tma[s], kTx);
                 tma_load_3d(stg[s].a, &tmA, kb * BK, m0, p, &ctl->full_tma[s]);
@@ -321,7 +355,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 break;
             }
             int n0, m0, p;
-            tile_coords(it / G, ntn, pb1, pb2, n0, m0, p);
+            bool half_item;
+            tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
             const size_t off = ((size_t)p * G + (size_t)(it % G)) * (size_t)M;
 #pragma unroll
             for (int u = 0; u < BM / 64; ++u) {
@@ -361,19 +396,24 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint64_t za1 = desc_noswz(smem_u32(szf[r].za + kZaBytes / 2), kZLbo, kZSbo);
             const uint64_t zbd = desc_noswz(smem_u32(stg[s].zb), kZLbo, kZSbo);
             const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
+            const bool half_item = is_half_item<!kTok>(it / G, ntiles);
             if (elect_one()) {
                 // half 0, then half 1, each committed on its own so the two
                 // fold warp groups start half a slab apart; each half's chain
-                // ends with the zero-point MMA (bf16, K = 16)
+                // ends with the zero-point MMA (bf16, K = 16).  A half item
+                // issues half 0 only; half 1's commit still signals its fold
+                // warps, which then only release the buffer.
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)   // +32 bytes along K inside the swizzle row
                     mma_f8(d0, ad0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
                 mma_bf16(d0, za0, zbd, kIdescZ, 1u);
                 mma_commit(&ctl->tmem_full[0][b]);
+                if (!half_item) {
 #pragma unroll
-                for (int kk = 0; kk < BK / 32; ++kk)
-                    mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
-                mma_bf16(d1, za1, zbd, kIdescZ, 1u);
+                    for (int kk = 0; kk < BK / 32; ++kk)
+                        mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
+                    mma_bf16(d1, za1, zbd, kIdescZ, 1u);
+                }
                 // A stage that is never refilled gets no release: nothing would wait
                 // for that arrival, and an arrival still in flight when the CTA
                 // exits would land in the shared memory of the next CTA on this SM.
@@ -490,8 +530,32 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         bool bad = false;
         for (int i = 0; i < my_tiles; ++i) {
             int n0, m0, p;
-            tile_coords(i, ntn, pb1, pb2, n0, m0, p);
+            bool half_item;
+            tile_coords<!kTok>(i, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
             const int mb = m0 + row0;     // rows mb + 8 * ri
+            if (half_item && h == 1) {
+                // a half item: nothing to fold here; keep the barriers in step
+                for (int kb = 0; kb < G && !bad; ++kb) {
+                    const int it = i * G + kb;
+                    const int b = it & 1, tuse = it >> 1;
+                    const int r = it % kSzfRing, ruse = it / kSzfRing;
+                    if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
+                                        &ctl->szf_full[r], ruse & 1, abort_flag)) {
+                        if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
+                        bad = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&ctl->tmem_empty[b]);
+                        mbar_arrive(&ctl->szf_empty[r]);
+                    }
+                }
+                if (i == my_tiles - 1) pdl_trigger();
+                continue;
+            }
             uint64_t acc[4][16];
 #pragma unroll
             for (int ri = 0; ri < 4; ++ri)
