@@ -414,9 +414,9 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=70999552 + 41818624, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        bytes=71439104 + 38536192, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="4c2810280826855a442f5cf46d9e9724eeee14d8f36bb3568f79cc19cc001203"),
+        sha256="6d41b3b6db58ae9e51c19a254fd45c979f266346094f9ab778cc65a85485a7c3"),
     ("pq_gemm_tcn", "decode:16"): dict(
         bytes=47468032 + 1024, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
