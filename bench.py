@@ -416,11 +416,11 @@ NCU_TRAFFIC = {
     ("pq_gemm_tc", "prefill"): dict(
         bytes=71439104 + 38536192, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="6d41b3b6db58ae9e51c19a254fd45c979f266346094f9ab778cc65a85485a7c3"),
+        sha256="5a1ca71fc19fa2efbf5e35208f66d2d2927c8537f6d05e31c8b4c271f433451a"),
     ("pq_gemm_tcn", "decode:16"): dict(
         bytes=47468032 + 1024, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="ab71aa5286337e7dda8c7d9ce3fbc5b94507a8a6571a7b9e4ef684983cd3428b"),
+        sha256="f7c8c427fb980ceecccb65a0d1e6f03d2080a7b39fe97ee2130805af401b39a4"),
 }
 
 

@@ -47,6 +47,12 @@
 // per token and partition, plain row-sums): the row warps copy rs only, the
 // fold is acc += (2^9 sc') * D'' (one packed operation per two elements) and
 // the epilogue multiplies each row by its As.
+// int5 weights ("2026-09-10: int5 W5A8 ParoQuant": low nibbles as for int4,
+// fifth bits in [N][K/8] planes): each stage also receives the slab's
+// 16-byte x 128-row fifth-bit box, the expansion writes the e4m3 bytes of
+// (c - 16) * 2^-9 (expand16_int5), and zq drops its 8 sc term.
+// Persistent grid: when the last round of tiles would fill at most half the
+// grid, its tiles run as 128-row half items (per-group kernels only).
 //
 // Every wait is bounded (%globaltimer); a wait that gives up marks the CTA as
 // aborted, lets in-flight copies and MMAs finish, frees TMEM, fills its tile

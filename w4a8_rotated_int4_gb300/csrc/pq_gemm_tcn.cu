@@ -4,8 +4,11 @@
 // Source: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", "Design"
 // items 1 (zero point as a row-sum correction, SZ table), 2 (per-group fp8
 // activation scales folded once per 128-k group) and 4 (partition select per
-// n-block).  Same arithmetic as the prefill kernel; the operands swap roles
-// so that a handful of tokens still fills the MMA:
+// n-block); int5 weights as in the prefill kernel ("2026-09-10: int5 W5A8
+// ParoQuant": (c - 16) fed to the MMA, the correction -zscale), with the
+// packed nibbles sharing their bytes with the expanded tile.  Same arithmetic
+// as the prefill kernel; the operands swap roles so that a handful of tokens
+// still fills the MMA:
 //
 //   D'[n][m] = sum_{k in group} c[n][k] * dec(a[m][k])     (c in 0..15, exact)
 //   y[m][n] += asg[m,g] * (sc[g,n] * D' - (zscale + 8 sc)[g,n] * rs[m,g])
