@@ -15,7 +15,7 @@
 // v[k][token] (fp32), token fastest: in a Givens layer every warp works on one
 // pair (i, j) at a time with lane = token, so the 32 lanes read v[i][0..31]
 // and v[j][0..31] -- consecutive words, free of bank conflicts whatever the
-// pair permutation is.  Each of the 4 warps takes 16 of the 64 disjoint pairs
+// pair permutation is.  Each of the 8 warps takes 8 of the 64 disjoint pairs
 // of a layer; the layers are separated by __syncthreads.  Every multiply, add,
 // subtract and divide is a separately rounded IEEE operation (explicit .rn
 // intrinsics), so results are bit-identical to an fp32 CPU evaluation in the
@@ -51,8 +51,12 @@ __device__ __forceinline__ void sts_f32x2(uint32_t addr, float2 f) {
 // every shared-memory access moves both with one 8-byte instruction); warp w
 // rotates pairs 16w..16w+15 of every layer.
 constexpr int kTok = 64;              // tokens per CTA
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
+constexpr int kPairsPerWarp = 64 / kWarps;     // pairs of a layer per warp
+constexpr int kBatch = 4;                      // pairs loaded together before any store
+constexpr int kChPerWarp = 128 / kWarps;       // channels per warp in the fill and the quantise
+static_assert(kPairsPerWarp % kBatch == 0 && kChPerWarp % 16 == 0, "work split");
 constexpr int kXsStride = 65;         // words per staged x row (64 + 1 pad)
 constexpr int kCodeStride = 144;      // bytes per staged code row
 
@@ -60,12 +64,14 @@ struct __align__(16) Smem {
     float2 v[128][kTok / 2];          // 32 KB, v[k][token pair]: (token 2l, token 2l+1)
     union {
         uint32_t xs[kTok][kXsStride]; // x tile, two bf16 per word (before the layers)
-        uint8_t codes[kTok][kCodeStride];   // e4m3 codes (after them)
+        struct {                      // after them
+            uint8_t codes[kTok][kCodeStride];   // e4m3 codes
+            float red_max[kWarps][kTok];        // per-warp amax
+            int red_sum[kWarps][kTok];          // per-warp row-sums (x 2^9)
+        };
     };
     uint2 rec[8][64];                 // records of (p, g): byte offsets of v[i] | v[j] << 16; f16 cos | sin << 16
     float cs[128];
-    float red_max[kWarps][kTok];
-    int red_sum[kWarps][kTok];
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -144,7 +150,7 @@ __device__ __forceinline__ void givens(float c, float s, float &vi, float &vj) {
 // bf16 into xr [P][M][K] and each group's scale fl(max |xr| * fl(1/448)) into
 // asg (the token-quant pass reads them back); a and rs are not touched.
 template <bool kRot>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P,
                     const uint2 *__restrict__ rec, const uint16_t *__restrict__ cs,
                     uint8_t *__restrict__ a, float *__restrict__ asg, float *__restrict__ rs,
@@ -158,9 +164,10 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
     pdl_trigger();
 
     // x tile (64 rows of 256 bytes): issued together with the records and scales
-    uint4 xv[8];
+    constexpr int kXv = kTok * 16 / kThreads;     // 16-byte pieces of the tile per thread
+    uint4 xv[kXv];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
+    for (int it = 0; it < kXv; ++it) {
         const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
         xv[it] = make_uint4(0, 0, 0, 0);
         if (m0 + row < M)
@@ -169,22 +176,23 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
 
     {
         const int p = blockIdx.z;      // one partition per CTA: partitions run side by side
-        uint4 rv[2];
+        constexpr int kRv = 256 / kThreads;           // 16-byte pieces of the 8 x 64 records
+        uint4 rv[kRv];
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
+        for (int it = 0; it < kRv; ++it) {
             const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
             rv[it] = __ldg(reinterpret_cast<const uint4 *>(rec + ((size_t)(p * 8 + r) * G + g) * 64) + q);
         }
-        const uint16_t csv = __ldg(cs + (size_t)p * K + 128 * g + tid);
+        const uint16_t csv = tid < 128 ? __ldg(cs + (size_t)p * K + 128 * g + tid) : (uint16_t)0;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
+        for (int it = 0; it < kXv; ++it) {
             const int c = tid + it * kThreads, row = c >> 4, q = c & 15;
             uint32_t *d = &sm.xs[row][4 * q];
             d[0] = xv[it].x; d[1] = xv[it].y; d[2] = xv[it].z; d[3] = xv[it].w;
         }
         // decoded records: shared-memory byte offsets of v[i][0], v[j][0]; f16 cos, sin
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
+        for (int it = 0; it < kRv; ++it) {
             const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
             const uint32_t w0[2] = {rv[it].x, rv[it].z}, w1[2] = {rv[it].y, rv[it].w};
 #pragma unroll
@@ -193,13 +201,13 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
                 sm.rec[r][2 * q + h] = make_uint2(i * (uint32_t)(kTok * 4) | (j * (uint32_t)(kTok * 4)) << 16, w1[h]);
             }
         }
-        sm.cs[tid] = half_to_float(csv);
+        if (tid < 128) sm.cs[tid] = half_to_float(csv);
         __syncthreads();
 
         // v[k][t] = x[t][k] * cs[k] (exact: bf16 x f16 fits in 24 bits)
 #pragma unroll 4
-        for (int q = 0; q < 16; ++q) {
-            const int kw = 16 * warp + q;                 // word index: channels 2kw, 2kw+1
+        for (int q = 0; q < kChPerWarp / 2; ++q) {
+            const int kw = (kChPerWarp / 2) * warp + q;   // word index: channels 2kw, 2kw+1
             const uint32_t w0 = sm.xs[2 * lane][kw], w1 = sm.xs[2 * lane + 1][kw];
             sm.v[2 * kw][lane] = make_float2(__fmul_rn(bf16lo(w0), sm.cs[2 * kw]),
                                              __fmul_rn(bf16lo(w1), sm.cs[2 * kw]));
@@ -213,13 +221,13 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
         const uint32_t vlane = smem_addr(&sm.v[0][lane]);
         for (int r = 0; r < 8; ++r) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float2 vi[8], vj[8];
-                float cc[8], ss[8];
-                uint32_t ai[8], aj[8];
+            for (int half = 0; half < kPairsPerWarp / kBatch; ++half) {
+                float2 vi[kBatch], vj[kBatch];
+                float cc[kBatch], ss[kBatch];
+                uint32_t ai[kBatch], aj[kBatch];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint2 rr = sm.rec[r][16 * warp + 8 * half + q];
+                for (int q = 0; q < kBatch; ++q) {
+                    const uint2 rr = sm.rec[r][kPairsPerWarp * warp + kBatch * half + q];
                     ai[q] = vlane + (rr.x & 0xFFFFu);
                     aj[q] = vlane + (rr.x >> 16);
                     cc[q] = half_to_float((uint16_t)(rr.y & 0xFFFFu));
@@ -228,7 +236,7 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
                     vj[q] = lds_f32x2(aj[q]);
                 }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < kBatch; ++q) {
                     givens(cc[q], ss[q], vi[q].x, vj[q].x);
                     givens(cc[q], ss[q], vi[q].y, vj[q].y);
                     sts_f32x2(ai[q], vi[q]);
@@ -238,40 +246,43 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
             __syncthreads();
         }
 
-        // quantise: warp w takes channels 32w..32w+31 of both tokens of the lane
-        float2 vals[32];
+        // quantise: warp w takes channels kChPerWarp w .. + kChPerWarp - 1 of
+        // both tokens of the lane
+        constexpr int kC = kChPerWarp;
+        float2 vals[kC];
         float amax0 = 0.0f, amax1 = 0.0f;
         if constexpr (kRot) {
             // bf16 rows straight to xr (64 contiguous bytes per token and
             // warp); amax over the rounded values
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                uint32_t pk[16];
+                uint32_t pk[kC / 2];
                 float am = 0.0f;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float2 lo = sm.v[32 * warp + 2 * q][lane], hi = sm.v[32 * warp + 2 * q + 1][lane];
+                for (int q = 0; q < kC / 2; ++q) {
+                    const float2 lo = sm.v[kC * warp + 2 * q][lane], hi = sm.v[kC * warp + 2 * q + 1][lane];
                     pk[q] = bf16_pack2(t ? lo.y : lo.x, t ? hi.y : hi.x);
                     am = fmaxf(am, fmaxf(fabsf(bf16lo(pk[q])), fabsf(bf16hi(pk[q]))));
                 }
                 const int tok = 2 * lane + t;
                 sm.red_max[warp][tok] = am;
                 if (m0 + tok < M) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(xr + ((size_t)p * M + m0 + tok) * K + 128 * g + 32 * warp);
+                    uint4 *dst = reinterpret_cast<uint4 *>(xr + ((size_t)p * M + m0 + tok) * K + 128 * g + kC * warp);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    for (int q = 0; q < kC / 8; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
             __syncthreads();
             if (tid < kTok && m0 + tid < M) {
-                const float amax = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
-                                         fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
+                float amax = sm.red_max[0][tid];
+#pragma unroll
+                for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, sm.red_max[w][tid]);
                 asg[((size_t)p * G + g) * M + m0 + tid] = __fmul_rn(amax, inv448);
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                vals[q] = sm.v[32 * warp + q][lane];
+            for (int q = 0; q < kC; ++q) {
+                vals[q] = sm.v[kC * warp + q][lane];
                 amax0 = fmaxf(amax0, fabsf(vals[q].x));
                 amax1 = fmaxf(amax1, fabsf(vals[q].y));
             }
@@ -281,13 +292,14 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int tok = 2 * lane + t;
-                const float amax = fmaxf(fmaxf(sm.red_max[0][tok], sm.red_max[1][tok]),
-                                         fmaxf(sm.red_max[2][tok], sm.red_max[3][tok]));
+                float amax = sm.red_max[0][tok];
+#pragma unroll
+                for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, sm.red_max[w][tok]);
                 const float scale = __fmul_rn(amax, inv448);
-                uint32_t packed[8];
+                uint32_t packed[kC / 4];
                 int sum512 = 0;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < kC / 4; ++q) {
                     uint32_t word = 0;
                     if (scale != 0.0f) {
                         const float e0 = t ? vals[4 * q].y : vals[4 * q].x, e1 = t ? vals[4 * q + 1].y : vals[4 * q + 1].x;
@@ -300,9 +312,10 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
 #pragma unroll
                     for (int b = 0; b < 4; ++b) sum512 += e4m3_times512((word >> (8 * b)) & 0xFF);
                 }
-                uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[tok][32 * warp]);
-                cdst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                cdst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[tok][kC * warp]);
+#pragma unroll
+                for (int q = 0; q < kC / 16; ++q)
+                    cdst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 sm.red_sum[warp][tok] = sum512;
                 if (warp == 0 && m0 + tok < M) asg[((size_t)p * G + g) * M + m0 + tok] = scale;
             }
@@ -317,7 +330,9 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
             }
             if (tid < kTok && m0 + tid < M) {
                 const size_t o = ((size_t)p * G + g) * M + m0 + tid;
-                const int s = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
+                int s = 0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) s += sm.red_sum[w][tid];
                 rs[o] = __fmul_rn(__int2float_rn(s), 1.0f / 512.0f);
             }
         }  // !kRot
