@@ -129,6 +129,28 @@ __device__ __forceinline__ float div_scale(float a, float b, float y, bool ok) {
     return ok ? quot_rn(a, b, y) : __fdiv_rn(a, b);
 }
 
+// acc + the values of the four e4m3 codes of word w.  The hardware convert
+// gives each value exactly in f16 (every e4m3 value is one), and the mixed
+// f16 -> f32 multiply-add by 1 adds it exactly while the sum stays a multiple
+// of 2^-9 below 2^14 (24 significant bits): so for up to 32 codes the result
+// is the exact sum, whatever the order.
+__device__ __forceinline__ float e4m3x4_accumulate(uint32_t w, float acc) {
+    uint32_t h01, h23;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((uint16_t)(w & 0xFFFFu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((uint16_t)(w >> 16)));
+    asm("{\n.reg .f16 a0, a1, a2, a3, one;\n"
+        "mov.b16 one, 0x3C00;\n"
+        "mov.b32 {a0, a1}, %1;\n"
+        "mov.b32 {a2, a3}, %2;\n"
+        "fma.rn.f32.f16 %0, a0, one, %0;\n"
+        "fma.rn.f32.f16 %0, a1, one, %0;\n"
+        "fma.rn.f32.f16 %0, a2, one, %0;\n"
+        "fma.rn.f32.f16 %0, a3, one, %0;\n}"
+        : "+f"(acc)
+        : "r"(h01), "r"(h23));
+    return acc;
+}
+
 // dec(code) * 2^9 as an integer (exact; |value| <= 448 * 512)
 __device__ __forceinline__ int e4m3_times512(uint32_t c) {
     const int e = (c >> 3) & 15, m = c & 7;
@@ -297,7 +319,7 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
                 for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, sm.red_max[w][tok]);
                 const float scale = __fmul_rn(amax, inv448);
                 uint32_t packed[kC / 4];
-                int sum512 = 0;
+                float vsum = 0.0f;     // exact: kC codes
 #pragma unroll
                 for (int q = 0; q < kC / 4; ++q) {
                     uint32_t word = 0;
@@ -309,9 +331,9 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
                         word = c01 | (c23 << 16);
                     }
                     packed[q] = word;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) sum512 += e4m3_times512((word >> (8 * b)) & 0xFF);
+                    vsum = e4m3x4_accumulate(word, vsum);
                 }
+                const int sum512 = __float2int_rn(__fmul_rn(vsum, 512.0f));
                 uint4 *cdst = reinterpret_cast<uint4 *>(&sm.codes[tok][kC * warp]);
 #pragma unroll
                 for (int q = 0; q < kC / 16; ++q)
@@ -715,9 +737,7 @@ token_quant_kernel(const uint16_t *__restrict__ xr, int M, int K, const float *g
                 hi = e4m3x4_scaled(make_uint2(v.z, v.w), as, rcp, ok);
             }
             reinterpret_cast<uint2 *>(arow)[c8] = make_uint2(lo, hi);
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                sum512 += e4m3_times512((lo >> (8 * b)) & 0xFF) + e4m3_times512((hi >> (8 * b)) & 0xFF);
+            sum512 = __float2int_rn(__fmul_rn(e4m3x4_accumulate(hi, e4m3x4_accumulate(lo, 0.0f)), 512.0f));
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) sum512 += __shfl_xor_sync(0xFFFFFFFFu, sum512, o);
