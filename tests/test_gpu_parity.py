@@ -777,6 +777,32 @@ def test_gemm5_full_workload_sampled(pq, orc, name, M):
     assert_close(y.float().cpu().numpy()[ms, ns], y64, "int5 %s M=%d" % (name, prob.M))
 
 
+# ---------------------------------------------------------------- graph API
+@pytest.mark.parametrize("M", [1, 3, 40])
+def test_layer_graph_replays_the_step(pq, orc, M):
+    """PQLinear.make_graph: each replay copies the pinned input in, runs the
+    prologue and GEMM, and copies y out; bit-equal to the eager call, also
+    after new values are written into the pinned input."""
+    prob = pqgen.make_problem(M, 512, 256, seed=55 + M)
+    layer = pq.PQLinear(prob.qweight, prob.qzeros, prob.scales, prob.pairs, prob.theta, prob.cs)
+    xh = torch.from_numpy(prob.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((M, 256), dtype=torch.bfloat16).pin_memory()
+    step = layer.make_graph(xh, yh)
+    for seed in (55 + M, 155 + M):
+        x = pqgen.make_problem(M, 512, 256, seed=seed).x
+        xh.copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+        yh.fill_(float("nan"))
+        step()
+        torch.cuda.synchronize()
+        y_eager = layer(dev_u16(x).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_eager.cpu().view(torch.int16))
+        t = orc.pack(prob)
+        a_o, asg_o, rs_o = orc.rotate_quant(x, prob.cs, t["rec"])
+        assert_close(yh.float().numpy(), orc.gemm_f64(a_o, asg_o, rs_o, t["codes"], t["sz"], 256, 256),
+                     "graph M=%d" % M)
+
+
 # ---------------------------------------------------------------- repeated launches
 @pytest.mark.parametrize("path", ["skinny", "tcn", "tc"])
 def test_gemm_repeated_graph_launches_status_clean(pq, orc, path):

@@ -396,8 +396,55 @@ class PQLinear:
         self.cs = torch.from_numpy(np.ascontiguousarray(cs, dtype=np.uint16).view(np.int16)
                                    .reshape(self.P, self.K)).to(device)
 
+    @classmethod
+    def from_tables(cls, rec, sz, w, cs, pb=None):
+        """A layer over device tables already packed by pq_pack (rec uint8, sz
+        and cs int16 bit patterns, w uint8, all on one CUDA device)."""
+        self = cls.__new__(cls)
+        self.rec, self.sz, self.w, self.cs = rec, sz, w, cs
+        self.P, self.K, self.N = rec.shape[0], w.shape[1] * 2, w.shape[0]
+        self.pb1, self.pb2 = pb if pb is not None else (self.N, self.N)
+        return self
+
     def forward(self, x, y=None, stream=None):
         a, asg, rs = pq_rotate_quant(x, self.rec, self.cs, stream=stream)
         return pq_gemm(a, asg, rs, self.w, self.sz, self.pb1, self.pb2, y=y, stream=stream)
 
     __call__ = forward
+
+    def make_graph(self, x_host, y_host):
+        """One step as a CUDA graph on pinned host buffers: copy x_host (bf16
+        [M, K], pinned) to the device, the prologue and the GEMM, copy y back to
+        y_host (bf16 [M, N], pinned).  Returns a function that replays the step
+        on the current stream; each replay reads whatever x_host holds then.
+        The device buffers live as long as the returned function."""
+        torch = _torch()
+        dev = self.w.device
+        M, K = x_host.shape
+        G = K // 128
+        x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        y_dev = torch.empty((M, self.N), dtype=torch.bfloat16, device=dev)
+        a = torch.empty((self.P, M, K), dtype=torch.uint8, device=dev)
+        asg = torch.empty((self.P, G, M), dtype=torch.float32, device=dev)
+        rs = torch.empty((self.P, G, M), dtype=torch.float32, device=dev)
+
+        def body():
+            x_dev.copy_(x_host, non_blocking=True)
+            pq_rotate_quant(x_dev, self.rec, self.cs, a=a, asg=asg, rs=rs)
+            pq_gemm(a, asg, rs, self.w, self.sz, self.pb1, self.pb2, y=y_dev)
+            y_host.copy_(y_dev, non_blocking=True)
+
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body()                                  # first run outside the capture
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            body()
+
+        def replay():
+            graph.replay()
+
+        replay.buffers = (graph, x_dev, y_dev, a, asg, rs, x_host, y_host)
+        return replay
