@@ -60,7 +60,11 @@
 extern "C" {
 #endif
 
-#define PQ_ABI_VERSION 1
+/* 1: pack, prologue, the three GEMM kernels, the e4m3 encoder.
+ * 2: adds the fused producers, the per-token path (pq_rotate_tokquant,
+ *    pq_gemm_ptok) and int5 weights (pq_pack5, pq_gemm5*); version 1's calls
+ *    are unchanged. */
+#define PQ_ABI_VERSION 2
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
