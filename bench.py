@@ -437,13 +437,13 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=71439104 + 38536192, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        bytes=72353536 + 38940160, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="5a1ca71fc19fa2efbf5e35208f66d2d2927c8537f6d05e31c8b4c271f433451a"),
+        sha256="314a982c0f321ff369b4b86d9429ada4a8da04871269c042b2e21b665ebc521a"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47468032 + 1024, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
+        bytes=47469312 + 0, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="f7c8c427fb980ceecccb65a0d1e6f03d2080a7b39fe97ee2130805af401b39a4"),
+        sha256="49a5fd8537d1027988459d0b3514407c2974387ddba253c3aafdf2e65d737a66"),
 }
 
 

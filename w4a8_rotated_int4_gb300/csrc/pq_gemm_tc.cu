@@ -388,8 +388,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // the accumulator's first use waits on nothing: the phase before
             // the first reads as complete
             const bool ok = __all_sync(0xFFFFFFFFu,
-                                       wait3_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
-                                                      &ctl->full_b[s], use & 1, abort_flag));
+                                       wait2_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
+                                                      abort_flag));
             if (!ok) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull | kStatusWaitTmem);
                 break;
@@ -545,8 +545,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     const int it = i * G + kb;
                     const int b = it & 1, tuse = it >> 1;
                     const int r = it % kSzfRing, ruse = it / kSzfRing;
-                    if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
-                                        &ctl->szf_full[r], ruse & 1, abort_flag)) {
+                    if (!wait2_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
+                                        abort_flag)) {
                         if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                         bad = true;
                         break;
@@ -571,8 +571,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int it = i * G + kb;
                 const int b = it & 1, tuse = it >> 1;
                 const int r = it % kSzfRing, ruse = it / kSzfRing;
-                if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
-                                    &ctl->szf_full[r], ruse & 1, abort_flag)) {
+                if (!wait2_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
+                                    abort_flag)) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     bad = true;
                     break;

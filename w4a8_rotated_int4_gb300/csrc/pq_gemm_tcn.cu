@@ -267,8 +267,8 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             // full_b, and the accumulator's release by the fold (its first use
             // waits on nothing: the phase before the first reads as complete)
             const bool ok = __all_sync(0xFFFFFFFFu,
-                                       wait3_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
-                                                      &ctl->full_b[s], use & 1, abort_flag));
+                                       wait2_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
+                                                      abort_flag));
             if (!ok) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull | kStatusWaitTmem);
                 break;

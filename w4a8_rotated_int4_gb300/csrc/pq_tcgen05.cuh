@@ -161,6 +161,25 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
+// Bounded wait for two phases: one overlapped test of both first, then each
+// barrier in turn (the common case, both complete, costs one round trip).
+__device__ __forceinline__ uint32_t mbar_test2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred q0, q1;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n"
+        "and.pred q0, q0, q1;\nselp.u32 %0, 1, 0, q0;\n}"
+        : "=r"(r)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+        : "memory");
+    return r;
+}
+__device__ __forceinline__ bool wait2_or_abort(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
+                                               volatile int *abort_flag) {
+    if (mbar_test2(b0, p0, b1, p1)) return true;
+    return wait_or_abort(b0, p0, abort_flag) && wait_or_abort(b1, p1, abort_flag);
+}
 // Bounded wait for three phases: one overlapped test first, then each barrier
 // in turn (the common case, all three complete, costs one round trip).
 __device__ __forceinline__ bool wait3_or_abort(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
@@ -210,6 +229,11 @@ __device__ __forceinline__ uint4 expand16(uint2 pk) {
 __device__ __forceinline__ uint32_t even_bit_mask(uint32_t b) {
     return prmt((b & 0x55u) * 0x02082080u, 0u, 0xBA98u);
 }
+// The same for the odd bits 2j + 1: the constant is the even one halved, so
+// the products land on the same positions without a shift first.
+__device__ __forceinline__ uint32_t odd_bit_mask(uint32_t b) {
+    return prmt((b & 0xAAu) * 0x01041040u, 0u, 0xBA98u);
+}
 
 // int5 weights: sixteen packed low nibbles plus their sixteen fifth bits
 // (bit i of hb = the fifth bit of k = i) -> sixteen e4m3 bytes of value
@@ -222,11 +246,11 @@ __device__ __forceinline__ uint32_t even_bit_mask(uint32_t b) {
 __device__ __forceinline__ uint4 expand16_int5(uint2 pk, uint32_t hb) {
     uint32_t nib[4] = {pk.x & 0x0F0F0F0Fu, (pk.x >> 4) & 0x0F0F0F0Fu, pk.y & 0x0F0F0F0Fu,
                        (pk.y >> 4) & 0x0F0F0F0Fu};
+    // word q holds k = 8 (q / 2) + (q % 2) + 2j in byte j
+    const uint32_t hb8 = hb >> 8;
+    const uint32_t msk[4] = {even_bit_mask(hb), odd_bit_mask(hb), even_bit_mask(hb8), odd_bit_mask(hb8)};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {     // q: k = 8 (q / 2) + (q % 2) + 2j in byte j
-        const uint32_t m = even_bit_mask(hb >> (8 * (q >> 1) + (q & 1)));
-        nib[q] = (nib[q] & m) | ((0x90909090u - nib[q]) & ~m);
-    }
+    for (int q = 0; q < 4; ++q) nib[q] = (nib[q] & msk[q]) | ((0x90909090u - nib[q]) & ~msk[q]);
     uint4 o;
     o.x = prmt(nib[0], nib[1], 0x5140u);
     o.y = prmt(nib[0], nib[1], 0x7362u);
