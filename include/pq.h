@@ -28,6 +28,8 @@
  *   - Every buffer is owned by the caller, who allocates and frees it.  The
  *     library allocates no memory (host or device), keeps no state besides a
  *     per-thread error string, and may be called from several host threads.
+ *     The one exception is pq_rotate_tokquant_noalloc, whose scratch is a
+ *     fixed array in the library's device image (see there).
  *   - Device calls are asynchronous on `stream` (a cudaStream_t passed as
  *     void*; NULL = the legacy default stream) and never synchronise.  All
  *     argument checks run on the host before any launch; a failed check
@@ -63,8 +65,9 @@ extern "C" {
 /* 1: pack, prologue, the three GEMM kernels, the e4m3 encoder.
  * 2: adds the fused producers, the per-token path (pq_rotate_tokquant,
  *    pq_gemm_ptok) and int5 weights (pq_pack5, pq_gemm5*); version 1's calls
- *    are unchanged. */
-#define PQ_ABI_VERSION 2
+ *    are unchanged.
+ * 3: adds pq_rotate_tokquant_noalloc; earlier calls are unchanged. */
+#define PQ_ABI_VERSION 3
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
@@ -334,6 +337,38 @@ Two launches: pass A writes xr and the group scales (into rs); pass C reads
  */
 pq_status pq_rotate_tokquant(const void *x, int M, int K, int ldx, int P, const void *rec,
                              const void *cs, void *xr, void *a, float *As, float *rs, void *stream);
+
+/*
+ * pq_rotate_tokquant for callers that cannot allocate device memory.  It has
+ * no counterpart in the engineering log: it exists for code that must not
+ * call cudaMalloc or any allocator -- for instance a plugin inside an engine
+ * that owns every byte of device memory through its own pool, a caller that
+ * only receives its input and output tensors, or a latency-critical path
+ * where an allocation could synchronise the device.  Such a caller cannot
+ * provide pq_rotate_tokquant's xr scratch.  This entry point keeps the
+ * rotated rows in a fixed bf16 array inside the library instead (16 MiB of
+ * device memory on every GPU that loads the library, held until the process
+ * exits), and allocates nothing itself.
+ *
+ * Same result and arguments as pq_rotate_tokquant, without xr:
+ *   x, rec, cs, a, As, rs   as for pq_rotate_tokquant
+ * Limits and rules:
+ *   - P * M * K <= PQ_TOKQUANT_NOALLOC_MAX_ELEMS; a larger problem returns
+ *     PQ_ERR_SHAPE and launches nothing (use pq_rotate_tokquant).
+ *   - Every call on a device uses the same array, and a call leaves its rows
+ *     there; each call overwrites every element it reads, so old contents do
+ *     not matter.  Calls whose kernels overlap on the GPU (different streams
+ *     without ordering between them, or several host threads) race on the
+ *     array and give wrong results: order them on one stream.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress, which may load the
+ *     library's device code); make that first call before any stream capture.
+ * Errors: as pq_rotate_tokquant, plus PQ_ERR_SHAPE for P * M * K above the
+ * limit and PQ_ERR_CUDA if the address lookup fails.
+ */
+#define PQ_TOKQUANT_NOALLOC_MAX_ELEMS (8u * 1024u * 1024u)
+pq_status pq_rotate_tokquant_noalloc(const void *x, int M, int K, int ldx, int P, const void *rec,
+                                     const void *cs, void *a, float *As, float *rs, void *stream);
 
 /*
  * The GEMM on per-token scales ([PTOK] "PTOK GEMM"):

@@ -26,7 +26,7 @@ EXPORTS = (
     "pq_rotate_quant", "pq_add_rms_rotate_quant", "pq_silu_mul_rotate_quant", "pq_gemm", "pq_gemm_skinny_max_m", "pq_gemm_skinny",
     "pq_gemm_tc",
     "pq_gemm_tcn",
-    "pq_rotate_tokquant", "pq_gemm_ptok",
+    "pq_rotate_tokquant", "pq_rotate_tokquant_noalloc", "pq_gemm_ptok",
     "pq_pack5", "pq_gemm5", "pq_gemm5_tc", "pq_gemm5_tcn",
     "pq_e4m3_encode",
 )
@@ -82,6 +82,8 @@ def lib() -> C.CDLL:
         f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
     L.pq_rotate_tokquant.restype = i32
     L.pq_rotate_tokquant.argtypes = [vp, i32, i32, i32, i32] + [vp] * 7
+    L.pq_rotate_tokquant_noalloc.restype = i32
+    L.pq_rotate_tokquant_noalloc.argtypes = [vp, i32, i32, i32, i32] + [vp] * 6
     L.pq_gemm_ptok.restype = i32
     L.pq_gemm_ptok.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, i32, vp, vp]
     L.pq_pack5.restype = i32
@@ -337,6 +339,19 @@ def pq_rotate_tokquant(x, rec, cs, xr=None, a=None, As=None, rs=None, stream=Non
     _check(lib().pq_rotate_tokquant(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(xr), _dptr(a),
                                     _dptr(As), _dptr(rs), _stream(stream)), "pq_rotate_tokquant")
     return xr, a, As, rs
+
+
+def pq_rotate_tokquant_noalloc(x, rec, cs, a, As, rs, stream=None):
+    """pq_rotate_tokquant with the library's fixed scratch instead of xr:
+    for callers that cannot allocate device memory, so every output (a uint8
+    [P,M,K], As f32 [P,M], rs f32 [P,G,M]) is the caller's; P * M * K must not
+    exceed the library's limit.  Returns (a, As, rs)."""
+    M, ldx = x.shape
+    P, K = cs.shape
+    _check(lib().pq_rotate_tokquant_noalloc(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(a),
+                                            _dptr(As), _dptr(rs), _stream(stream)),
+           "pq_rotate_tokquant_noalloc")
+    return a, As, rs
 
 
 def pq_gemm_ptok(a, As, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):

@@ -379,6 +379,27 @@ extern "C" pq_status pq_rotate_tokquant(const void *x, int M, int K, int ldx, in
     return launch_rotate_tokquant(x, M, K, ldx, P, rec, cs, xr, a, As, rs, stream);
 }
 
+extern "C" pq_status pq_rotate_tokquant_noalloc(const void *x, int M, int K, int ldx, int P, const void *rec,
+                                                const void *cs, void *a, float *As, float *rs, void *stream) {
+    clear_error();
+    if (!x || !rec || !cs || !a || !As || !rs) return fail(PQ_ERR_NULL, "NULL buffer");
+    if (M < 1 || K < 128 || K % 128 || ldx < K)
+        return fail(PQ_ERR_SHAPE, "M = %d, K = %d, ldx = %d", M, K, ldx);
+    if ((long long)M * ldx > (1ll << 40)) return fail(PQ_ERR_SHAPE, "sizes too large");
+    if (P < 1 || P > PQ_MAX_PARTITIONS) return fail(PQ_ERR_PARTITION, "P = %d outside 1..3", P);
+    if ((unsigned long long)P * (unsigned long long)M * (unsigned long long)K > PQ_TOKQUANT_NOALLOC_MAX_ELEMS)
+        return fail(PQ_ERR_SHAPE,
+                    "pq_rotate_tokquant_noalloc: P * M * K = %llu exceeds its fixed scratch of %u elements; "
+                    "use pq_rotate_tokquant with a caller buffer",
+                    (unsigned long long)P * M * K, (unsigned)PQ_TOKQUANT_NOALLOC_MAX_ELEMS);
+    if (!aligned(x, 16) || !aligned(rec, 16) || !aligned(cs, 16) || !aligned(a, 16) || !aligned(As, 4) ||
+        !aligned(rs, 4) || ldx % 8)
+        return fail(PQ_ERR_ALIGN, "x, rec, cs, a need 16-byte alignment, As/rs 4-byte, ldx a multiple of 8");
+    pq_status st = check_device(nullptr);
+    if (st != PQ_OK) return st;
+    return launch_rotate_tokquant_noalloc(x, M, K, ldx, P, rec, cs, a, As, rs, stream);
+}
+
 extern "C" pq_status pq_gemm_ptok(const void *a, const float *As, const float *rs, int M, int N, int K,
                                   int P, int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
                                   unsigned int *dev_status, void *stream) {

@@ -36,6 +36,8 @@ pq_status launch_rotate_quant(const void *x, int M, int K, int ldx, int P, const
                               const void *cs, void *a, float *asg, float *rs, void *stream);
 pq_status launch_rotate_tokquant(const void *x, int M, int K, int ldx, int P, const void *rec, const void *cs,
                                  void *xr, void *a, float *As, float *rs, void *stream);
+pq_status launch_rotate_tokquant_noalloc(const void *x, int M, int K, int ldx, int P, const void *rec,
+                                         const void *cs, void *a, float *As, float *rs, void *stream);
 pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream);
 pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, int M, int N,
                              int K, int P, int pb1, int pb2, const void *w, const void *sz,

@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "pq_device.cuh"
 #include "pq_internal.h"
@@ -891,6 +892,51 @@ pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stre
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PQ_ERR_CUDA, "e4m3_encode launch: %s", cudaGetErrorString(e));
     return PQ_OK;
+}
+
+// ------------------------------------------------ the per-token prologue without caller scratch
+// The bf16 rotated rows that pass A hands to pass C live in this fixed array
+// instead of a caller buffer.  It is part of the library's device image, so
+// every GPU that loads the library holds its 16 MiB until the process exits.
+// Pass A writes every element pass C reads, so nothing in it needs clearing.
+static __device__ __align__(256) uint16_t g_tokquant_xr[PQ_TOKQUANT_NOALLOC_MAX_ELEMS];
+
+namespace {
+// Device address of g_tokquant_xr on the current device.  In host code the
+// symbol names a host-side stand-in, never device memory, so the address is
+// looked up once per device (with that device current) and cached.
+pq_status tokquant_scratch(void **out) {
+    static std::mutex mu;
+    static void *cached[64];
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return fail(PQ_ERR_ARCH, "cudaGetDevice: %s", cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 64 && cached[dev]) {
+        *out = cached[dev];
+        return PQ_OK;
+    }
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_tokquant_xr);
+    if (e != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return fail(PQ_ERR_CUDA, "cudaGetSymbolAddress(g_tokquant_xr): %s", cudaGetErrorString(e));
+    }
+    if (dev < 64) cached[dev] = ptr;
+    *out = ptr;
+    return PQ_OK;
+}
+}  // namespace
+
+pq_status launch_rotate_tokquant_noalloc(const void *x, int M, int K, int ldx, int P, const void *rec,
+                                         const void *cs, void *a, float *As, float *rs, void *stream) {
+    void *xr = nullptr;
+    const pq_status st = tokquant_scratch(&xr);
+    if (st != PQ_OK) return st;
+    return launch_rotate_tokquant(x, M, K, ldx, P, rec, cs, xr, a, As, rs, stream);
 }
 
 }  // namespace pq
