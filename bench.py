@@ -433,15 +433,15 @@ def e2e_graph_workload(pq, torch, wl, steps, warmup, stream):
 _CSRC = "w4a8_rotated_int4_gb300/csrc/"
 NCU_TRAFFIC = {
     ("pq_gemm_skinny", "decode:1"): dict(
-        bytes=47379968 + 0, profile="profiles/pq_gemm_skinny_decode_gate_up_m1.md",
+        bytes=47379968 + 0,
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=72353536 + 38940160, profile="profiles/pq_gemm_tc_prefill_gate_up.md",
+        bytes=72353536 + 38940160,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
         sha256="314a982c0f321ff369b4b86d9429ada4a8da04871269c042b2e21b665ebc521a"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47469312 + 0, profile="profiles/pq_gemm_tcn_decode_gate_up_m16.md",
+        bytes=47469312 + 0,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
         sha256="49a5fd8537d1027988459d0b3514407c2974387ddba253c3aafdf2e65d737a66"),
 }

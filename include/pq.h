@@ -275,8 +275,16 @@ pq_status pq_silu_mul_rotate_quant(const void *y, int M, int I, int ldy, int P, 
  *   pb1, pb2    partition boundaries, multiples of 128:
  *               P = 1: pb1 = pb2 = N;  P = 2: 0 < pb1 < pb2 = N;
  *               P = 3: 0 < pb1 < pb2 < N
- * Dispatch: M <= pq_gemm_skinny_max_m() runs the CUDA-core decode kernel,
- * larger M the tcgen05 tensor-core kernel; one launch in both cases.
+ * Dispatch (one launch in every case; S = the device's SM count):
+ *   M = 1, K <= 16384                   -> pq_gemm_skinny (CUDA cores)
+ *   2 <= M <= 16, 2 * (N / 128) >= S    -> pq_gemm_tcn (narrow tensor-core kernel)
+ *   2 <= M <= 16, 2 * (N / 128) < S,
+ *     K <= 16384                        -> pq_gemm_skinny
+ *   M <= 16, K > 16384                  -> pq_gemm_tcn
+ *   M > 16                              -> pq_gemm_tc (prefill tensor-core kernel)
+ * Layouts differ from a plain [G][N][2] SZ table and [P][M][G] scales on
+ * purpose: the SZ words are octet-major ([N/8][G][8], see pq_pack) and asg/rs
+ * are [P][G][M], so that each kernel reads them with one contiguous copy.
  * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE, PQ_ERR_ALIGN, PQ_ERR_PARTITION,
  * PQ_ERR_ARCH, PQ_ERR_CUDA.
  */
@@ -284,7 +292,8 @@ pq_status pq_gemm(const void *a, const float *asg, const float *rs, int M, int N
                   int pb1, int pb2, const void *w, const void *sz, void *y, int ldy,
                   void *stream);
 
-/* Largest M that pq_gemm sends to the CUDA-core decode kernel. */
+/* Largest M that pq_gemm may send to the CUDA-core decode kernel (see the
+ * dispatch rule of pq_gemm; pq_gemm_skinny itself also needs K <= 16384). */
 int pq_gemm_skinny_max_m(void);
 
 /*
@@ -293,7 +302,8 @@ int pq_gemm_skinny_max_m(void);
  * accumulated in fp32) accepts 1 <= M <= 16; pq_gemm_tcn (tensor cores,
  * operands swapped: 128 output features x up to 16 tokens per MMA, weights
  * streamed once) accepts 1 <= M <= 16; pq_gemm_tc (tensor cores, 256-token x
- * 128-feature tiles) accepts any M >= 1.  A larger M returns PQ_ERR_SHAPE.
+ * 128-feature tiles) accepts any M >= 1.  A larger M returns PQ_ERR_SHAPE, and
+ * so does pq_gemm_skinny for K > 16384.
  *
  * dev_status (device, 4-byte aligned, may be NULL): every wait inside the
  * kernels is bounded; a wait that gives up (never expected) ORs a nonzero

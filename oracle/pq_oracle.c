@@ -18,7 +18,9 @@
  *          decoded codes, partition select) and "Gates passed"
  *          (scale = amax * (1/448.f)).
  *   [CVT]  same page, section "2026-09-15: hardware e4m3 convert in the
- *          producers" (NaN -> 0, -0 -> +0, clamp +-448, then RNE convert).
+ *          producers": the encoder maps a NaN to code zero and a negative
+ *          zero to positive zero, saturates magnitudes at 448 and rounds to
+ *          nearest even.
  *
  * Readings of points the pages leave open:
  *   R1 pairs: entries 2t and 2t+1 of a layer's 128-group form pair t, and the
@@ -52,12 +54,14 @@
  *        inv   = fl32(1 / fl32(sqrt(fl32(fl32(ss / K) + eps))))  (correctly
  *                rounded sqrt and division)
  *        h[k]  = bf16_RNE(fl32(fl32(s[k] * inv) * fl32(1 + gamma[k])))
- *      then the pq_rotate_quant semantics on h.  The pages fix the op order
- *      ("in vLLM's exact op order": s * rsqrt(mean(s^2) + eps) * (1 + w)) but
- *      not the reduction order or the rsqrt rounding; these are the readings.
+ *      then the pq_rotate_quant semantics on h.  The page fixes the order of
+ *      the operations (the serving engine's own: s times the reciprocal root
+ *      of mean(s^2) + eps, times 1 + w) but not the reduction order or the
+ *      rounding of the reciprocal root; these are the readings.
  *   R17 silu-mul producer ([LOG] "2026-09-03: rotation stream 2 (silu-mul,
- *      ...)": "MODE 0 silu(g)*u (bf16-rounded silu, bf16 product)" + the
- *      rotate_quant body).  The merged gate/up output y holds g in columns
+ *      ...)", its first mode: silu of the gate rounded to bf16, multiplied by
+ *      the up value and rounded to bf16 again, followed by the rotate_quant
+ *      body).  The merged gate/up output y holds g in columns
  *      [0, I) and u in [I, 2I).  Per element:
  *        e   = exp32(-g)        (below)
  *        sg  = bf16_RNE(fl32(g / fl32(1 + e)))

@@ -373,6 +373,27 @@ def test_gemm_full_vs_oracle(pq, orc, M, K, N, P, pb):
         assert_close(y, y64, "%s M=%d K=%d N=%d P=%d" % (name, M, K, N, P))
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_gemm_dispatch_beyond_skinny_k(pq, orc, M):
+    """pq_gemm at M <= 16 with K above the CUDA-core kernel's limit (16384):
+    the dispatcher must hand it to the narrow tensor-core kernel, which has no
+    K limit, and the result must stay within the bf16 floor.  The CUDA-core
+    kernel itself refuses that K."""
+    K, N = 17408, 256
+    prob = pqgen.make_problem(M, K, N, seed=K + M)
+    L = Problem(pq, orc, prob)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, L.t["rec"])
+    assert np.array_equal(a.cpu().numpy(), a_o)
+    y64 = orc.gemm_f64(a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
+    y = pq.pq_gemm(a, asg, rs, L.w_d, L.sz_d)
+    torch.cuda.synchronize()
+    assert_close(y.float().cpu().numpy(), y64, "pq_gemm M=%d K=%d" % (M, K))
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_gemm_skinny(a, asg, rs, L.w_d, L.sz_d)
+    assert e.value.status == 2
+
+
 @pytest.mark.parametrize("subnormal", [False, True])
 def test_gemm_random_codes(pq, orc, subnormal):
     """Codes drawn uniformly from all 254 finite e4m3 codes (incl. 0x80 and

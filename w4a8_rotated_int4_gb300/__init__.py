@@ -198,6 +198,47 @@ def _dptr(t) -> C.c_void_p:
     return C.c_void_p(t.data_ptr())
 
 
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _expect(t, what, dtype=None, shape=None, nbytes=None):
+    """Raise PQError unless tensor t has the given dtype, shape and byte size:
+    the C ABI takes raw pointers, so a mis-sized tensor would be read or
+    written out of bounds on the device."""
+    if dtype is not None and t.dtype != dtype:
+        raise PQError("%s: dtype %s, expected %s" % (what, t.dtype, dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise PQError("%s: shape %s, expected %s" % (what, tuple(t.shape), tuple(shape)))
+    if nbytes is not None and _nbytes(t) != nbytes:
+        raise PQError("%s: %d bytes, expected %d" % (what, _nbytes(t), nbytes))
+
+
+def _rotation_args(x, rec, cs, what):
+    """Checks shared by the prologues: x bf16 [M, ldx], cs 2-byte [P, K],
+    rec pq_pack's record table for (P, K).  Returns (M, ldx, P, K, G)."""
+    torch = _torch()
+    _expect(x, what + " x", dtype=torch.bfloat16)
+    if x.dim() != 2:
+        raise PQError("%s x: expected a 2-D [M, ldx] tensor" % what)
+    if cs.dim() != 2 or cs.element_size() != 2:
+        raise PQError("%s cs: expected a 2-byte [P, K] tensor" % what)
+    M, ldx = x.shape
+    P, K = cs.shape
+    if K % 128 or K < 128 or ldx < K:
+        raise PQError("%s: K = %d must be a positive multiple of 128 and <= ldx = %d" % (what, K, ldx))
+    G = K // 128
+    _expect(rec, what + " rec", nbytes=P * 8 * G * 64 * 8)
+    return M, ldx, P, K, G
+
+
+def _quant_outputs(what, P, M, K, G, a, asg, rs):
+    torch = _torch()
+    _expect(a, what + " a", dtype=torch.uint8, shape=(P, M, K))
+    _expect(asg, what + " asg", dtype=torch.float32, shape=(P, G, M))
+    _expect(rs, what + " rs", dtype=torch.float32, shape=(P, G, M))
+
+
 def _stream(stream):
     torch = _torch()
     s = torch.cuda.current_stream() if stream is None else stream
@@ -208,9 +249,7 @@ def pq_rotate_quant(x, rec, cs, a=None, asg=None, rs=None, stream=None):
     """x bf16 [M, ldx>=K] (CUDA), rec uint8 (device copy of pq_pack's rec),
     cs f16 [P, K].  Returns (a uint8 [P,M,K] e4m3 codes, asg f32 [P,G,M], rs f32 [P,G,M])."""
     torch = _torch()
-    M, ldx = x.shape
-    P, K = cs.shape
-    G = K // 128
+    M, ldx, P, K, G = _rotation_args(x, rec, cs, "pq_rotate_quant")
     dev = x.device
     if a is None:
         a = torch.empty((P, M, K), dtype=torch.uint8, device=dev)
@@ -218,6 +257,7 @@ def pq_rotate_quant(x, rec, cs, a=None, asg=None, rs=None, stream=None):
         asg = torch.empty((P, G, M), dtype=torch.float32, device=dev)
     if rs is None:
         rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _quant_outputs("pq_rotate_quant", P, M, K, G, a, asg, rs)
     _check(lib().pq_rotate_quant(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(a),
                                  _dptr(asg), _dptr(rs), _stream(stream)), "pq_rotate_quant")
     return a, asg, rs
@@ -230,11 +270,11 @@ def pq_add_rms_rotate_quant(x, residual, gamma, eps, rec, cs, residual_out=None,
     float, rec and cs as for pq_rotate_quant.  Returns (residual_out bf16
     [M,K], h bf16 [M,K], a uint8 [P,M,K], asg f32 [P,G,M], rs f32 [P,G,M])."""
     torch = _torch()
-    M, ldx = x.shape
+    M, ldx, P, K, G = _rotation_args(x, rec, cs, "pq_add_rms_rotate_quant")
     if tuple(residual.shape) != (M, ldx) or residual.stride(0) != x.stride(0):
         raise PQError("residual must have x's shape and row stride")
-    P, K = cs.shape
-    G = K // 128
+    _expect(residual, "pq_add_rms_rotate_quant residual", dtype=torch.bfloat16)
+    _expect(gamma, "pq_add_rms_rotate_quant gamma", dtype=torch.bfloat16, nbytes=2 * K)
     dev = x.device
     if residual_out is None:
         residual_out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
@@ -246,6 +286,9 @@ def pq_add_rms_rotate_quant(x, residual, gamma, eps, rec, cs, residual_out=None,
         asg = torch.empty((P, G, M), dtype=torch.float32, device=dev)
     if rs is None:
         rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _expect(residual_out, "pq_add_rms_rotate_quant residual_out", dtype=torch.bfloat16, shape=(M, K))
+    _expect(h, "pq_add_rms_rotate_quant h", dtype=torch.bfloat16, shape=(M, K))
+    _quant_outputs("pq_add_rms_rotate_quant", P, M, K, G, a, asg, rs)
     _check(lib().pq_add_rms_rotate_quant(_dptr(x), _dptr(residual), _dptr(gamma), C.c_float(eps), M, K,
                                          x.stride(0), P, _dptr(rec), _dptr(cs), _dptr(residual_out),
                                          _dptr(h), _dptr(a), _dptr(asg), _dptr(rs), _stream(stream)),
@@ -259,9 +302,15 @@ def pq_silu_mul_rotate_quant(y, rec, cs, act=None, a=None, asg=None, rs=None, st
     cs for the down projection (cs f16 [P, I]).  Returns (act bf16 [M, I],
     a uint8 [P, M, I], asg f32 [P, G, M], rs f32 [P, G, M])."""
     torch = _torch()
+    _expect(y, "pq_silu_mul_rotate_quant y", dtype=torch.bfloat16)
+    if y.dim() != 2 or cs.dim() != 2 or cs.element_size() != 2:
+        raise PQError("pq_silu_mul_rotate_quant: y must be 2-D [M, ldy], cs a 2-byte [P, I] tensor")
     M, ldy = y.shape
     P, I = cs.shape
+    if I % 128 or I < 128 or ldy < 2 * I:
+        raise PQError("pq_silu_mul_rotate_quant: I = %d must be a positive multiple of 128, ldy >= 2I" % I)
     G = I // 128
+    _expect(rec, "pq_silu_mul_rotate_quant rec", nbytes=P * 8 * G * 64 * 8)
     dev = y.device
     if act is None:
         act = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
@@ -271,20 +320,40 @@ def pq_silu_mul_rotate_quant(y, rec, cs, act=None, a=None, asg=None, rs=None, st
         asg = torch.empty((P, G, M), dtype=torch.float32, device=dev)
     if rs is None:
         rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _expect(act, "pq_silu_mul_rotate_quant act", dtype=torch.bfloat16, shape=(M, I))
+    _quant_outputs("pq_silu_mul_rotate_quant", P, M, I, G, a, asg, rs)
     _check(lib().pq_silu_mul_rotate_quant(_dptr(y), M, I, y.stride(0), P, _dptr(rec), _dptr(cs), _dptr(act),
                                           _dptr(a), _dptr(asg), _dptr(rs), _stream(stream)),
            "pq_silu_mul_rotate_quant")
     return act, a, asg, rs
 
 
-def _gemm_args(a, asg, rs, w, sz, pb1, pb2, y):
+def _gemm_args(a, asg, rs, w, sz, pb1, pb2, y, per_token=False, whi=None):
+    """Shapes of a GEMM call, checked against (P, M, K) from a and N from w:
+    a uint8 [P, M, K]; asg, rs f32 [P, G, M] (per-token: As f32 [P, M]);
+    w uint8 [N, K/2]; sz G * N 4-byte words; whi uint8 [N, K/8]; y bf16
+    [M, >= N]."""
     torch = _torch()
+    if a.dim() != 3 or w.dim() != 2:
+        raise PQError("GEMM: a must be [P, M, K] and w [N, K/2]")
     P, M, K = a.shape
     N = w.shape[0]
+    G = K // 128
+    _expect(a, "GEMM a", dtype=torch.uint8)
+    _expect(w, "GEMM w", dtype=torch.uint8, shape=(N, K // 2))
+    _expect(asg, "GEMM As" if per_token else "GEMM asg", dtype=torch.float32,
+            shape=(P, M) if per_token else (P, G, M))
+    _expect(rs, "GEMM rs", dtype=torch.float32, shape=(P, G, M))
+    _expect(sz, "GEMM sz", nbytes=4 * G * N)
+    if whi is not None:
+        _expect(whi, "GEMM whi", dtype=torch.uint8, nbytes=N * K // 8)
     if pb1 is None:
         pb1 = pb2 = N
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _expect(y, "GEMM y", dtype=torch.bfloat16)
+    if y.dim() != 2 or y.shape[0] != M or y.shape[1] < N:
+        raise PQError("GEMM y: shape %s, expected [%d, >= %d]" % (tuple(y.shape), M, N))
     return P, M, K, N, pb1, pb2, y
 
 
@@ -296,9 +365,17 @@ def pq_gemm(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, stream=None):
     return y
 
 
-def _gemm_path(fn, name, a, asg, rs, w, sz, pb1, pb2, y, dev_status, stream):
-    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
-    st = _dptr(dev_status) if dev_status is not None else None
+def _status_ptr(dev_status):
+    if dev_status is None:
+        return None
+    if _nbytes(dev_status) < 4:
+        raise PQError("dev_status: needs at least one 4-byte word")
+    return _dptr(dev_status)
+
+
+def _gemm_path(fn, name, a, asg, rs, w, sz, pb1, pb2, y, dev_status, stream, per_token=False):
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y, per_token=per_token)
+    st = _status_ptr(dev_status)
     _check(fn(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w), _dptr(sz),
               _dptr(y), y.stride(0), st, _stream(stream)), name)
     return y
@@ -319,14 +396,19 @@ def pq_gemm_tcn(a, asg, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, 
                       dev_status, stream)
 
 
+def _tokquant_outputs(what, P, M, K, G, a, As, rs):
+    torch = _torch()
+    _expect(a, what + " a", dtype=torch.uint8, shape=(P, M, K))
+    _expect(As, what + " As", dtype=torch.float32, shape=(P, M))
+    _expect(rs, what + " rs", dtype=torch.float32, shape=(P, G, M))
+
+
 def pq_rotate_tokquant(x, rec, cs, xr=None, a=None, As=None, rs=None, stream=None):
     """Per-token prologue: x bf16 [M, ldx>=K] (CUDA), rec, cs as for
     pq_rotate_quant.  Returns (xr bf16 [P,M,K] rotated rows, a uint8 [P,M,K]
     e4m3 codes, As f32 [P,M] token scales, rs f32 [P,G,M] plain row-sums)."""
     torch = _torch()
-    M, ldx = x.shape
-    P, K = cs.shape
-    G = K // 128
+    M, ldx, P, K, G = _rotation_args(x, rec, cs, "pq_rotate_tokquant")
     dev = x.device
     if xr is None:
         xr = torch.empty((P, M, K), dtype=torch.bfloat16, device=dev)
@@ -336,6 +418,8 @@ def pq_rotate_tokquant(x, rec, cs, xr=None, a=None, As=None, rs=None, stream=Non
         As = torch.empty((P, M), dtype=torch.float32, device=dev)
     if rs is None:
         rs = torch.empty((P, G, M), dtype=torch.float32, device=dev)
+    _expect(xr, "pq_rotate_tokquant xr", dtype=torch.bfloat16, shape=(P, M, K))
+    _tokquant_outputs("pq_rotate_tokquant", P, M, K, G, a, As, rs)
     _check(lib().pq_rotate_tokquant(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(xr), _dptr(a),
                                     _dptr(As), _dptr(rs), _stream(stream)), "pq_rotate_tokquant")
     return xr, a, As, rs
@@ -346,8 +430,8 @@ def pq_rotate_tokquant_noalloc(x, rec, cs, a, As, rs, stream=None):
     for callers that cannot allocate device memory, so every output (a uint8
     [P,M,K], As f32 [P,M], rs f32 [P,G,M]) is the caller's; P * M * K must not
     exceed the library's limit.  Returns (a, As, rs)."""
-    M, ldx = x.shape
-    P, K = cs.shape
+    M, ldx, P, K, G = _rotation_args(x, rec, cs, "pq_rotate_tokquant_noalloc")
+    _tokquant_outputs("pq_rotate_tokquant_noalloc", P, M, K, G, a, As, rs)
     _check(lib().pq_rotate_tokquant_noalloc(_dptr(x), M, K, ldx, P, _dptr(rec), _dptr(cs), _dptr(a),
                                             _dptr(As), _dptr(rs), _stream(stream)),
            "pq_rotate_tokquant_noalloc")
@@ -357,20 +441,20 @@ def pq_rotate_tokquant_noalloc(x, rec, cs, a, As, rs, stream=None):
 def pq_gemm_ptok(a, As, rs, w, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
     """y bf16 [M, N] from the per-token prologue's outputs (As in the epilogue)."""
     return _gemm_path(lib().pq_gemm_ptok, "pq_gemm_ptok", a, As, rs, w, sz, pb1, pb2, y,
-                      dev_status, stream)
+                      dev_status, stream, per_token=True)
 
 
 def pq_gemm5(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, stream=None):
     """y bf16 [M, N]: the group GEMM on int5 weights (pq_pack5's w, whi, sz)."""
-    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y, whi=whi)
     _check(lib().pq_gemm5(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w), _dptr(whi),
                           _dptr(sz), _dptr(y), y.stride(0), _stream(stream)), "pq_gemm5")
     return y
 
 
 def _gemm5_path(fn, name, a, asg, rs, w, whi, sz, pb1, pb2, y, dev_status, stream):
-    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y)
-    st = _dptr(dev_status) if dev_status is not None else None
+    P, M, K, N, pb1, pb2, y = _gemm_args(a, asg, rs, w, sz, pb1, pb2, y, whi=whi)
+    st = _status_ptr(dev_status)
     _check(fn(_dptr(a), _dptr(asg), _dptr(rs), M, N, K, P, pb1, pb2, _dptr(w), _dptr(whi), _dptr(sz),
               _dptr(y), y.stride(0), st, _stream(stream)), name)
     return y
@@ -389,8 +473,10 @@ def pq_gemm5_tcn(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, dev_status=
 def pq_e4m3_encode(x, out=None, stream=None):
     """The prologue's device e4m3 encoder on an fp32 CUDA tensor."""
     torch = _torch()
+    _expect(x, "pq_e4m3_encode x", dtype=torch.float32)
     if out is None:
         out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _expect(out, "pq_e4m3_encode out", dtype=torch.uint8, nbytes=x.numel())
     _check(lib().pq_e4m3_encode(_dptr(x), _dptr(out), x.numel(), _stream(stream)),
            "pq_e4m3_encode")
     return out

@@ -529,9 +529,10 @@ extern "C" pq_status pq_gemm(const void *a, const float *asg, const float *rs, i
     // 2 <= M <= 16: the narrow tensor-core kernel, when its 128-feature tiles cover
     // at least half the SMs (it streams each tile from one SM); otherwise the
     // CUDA-core kernel, which spreads 8-feature octets over every SM.
+    // Any M <= 16 with K above the CUDA-core kernel's limit: the narrow kernel.
     // M > 16: the prefill tensor-core kernel.
     if (M <= kSkinnyMaxM) {
-        if (M >= 2 && M <= kTcnMaxM && 2 * (N / 128) >= sms)
+        if ((M >= 2 && M <= kTcnMaxM && 2 * (N / 128) >= sms) || K > kSkinnyMaxK)
             return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream);
         return launch_gemm_skinny(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream,
                                   sms);

@@ -58,7 +58,7 @@
 namespace pq {
 namespace {
 
-constexpr int kMaxK = 16384;          // 16 compute warps + producer; larger K uses the tcgen05 path
+constexpr int kMaxK = kSkinnyMaxK;    // 16 compute warps + producer; pq_gemm sends larger K to the narrow tcgen05 kernel
 constexpr int kSmemBudget = 220 * 1024;    // per SM, over all resident CTAs
 
 struct SkinnyParams {

@@ -261,6 +261,9 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         // and one elected lane issues the MMAs and commits.
         const int j = warp - kMmaWarp0;
         int committed = -1;
+        // the bounded waits below start their clocks only once the preceding
+        // kernel has completed, so a long predecessor cannot run them out
+        pdl_wait();
         for (int it = j; it < G; it += kMmaWarps) {
             const int s = it % kStages, use = it / kStages;
             const int b = it % kTmemBufs, tuse = it / kTmemBufs;
@@ -320,6 +323,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const int eg = (warp - kExpWarp0) / kExpWarps;   // this warp's group
         const int et = threadIdx.x - (kExpWarp0 + kExpWarps * eg) * 32;   // 0..127
         const int chunk = et & 7;
+        pdl_wait();        // as for the MMA warps: the wait clocks start after the predecessor
         for (int it = eg; it < G; it += kExpGroups) {
             const int s = it % kStages, use = it / kStages;
             if (!wait_or_abort(&ctl->full_tma[s], use & 1, abort_flag)) {

@@ -53,6 +53,7 @@ pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int 
                           int ldy, unsigned int *dev_status, void *stream, const void *whi = nullptr);
 
 constexpr int kSkinnyMaxM = 16;   // largest M the CUDA-core decode kernel accepts
+constexpr int kSkinnyMaxK = 16384;   // largest K it accepts (one compute warp per 1024 k, plus the producer)
 constexpr int kTcnMaxM = 16;      // largest M the narrow tensor-core kernel accepts
 
 }  // namespace pq

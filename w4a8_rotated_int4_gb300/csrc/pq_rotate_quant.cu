@@ -5,18 +5,22 @@
 // Source: "ParoQuant (PARO) W4A8 on gfx1201 -- engineering log", "Design"
 // items 2 (per-group fp8 activation scales, no cross-block sync) and 3 (fused
 // prologue; records read once per chunk; row-sum = sum of what the codes decode
-// to), "Gates passed" (scale = amax * (1/448.f), bit-exact to a CPU reference),
-// and "2026-09-15: hardware e4m3 convert" (NaN -> 0, -0 -> +0, clamp +-448,
-// then the hardware round-to-nearest-even convert).
+// to), "Gates passed" (the scale is amax times the fp32 reciprocal of 448; the
+// outputs match a CPU evaluation bit for bit) and "2026-09-15: hardware e4m3
+// convert" (the hardware round-to-nearest-even convert, wrapped so that a NaN
+// gives code zero, a negative zero gives positive zero and magnitudes
+// saturate at 448).
 //
-// Layout on the GPU (M > 16).  One CTA owns a tile of 32 tokens x one
-// 128-group and loops over the partitions; the records of (p, g) are decoded
-// once into shared-memory offsets and fp32 cos/sin.  The tile is held in shared memory as
-// v[k][token] (fp32), token fastest: in a Givens layer every warp works on one
-// pair (i, j) at a time with lane = token, so the 32 lanes read v[i][0..31]
-// and v[j][0..31] -- consecutive words, free of bank conflicts whatever the
-// pair permutation is.  Each of the 8 warps takes 8 of the 64 disjoint pairs
-// of a layer; the layers are separated by __syncthreads.  Every multiply, add,
+// Layout on the GPU (M > 16).  One CTA owns a tile of 64 tokens x one
+// 128-group x one partition (the partition is the grid's z dimension); the
+// records of (p, g) are decoded once into shared-memory byte offsets and f16
+// cos/sin.  The tile is held in shared memory as v[k][token pair] (two fp32
+// values, tokens 2l and 2l+1, per 8-byte word): in a Givens layer lane l of a
+// warp works on its two tokens of one pair (i, j) at a time, so the 32 lanes
+// read v[i][0..31] and v[j][0..31] -- consecutive 8-byte words, free of bank
+// conflicts whatever the pair permutation is.  Each of the 8 warps takes 8
+// of the 64 disjoint pairs of a layer (in two batches of 4: all loads, then
+// all stores); the layers are separated by __syncthreads.  Every multiply, add,
 // subtract and divide is a separately rounded IEEE operation (explicit .rn
 // intrinsics), so results are bit-identical to an fp32 CPU evaluation in the
 // same order.
@@ -50,7 +54,7 @@ __device__ __forceinline__ void sts_f32x2(uint32_t addr, float2 f) {
 
 // Many tokens: lane l holds tokens 2l and 2l+1 of the CTA's 64 (adjacent, so
 // every shared-memory access moves both with one 8-byte instruction); warp w
-// rotates pairs 16w..16w+15 of every layer.
+// rotates pairs 8w..8w+7 of every layer.
 constexpr int kTok = 64;              // tokens per CTA
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
@@ -596,7 +600,7 @@ add_rms_norm_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__
 
 // ---------------------------------------------------------------------------
 // silu-mul producer ("2026-09-03: rotation stream 2 (silu-mul, GDN gated norm,
-// attention gate fused with rotate+quant)", MODE 0): the merged gate/up
+// attention gate fused with rotate+quant)", its first mode): the merged gate/up
 // output y holds g in columns [0, I) and u in [I, 2I);
 //   act = bf16(bf16(g / (1 + exp(-g))) * u),  then the pq_rotate_quant steps
 // on act (K = I).  exp is the fixed sequence below, so the result is the
