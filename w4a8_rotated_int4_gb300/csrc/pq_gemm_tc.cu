@@ -86,13 +86,6 @@ constexpr uint32_t kSzBytes = BN * 4;
 constexpr uint32_t kTxBytes = kABytes + kBpBytes + kSzBytes;
 constexpr uint32_t kTmemCols = 512;    // 2 buffers x 2 halves x 128 columns
 
-// The zero-point MMA's operands: K = 16 bf16 per row (only k = 0..2 are
-// nonzero), K-major without swizzle: core matrices of 8 rows x 16 bytes, the
-// k = 0..7 one at (row / 8) * 256 + (row % 8) * 16 and the k = 8..15 one
-// (always zero) 128 bytes after it.
-constexpr uint32_t kZLbo = 128, kZSbo = 256;
-constexpr uint32_t kZaBytes = BM * 32, kZbBytes = BN * 32;
-
 // int5 weights: the fifth bits of the slab, 128 rows x 16 B (one bit per k)
 constexpr uint32_t kBhBytes = BN * BK / 8;
 
@@ -102,33 +95,30 @@ struct __align__(1024) StageT {
     uint8_t bx[kBxBytes];     // 128 rows x 128 B, SWIZZLE_128B (expand warps)
     uint8_t bp[kBpBytes];     // 128 rows x 64 B packed nibbles (TMA)
     uint32_t sz[BN];          // f16 (sc, zscale) per column
-    uint8_t zb[kZbBytes];     // zero-point operand per column (expand warps)
     uint8_t bh[kBits == 5 ? kBhBytes : 16];   // int5: fifth-bit planes (TMA)
 };
 
 // fp32 scales of one slab for the fold warps, in a ring of their own so a
 // stage is free as soon as its MMAs complete (the fold lags the MMA).  The
 // column part comes from the expansion warps; the row part is copied straight
-// from global memory by the row warp (cp.async), which runs up to a ring's
-// depth ahead, so no global-load latency reaches the fold warps.  int5 keeps
-// three slots (its stages carry the fifth-bit tiles).
-constexpr int kSzfRingMax = 4;
-template <int kBits>
-constexpr int kSzfRingOf = kBits == 5 ? 3 : 4;
+// from global memory by the row warps (cp.async), which run up to a ring's
+// depth ahead, so no global-load latency reaches the fold warps.
+constexpr int kSzfRing = 4;
 struct __align__(16) SzfSlot {
-    float2 sc[BN / 2];        // (2^9 sc'[n], 2^9 sc'[n+1]) for even n (sc' = sc, or 1 where sc = 0)
-    float row[BM];            // asg of tile row i (0 past M)
-    float rsv[BM];            // rs of tile row i (0 past M), staging for za
-    uint8_t za[kZaBytes];     // zero-point operand per row (row warp)
+    // column pair j (columns 2j, 2j+1): (2^9 sc, 2^9 sc', -zs8, -zs8') with
+    // zs8 = zscale + 8 sc (int4) or zscale (int5)
+    float4 col[BN / 2];
+    float row[BM];            // asg of tile row i (0 past M); per-token: unused
+    float rsv[BM];            // rs of tile row i (0 past M)
 };
 
 struct Ctrl {
     uint64_t full_tma[kStages];
     uint64_t full_b[kStages];
     uint64_t empty[kStages];
-    uint64_t szf_full[kSzfRingMax];
-    uint64_t szf_empty[kSzfRingMax];
-    uint64_t rows_full[kSzfRingMax];   // the row warps' copies of a slab's asg and rs have landed
+    uint64_t szf_full[kSzfRing];
+    uint64_t szf_empty[kSzfRing];
+    uint64_t rows_full[kSzfRing];   // the row warps' copies of a slab's asg and rs have landed
     uint64_t tmem_full[2][2];     // [m-half][accumulator buffer]
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
@@ -137,7 +127,7 @@ struct Ctrl {
 
 template <int kBits>
 constexpr size_t smem_bytes() {
-    return kStages * sizeof(StageT<kBits>) + kSzfRingOf<kBits> * sizeof(SzfSlot) + sizeof(Ctrl) + 1024;
+    return kStages * sizeof(StageT<kBits>) + kSzfRing * sizeof(SzfSlot) + sizeof(Ctrl) + 1024;
 }
 static_assert(smem_bytes<4>() <= 232448 && smem_bytes<5>() <= 232448, "shared memory per CTA");
 
@@ -153,39 +143,46 @@ struct TcParams {
 // ---------------------------------------------------------------- PTX helpers
 using namespace tc;
 constexpr uint32_t kIdesc = idesc_f8(128, BN);     // one M=128 half x BN columns
-constexpr uint32_t kIdescZ = idesc_bf16(128, BN);  // the zero-point MMA of a half
 
 __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsigned int code) {
     if (status) atomicOr(status, code);
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
-// Fold one 16x256b.x4 load: four column pairs for two rows (lo: d[4j..4j+1],
-// hi: d[4j+2..4j+3]).  The accumulator already holds D'' = D' - rs * zq (the
-// zero-point MMA), so acc += (asg * sc) * D'' with z[j] = the sc pair of
-// column pair j and sa = the row's asg splat: two packed operations per two
-// elements.
-__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64_t (&z)[4], uint64_t *acc_lo,
-                                           uint64_t *acc_hi, uint64_t sa_lo, uint64_t sa_hi) {
+// The fold of one 16x256b.x4 load: four column pairs j for two rows (lo:
+// d[4j], d[4j+1]; hi: d[4j+2], d[4j+3]).  The accumulator holds
+// D' = 2^-9 sum_k dec(a) c of the slab, so with z[j] = the (2^9 sc) pair and
+// zz[j] = the -zs8 pair of column pair j, sa = the row's asg splat and
+// ar = the row's asg * rs splat:
+//   acc += (sa * z) * D' + ar * zz = asg * (sc * (D' 2^9) - zs8 * rs)
+// which is asg * (sc * D - zscale * rs) with D = 2^9 D' - 8 rs the sum over
+// (c - 8) (int5: c - 16 is fed directly and zs8 = zscale).  Three packed
+// operations per two elements.
+__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64_t (&z)[4], const uint64_t (&zz)[4],
+                                           uint64_t *acc_lo, uint64_t *acc_hi, uint64_t sa_lo, uint64_t sa_hi,
+                                           uint64_t ar_lo, uint64_t ar_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint64_t t_lo = fmul2v(sa_lo, z[j]), t_hi = fmul2v(sa_hi, z[j]);
-        acc_lo[j] = ffma2v(t_lo, f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), acc_lo[j]);
-        acc_hi[j] = ffma2v(t_hi, f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                           acc_hi[j]);
+        acc_lo[j] = ffma2v(fmul2v(sa_lo, z[j]), f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
+                           ffma2v(ar_lo, zz[j], acc_lo[j]));
+        acc_hi[j] = ffma2v(fmul2v(sa_hi, z[j]),
+                           f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                           ffma2v(ar_hi, zz[j], acc_hi[j]));
     }
 }
 
-// The per-token fold: the accumulator holds D'' and the token scale is
-// applied in the epilogue, so acc += (2^9 sc') * D'': one packed operation
-// per two elements.
-__device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const uint64_t (&z)[4], uint64_t *acc_lo,
-                                               uint64_t *acc_hi) {
+// The per-token fold: the token scale is applied in the epilogue and rs is
+// the plain row-sum, so acc += z * D' + rs * zz: two packed operations per two
+// elements.
+__device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const uint64_t (&z)[4],
+                                               const uint64_t (&zz)[4], uint64_t *acc_lo, uint64_t *acc_hi,
+                                               uint64_t rs_lo, uint64_t rs_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        acc_lo[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), acc_lo[j]);
+        acc_lo[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
+                           ffma2v(rs_lo, zz[j], acc_lo[j]));
         acc_hi[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                           acc_hi[j]);
+                           ffma2v(rs_hi, zz[j], acc_hi[j]));
     }
 }
 
@@ -240,10 +237,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmH,
           const TcParams prm) {
     using Stage = StageT<kBits>;
-    constexpr int kSzfRing = kSzfRingOf<kBits>;
     constexpr uint32_t kTx = kTxBytes + (kBits == 5 ? kBhBytes : 0u);
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base (SWIZZLE_128B tiles), offset from the shared
+    // array itself so that every access stays a shared-memory instruction
+    const uint32_t smem_off = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + (((smem_off + 1023u) & ~1023u) - smem_off);
     Stage *stg = reinterpret_cast<Stage *>(base);
     SzfSlot *szf = reinterpret_cast<SzfSlot *>(base + kStages * sizeof(Stage));
     Ctrl *ctl = reinterpret_cast<Ctrl *>(base + kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot));
@@ -276,14 +275,6 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         ctl->abort = 0;
         fence_mbar_init();
     }
-    // the zero-point operands' k = 3..15 stay zero for the whole launch; the
-    // roles rewrite only k = 0..2 of each row
-    for (int s = 0; s < kStages; ++s)
-        for (uint32_t o = threadIdx.x * 16; o < kZbBytes; o += kThreads * 16)
-            *reinterpret_cast<uint4 *>(stg[s].zb + o) = make_uint4(0u, 0u, 0u, 0u);
-    for (int r = 0; r < kSzfRing; ++r)
-        for (uint32_t o = threadIdx.x * 16; o < kZaBytes; o += kThreads * 16)
-            *reinterpret_cast<uint4 *>(szf[r].za + o) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -381,10 +372,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // full_tma: the expand warps waited for the stage's copies before they
         // arrived on full_b, after writing the zero-point operands.
         int committed = 0;
+        // the bounded waits below start their clocks only once the preceding
+        // kernel has completed, so a long predecessor cannot run them out
+        pdl_wait();
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages, use = it / kStages;
             const int b = it & 1, tuse = it >> 1;
-            const int r = it % kSzfRing;
             // the accumulator's first use waits on nothing: the phase before
             // the first reads as complete
             const bool ok = __all_sync(0xFFFFFFFFu,
@@ -398,27 +391,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint64_t ad0 = desc_sw128(smem_u32(stg[s].a));
             const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
             const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
-            const uint64_t za0 = desc_noswz(smem_u32(szf[r].za), kZLbo, kZSbo);
-            const uint64_t za1 = desc_noswz(smem_u32(szf[r].za + kZaBytes / 2), kZLbo, kZSbo);
-            const uint64_t zbd = desc_noswz(smem_u32(stg[s].zb), kZLbo, kZSbo);
             const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
             const bool half_item = is_half_item<!kTok>(it / G, ntiles);
             if (elect_one()) {
                 // half 0, then half 1, each committed on its own so the two
-                // fold warp groups start half a slab apart; each half's chain
-                // ends with the zero-point MMA (bf16, K = 16).  A half item
+                // fold warp groups start half a slab apart.  A half item
                 // issues half 0 only; half 1's commit still signals its fold
                 // warps, which then only release the buffer.
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)   // +32 bytes along K inside the swizzle row
                     mma_f8(d0, ad0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
-                mma_bf16(d0, za0, zbd, kIdescZ, 1u);
                 mma_commit(&ctl->tmem_full[0][b]);
                 if (!half_item) {
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk)
                         mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
-                    mma_bf16(d1, za1, zbd, kIdescZ, 1u);
                 }
                 // A stage that is never refilled gets no release: nothing would wait
                 // for that arrival, and an arrival still in flight when the CTA
@@ -443,16 +430,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // ------------------------------------------------ nibble expansion
         const int et = threadIdx.x - kFoldWarps * 32;    // 0..127
         const int chunk = et & 7;
+        pdl_wait();        // as for the MMA warp: the wait clocks start after the predecessor
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages, use = it / kStages;
             const int r = it % kSzfRing, ruse = it / kSzfRing;
-            // the stage's copies, the ring slot free (its previous slab folded;
-            // the phase before the first reads as complete) and the slab's row
-            // copies landed; warp-uniform, so the warp stays converged for its
-            // votes and syncs
-            if (!__all_sync(0xFFFFFFFFu,
-                            wait3_or_abort(&ctl->full_tma[s], use & 1, &ctl->szf_empty[r], (ruse - 1) & 1,
-                                           &ctl->rows_full[r], ruse & 1, abort_flag))) {
+            // the stage's copies and the ring slot free (its previous slab
+            // folded; the phase before the first reads as complete);
+            // warp-uniform, so the warp stays converged for its votes and syncs
+            if (!__all_sync(0xFFFFFFFFu, wait2_or_abort(&ctl->full_tma[s], use & 1, &ctl->szf_empty[r],
+                                                        (ruse - 1) & 1, abort_flag))) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
@@ -468,12 +454,6 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if constexpr (kBits == 5)
                     hb[i] = *reinterpret_cast<const uint16_t *>(st.bh + ((et >> 3) + 16 * i) * (BK / 8) + chunk * 2);
             }
-            // A column with sc = 0 dequantizes to -zs whatever its codes, so its
-            // codes must not reach the MMA: the fold then scales it by 1 and
-            // the zero-point MMA alone gives -zs * rs.  Lane l checks row
-            // 4w + l % 4 + 16 (l / 4) of this warp's 32 rows.
-            const bool any_zero_sc = __any_sync(
-                0xFFFFFFFFu, (st.sz[4 * (et >> 5) + (lane & 3) + 16 * (lane >> 2)] & 0x7FFFu) == 0u);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = (et >> 3) + 16 * i;
@@ -482,40 +462,20 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     e = expand16_int5(pk[i], hb[i]);
                 else
                     e = expand16(pk[i]);
-                if (any_zero_sc && (st.sz[row] & 0x7FFFu) == 0u) e = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
             }
-            // the zero-point MMA's column operand (zh, zm, zh, zl, zh, zm) in
-            // bf16 parts of zq = 2^-9 (zscale + 8 sc) / sc', sc' = sc, or 1 where
-            // sc = 0 (2^-9: the unit of the MMA's sum, see expand16); one
-            // column per thread.  zq only corrects, so a division to 2 ulp
-            // (about 2^-23) is accurate enough.  int5 feeds c - 16 itself
-            // (expand16_int5), so its zq is 2^-9 zscale / sc'.
-            const float sc = f16lo(wcol);
-            const float sce = sc != 0.0f ? sc : 1.0f;
+            // the fold's column values of column et: 2^9 sc (the MMA sums
+            // a * c * 2^-9, see expand16) and -zs8 with zs8 = zscale + 8 sc
+            // (int4: the MMA sums raw c, so the -8 moves here; int5 feeds
+            // c - 16 itself).  A column with sc = 0 gets 2^9 sc = 0, so it
+            // contributes -zscale * rs alone whatever its (finite) sum.
             {
-                const float zoff = kBits == 5 ? f16hi(wcol) : f16hi(wcol) + 8.0f * sc;
-                const float zq = __fdividef(zoff, sce) * (1.0f / kNibbleScale);
-                uint32_t h, m, l;
-                bf16_split3(zq, h, m, l);
-                *reinterpret_cast<uint4 *>(st.zb + (et >> 3) * kZSbo + (et & 7) * 16) =
-                    make_uint4(h | (m << 16), h | (l << 16), h | (m << 16), 0u);
+                const float sc = f16lo(wcol);
+                const float zs8 = kBits == 5 ? f16hi(wcol) : f16hi(wcol) + 8.0f * sc;
+                float *cv = reinterpret_cast<float *>(&szf[r].col[et >> 1]);
+                cv[et & 1] = kNibbleScale * sc;
+                cv[2 + (et & 1)] = -zs8;
             }
-            // the zero-point MMA's row operand for rows et and et + 128: with
-            // rs = h + m + l and zq = zh + zm + zl (bf16 parts, bf16_split3),
-            // k = 0..5 carry -(h, h, m, h, l, m) against (zh, zm, zh, zl, zh, zm),
-            // so the MMA adds -(every product of parts whose orders sum to
-            // <= 2) = -rs * zq to about 2^-24 relative
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int i = et + 128 * u;
-                uint32_t h, m, l;
-                bf16_split3(-szf[r].rsv[i], h, m, l);
-                *reinterpret_cast<uint4 *>(szf[r].za + (i >> 3) * kZSbo + (i & 7) * 16) =
-                    make_uint4(h | (h << 16), m | (h << 16), l | (m << 16), 0u);
-            }
-            // the MMA sums a * c * 2^-9 (expand16), so sc' carries 2^9
-            reinterpret_cast<float *>(szf[r].sc)[et] = kNibbleScale * sce;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -545,8 +505,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     const int it = i * G + kb;
                     const int b = it & 1, tuse = it >> 1;
                     const int r = it % kSzfRing, ruse = it / kSzfRing;
-                    if (!wait2_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
-                                        abort_flag)) {
+                    if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r], ruse & 1,
+                                        &ctl->tmem_full[h][b], tuse & 1, abort_flag)) {
                         if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                         bad = true;
                         break;
@@ -571,8 +531,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int it = i * G + kb;
                 const int b = it & 1, tuse = it >> 1;
                 const int r = it % kSzfRing, ruse = it / kSzfRing;
-                if (!wait2_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
-                                    abort_flag)) {
+                if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r], ruse & 1, &ctl->tmem_full[h][b],
+                                    tuse & 1, abort_flag)) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     bad = true;
                     break;
@@ -584,16 +544,24 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // while step k is folded
                 uint32_t dbuf[2][16];
                 tmem_issue256(taddr, dbuf[0]);
-                uint64_t sa2[4];
-                if constexpr (!kTok) {
+                // per row: asg and asg * rs (per-token: rs) as splats
+                uint64_t sa2[4], ar2[4];
 #pragma unroll
-                    for (int ri = 0; ri < 4; ++ri) {
+                for (int ri = 0; ri < 4; ++ri) {
+                    const float rsv = szf[r].rsv[row0 + 8 * ri];
+                    if constexpr (kTok) {
+                        sa2[ri] = 0;
+                        ar2[ri] = f2pack(rsv, rsv);
+                    } else {
                         const float v = szf[r].row[row0 + 8 * ri];
+                        const float ar = __fmul_rn(v, rsv);
                         sa2[ri] = f2pack(v, v);
+                        ar2[ri] = f2pack(ar, ar);
                     }
                 }
-                const uint64_t *zf = reinterpret_cast<const uint64_t *>(szf[r].sc) + c4;
-                uint64_t z[4];
+                // column pair 8 J + 2 c4 (J = 0..15) of the slab: col[4 J + c4]
+                const float4 *cf = szf[r].col + c4;
+                uint64_t z[4], zz[4];
                 tmem_wait16(dbuf[0]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -608,13 +576,18 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     }
                     if (sh == 0) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) z[j] = zf[4 * (4 * cb + j)];
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 v = cf[4 * (4 * cb + j)];
+                            z[j] = f2pack(v.x, v.y);
+                            zz[j] = f2pack(v.z, v.w);
+                        }
                     }
                     if constexpr (kTok)
-                        fold_block_tok(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb);
+                        fold_block_tok(dbuf[cur], z, zz, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb,
+                                       ar2[2 * sh], ar2[2 * sh + 1]);
                     else
-                        fold_block(dbuf[cur], z, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
-                                   sa2[2 * sh + 1]);
+                        fold_block(dbuf[cur], z, zz, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
+                                   sa2[2 * sh + 1], ar2[2 * sh], ar2[2 * sh + 1]);
                     if (k + 1 < 8) tmem_wait16(dbuf[cur ^ 1]);
                 }
                 __syncwarp();

@@ -163,7 +163,10 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     using Stage = StageT<kBits>;
     constexpr uint32_t kTx = kTxBytes + (kBits == 5 ? kBhBytes : 0u);
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base (SWIZZLE_128B tiles), offset from the shared
+    // array itself so that every access stays a shared-memory instruction
+    const uint32_t smem_off = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + (((smem_off + 1023u) & ~1023u) - smem_off);
     Stage *stg = reinterpret_cast<Stage *>(base);
     SzfSlot *szf = reinterpret_cast<SzfSlot *>(base + kStages * sizeof(Stage));
     RowSlot *rows = reinterpret_cast<RowSlot *>(base + kStages * sizeof(Stage) + kSzfRing * sizeof(SzfSlot));
