@@ -265,6 +265,27 @@ def _capture(torch, fn):
     return g
 
 
+def time_graph(torch, g, calls_per_replay, stream, min_ms=150.0, min_reps=5, max_reps=2000):
+    """Replays graph g (already warm) back to back, one CUDA-event pair per
+    replay on `stream`, for at least min_ms of device time and min_reps
+    replays (the count is set from one probe replay).  Returns ms per call:
+    (mean, median, best)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    b.synchronize()
+    n = int(min(max_reps, max(min_reps, min_ms / max(a.elapsed_time(b), 1e-3) + 1)))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per = [e0.elapsed_time(e1) / calls_per_replay for e0, e1 in ev]
+    return float(np.mean(per)), float(np.median(per)), float(np.min(per))
+
+
 def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=None):
     """Times exactly `steps` steps replayed from CUDA graphs (one graph holds one
     step per input copy, so consecutive steps never share inputs), then the two
@@ -299,18 +320,13 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
     if barrier:
         barrier()
     total_ms = e0.elapsed_time(e1)
-    reps = max(1, steps // C // 2)
-    per = {}
+    per, stats = {}, {}
     for key, g in (("pro", g_pro), ("gemm", g_gem)):
         g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        per[key] = a.elapsed_time(b) / (reps * C)
+        mean, med, best = time_graph(torch, g, C, stream)
+        per[key] = mean
+        stats[key] = (mean, med, best)
 
     def time_each(call):
         """ms per call of call(pq, j, None), from a graph of one call per copy"""
@@ -320,22 +336,16 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
         g = _capture(torch, lambda: [call(pq, j, None) for j in range(C)])
         g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / (reps * C)
+        return time_graph(torch, g, C, stream, min_ms=60.0)[0]
 
     # the fused producer (residual add + RMSNorm + rotate + quant) on its own
     wl.producer_buffers(torch, wl.x[0].device)
     per["prod"] = time_each(wl.producer)
     # the silu-mul producer on its own
     per["silu"] = time_each(wl.silu_producer)
-    paths = time_gemm_paths(pq, torch, wl, reps, stream) if wl.c["M"] <= 16 else {}
+    paths = time_gemm_paths(pq, torch, wl, stream) if wl.c["M"] <= 16 else {}
     out = dict(total_ms=total_ms, wall_s=wall, pro_ms=per["pro"], gemm_ms=per["gemm"], paths=paths,
-               prod_ms=per["prod"], silu_ms=per["silu"])
+               prod_ms=per["prod"], silu_ms=per["silu"], stats=stats)
     # the same GEMM on int5 weights
     wl.int5_buffers(pq, torch, wl.x[0].device)
     out["int5_gemm_ms"] = time_each(wl.gemm5)
@@ -347,9 +357,10 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
     return out
 
 
-def time_gemm_paths(pq, torch, wl, reps, stream):
+def time_gemm_paths(pq, torch, wl, stream):
     """GEMM-only time per launch (ms) of every kernel that accepts this M,
-    each from a graph of one launch per input copy, replayed `reps` times."""
+    each from a graph of one launch per input copy, replayed for at least
+    60 ms."""
     M = wl.c["M"]
     paths = [("tc", pq.pq_gemm_tc)]
     if M <= pq.pq_gemm_skinny_max_m():
@@ -360,13 +371,7 @@ def time_gemm_paths(pq, torch, wl, reps, stream):
         g = _capture(torch, lambda: [wl.gemm(pq, j, None, fn) for j in range(C)])
         g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        out[name] = a.elapsed_time(b) / (reps * C)
+        out[name] = time_graph(torch, g, C, stream, min_ms=60.0)[0]
     return out
 
 
@@ -468,7 +473,13 @@ def ncu_traffic(kernel, workload):
 KERNEL_NAMES = {"skinny": "pq_gemm_skinny", "tcn": "pq_gemm_tcn", "tcgen05": "pq_gemm_tc"}
 
 
-def roofline(wl, r, peaks, traffic=None):
+# Dense FP8 MMA throughput per SM and clock: an isolated probe kernel issued
+# tcgen05 m128n128k32 e4m3 MMAs back to back at one per 64 cycles
+# (2 * 128 * 128 * 32 / 64 = 16384 FLOP per cycle per SM).
+FP8_FLOP_PER_CLK_SM = 16384
+
+
+def roofline(wl, r, peaks, traffic=None, sm_mhz=None, sms=None):
     if wl.gemm_kernel in ("skinny", "tcn"):      # decode band: weights streamed once
         achieved = wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9
         return {"kernel": KERNEL_NAMES[wl.gemm_kernel], "bound": "hbm", "achieved": round(achieved, 1),
@@ -476,17 +487,28 @@ def roofline(wl, r, peaks, traffic=None):
                 "peak_source": peaks["src"] + " (hbm_gbs)", "traffic": traffic}
     fp8_peak = 2.0 * peaks["bf16"]
     achieved = wl.flops / (r["gemm_ms"] * 1e-3) / 1e12
-    return {"kernel": "pq_gemm_tc", "bound": "tensor", "achieved": round(achieved, 1),
-            "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-            "peak_source": peaks["src"] + " bf16_tflops x 2 (dense fp8 : bf16 nominal ratio)",
-            "traffic": traffic}
+    out = {"kernel": "pq_gemm_tc", "bound": "tensor", "achieved": round(achieved, 1),
+           "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+           "peak_source": peaks["src"] + " bf16_tflops x 2 (dense fp8 : bf16 nominal ratio)",
+           "traffic": traffic}
+    if sm_mhz and sms:
+        # the same against the FP8 rate the tensor cores reach at the SM clock
+        # sampled during this workload's timing
+        clk_peak = FP8_FLOP_PER_CLK_SM * sms * sm_mhz * 1e6 / 1e12
+        out["peak_at_sampled_clock"] = round(clk_peak, 1)
+        out["frac_at_sampled_clock"] = round(achieved / clk_peak, 4)
+    return out
 
 
-def summarize(wl, r, steps, peaks):
+def summarize(wl, r, steps, peaks, clocks=None, sms=None):
     step_us = r["total_ms"] * 1e3 / steps
+    st = r.get("stats", {})
     return {
         "workload": wl.label, "us_per_step": round(step_us, 3),
         "prologue_us": round(r["pro_ms"] * 1e3, 3), "gemm_us": round(r["gemm_ms"] * 1e3, 3),
+        # per-launch times over the replays: mean (used above), median, best
+        "prologue_us_median_best": [round(v * 1e3, 3) for v in st["pro"][1:]] if "pro" in st else None,
+        "gemm_us_median_best": [round(v * 1e3, 3) for v in st["gemm"][1:]] if "gemm" in st else None,
         "gemm_kernel": wl.gemm_kernel,
         "gemm_tflops": round(wl.flops / (r["gemm_ms"] * 1e-3) / 1e12, 2),
         "gemm_gbs": round(wl.gemm_bytes / (r["gemm_ms"] * 1e-3) / 1e9, 1),
@@ -496,7 +518,9 @@ def summarize(wl, r, steps, peaks):
         "producer_gbs": round(wl.prod_bytes / (r["prod_ms"] * 1e-3) / 1e9, 1),
         # the silu-mul producer (silu(gate) * up + rotate + quant, I = K) alone
         "silu_producer_us": round(r["silu_ms"] * 1e3, 3),
-        "roofline": roofline(wl, r, peaks, ncu_traffic(KERNEL_NAMES[wl.gemm_kernel], wl.name)),
+        "roofline": roofline(wl, r, peaks, ncu_traffic(KERNEL_NAMES[wl.gemm_kernel], wl.name),
+                             (clocks or {}).get("sm_mhz"), sms),
+        "clocks": clocks,
         # per-token activation scales (M > 16): prologue (two passes) and GEMM
         "ptok": ({"prologue_us": round(r["ptok_pro_ms"] * 1e3, 3), "gemm_us": round(r["ptok_gemm_ms"] * 1e3, 3),
                   "gemm_tflops": round(wl.flops / (r["ptok_gemm_ms"] * 1e-3) / 1e12, 2),
@@ -521,9 +545,11 @@ class OracleSample:
     so one step takes about `step_budget_s`.  Inputs are generated and packed
     once."""
 
-    def __init__(self, name, M=None, step_budget_s=1.0):
+    def __init__(self, name, M=None, step_budget_s=1.0, threads=None):
         import oracle
         self.oracle = oracle
+        self.threads = threads
+        self._use_threads()
         c, self.label = describe(name, M)
         self.c = c
         self.prob = pqgen.make_problem(**c)
@@ -566,7 +592,12 @@ class OracleSample:
         self.oracle.gemm_f64(self.a, self.asg, self.rs, self.codes, self.sz, pb[0], pb[1])
         return time.perf_counter() - t0
 
+    def _use_threads(self):
+        if self.threads is not None:
+            self.oracle.set_num_threads(self.threads)
+
     def step_us(self):
+        self._use_threads()
         t_pro = self._time_prologue() * (self.c["M"] / self.mtok)
         t_g = self._gemm() * (self.c["N"] / self.ncols)
         return (t_pro + t_g) * 1e6
@@ -576,7 +607,50 @@ class OracleSample:
                 "both scaled to the whole workload" % (self.mtok, self.c["M"], self.ncols, self.c["N"]))
 
     def cores(self):
+        self._use_threads()
         return self.oracle.num_threads()
+
+
+def cpu_model():
+    """The host CPU's model from /proc/cpuinfo (Arm cores report implementer
+    and part numbers instead of a model name)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in info.splitlines():
+        k, _, v = line.partition(":")
+        fields.setdefault(k.strip(), v.strip())
+    if fields.get("model name"):
+        return fields["model name"]
+    parts = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+             ("0x41", "0xd0c"): "Arm Neoverse-N1"}
+    imp, part = fields.get("CPU implementer"), fields.get("CPU part")
+    if imp and part:
+        return parts.get((imp, part), "Arm implementer %s part %s" % (imp, part))
+    return "unknown"
+
+
+def cpu_baseline(name, M, budget_s=4.0, reps=3):
+    """The oracle on the host cores: all hardware threads (OpenMP) and one
+    thread, each on a bounded sample of the workload scaled to the whole
+    workload; median and best of `reps` steps."""
+    import oracle
+    n_all = oracle.num_threads()
+    out = {}
+    for key, threads, budget in (("all", n_all, budget_s), ("single", 1, budget_s / 2)):
+        orc = OracleSample(name, M, step_budget_s=budget, threads=threads)
+        v = [orc.step_us() for _ in range(reps)]
+        out[key] = dict(median=float(np.median(v)), best=float(np.min(v)), cores=orc.cores(),
+                        sample=orc.describe())
+    oracle.set_num_threads(n_all)
+    a, one = out["all"], out["single"]
+    return {"value": round(a["median"], 1), "unit": "us", "cores": a["cores"], "kind": "oracle",
+            "sample": a["sample"] + ", median of %d" % reps, "best": round(a["best"], 1),
+            "cpu_model": cpu_model(),
+            "single_thread": {"value": round(one["median"], 1), "best": round(one["best"], 1), "cores": 1,
+                              "sample": one["sample"] + ", median of %d" % reps}}
 
 
 # ---------------------------------------------------------------- main
@@ -646,7 +720,7 @@ def main():
                 "vs_baseline": None, "dtype": "f32 prologue, f64 GEMM (CPU oracle)",
                 "data": "synthetic", "config": {"workload": label},
                 "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": cores,
-                                 "kind": "oracle", "sample": desc},
+                                 "kind": "oracle", "sample": desc, "cpu_model": cpu_model()},
                 "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -664,6 +738,7 @@ def main():
     barrier = (lambda: dist.barrier()) if dist else None
 
     wl = Workload(pq, torch, name, M, dev)
+    sms = torch_sms(torch)
     sampler = ClockSampler(local) if rank == 0 else None
     r = time_workload(pq, torch, wl, args.steps, args.warmup, stream, barrier, sampler)
     total_ms, value = combine_ranks(r["total_ms"], args.steps, ws, dist, dev)
@@ -672,7 +747,8 @@ def main():
         pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, dev)
     e2e_graph_ms = None if args.no_e2e else e2e_graph_workload(
         pq, torch, wl, max(50, args.steps // 10), args.warmup, stream)
-    head = summarize(wl, dict(r, total_ms=total_ms), args.steps, peaks)
+    clocks = sampler.summary() if sampler else {}
+    head = summarize(wl, dict(r, total_ms=total_ms), args.steps, peaks, clocks, sms)
 
     extra = []
     if not args.no_extra:
@@ -680,14 +756,16 @@ def main():
             if (en, em) == (name, M):
                 continue
             w2 = Workload(pq, torch, en, em, dev)
-            r2 = time_workload(pq, torch, w2, args.extra_steps, args.warmup, stream, barrier)
-            extra.append(summarize(w2, r2, args.extra_steps, peaks))
+            # clocks sampled over this workload's whole timing (steps and kernels)
+            s2 = ClockSampler(local) if rank == 0 else None
+            with (s2 if s2 is not None else _Null()):
+                r2 = time_workload(pq, torch, w2, args.extra_steps, args.warmup, stream, barrier)
+            extra.append(summarize(w2, r2, args.extra_steps, peaks, s2.summary() if s2 else None, sms))
             del w2
             torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    clocks = sampler.summary() if sampler else {}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "us", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_us / 1e3, 6),
@@ -715,10 +793,7 @@ def main():
         "peaks": peaks,
     }
     if not args.no_cpu_baseline:
-        orc = OracleSample(name, M, step_budget_s=4.0)
-        us = float(np.mean([orc.step_us() for _ in range(3)]))
-        line["cpu_baseline"] = {"value": round(us, 1), "unit": "us", "cores": orc.cores(),
-                                "kind": "oracle", "sample": orc.describe() + ", mean of 3"}
+        line["cpu_baseline"] = cpu_baseline(name, M)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -76,7 +76,8 @@ constexpr int BM = 256, BN = 128, BK = 128;    // BM = two M=128 MMA halves
 constexpr int kStages = 3;
 constexpr int kFoldWarps = 8;     // warps 0..7: warp w folds rows 128(w/4) + 32(w%4)..+31, all columns
 constexpr int kExpWarps = 4;      // warps 8..11
-constexpr int kTmaWarp = 12, kMmaWarp = 13, kRowWarp = 14;   // row warps 14 and 15: tile half 0, 1
+// row warps 12 and 13 (tile half 0, 1), TMA warp 14, MMA warp 15
+constexpr int kRowWarp = 12, kTmaWarp = 14, kMmaWarp = 15;
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kFoldRegs = 216, kOtherRegs = 40;   // 256 * 216 + 256 * 40 = 65536
 constexpr uint32_t kABytes = BM * BK;
@@ -149,6 +150,19 @@ __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsig
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+// Packed fp32 pair operations for the fold; not volatile, so the compiler
+// interleaves the independent chains of a step.
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // The fold of one 16x256b.x4 load: four column pairs j for two rows (lo:
 // d[4j], d[4j+1]; hi: d[4j+2], d[4j+3]).  The accumulator holds
 // D' = 2^-9 sum_k dec(a) c of the slab, so with z[j] = the (2^9 sc) pair and
@@ -163,11 +177,11 @@ __device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64
                                            uint64_t ar_lo, uint64_t ar_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        acc_lo[j] = ffma2v(fmul2v(sa_lo, z[j]), f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
-                           ffma2v(ar_lo, zz[j], acc_lo[j]));
-        acc_hi[j] = ffma2v(fmul2v(sa_hi, z[j]),
+        acc_lo[j] = ffma2(fmul2(sa_lo, z[j]), f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
+                           ffma2(ar_lo, zz[j], acc_lo[j]));
+        acc_hi[j] = ffma2(fmul2(sa_hi, z[j]),
                            f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                           ffma2v(ar_hi, zz[j], acc_hi[j]));
+                           ffma2(ar_hi, zz[j], acc_hi[j]));
     }
 }
 
@@ -179,10 +193,10 @@ __device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const ui
                                                uint64_t rs_lo, uint64_t rs_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        acc_lo[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
-                           ffma2v(rs_lo, zz[j], acc_lo[j]));
-        acc_hi[j] = ffma2v(z[j], f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                           ffma2v(rs_hi, zz[j], acc_hi[j]));
+        acc_lo[j] = ffma2(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
+                           ffma2(rs_lo, zz[j], acc_lo[j]));
+        acc_hi[j] = ffma2(z[j], f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                           ffma2(rs_hi, zz[j], acc_hi[j]));
     }
 }
 
@@ -296,39 +310,51 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             prefetch_map(&tmB);
             prefetch_map(&tmS);
             if constexpr (kBits == 5) prefetch_map(&tmH);
-            int n0, m0, p;
+            // slab coordinates, stepped without divisions: tile ti of this
+            // CTA, group kb
+            int ti = 0, kb = 0, n0 = 0, m0 = 0, p = 0;
             bool half_item;
+            if (total > 0) tile_coords<!kTok>(0, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
+            auto next_slab = [&]() {
+                if (++kb == G) {
+                    kb = 0;
+                    if (++ti < my_tiles) tile_coords<!kTok>(ti, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
+                }
+            };
             // first stages: weights and SZ (load-time tables) before the
             // preceding kernel has finished, activations after pdl_wait
             const int pre = total < kStages ? total : kStages;
+            int pre_kb[kStages], pre_m0[kStages], pre_p[kStages];
             for (int it = 0; it < pre; ++it) {
-                tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
-                const int kb = it % G;
+                pre_kb[it] = kb;
+                pre_m0[it] = m0;
+                pre_p[it] = p;
                 mbar_arrive_expect_tx(&ctl->full_tma[it], kTx);
                 tma_load_2d(stg[it].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[it]);
                 tma_load_2d(stg[it].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[it]);
                 if constexpr (kBits == 5) tma_load_2d(stg[it].bh, &tmH, kb * (BK / 8), n0, &ctl->full_tma[it]);
+                next_slab();
             }
             pdl_wait();
-            for (int it = 0; it < pre; ++it) {
-                tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
-                tma_load_3d(stg[it].a, &tmA, (it % G) * BK, m0, p, &ctl->full_tma[it]);
-            }
+            for (int it = 0; it < pre; ++it)
+                tma_load_3d(stg[it].a, &tmA, pre_kb[it] * BK, pre_m0[it], pre_p[it], &ctl->full_tma[it]);
             int issued = pre;
-            for (int it = pre; it < total; ++it) {
-                const int s = it % kStages, use = it / kStages;
-                if (!wait_or_abort(&ctl->empty[s], (use - 1) & 1, abort_flag)) {
+            for (int it = pre, s = 0, par = 0; it < total; ++it) {   // s = it % kStages, par = (it / kStages - 1) & 1
+                if (!wait_or_abort(&ctl->empty[s], (uint32_t)par, abort_flag)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
-                tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
-                const int kb = it % G;
                 mbar_arrive_expect_tx(&ctl->full_tma[s], kTx);
                 tma_load_3d(stg[s].a, &tmA, kb * BK, m0, p, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].bp, &tmB, kb * (BK / 2), n0, &ctl->full_tma[s]);
                 tma_load_2d(stg[s].sz, &tmS, 8 * kb, n0 / 8, &ctl->full_tma[s]);
                 if constexpr (kBits == 5) tma_load_2d(stg[s].bh, &tmH, kb * (BK / 8), n0, &ctl->full_tma[s]);
                 issued = it + 1;
+                next_slab();
+                if (++s == kStages) {
+                    s = 0;
+                    par ^= 1;
+                }
             }
             if (*abort_flag) {   // let issued copies land before shared memory is released
                 for (int s = 0; s < kStages && s < issued; ++s) {
@@ -338,31 +364,49 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
             }
         }
-    } else if (warp >= kRowWarp) {
+    } else if (warp == kRowWarp || warp == kRowWarp + 1) {
         // ------------------------------------------------ per-row scales
         // asg and rs of a slab's rows by cp.async into the slab's ring slot,
-        // up to a ring's depth ahead; the expansion warps turn rs into the
-        // zero-point MMA's row operand.  Row warp hw copies tile half hw.
-        const int row0 = (BM / 2) * (warp - kRowWarp);
+        // up to a ring's depth ahead.  Row warp hw copies tile half hw; lane
+        // l copies rows 128 hw + l + 32 u (u = 0..3).  Coordinates and row
+        // pointers are stepped per slab without divisions.
+        const int row0 = (BM / 2) * (warp - kRowWarp) + lane;
         pdl_wait();        // asg and rs are the preceding prologue's output
-        for (int it = 0; it < total; ++it) {
-            const int r = it % kSzfRing, ruse = it / kSzfRing;
+        int ti = 0, kb = 0, n0 = 0, m0 = 0, p = 0;
+        bool half_item;
+        uint32_t ok = 0;            // bit u: row row0 + 32 u of the tile is below M
+        size_t off = 0;             // (p * G + kb) * M
+        auto tile_start = [&]() {
+            tile_coords<!kTok>(ti, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
+            ok = 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ok |= (m0 + row0 + 32 * u < M ? 1u : 0u) << u;
+            off = (size_t)p * G * (size_t)M;
+        };
+        if (total > 0) tile_start();
+        for (int it = 0, r = 0, ruse = 0; it < total; ++it) {   // r = it % kSzfRing, ruse = it / kSzfRing
             if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag)) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitEmpty);
                 break;
             }
-            int n0, m0, p;
-            bool half_item;
-            tile_coords<!kTok>(it / G, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
-            const size_t off = ((size_t)p * G + (size_t)(it % G)) * (size_t)M;
+            const float *ga = prm.asg + off + m0 + row0, *gr = prm.rs + off + m0 + row0;
 #pragma unroll
             for (int u = 0; u < BM / 64; ++u) {
-                const int i = row0 + lane + 32 * u, m = m0 + i;
-                const bool ok = m < M;     // rows past M are zero-filled
-                if constexpr (!kTok) cp_async4(&szf[r].row[i], ok ? prm.asg + off + m : prm.asg, ok);
-                cp_async4(&szf[r].rsv[i], ok ? prm.rs + off + m : prm.rs, ok);
+                const bool v = (ok >> u) & 1u;     // rows past M are zero-filled
+                if constexpr (!kTok) cp_async4(&szf[r].row[row0 + 32 * u], v ? ga + 32 * u : prm.asg, v);
+                cp_async4(&szf[r].rsv[row0 + 32 * u], v ? gr + 32 * u : prm.rs, v);
             }
             cp_async_arrive(&ctl->rows_full[r]);
+            if (++kb == G) {
+                kb = 0;
+                if (++ti < my_tiles) tile_start();
+            } else {
+                off += (size_t)M;
+            }
+            if (++r == kSzfRing) {
+                r = 0;
+                ++ruse;
+            }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
     } else if (warp == kMmaWarp) {
@@ -372,6 +416,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // full_tma: the expand warps waited for the stage's copies before they
         // arrived on full_b, after writing the zero-point operands.
         int committed = 0;
+        int tim = 0, kbm = 0;       // tile and group of slab it
+        bool half_item = false;
         // the bounded waits below start their clocks only once the preceding
         // kernel has completed, so a long predecessor cannot run them out
         pdl_wait();
@@ -392,7 +438,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
             const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
             const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
-            const bool half_item = is_half_item<!kTok>(it / G, ntiles);
+            if (kbm == 0) half_item = is_half_item<!kTok>(tim, ntiles);   // once per tile
             if (elect_one()) {
                 // half 0, then half 1, each committed on its own so the two
                 // fold warp groups start half a slab apart.  A half item
@@ -415,6 +461,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             __syncwarp();
             committed = it + 1;
+            if (++kbm == G) {
+                kbm = 0;
+                ++tim;
+            }
         }
         if (*abort_flag && committed > 0 && lane == 0) {   // MMAs and their arrivals must land before exit
             const int it = committed - 1;
@@ -539,11 +589,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + h * BN);
-                // eight steps (32-column block cb, 16-lane half sh), one
-                // 16x256b.x4 load each; the load of step k+1 is in flight
-                // while step k is folded
-                uint32_t dbuf[2][16];
-                tmem_issue256(taddr, dbuf[0]);
+                // four steps (32-column block cb), each two 16x256b.x4 loads
+                // (16-lane halves sh = 0, 1) in flight behind one wait
                 // per row: asg and asg * rs (per-token: rs) as splats
                 uint64_t sa2[4], ar2[4];
 #pragma unroll
@@ -561,34 +608,31 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
                 // column pair 8 J + 2 c4 (J = 0..15) of the slab: col[4 J + c4]
                 const float4 *cf = szf[r].col + c4;
-                uint64_t z[4], zz[4];
-                tmem_wait16(dbuf[0]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int cb = k >> 1, sh = k & 1, cur = k & 1;
-                    if (k + 1 < 8) {
-                        tmem_issue256(taddr + ((uint32_t)(16 * ((k + 1) & 1)) << 16) + 32 * ((k + 1) >> 1),
-                                      dbuf[cur ^ 1]);
-                    } else {       // every load of this buffer has completed
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t d0[16], d1[16];
+                    tmem_issue256(taddr + 32 * cb, d0);
+                    tmem_issue256(taddr + ((uint32_t)16 << 16) + 32 * cb, d1);
+                    uint64_t z[4], zz[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 v = cf[4 * (4 * cb + j)];
+                        z[j] = f2pack(v.x, v.y);
+                        zz[j] = f2pack(v.z, v.w);
+                    }
+                    tmem_wait32(d0, d1);
+                    if (cb == 3) {       // every load of this buffer has completed
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&ctl->tmem_empty[b]);
                     }
-                    if (sh == 0) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 v = cf[4 * (4 * cb + j)];
-                            z[j] = f2pack(v.x, v.y);
-                            zz[j] = f2pack(v.z, v.w);
-                        }
+                    if constexpr (kTok) {
+                        fold_block_tok(d0, z, zz, acc[0] + 4 * cb, acc[1] + 4 * cb, ar2[0], ar2[1]);
+                        fold_block_tok(d1, z, zz, acc[2] + 4 * cb, acc[3] + 4 * cb, ar2[2], ar2[3]);
+                    } else {
+                        fold_block(d0, z, zz, acc[0] + 4 * cb, acc[1] + 4 * cb, sa2[0], sa2[1], ar2[0], ar2[1]);
+                        fold_block(d1, z, zz, acc[2] + 4 * cb, acc[3] + 4 * cb, sa2[2], sa2[3], ar2[2], ar2[3]);
                     }
-                    if constexpr (kTok)
-                        fold_block_tok(dbuf[cur], z, zz, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb,
-                                       ar2[2 * sh], ar2[2 * sh + 1]);
-                    else
-                        fold_block(dbuf[cur], z, zz, acc[2 * sh] + 4 * cb, acc[2 * sh + 1] + 4 * cb, sa2[2 * sh],
-                                   sa2[2 * sh + 1], ar2[2 * sh], ar2[2 * sh + 1]);
-                    if (k + 1 < 8) tmem_wait16(dbuf[cur ^ 1]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->szf_empty[r]);

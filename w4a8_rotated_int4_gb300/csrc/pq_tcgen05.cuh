@@ -283,6 +283,18 @@ __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
+// Wait for the thread's outstanding TMEM loads, carrying two load buffers
+// through the wait so their uses stay after it.
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[16], uint32_t (&t)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(t[0]), "+r"(t[1]), "+r"(t[2]), "+r"(t[3]), "+r"(t[4]),
+                   "+r"(t[5]), "+r"(t[6]), "+r"(t[7]), "+r"(t[8]), "+r"(t[9]), "+r"(t[10]), "+r"(t[11]),
+                   "+r"(t[12]), "+r"(t[13]), "+r"(t[14]), "+r"(t[15])
+                 :
+                 : "memory");
+}
 // 16x256b.x4 TMEM load (no wait): for repetition j (columns 8j..8j+7 of the
 // address), d[4j], d[4j+1] = lane base + g4, columns 8j + 2c4 + {0, 1};
 // d[4j+2], d[4j+3] = lane base + 8 + g4, same columns (g4 = lane / 4, c4 = lane % 4).
