@@ -67,7 +67,7 @@ extern "C" {
  *    pq_gemm_ptok) and int5 weights (pq_pack5, pq_gemm5*); version 1's calls
  *    are unchanged.
  * 3: adds pq_rotate_tokquant_noalloc; earlier calls are unchanged. */
-#define PQ_ABI_VERSION 3
+#define PQ_ABI_VERSION 4
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
@@ -423,6 +423,18 @@ pq_status pq_gemm5_tcn(const void *a, const float *asg, const float *rs, int M, 
  * alignment suffice.  Errors: PQ_ERR_NULL, PQ_ERR_ARCH, PQ_ERR_CUDA.
  */
 pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream);
+
+/*
+ * Test hook, not for production use (the pages have no counterpart).  Sets
+ * the bound of the GEMM kernels' pipeline waits (see dev_status above) for
+ * every launch made after the call, process-wide: ns = 0 restores the
+ * product bound of 2 s; 0 < ns <= 2e9 shortens it, so that on a healthy GPU
+ * the waits give up and the give-up path (status code, NaN tile, release of
+ * tensor memory, return) runs.  The waits that let in-flight copies and MMAs
+ * land after a give-up keep 2 s.  Not thread-safe with respect to launches
+ * on other threads.  Errors: PQ_ERR_SHAPE for ns > 2e9.
+ */
+pq_status pq_test_set_wait_limit_ns(unsigned long long ns);
 
 #ifdef __cplusplus
 }

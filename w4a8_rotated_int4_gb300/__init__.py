@@ -28,7 +28,7 @@ EXPORTS = (
     "pq_gemm_tcn",
     "pq_rotate_tokquant", "pq_rotate_tokquant_noalloc", "pq_gemm_ptok",
     "pq_pack5", "pq_gemm5", "pq_gemm5_tc", "pq_gemm5_tcn",
-    "pq_e4m3_encode",
+    "pq_e4m3_encode", "pq_test_set_wait_limit_ns",
 )
 
 STATUS = {0: "PQ_OK", 1: "PQ_ERR_NULL", 2: "PQ_ERR_SHAPE", 3: "PQ_ERR_ALIGN", 4: "PQ_ERR_PAIRS",
@@ -96,6 +96,8 @@ def lib() -> C.CDLL:
         f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, vp, i32, vp, vp]
     L.pq_e4m3_encode.restype = i32
     L.pq_e4m3_encode.argtypes = [vp, vp, st, vp]
+    L.pq_test_set_wait_limit_ns.restype = i32
+    L.pq_test_set_wait_limit_ns.argtypes = [C.c_ulonglong]
     _lib = L
     return L
 
@@ -480,6 +482,11 @@ def pq_e4m3_encode(x, out=None, stream=None):
     _check(lib().pq_e4m3_encode(_dptr(x), _dptr(out), x.numel(), _stream(stream)),
            "pq_e4m3_encode")
     return out
+
+
+def pq_test_set_wait_limit_ns(ns):
+    """Test hook: the GEMM kernels' pipeline-wait bound in ns (0 = product bound)."""
+    _check(lib().pq_test_set_wait_limit_ns(int(ns)), "pq_test_set_wait_limit_ns")
 
 
 class PQLinear:

@@ -8,6 +8,7 @@
 // 4 (partition select from two boundary columns).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -44,6 +45,17 @@ pq_status fail(pq_status st, const char *fmt, ...) {
 }
 
 void clear_error() { g_err.clear(); }
+
+namespace {
+// 0: the product bound kWaitLimitNs; otherwise the test bound in ns.
+std::atomic<unsigned long long> g_test_wait_ns{0};
+}  // namespace
+
+WaitBound pipeline_wait_bound() {
+    const unsigned long long t = g_test_wait_ns.load(std::memory_order_relaxed);
+    if (t == 0) return WaitBound{kWaitLimitNs, kSuspendHintNs};
+    return WaitBound{t, t < kSuspendHintNs ? (uint32_t)t : kSuspendHintNs};
+}
 
 pq_status check_device(int *sm_count) {
     // Per-device cache of (checked, ok, SMs); devices are few and fixed.
@@ -538,4 +550,11 @@ extern "C" pq_status pq_gemm(const void *a, const float *asg, const float *rs, i
                                   sms);
     }
     return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, sms);
+}
+
+extern "C" pq_status pq_test_set_wait_limit_ns(unsigned long long ns) {
+    clear_error();
+    if (ns > pq::kWaitLimitNs) return pq::fail(PQ_ERR_SHAPE, "wait limit %llu ns above the product bound", ns);
+    pq::g_test_wait_ns.store(ns, std::memory_order_relaxed);
+    return PQ_OK;
 }

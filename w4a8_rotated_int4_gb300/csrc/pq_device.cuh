@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <utility>
 
+#include "pq_internal.h"
+
 namespace pq {
 
 // Programmatic dependent launch.  pdl_wait(): block until the preceding grid
@@ -43,10 +45,6 @@ enum : unsigned int {
     kStatusDrain = 8u,        // copies still in flight when the CTA gave up
 };
 
-// Give up a wait after this many nanoseconds of %globaltimer (never reached by
-// a correct pipeline; it bounds the damage of a bug to one slow launch).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -77,29 +75,37 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// One try_wait; the thread may be suspended by the hardware for up to
-// kSuspendHintNs while the phase is incomplete (it resumes as soon as the
-// phase completes), so waiting warps do not spin on the issue slots.
-constexpr uint32_t kSuspendHintNs = 100000u;
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t hint = kSuspendHintNs) {
     uint32_t ok;
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint)
         : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false if it did not complete within kWaitLimitNs.
+// false if it did not complete within kWaitLimitNs (the drain waits).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA has
+// aborted (a pipeline wait: its bound is the launch's).
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              const WaitBound &wb) {
+    if (mbar_try_wait(bar, parity, wb.hint)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity, wb.hint)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > wb.ns) return false;
     }
 }
 

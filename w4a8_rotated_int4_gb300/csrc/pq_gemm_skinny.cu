@@ -72,6 +72,7 @@ struct SkinnyParams {
     int M, N, K, G, pb1, pb2, ldy;
     int oct_per_cta, n_oct, nkw, ngrp, stages;
     uint32_t stage_bytes, w_bytes;
+    WaitBound wait;           // the pipeline waits' bound
 };
 
 __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_codes) {
@@ -128,8 +129,9 @@ __device__ __forceinline__ void split_step(const float (&in)[NC], float (&out)[N
 // and its SZ words (G x 32 contiguous bytes) with two bulk copies completing
 // on full[s]; a stage is refilled once its consumer group has released it on
 // empty[s].  (Weights and SZ words are load-time tables, not written by the
-// preceding kernel, so they stream before its completion.)
-__device__ __forceinline__ void produce_octets(const SkinnyParams &prm, uint8_t *smem, uint64_t *full,
+// preceding kernel, so they stream before its completion.)  Returns the
+// number of octets issued.
+__device__ __forceinline__ int produce_octets(const SkinnyParams &prm, uint8_t *smem, uint64_t *full,
                                                uint64_t *empty, volatile int *abort_flag, int oct0,
                                                int noct) {
     const int S = prm.stages, K = prm.K, G = prm.G;
@@ -140,7 +142,7 @@ __device__ __forceinline__ void produce_octets(const SkinnyParams &prm, uint8_t 
             ++use;
         }
         if (*abort_flag) break;
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+        if (use > 0 && !wait_or_abort(&empty[s], (use - 1) & 1, abort_flag, prm.wait)) {
             if (prm.status) atomicOr(prm.status, kStatusWaitEmpty);
             *abort_flag = 1;
             break;
@@ -152,13 +154,7 @@ __device__ __forceinline__ void produce_octets(const SkinnyParams &prm, uint8_t 
         bulk_g2s(st + prm.w_bytes, prm.sz + (size_t)o * G * 8, 32u * (uint32_t)G, &full[s]);
         issued = i + 1;
     }
-    // on abort: let every copy already issued land before shared memory is released
-    if (*abort_flag) {
-        for (int s = 0; s < S && s < issued; ++s) {
-            const int last_use = (issued - 1 - s) / S;
-            if (!mbar_wait(&full[s], last_use & 1) && prm.status) atomicOr(prm.status, kStatusDrain);
-        }
-    }
+    return issued;
 }
 
 template <int MT>
@@ -189,8 +185,9 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
     __syncthreads();
 
     pdl_trigger();
+    int issued = 0;     // octets the producer issued, for the drain after a give-up
     if (warp == ngrp * nkw) {
-        if (lane == 0) produce_octets(prm, smem, full, empty, abort_flag, oct0, noct);
+        if (lane == 0) issued = produce_octets(prm, smem, full, empty, abort_flag, oct0, noct);
     } else {
         // ---------------- compute warps ----------------
         const int grp = warp / nkw, kw = warp - grp * nkw;
@@ -246,8 +243,8 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                     }
                 }
             }
-            if (*abort_flag) break;
-            if (!mbar_wait(&full[s], use & 1)) {
+            // warp-uniform: the shuffles below need the whole warp
+            if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&full[s], use & 1, abort_flag, prm.wait))) {
                 if (lane == 0) {
                     if (prm.status) atomicOr(prm.status, kStatusWaitFull);
                     *abort_flag = 1;
@@ -316,6 +313,15 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
 
     // reduce the k-warps in a fixed order and store bf16 rows (NaN after an abort)
     const bool bad = *abort_flag != 0;
+    // after a give-up (the flag is final once every warp has left its loop):
+    // every copy already issued lands before shared memory is released (these
+    // waits keep the full bound)
+    if (bad && warp == ngrp * nkw && lane == 0) {
+        for (int s = 0; s < S && s < issued; ++s) {
+            const int last_use = (issued - 1 - s) / S;
+            if (!mbar_wait(&full[s], last_use & 1) && prm.status) atomicOr(prm.status, kStatusDrain);
+        }
+    }
     const int cols = noct * 8;
     for (int e = threadIdx.x; e < MT * cols; e += blockDim.x) {
         const int m = e / cols, c = e - m * cols;
@@ -414,6 +420,7 @@ pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, i
     prm.pb1 = pb1;
     prm.pb2 = pb2;
     prm.ldy = ldy;
+    prm.wait = pipeline_wait_bound();
     prm.n_oct = N / 8;
     prm.nkw = (K + 1023) / 1024;
     prm.w_bytes = (uint32_t)(8 * (K / 2));

@@ -124,6 +124,7 @@ struct Ctrl {
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
     int abort;
+    int issued;               // slabs the TMA producer issued (the drain after a give-up)
 };
 
 template <int kBits>
@@ -139,6 +140,7 @@ struct TcParams {
     __nv_bfloat16 *y;
     unsigned int *status;
     int M, N, K, pb1, pb2, ldy;
+    WaitBound wait;           // the pipeline waits' bound
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -149,6 +151,13 @@ __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsig
     if (status) atomicOr(status, code);
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
+
+// Named barrier 1 over the whole CTA, reached by every role once it has left
+// its loop.  From then on the abort flag is final, so the TMA producer and the
+// MMA warp know whether the copies and MMAs they issued must still be waited
+// for (a consumer that gave up never saw them land) before shared and tensor
+// memory are released.  Those drain waits keep the full bound.
+__device__ __forceinline__ void roles_done() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
 // Packed fp32 pair operations for the fold; not volatile, so the compiler
 // interleaves the independent chains of a step.
@@ -287,6 +296,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_init(&ctl->tmem_empty[b], kFoldWarps);
         }
         ctl->abort = 0;
+        ctl->issued = 0;
         fence_mbar_init();
     }
     fence_proxy_async_smem();
@@ -340,7 +350,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 tma_load_3d(stg[it].a, &tmA, pre_kb[it] * BK, pre_m0[it], pre_p[it], &ctl->full_tma[it]);
             int issued = pre;
             for (int it = pre, s = 0, par = 0; it < total; ++it) {   // s = it % kStages, par = (it / kStages - 1) & 1
-                if (!wait_or_abort(&ctl->empty[s], (uint32_t)par, abort_flag)) {
+                if (!wait_or_abort(&ctl->empty[s], (uint32_t)par, abort_flag, prm.wait)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
@@ -356,12 +366,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     par ^= 1;
                 }
             }
-            if (*abort_flag) {   // let issued copies land before shared memory is released
-                for (int s = 0; s < kStages && s < issued; ++s) {
-                    const int last = (issued - 1 - s) / kStages;
-                    if (!mbar_wait(&ctl->full_tma[s], last & 1) && prm.status)
-                        atomicOr(prm.status, kStatusDrain);
-                }
+            ctl->issued = issued;
+        }
+        roles_done();
+        if (*abort_flag && lane == 0) {   // after a give-up: every issued copy lands first
+            const int issued = ctl->issued;
+            for (int s = 0; s < kStages && s < issued; ++s) {
+                const int last = (issued - 1 - s) / kStages;
+                if (!mbar_wait(&ctl->full_tma[s], last & 1) && prm.status) atomicOr(prm.status, kStatusDrain);
             }
         }
     } else if (warp == kRowWarp || warp == kRowWarp + 1) {
@@ -385,8 +397,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         };
         if (total > 0) tile_start();
         for (int it = 0, r = 0, ruse = 0; it < total; ++it) {   // r = it % kSzfRing, ruse = it / kSzfRing
-            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag)) {
-                if (lane == 0) set_abort(ctl, prm.status, kStatusWaitEmpty);
+            // lanes decide on their own (nothing below is warp-wide), so each
+            // lane that gives up reports it
+            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag, prm.wait)) {
+                set_abort(ctl, prm.status, kStatusWaitEmpty);
                 break;
             }
             const float *ga = prm.asg + off + m0 + row0, *gr = prm.rs + off + m0 + row0;
@@ -409,6 +423,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
+        roles_done();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         // The whole warp runs the loop (so the descriptors stay warp-uniform)
@@ -428,7 +443,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // the first reads as complete
             const bool ok = __all_sync(0xFFFFFFFFu,
                                        wait2_or_abort(&ctl->full_b[s], use & 1, &ctl->tmem_empty[b], (tuse - 1) & 1,
-                                                      abort_flag));
+                                                      abort_flag, prm.wait));
             if (!ok) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull | kStatusWaitTmem);
                 break;
@@ -466,14 +481,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 ++tim;
             }
         }
-        if (*abort_flag && committed > 0 && lane == 0) {   // MMAs and their arrivals must land before exit
+        roles_done();
+        if (*abort_flag && committed > 0 && lane == 0) {
+            // after a give-up: the last slab's three commits land first (later
+            // commits complete after earlier ones)
             const int it = committed - 1;
             if (!mbar_wait(&ctl->tmem_full[0][it & 1], (it >> 1) & 1) && prm.status)
                 atomicOr(prm.status, kStatusDrain);
             if (!mbar_wait(&ctl->tmem_full[1][it & 1], (it >> 1) & 1) && prm.status)
                 atomicOr(prm.status, kStatusDrain);
-            if (it + kStages < total && !mbar_wait(&ctl->empty[it % kStages], (it / kStages) & 1) &&
-                prm.status)
+            if (it + kStages < total && !mbar_wait(&ctl->empty[it % kStages], (it / kStages) & 1) && prm.status)
                 atomicOr(prm.status, kStatusDrain);
         }
     } else if (warp >= kFoldWarps && warp < kFoldWarps + kExpWarps) {
@@ -488,7 +505,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // folded; the phase before the first reads as complete);
             // warp-uniform, so the warp stays converged for its votes and syncs
             if (!__all_sync(0xFFFFFFFFu, wait2_or_abort(&ctl->full_tma[s], use & 1, &ctl->szf_empty[r],
-                                                        (ruse - 1) & 1, abort_flag))) {
+                                                        (ruse - 1) & 1, abort_flag, prm.wait))) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
@@ -533,6 +550,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 mbar_arrive(&ctl->szf_full[r]);
             }
         }
+        roles_done();
     } else if (warp < kFoldWarps) {
         // ------------------------------------------------ fold warps
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFoldRegs));
@@ -555,8 +573,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     const int it = i * G + kb;
                     const int b = it & 1, tuse = it >> 1;
                     const int r = it % kSzfRing, ruse = it / kSzfRing;
-                    if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r], ruse & 1,
-                                        &ctl->tmem_full[h][b], tuse & 1, abort_flag)) {
+                    if (!__all_sync(0xFFFFFFFFu, wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r],
+                                                                ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
+                                                                abort_flag, prm.wait))) {
                         if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                         bad = true;
                         break;
@@ -581,8 +600,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int it = i * G + kb;
                 const int b = it & 1, tuse = it >> 1;
                 const int r = it % kSzfRing, ruse = it / kSzfRing;
-                if (!wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r], ruse & 1, &ctl->tmem_full[h][b],
-                                    tuse & 1, abort_flag)) {
+                // warp-uniform: the TMEM loads and syncs below need the whole warp
+                if (!__all_sync(0xFFFFFFFFu, wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r],
+                                                            ruse & 1, &ctl->tmem_full[h][b], tuse & 1, abort_flag,
+                                                            prm.wait))) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     bad = true;
                     break;
@@ -638,7 +659,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if (lane == 0) mbar_arrive(&ctl->szf_empty[r]);
             }
             if (i == my_tiles - 1) pdl_trigger();
-            bad = bad || *abort_flag != 0;
+            bad = __any_sync(0xFFFFFFFFu, bad || *abort_flag != 0);     // one verdict per warp
             // epilogue: bf16 pairs (NaN once the CTA has aborted); per-token:
             // times the row's As first
 #pragma unroll
@@ -660,14 +681,17 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
             }
         }
+        roles_done();
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp)
+    if (warp == kMmaWarp) {
+        __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -741,6 +765,7 @@ pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M
     prm.pb1 = pb1;
     prm.pb2 = pb2;
     prm.ldy = ldy;
+    prm.wait = pipeline_wait_bound();
     const long long ntiles = (long long)(N / BN) * ((M + BM - 1) / BM);
     if (ntiles > 0x7FFFFFFF) return fail(PQ_ERR_SHAPE, "pq_gemm_tc: M = %d too large", M);
     const int ctas = (int)(ntiles < sm_count ? ntiles : (sm_count > 0 ? sm_count : 1));

@@ -172,6 +172,7 @@ struct TcnParams {
     __nv_bfloat16 *y;
     unsigned int *status;
     int M, N, K, pb1, pb2, ldy;
+    WaitBound wait;           // the pipeline waits' bound
 };
 
 __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsigned int code) {
@@ -244,6 +245,9 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const uint32_t tmem = ctl->tmem_base;
     pdl_trigger();     // the next kernel may start its own load-time prefetch
 
+    // the last block (weight producers) or slab (activation producer) issued
+    // and the last slab an MMA warp committed, for the drain after a give-up
+    int last = -1;
     if (warp < kTmaWWarps) {
         // ------------------------------------------------ weight producers
         // Weights, SZ words and fifth bits are load-time tables, not written by
@@ -256,10 +260,9 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             // weight block wb = slabs kWSlabs wb .. +kWSlabs-1 (a box past K
             // reads as zero)
             const int nwb = (G + kWSlabs - 1) / kWSlabs;
-            int last = -1;             // the last block this producer issued
             for (int wb = tw; wb < nwb; wb += kTmaWWarps) {
                 const int s = wb % kW, use = wb / kW;
-                if (use > 0 && !wait_or_abort(&ctl->w_empty[s], (use - 1) & 1, abort_flag)) {
+                if (use > 0 && !wait_or_abort(&ctl->w_empty[s], (use - 1) & 1, abort_flag, prm.wait)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
@@ -270,22 +273,15 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 if constexpr (kBits == 5) tma_load_2d(ws[s].bh, &tmH, it * (BK / 8), n0, &ctl->w_full[s]);
                 last = wb;
             }
-            if (*abort_flag) {   // let this producer's copies land before shared memory is released
-                for (int wb = last; wb >= 0 && wb > last - kW; wb -= kTmaWWarps) {
-                    if (!mbar_wait(&ctl->w_full[wb % kW], (wb / kW) & 1) && prm.status)
-                        atomicOr(prm.status, kStatusDrain);
-                }
-            }
         }
     } else if (warp == kTmaAWarp) {
         // ------------------------------------------------ activation producer
         if (lane == 0) {
             prefetch_map(&tmA);
             pdl_wait();        // the activations are the preceding prologue's output
-            int last = -1;
             for (int it = 0; it < G; ++it) {
                 const int s = it % kX, use = it / kX;
-                if (use > 0 && !wait_or_abort(&ctl->x_empty[s], (use - 1) & 1, abort_flag)) {
+                if (use > 0 && !wait_or_abort(&ctl->x_empty[s], (use - 1) & 1, abort_flag, prm.wait)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
                     break;
                 }
@@ -293,19 +289,12 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 tma_load_3d(xs[s].aa, &tmA, it * BK, 0, p, &ctl->x_full_a[s]);
                 last = it;
             }
-            if (*abort_flag) {
-                for (int it = last; it >= 0 && it > last - kX; --it) {
-                    if (!mbar_wait(&ctl->x_full_a[it % kX], (it / kX) & 1) && prm.status)
-                        atomicOr(prm.status, kStatusDrain);
-                }
-            }
         }
     } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps) {
         // ------------------------------------------------ MMA issuers
         // The whole warp runs the loop (so the descriptors stay warp-uniform)
         // and one elected lane issues the MMAs and commits.
         const int j = warp - kMmaWarp0;
-        int committed = -1;
         // the bounded waits below start their clocks only once the preceding
         // kernel has completed, so a long predecessor cannot run them out
         pdl_wait();
@@ -318,8 +307,8 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             // and, for a slab that exists, the expanded and activation tiles
             const bool ok = __all_sync(
                 0xFFFFFFFFu, it < G ? wait3_or_abort(&ctl->x_full_b[s], use & 1, &ctl->x_full_a[s], use & 1,
-                                                     &ctl->tmem_empty[b], (tuse - 1) & 1, abort_flag)
-                                    : wait_or_abort(&ctl->tmem_empty[b], (tuse - 1) & 1, abort_flag));
+                                                     &ctl->tmem_empty[b], (tuse - 1) & 1, abort_flag, prm.wait)
+                                    : wait_or_abort(&ctl->tmem_empty[b], (tuse - 1) & 1, abort_flag, prm.wait));
             if (!ok) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull | kStatusWaitTmem);
                 break;
@@ -346,22 +335,17 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 mma_commit(&ctl->tmem_full[b]);
             }
             __syncwarp();
-            committed = it;
-        }
-        if (*abort_flag && committed >= 0) {   // MMAs and their arrivals must land before exit
-            // one more commit, on a barrier of this warp's own: it completes
-            // once every MMA this thread issued has completed
-            if (elect_one()) mma_commit(&ctl->drain[j]);
-            __syncwarp();
-            if (lane == 0 && !mbar_wait(&ctl->drain[j], 0) && prm.status) atomicOr(prm.status, kStatusDrain);
+            last = it;
         }
     } else if (warp == kRowWarp) {
         // ------------------------------------------------ per-token scales
         pdl_wait();        // asg and rs are the preceding prologue's output
         for (int k = 0; k < nbatch; ++k) {
             const int r = k % kRowSlots, ruse = k / kRowSlots;
-            if (ruse > 0 && !wait_or_abort(&ctl->row_empty[r], (ruse - 1) & 1, abort_flag)) {
-                if (lane == 0) set_abort(ctl, prm.status, kStatusWaitEmpty);
+            // lanes decide on their own (nothing below is warp-wide), so each
+            // lane that gives up reports it
+            if (ruse > 0 && !wait_or_abort(&ctl->row_empty[r], (ruse - 1) & 1, abort_flag, prm.wait)) {
+                set_abort(ctl, prm.status, kStatusWaitEmpty);
                 break;
             }
             if (lane < MT) {
@@ -392,7 +376,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 // a slab past K in a weight block that holds an earlier slab:
                 // release this group's share of the slot once it has landed
                 // (so the arrival counts for this use)
-                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->w_full[ws_i], wuse & 1, abort_flag))) {
+                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->w_full[ws_i], wuse & 1, abort_flag, prm.wait))) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     break;
                 }
@@ -403,7 +387,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 const int xs_i = it % kX, xuse = it / kX;
                 // the slab's weights: read everything into registers, then
                 // release the weight slot
-                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->w_full[ws_i], wuse & 1, abort_flag))) {
+                if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->w_full[ws_i], wuse & 1, abort_flag, prm.wait))) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     break;
                 }
@@ -424,7 +408,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 if (lane == 0) mbar_arrive(&ctl->w_empty[ws_i]);
                 // the operand slot free (its previous slab's MMAs complete; the
                 // phase before the first reads as complete)
-                if (xuse > 0 && !__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->x_empty[xs_i], (xuse - 1) & 1, abort_flag))) {
+                if (xuse > 0 && !__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->x_empty[xs_i], (xuse - 1) & 1, abort_flag, prm.wait))) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     break;
                 }
@@ -447,7 +431,8 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             // j / 8, column j % 8: column n = j), into the batch slot; every
             // expand warp arrives once per batch, slab or not
             const int r = k % kSzfSlots, ruse = k / kSzfSlots;
-            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag)) {
+            if (ruse > 0 &&
+                !__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag, prm.wait))) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
@@ -472,8 +457,9 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             const int b = k % kTmemBufs, tuse = k / kTmemBufs;
             const int r = k % kSzfSlots, ruse = k / kSzfSlots;
             const int rr = k % kRowSlots, rruse = k / kRowSlots;
-            if (!wait3_or_abort(&ctl->row_full[rr], rruse & 1, &ctl->szf_full[r], ruse & 1,
-                                &ctl->tmem_full[b], tuse & 1, abort_flag)) {
+            // warp-uniform: the TMEM loads and syncs below need the whole warp
+            if (!__all_sync(0xFFFFFFFFu, wait3_or_abort(&ctl->row_full[rr], rruse & 1, &ctl->szf_full[r], ruse & 1,
+                                                        &ctl->tmem_full[b], tuse & 1, abort_flag, prm.wait))) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 bad = true;
                 break;
@@ -541,9 +527,37 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp0)
+    // After a give-up anywhere in the CTA -- the flag is final once every role
+    // has left its loop -- the copies and MMAs already issued must land before
+    // shared and tensor memory are released.  These waits keep the full bound.
+    if (*abort_flag) {
+        if (warp < kTmaWWarps && lane == 0) {
+            // this producer's blocks are last, last - 2, ...; each slot's latest
+            for (int wb = last; wb >= 0 && wb > last - kW; wb -= kTmaWWarps)
+                if (!mbar_wait(&ctl->w_full[wb % kW], (wb / kW) & 1) && prm.status) atomicOr(prm.status, kStatusDrain);
+        } else if (warp == kTmaAWarp && lane == 0) {
+            for (int it = last; it >= 0 && it > last - kX; --it)
+                if (!mbar_wait(&ctl->x_full_a[it % kX], (it / kX) & 1) && prm.status)
+                    atomicOr(prm.status, kStatusDrain);
+        } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMmaWarps && last >= 0) {
+            // one more commit, on a barrier of this warp's own: it completes
+            // once every MMA this warp's issuing lane issued has completed
+            const int j = warp - kMmaWarp0;
+            if (elect_one()) mma_commit(&ctl->drain[j]);
+            __syncwarp();
+            if (lane == 0 && !mbar_wait(&ctl->drain[j], 0) && prm.status) atomicOr(prm.status, kStatusDrain);
+        }
+        // every MMA warp's drain ends before the tensor memory is freed (the
+        // flag is final, so every thread takes this branch)
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (warp == kMmaWarp0) {
+        __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
+    }
 }
 
 }  // namespace
@@ -615,6 +629,7 @@ pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int 
     prm.pb1 = pb1;
     prm.pb2 = pb2;
     prm.ldy = ldy;
+    prm.wait = pipeline_wait_bound();
     auto kern = int5 ? tcn_kernel<5> : tcn_kernel<4>;
     const size_t smem = int5 ? smem_bytes<5>() : smem_bytes<4>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -52,6 +52,30 @@ pq_status launch_gemm_tcn(const void *a, const float *asg, const float *rs, int 
                           int P, int pb1, int pb2, const void *w, const void *sz, void *y,
                           int ldy, unsigned int *dev_status, void *stream, const void *whi = nullptr);
 
+// Give up a wait after this many nanoseconds of %globaltimer (never reached by
+// a correct pipeline; it bounds the damage of a bug to one slow launch).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// One try_wait; the thread may be suspended by the hardware for up to
+// kSuspendHintNs while the phase is incomplete (it resumes as soon as the
+// phase completes), so waiting warps do not spin on the issue slots.
+constexpr uint32_t kSuspendHintNs = 100000u;
+
+// The bound of a kernel's pipeline waits, passed in its parameters: kWaitLimitNs
+// in every product launch.  A test entry point may shorten it so that the
+// give-up path runs on a healthy GPU; `hint` (the try_wait suspend hint) is
+// then shortened too, so that one suspended try_wait cannot outlast the bound.
+// The waits that drain in-flight copies and MMAs after a give-up always keep
+// kWaitLimitNs.
+struct WaitBound {
+    unsigned long long ns;
+    uint32_t hint;
+};
+
+// The bound every launch puts in its kernel parameters: {kWaitLimitNs,
+// kSuspendHintNs} unless pq_test_set_wait_limit_ns has shortened it.
+WaitBound pipeline_wait_bound();
+
 constexpr int kSkinnyMaxM = 16;   // largest M the CUDA-core decode kernel accepts
 constexpr int kSkinnyMaxK = 16384;   // largest K it accepts (one compute warp per 1024 k, plus the producer)
 constexpr int kTcnMaxM = 16;      // largest M the narrow tensor-core kernel accepts

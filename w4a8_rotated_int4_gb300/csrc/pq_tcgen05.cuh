@@ -150,17 +150,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 // Bounded wait for two phases: one overlapped test of both first, then each
 // barrier in turn (the common case, both complete, costs one round trip).
 __device__ __forceinline__ uint32_t mbar_test2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1) {
@@ -176,17 +165,18 @@ __device__ __forceinline__ uint32_t mbar_test2(uint64_t *b0, uint32_t p0, uint64
     return r;
 }
 __device__ __forceinline__ bool wait2_or_abort(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
-                                               volatile int *abort_flag) {
+                                               volatile int *abort_flag, const WaitBound &wb) {
     if (mbar_test2(b0, p0, b1, p1)) return true;
-    return wait_or_abort(b0, p0, abort_flag) && wait_or_abort(b1, p1, abort_flag);
+    return wait_or_abort(b0, p0, abort_flag, wb) && wait_or_abort(b1, p1, abort_flag, wb);
 }
 // Bounded wait for three phases: one overlapped test first, then each barrier
 // in turn (the common case, all three complete, costs one round trip).
 __device__ __forceinline__ bool wait3_or_abort(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
-                                               uint64_t *b2, uint32_t p2, volatile int *abort_flag) {
+                                               uint64_t *b2, uint32_t p2, volatile int *abort_flag,
+                                               const WaitBound &wb) {
     if (mbar_test3(b0, p0, b1, p1, b2, p2)) return true;
-    return wait_or_abort(b0, p0, abort_flag) && wait_or_abort(b1, p1, abort_flag) &&
-           wait_or_abort(b2, p2, abort_flag);
+    return wait_or_abort(b0, p0, abort_flag, wb) && wait_or_abort(b1, p1, abort_flag, wb) &&
+           wait_or_abort(b2, p2, abort_flag, wb);
 }
 
 
