@@ -438,17 +438,25 @@ def e2e_graph_workload(pq, torch, wl, steps, warmup, stream):
 _CSRC = "w4a8_rotated_int4_gb300/csrc/"
 NCU_TRAFFIC = {
     ("pq_gemm_skinny", "decode:1"): dict(
-        bytes=47379968 + 0,
+        bytes=47382016 + 0,
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
-        sha256="c83880b7bd913f00b2336cde5bd37064250507bca5f0c0474a07b2c9fb5b3fa8"),
+        sha256="0ebbdb2eee124ec5ebab00ed8f81493a3ab4afc6a373a6d2942d003a60194e25"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=72353536 + 38940160,
+        bytes=71368704 + 38188032,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="314a982c0f321ff369b4b86d9429ada4a8da04871269c042b2e21b665ebc521a"),
+        sha256="b4b167abaf833e4182b5c12f4e50d2279f73a3e35c94bcc5d1ae6983a6ed24bc"),
+    ("pq_gemm_tc", "down"): dict(
+        bytes=99656960 + 55878656,
+        src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
+        sha256="b4b167abaf833e4182b5c12f4e50d2279f73a3e35c94bcc5d1ae6983a6ed24bc"),
+    ("pq_gemm_tc", "qkv"): dict(
+        bytes=30696704 + 0,
+        src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
+        sha256="b4b167abaf833e4182b5c12f4e50d2279f73a3e35c94bcc5d1ae6983a6ed24bc"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47469312 + 0,
+        bytes=47476992 + 0,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="49a5fd8537d1027988459d0b3514407c2974387ddba253c3aafdf2e65d737a66"),
+        sha256="2b6ae0ab29078568322b4742c952bbcee81f56981b0751307bc7d74cae279e88"),
 }
 
 
