@@ -615,8 +615,13 @@ class OracleSample:
                 "both scaled to the whole workload" % (self.mtok, self.c["M"], self.ncols, self.c["N"]))
 
     def cores(self):
+        """Threads the sample actually keeps busy: the oracle's loops are
+        parallel over tokens (the prologue over partitions x tokens), so a
+        decode workload of one token runs on one thread whatever the pool."""
         self._use_threads()
-        return self.oracle.num_threads()
+        P = 1 + (self.prob.pb1 < self.c["N"]) + (self.prob.pb2 < self.c["N"])
+        width = max(self.c["M"], P * self.mtok)
+        return min(self.oracle.num_threads(), width)
 
 
 def cpu_model():
@@ -654,7 +659,8 @@ def cpu_baseline(name, M, budget_s=4.0, reps=3):
                         sample=orc.describe())
     oracle.set_num_threads(n_all)
     a, one = out["all"], out["single"]
-    return {"value": round(a["median"], 1), "unit": "us", "cores": a["cores"], "kind": "oracle",
+    return {"value": round(a["median"], 1), "unit": "us", "cores": a["cores"], "threads_in_pool": n_all,
+            "kind": "oracle",
             "sample": a["sample"] + ", median of %d" % reps, "best": round(a["best"], 1),
             "cpu_model": cpu_model(),
             "single_thread": {"value": round(one["median"], 1), "best": round(one["best"], 1), "cores": 1,

@@ -873,3 +873,32 @@ def test_gemm_tail_slabs_repeated(pq, orc, M, K):
         for _ in range(20):
             y = run_gemm(fn, a, asg, rs, L, N, N, M, N)
             assert np.array_equal(y, first), name
+
+
+@pytest.mark.parametrize("bits,M", [(5, 4), (5, 16), (4, 4), (4, 16)])
+def test_narrow_kernel_repeated_launches_bit_identical(pq, orc, bits, M):
+    """The narrow tensor-core kernel at the decode gate_up size: eight launches
+    must give bit-identical outputs (a ring-ownership race shows up as run-to-run
+    differences in a few columns), and the first must match the fp64 oracle on
+    sampled outputs."""
+    K, N = 5120, 17408
+    prob = pqgen.make_problem(M, K, N, seed=41 + M + bits, bits=bits)
+    L = (Problem5 if bits == 5 else Problem)(pq, orc, prob, check_pack=False)
+    a, asg, rs = pq.pq_rotate_quant(L.x_d, L.rec_d, L.cs_d)
+    name = "pq_gemm5_tcn" if bits == 5 else None
+    outs = []
+    for _ in range(8):
+        if bits == 5:
+            y = run_gemm5(name, a, asg, rs, L, N, N, M, N)
+        else:
+            y = run_gemm(pq.pq_gemm_tcn, a, asg, rs, L, N, N, M, N)
+        outs.append(y)
+    for j in range(1, 8):
+        assert np.array_equal(outs[j], outs[0]), "launch %d differs" % j
+    ms, ns = _samples(M, N, N, N, 2000, 17)
+    a_h, s_h, r_h = a.cpu().numpy(), asg.cpu().numpy(), rs.cpu().numpy()
+    if bits == 5:
+        y64 = orc.gemm5_f64_sampled(ms, ns, a_h, s_h, r_h, L.t["codes"], L.t["sz"], N, N)
+    else:
+        y64 = orc.gemm_f64_sampled(ms, ns, a_h, s_h, r_h, L.t["codes"], L.t["sz"], N, N)
+    assert_close(outs[0][ms, ns], y64, "tcn int%d M=%d" % (bits, M))
