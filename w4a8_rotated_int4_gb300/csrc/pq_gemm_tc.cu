@@ -14,37 +14,39 @@
 //                zero-filled past M), the packed weight tile w[n0:n0+128]
 //                [64kb:+64] and the slab's 128 SZ words (16 octets x 8 words
 //                of the [N/8][G][8] table) into stage s.
-//   row warps    copy the slab's per-row asg and rs (cp.async) into a ring
-//                slot of their own, up to the ring's depth ahead.
+//   row warps    load the slab's per-row asg and rs (one slab ahead of their
+//                stores) into a ring slot of their own, up to the ring's depth
+//                ahead: asg for the fold, and the zero-point MMA's row
+//                operand, -rs / 2 as three bf16 parts.
 //   expand warps turn each nibble c into the e4m3 byte of value c * 2^-9 (the
 //                nibble alone in its byte) in the canonical K-major
-//                SWIZZLE_128B layout the MMA reads, and write the zero-point
-//                MMA's operands: per column zq = 2^-9 (zscale + 8 sc) / sc',
-//                per row -rs, each as three bf16 parts (below), plus the
-//                fold's column scale 2^9 sc'.  sc' = sc, or 1 where sc = 0,
-//                whose codes are masked to 0.
+//                SWIZZLE_128B layout the MMA reads, and write per column the
+//                fold's 2^9 sc' and the zero-point MMA's column operand: the
+//                bf16 parts of zq = 2^-9 (zscale + 8 sc) / sc'.  sc' = sc, or
+//                1 where sc = 0, whose codes are masked to 0.
 //   MMA warp     per half: 4 tcgen05.mma m128n128k32 (kind::f8f6f4, fp32
 //                accumulate), then one m128n128k16 kind::f16 (bf16) MMA of the
 //                zero-point operands into the same accumulator, so TMEM holds
 //                D'' = 2^-9 (sum_k dec(a) c - rs * zq); two accumulator sets,
 //                so the MMAs of slab kb+1 run while slab kb is folded.
-//   fold warps   (one thread per row, 128 columns each) tcgen05.ld D'' and
-//                fold it into fp32 registers with packed f32x2 operations:
-//                acc += (asg * 2^9 sc') * D''.  That is
+//   fold warps   tcgen05.ld D'' and fold it into fp32 registers with packed
+//                f32x2 operations: acc += (asg * 2^9 sc') * D''.  That is
 //                asg * (sc * D' - (zscale + 8 sc) * rs) with D' = sum dec(a) c
 //                = D + 8 rs, D the sum over (c - 8): the zero point of the
-//                method, moved onto the tensor core (two fp32 operations per
-//                element and slab instead of three).
+//                method, moved onto the tensor core, leaves two fp32 operations
+//                per element and slab instead of three.
 // Zero-point operand precision: with rs = h + m + l and zq = zh + zm + zl
 // (bf16_split3, 24 significant bits each), k = 0..5 of the row operand carry
-// -(h, h, m, h, l, m) against (zh, zm, zh, zl, zh, zm) in the column operand:
-// every product of parts whose orders sum to <= 2, so the MMA adds -rs * zq
-// to about 2^-24 relative (products are exact, sums fp32).
-// The fold warpgroups raise their register budget (setmaxnreg) to hold the
-// 128 accumulators; the others lower theirs.
+// -(h, h, m, h, l, m) / 2 against (zh, zm, zh, zl, zh, zm) in the column
+// operand, and the MMA reads each row's eight values twice (its two K core
+// matrices are the same bytes): every product of parts whose orders sum to
+// <= 2, so the MMA adds -rs * zq to about 2^-24 relative (products are exact,
+// sums fp32).
+// The fold warps raise their register budget (setmaxnreg) to hold the 128
+// accumulators; the others lower theirs.
 // Epilogue: bf16 rows < M are stored; nothing else is written.
 // Per-token mode (the "Numbers" section's PTOK GEMM: one activation scale As
-// per token and partition, plain row-sums): the row warps copy rs only, the
+// per token and partition, plain row-sums): the row warps load rs only, the
 // fold is acc += (2^9 sc') * D'' (one packed operation per two elements) and
 // the epilogue multiplies each row by its As.
 // int5 weights ("2026-09-10: int5 W5A8 ParoQuant": low nibbles as for int4,
@@ -105,12 +107,16 @@ struct __align__(1024) StageT {
 // from global memory by the row warps (cp.async), which run up to a ring's
 // depth ahead, so no global-load latency reaches the fold warps.
 constexpr int kSzfRing = 4;
-struct __align__(16) SzfSlot {
-    // column pair j (columns 2j, 2j+1): (2^9 sc, 2^9 sc', -zs8, -zs8') with
-    // zs8 = zscale + 8 sc (int4) or zscale (int5)
-    float4 col[BN / 2];
+// The zero-point MMA's operands: K = 16 bf16, K-major without swizzle, 8-row
+// x 16-byte core matrices 128 bytes apart along M/N.  The two core matrices
+// along K are the same bytes (leading byte offset 0), so each row's eight
+// values enter the sum twice; the row operand carries -rs / 2.
+constexpr uint32_t kZLbo = 0, kZSbo = 128;
+struct __align__(128) SzfSlot {
+    uint8_t za[BM * 16];      // row operand: (h, h, m, h, l, m, 0, 0) of -rs / 2 (row warps)
+    uint8_t zb[BN * 16];      // column operand: (zh, zm, zh, zl, zh, zm, 0, 0) of zq (expand warps)
+    float2 col[BN / 2];       // column pair j: (2^9 sc', 2^9 sc'') of columns 2j, 2j + 1
     float row[BM];            // asg of tile row i (0 past M); per-token: unused
-    float rsv[BM];            // rs of tile row i (0 past M)
 };
 
 struct Ctrl {
@@ -119,7 +125,7 @@ struct Ctrl {
     uint64_t empty[kStages];
     uint64_t szf_full[kSzfRing];
     uint64_t szf_empty[kSzfRing];
-    uint64_t rows_full[kSzfRing];   // the row warps' copies of a slab's asg and rs have landed
+    uint64_t rows_full[kSzfRing];   // the row warps have written a slab's asg and zero-point row operand
     uint64_t tmem_full[2][2];     // [m-half][accumulator buffer]
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
@@ -146,6 +152,7 @@ struct TcParams {
 // ---------------------------------------------------------------- PTX helpers
 using namespace tc;
 constexpr uint32_t kIdesc = idesc_f8(128, BN);     // one M=128 half x BN columns
+constexpr uint32_t kIdescZ = idesc_bf16(128, BN);  // the zero-point MMA of a half
 
 __device__ __forceinline__ void set_abort(Ctrl *ctl, unsigned int *status, unsigned int code) {
     if (status) atomicOr(status, code);
@@ -174,38 +181,32 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 
 // The fold of one 16x256b.x4 load: four column pairs j for two rows (lo:
 // d[4j], d[4j+1]; hi: d[4j+2], d[4j+3]).  The accumulator holds
-// D' = 2^-9 sum_k dec(a) c of the slab, so with z[j] = the (2^9 sc) pair and
-// zz[j] = the -zs8 pair of column pair j, sa = the row's asg splat and
-// ar = the row's asg * rs splat:
-//   acc += (sa * z) * D' + ar * zz = asg * (sc * (D' 2^9) - zs8 * rs)
-// which is asg * (sc * D - zscale * rs) with D = 2^9 D' - 8 rs the sum over
-// (c - 8) (int5: c - 16 is fed directly and zs8 = zscale).  Three packed
-// operations per two elements.
-__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64_t (&z)[4], const uint64_t (&zz)[4],
-                                           uint64_t *acc_lo, uint64_t *acc_hi, uint64_t sa_lo, uint64_t sa_hi,
-                                           uint64_t ar_lo, uint64_t ar_hi) {
+// D'' = 2^-9 (sum_k dec(a) c - rs zq) of the slab (the zero-point MMA added
+// the second term), so with z[j] = the (2^9 sc') pair of column pair j and
+// sa = the row's asg splat:
+//   acc += (sa * z) * D'' = asg * (sc' sum_k dec(a) c - zs8 rs)
+// which is asg * (sc * D - zscale * rs) with D = sum over (c - 8) (int5:
+// c - 16 is fed directly and zs8 = zscale).  Two packed operations per two
+// elements.
+__device__ __forceinline__ void fold_block(const uint32_t (&d)[16], const uint64_t (&z)[4], uint64_t *acc_lo,
+                                           uint64_t *acc_hi, uint64_t sa_lo, uint64_t sa_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         acc_lo[j] = ffma2(fmul2(sa_lo, z[j]), f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
-                           ffma2(ar_lo, zz[j], acc_lo[j]));
-        acc_hi[j] = ffma2(fmul2(sa_hi, z[j]),
-                           f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                           ffma2(ar_hi, zz[j], acc_hi[j]));
+                          acc_lo[j]);
+        acc_hi[j] = ffma2(fmul2(sa_hi, z[j]), f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                          acc_hi[j]);
     }
 }
 
-// The per-token fold: the token scale is applied in the epilogue and rs is
-// the plain row-sum, so acc += z * D' + rs * zz: two packed operations per two
-// elements.
-__device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const uint64_t (&z)[4],
-                                               const uint64_t (&zz)[4], uint64_t *acc_lo, uint64_t *acc_hi,
-                                               uint64_t rs_lo, uint64_t rs_hi) {
+// The per-token fold: the token scale is applied in the epilogue, so
+// acc += z * D'': one packed operation per two elements.
+__device__ __forceinline__ void fold_block_tok(const uint32_t (&d)[16], const uint64_t (&z)[4], uint64_t *acc_lo,
+                                               uint64_t *acc_hi) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        acc_lo[j] = ffma2(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
-                           ffma2(rs_lo, zz[j], acc_lo[j]));
-        acc_hi[j] = ffma2(z[j], f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                           ffma2(rs_hi, zz[j], acc_hi[j]));
+        acc_lo[j] = ffma2(z[j], f2pack(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), acc_lo[j]);
+        acc_hi[j] = ffma2(z[j], f2pack(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), acc_hi[j]);
     }
 }
 
@@ -287,7 +288,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
         for (int r = 0; r < kSzfRing; ++r) {
             mbar_init(&ctl->szf_full[r], kExpWarps);
-            mbar_init(&ctl->rows_full[r], 64);              // every lane of the two row warps (cp.async)
+            mbar_init(&ctl->rows_full[r], 64);              // every lane of the two row warps
             mbar_init(&ctl->szf_empty[r], kFoldWarps);
         }
         for (int b = 0; b < 2; ++b) {
@@ -378,15 +379,17 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
     } else if (warp == kRowWarp || warp == kRowWarp + 1) {
         // ------------------------------------------------ per-row scales
-        // asg and rs of a slab's rows by cp.async into the slab's ring slot,
-        // up to a ring's depth ahead.  Row warp hw copies tile half hw; lane
-        // l copies rows 128 hw + l + 32 u (u = 0..3).  Coordinates and row
-        // pointers are stepped per slab without divisions.
+        // asg and rs of a slab's rows into the slab's ring slot, up to a
+        // ring's depth ahead: asg for the fold warps, and -rs / 2 split into
+        // three bf16 parts as the zero-point MMA's row operand.  Row warp hw
+        // covers tile half hw; lane l rows 128 hw + l + 32 u (u = 0..3).  The
+        // loads of slab it + 1 are issued before slab it is stored, so their
+        // latency overlaps the wait for the slab's slot.
         const int row0 = (BM / 2) * (warp - kRowWarp) + lane;
         pdl_wait();        // asg and rs are the preceding prologue's output
-        int ti = 0, kb = 0, n0 = 0, m0 = 0, p = 0;
+        int ti = 0, kb = 0, n0 = 0, m0 = 0, p = 0;   // the slab whose rows are loaded next
         bool half_item;
-        uint32_t ok = 0;            // bit u: row row0 + 32 u of the tile is below M
+        uint32_t ok = 0;            // bit u: row row0 + 32 u of that slab's tile is below M
         size_t off = 0;             // (p * G + kb) * M
         auto tile_start = [&]() {
             tile_coords<!kTok>(ti, ntn, ntiles, pb1, pb2, n0, m0, p, half_item);
@@ -395,41 +398,68 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             for (int u = 0; u < 4; ++u) ok |= (m0 + row0 + 32 * u < M ? 1u : 0u) << u;
             off = (size_t)p * G * (size_t)M;
         };
-        if (total > 0) tile_start();
-        for (int it = 0, r = 0, ruse = 0; it < total; ++it) {   // r = it % kSzfRing, ruse = it / kSzfRing
-            // lanes decide on their own (nothing below is warp-wide), so each
-            // lane that gives up reports it
-            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag, prm.wait)) {
-                set_abort(ctl, prm.status, kStatusWaitEmpty);
-                break;
-            }
+        float av[4], rv[4];         // the slab it's asg and rs (0 past M)
+        auto load = [&](float (&a)[4], float (&rr)[4]) {
             const float *ga = prm.asg + off + m0 + row0, *gr = prm.rs + off + m0 + row0;
 #pragma unroll
-            for (int u = 0; u < BM / 64; ++u) {
-                const bool v = (ok >> u) & 1u;     // rows past M are zero-filled
-                if constexpr (!kTok) cp_async4(&szf[r].row[row0 + 32 * u], v ? ga + 32 * u : prm.asg, v);
-                cp_async4(&szf[r].rsv[row0 + 32 * u], v ? gr + 32 * u : prm.rs, v);
+            for (int u = 0; u < 4; ++u) {
+                const bool v = (ok >> u) & 1u;
+                a[u] = (!kTok && v) ? __ldg(ga + 32 * u) : 0.0f;
+                rr[u] = v ? __ldg(gr + 32 * u) : 0.0f;
             }
-            cp_async_arrive(&ctl->rows_full[r]);
             if (++kb == G) {
                 kb = 0;
                 if (++ti < my_tiles) tile_start();
             } else {
                 off += (size_t)M;
             }
+        };
+        if (total > 0) {
+            tile_start();
+            load(av, rv);
+        }
+        for (int it = 0, r = 0, ruse = 0; it < total; ++it) {   // r = it % kSzfRing, ruse = it / kSzfRing
+            float an[4], rn[4];
+            if (it + 1 < total) load(an, rn);
+            // lanes decide on their own (nothing below is warp-wide), so each
+            // lane that gives up reports it
+            if (ruse > 0 && !wait_or_abort(&ctl->szf_empty[r], (ruse - 1) & 1, abort_flag, prm.wait)) {
+                set_abort(ctl, prm.status, kStatusWaitEmpty);
+                break;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int row = row0 + 32 * u;
+                if constexpr (!kTok) szf[r].row[row] = av[u];
+                // rs = h + m + l (bf16 parts): the row operand (h, h, m, h, l, m)
+                // of -rs / 2 against (zh, zm, zh, zl, zh, zm) in the column
+                // operand; the MMA reads the eight values twice (kZLbo = 0), so
+                // it adds -(every product of parts whose orders sum to <= 2) =
+                // -rs * zq to about 2^-24 relative
+                uint32_t h, m, l;
+                bf16_split3(-0.5f * rv[u], h, m, l);
+                *reinterpret_cast<uint4 *>(szf[r].za + (row >> 3) * kZSbo + (row & 7) * 16) =
+                    make_uint4(h | (h << 16), m | (h << 16), l | (m << 16), 0u);
+            }
+            fence_proxy_async_smem();     // the row operand is read by the tensor core
+            mbar_arrive(&ctl->rows_full[r]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                av[u] = an[u];
+                rv[u] = rn[u];
+            }
             if (++r == kSzfRing) {
                 r = 0;
                 ++ruse;
             }
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
         roles_done();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         // The whole warp runs the loop (so the descriptors stay warp-uniform)
         // and one elected lane issues the MMAs and commits.  full_b implies
-        // full_tma: the expand warps waited for the stage's copies before they
-        // arrived on full_b, after writing the zero-point operands.
+        // full_tma and the slab's row operand: the expand warps waited for
+        // both before they arrived on full_b, after writing the column operand.
         int committed = 0;
         int tim = 0, kbm = 0;       // tile and group of slab it
         bool half_item = false;
@@ -439,6 +469,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages, use = it / kStages;
             const int b = it & 1, tuse = it >> 1;
+            const int r = it % kSzfRing;
             // the accumulator's first use waits on nothing: the phase before
             // the first reads as complete
             const bool ok = __all_sync(0xFFFFFFFFu,
@@ -452,21 +483,27 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint64_t ad0 = desc_sw128(smem_u32(stg[s].a));
             const uint64_t ad1 = desc_sw128(smem_u32(stg[s].a + kABytes / 2));
             const uint64_t bd = desc_sw128(smem_u32(stg[s].bx));
+            const uint64_t za0 = desc_noswz(smem_u32(szf[r].za), kZLbo, kZSbo);
+            const uint64_t za1 = desc_noswz(smem_u32(szf[r].za + BM * 8), kZLbo, kZSbo);
+            const uint64_t zbd = desc_noswz(smem_u32(szf[r].zb), kZLbo, kZSbo);
             const uint32_t d0 = tmem + (uint32_t)(b * 2 * BN), d1 = d0 + BN;
             if (kbm == 0) half_item = is_half_item<!kTok>(tim, ntiles);   // once per tile
             if (elect_one()) {
                 // half 0, then half 1, each committed on its own so the two
-                // fold warp groups start half a slab apart.  A half item
+                // fold warp groups start half a slab apart; each half's chain
+                // ends with the zero-point MMA (bf16, K = 16).  A half item
                 // issues half 0 only; half 1's commit still signals its fold
                 // warps, which then only release the buffer.
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)   // +32 bytes along K inside the swizzle row
                     mma_f8(d0, ad0 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
+                mma_bf16(d0, za0, zbd, kIdescZ, 1u);
                 mma_commit(&ctl->tmem_full[0][b]);
                 if (!half_item) {
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk)
                         mma_f8(d1, ad1 + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, kk > 0 ? 1u : 0u);
+                    mma_bf16(d1, za1, zbd, kIdescZ, 1u);
                 }
                 // A stage that is never refilled gets no release: nothing would wait
                 // for that arrival, and an arrival still in flight when the CTA
@@ -501,11 +538,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages, use = it / kStages;
             const int r = it % kSzfRing, ruse = it / kSzfRing;
-            // the stage's copies and the ring slot free (its previous slab
-            // folded; the phase before the first reads as complete);
+            // the stage's copies, the ring slot free (its previous slab folded;
+            // the phase before the first reads as complete) and the slab's row
+            // operand written (so that full_b, below, implies it for the MMA);
             // warp-uniform, so the warp stays converged for its votes and syncs
-            if (!__all_sync(0xFFFFFFFFu, wait2_or_abort(&ctl->full_tma[s], use & 1, &ctl->szf_empty[r],
-                                                        (ruse - 1) & 1, abort_flag, prm.wait))) {
+            if (!__all_sync(0xFFFFFFFFu, wait3_or_abort(&ctl->full_tma[s], use & 1, &ctl->szf_empty[r],
+                                                        (ruse - 1) & 1, &ctl->rows_full[r], ruse & 1, abort_flag,
+                                                        prm.wait))) {
                 if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                 break;
             }
@@ -521,6 +560,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if constexpr (kBits == 5)
                     hb[i] = *reinterpret_cast<const uint16_t *>(st.bh + ((et >> 3) + 16 * i) * (BK / 8) + chunk * 2);
             }
+            // A column with sc = 0 dequantizes to -zscale whatever its codes, so
+            // its codes must not reach the MMA: the fold then scales it by
+            // 2^9 * 1 and the zero-point MMA alone gives -zscale * rs.  Lane l
+            // checks row 4w + l % 4 + 16 (l / 4) of this warp's 32 rows.
+            const bool any_zero_sc = __any_sync(
+                0xFFFFFFFFu, (st.sz[4 * (et >> 5) + (lane & 3) + 16 * (lane >> 2)] & 0x7FFFu) == 0u);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = (et >> 3) + 16 * i;
@@ -529,19 +574,26 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     e = expand16_int5(pk[i], hb[i]);
                 else
                     e = expand16(pk[i]);
+                if (any_zero_sc && (st.sz[row] & 0x7FFFu) == 0u) e = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
             }
-            // the fold's column values of column et: 2^9 sc (the MMA sums
-            // a * c * 2^-9, see expand16) and -zs8 with zs8 = zscale + 8 sc
-            // (int4: the MMA sums raw c, so the -8 moves here; int5 feeds
-            // c - 16 itself).  A column with sc = 0 gets 2^9 sc = 0, so it
-            // contributes -zscale * rs alone whatever its (finite) sum.
+            // column et: the fold's 2^9 sc' (the MMA sums a * c * 2^-9, see
+            // expand16; sc' = sc, or 1 where sc = 0) and the zero-point MMA's
+            // column operand (zh, zm, zh, zl, zh, zm): the bf16 parts of
+            // zq = 2^-9 zs8 / sc' with zs8 = zscale + 8 sc (int4: the MMA sums
+            // raw c, so the -8 moves here; int5 feeds c - 16 itself, so
+            // zs8 = zscale).  zq only corrects, so a quotient to 2 ulp (about
+            // 2^-23 relative) is accurate enough.
             {
                 const float sc = f16lo(wcol);
+                const float sce = sc != 0.0f ? sc : 1.0f;
                 const float zs8 = kBits == 5 ? f16hi(wcol) : f16hi(wcol) + 8.0f * sc;
-                float *cv = reinterpret_cast<float *>(&szf[r].col[et >> 1]);
-                cv[et & 1] = kNibbleScale * sc;
-                cv[2 + (et & 1)] = -zs8;
+                const float zq = __fdividef(zs8, sce) * (1.0f / kNibbleScale);
+                uint32_t h, m, l;
+                bf16_split3(zq, h, m, l);
+                *reinterpret_cast<uint4 *>(szf[r].zb + (et >> 3) * kZSbo + (et & 7) * 16) =
+                    make_uint4(h | (m << 16), h | (l << 16), h | (m << 16), 0u);
+                reinterpret_cast<float *>(szf[r].col)[et] = kNibbleScale * sce;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -573,9 +625,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     const int it = i * G + kb;
                     const int b = it & 1, tuse = it >> 1;
                     const int r = it % kSzfRing, ruse = it / kSzfRing;
-                    if (!__all_sync(0xFFFFFFFFu, wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r],
-                                                                ruse & 1, &ctl->tmem_full[h][b], tuse & 1,
-                                                                abort_flag, prm.wait))) {
+                    if (!__all_sync(0xFFFFFFFFu, wait2_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b],
+                                                                tuse & 1, abort_flag, prm.wait))) {
                         if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                         bad = true;
                         break;
@@ -600,10 +651,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const int it = i * G + kb;
                 const int b = it & 1, tuse = it >> 1;
                 const int r = it % kSzfRing, ruse = it / kSzfRing;
-                // warp-uniform: the TMEM loads and syncs below need the whole warp
-                if (!__all_sync(0xFFFFFFFFu, wait3_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->rows_full[r],
-                                                            ruse & 1, &ctl->tmem_full[h][b], tuse & 1, abort_flag,
-                                                            prm.wait))) {
+                // the slab's column values (szf_full; the expand warps arrived on
+                // it after seeing the row warps' rows_full, so the row values
+                // are there too) and its accumulator; warp-uniform: the TMEM
+                // loads and syncs below need the whole warp
+                if (!__all_sync(0xFFFFFFFFu, wait2_or_abort(&ctl->szf_full[r], ruse & 1, &ctl->tmem_full[h][b],
+                                                            tuse & 1, abort_flag, prm.wait))) {
                     if (lane == 0) set_abort(ctl, prm.status, kStatusWaitFull);
                     bad = true;
                     break;
@@ -612,34 +665,29 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + h * BN);
                 // four steps (32-column block cb), each two 16x256b.x4 loads
                 // (16-lane halves sh = 0, 1) in flight behind one wait
-                // per row: asg and asg * rs (per-token: rs) as splats
-                uint64_t sa2[4], ar2[4];
+                // per row: the asg splat (per-token: none, As is applied at the end)
+                uint64_t sa2[4];
 #pragma unroll
                 for (int ri = 0; ri < 4; ++ri) {
-                    const float rsv = szf[r].rsv[row0 + 8 * ri];
                     if constexpr (kTok) {
                         sa2[ri] = 0;
-                        ar2[ri] = f2pack(rsv, rsv);
                     } else {
                         const float v = szf[r].row[row0 + 8 * ri];
-                        const float ar = __fmul_rn(v, rsv);
                         sa2[ri] = f2pack(v, v);
-                        ar2[ri] = f2pack(ar, ar);
                     }
                 }
                 // column pair 8 J + 2 c4 (J = 0..15) of the slab: col[4 J + c4]
-                const float4 *cf = szf[r].col + c4;
+                const float2 *cf = szf[r].col + c4;
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t d0[16], d1[16];
                     tmem_issue256(taddr + 32 * cb, d0);
                     tmem_issue256(taddr + ((uint32_t)16 << 16) + 32 * cb, d1);
-                    uint64_t z[4], zz[4];
+                    uint64_t z[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float4 v = cf[4 * (4 * cb + j)];
+                        const float2 v = cf[4 * (4 * cb + j)];
                         z[j] = f2pack(v.x, v.y);
-                        zz[j] = f2pack(v.z, v.w);
                     }
                     tmem_wait32(d0, d1);
                     if (cb == 3) {       // every load of this buffer has completed
@@ -648,11 +696,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                         if (lane == 0) mbar_arrive(&ctl->tmem_empty[b]);
                     }
                     if constexpr (kTok) {
-                        fold_block_tok(d0, z, zz, acc[0] + 4 * cb, acc[1] + 4 * cb, ar2[0], ar2[1]);
-                        fold_block_tok(d1, z, zz, acc[2] + 4 * cb, acc[3] + 4 * cb, ar2[2], ar2[3]);
+                        fold_block_tok(d0, z, acc[0] + 4 * cb, acc[1] + 4 * cb);
+                        fold_block_tok(d1, z, acc[2] + 4 * cb, acc[3] + 4 * cb);
                     } else {
-                        fold_block(d0, z, zz, acc[0] + 4 * cb, acc[1] + 4 * cb, sa2[0], sa2[1], ar2[0], ar2[1]);
-                        fold_block(d1, z, zz, acc[2] + 4 * cb, acc[3] + 4 * cb, sa2[2], sa2[3], ar2[2], ar2[3]);
+                        fold_block(d0, z, acc[0] + 4 * cb, acc[1] + 4 * cb, sa2[0], sa2[1]);
+                        fold_block(d1, z, acc[2] + 4 * cb, acc[3] + 4 * cb, sa2[2], sa2[3]);
                     }
                 }
                 __syncwarp();
