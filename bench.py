@@ -442,17 +442,17 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="0ebbdb2eee124ec5ebab00ed8f81493a3ab4afc6a373a6d2942d003a60194e25"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=71368704 + 38188032,
+        bytes=71116032 + 37804288,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="b4b167abaf833e4182b5c12f4e50d2279f73a3e35c94bcc5d1ae6983a6ed24bc"),
+        sha256="e7416b8a29542f363f98df4fd84ecfbfeac10fee93717762ca10e4d807ba5d19"),
     ("pq_gemm_tc", "down"): dict(
-        bytes=99656960 + 55878656,
+        bytes=99588864 + 54899200,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="b4b167abaf833e4182b5c12f4e50d2279f73a3e35c94bcc5d1ae6983a6ed24bc"),
+        sha256="e7416b8a29542f363f98df4fd84ecfbfeac10fee93717762ca10e4d807ba5d19"),
     ("pq_gemm_tc", "qkv"): dict(
-        bytes=30696704 + 0,
+        bytes=30700288 + 256,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="b4b167abaf833e4182b5c12f4e50d2279f73a3e35c94bcc5d1ae6983a6ed24bc"),
+        sha256="e7416b8a29542f363f98df4fd84ecfbfeac10fee93717762ca10e4d807ba5d19"),
     ("pq_gemm_tcn", "decode:16"): dict(
         bytes=47476992 + 0,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
