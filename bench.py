@@ -408,17 +408,19 @@ def e2e_workload(pq, torch, wl, steps, warmup, stream, dev):
     return e0.elapsed_time(e1) / steps, xh.numel() * 2, yh.numel() * 2
 
 
-def e2e_graph_workload(pq, torch, wl, steps, warmup, stream):
+def e2e_graph_workload(pq, torch, wl, steps, warmup, stream, zero_copy=True):
     """The same step through the public graph API (PQLinear.make_graph): each
-    replay copies x in from pinned host memory, runs the prologue and the
-    GEMM, and copies y back to pinned host memory.  One layer and graph per
-    weight copy, replayed round robin, so the weights stream from HBM as in the
-    timed region."""
+    replay moves x from pinned host memory to the GPU, runs the prologue and
+    the GEMM, and moves y back to pinned host memory.  zero_copy: the prologue
+    reads x from, and the GEMM writes y to, the pinned host buffers directly;
+    otherwise two copy operations.  One layer and graph per weight copy,
+    replayed round robin, so the weights stream from HBM as in the timed
+    region."""
     c = wl.c
     xh = torch.from_numpy(wl.prob.x.view(np.int16)).view(torch.bfloat16).pin_memory()
     yh = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory()
     steps_fns = [pq.PQLinear.from_tables(wl.rec[j], wl.sz[j], wl.w[j], wl.cs[j], (wl.pb1, wl.pb2))
-                 .make_graph(xh, yh) for j in range(wl.copies)]
+                 .make_graph(xh, yh, zero_copy=zero_copy) for j in range(wl.copies)]
     for i in range(max(warmup, wl.copies)):
         steps_fns[i % wl.copies]()
     torch.cuda.synchronize()
@@ -760,7 +762,9 @@ def main():
     e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else e2e_workload(
         pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, dev)
     e2e_graph_ms = None if args.no_e2e else e2e_graph_workload(
-        pq, torch, wl, max(50, args.steps // 10), args.warmup, stream)
+        pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, zero_copy=True)
+    e2e_copy_ms = None if args.no_e2e else e2e_graph_workload(
+        pq, torch, wl, max(50, args.steps // 10), args.warmup, stream, zero_copy=False)
     clocks = sampler.summary() if sampler else {}
     head = summarize(wl, dict(r, total_ms=total_ms), args.steps, peaks, clocks, sms)
 
@@ -795,9 +799,13 @@ def main():
         "gemm_us_by_kernel": head["gemm_us_by_kernel"],
         "e2e": None if e2e_ms is None else {
             "value": round(e2e_graph_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "how": "public API PQLinear.make_graph: one CUDA graph "
-            "replay per step = pinned H2D of x, pq_rotate_quant + pq_gemm, D2H of y to pinned "
-            "host memory; one graph per weight copy, round robin",
+            "d2h_bytes_per_step": d2h, "how": "public API PQLinear.make_graph(zero_copy=True): one CUDA "
+            "graph replay per step = pq_rotate_quant reading x from pinned host memory + pq_gemm "
+            "writing y to pinned host memory (the bytes cross the host link inside the kernels); "
+            "one graph per weight copy, round robin",
+            "copy_graph_value": round(e2e_copy_ms * 1e3, 3),
+            "copy_graph_how": "make_graph(zero_copy=False): the same graph with a pinned H2D copy of x "
+            "before the prologue and a D2H copy of y after the GEMM",
             "eager_value": round(e2e_ms * 1e3, 3),
             "eager_how": "public API per step, host-driven: pinned H2D of x, pq_rotate_quant + "
             "pq_gemm, D2H of y"},

@@ -66,8 +66,10 @@ extern "C" {
  * 2: adds the fused producers, the per-token path (pq_rotate_tokquant,
  *    pq_gemm_ptok) and int5 weights (pq_pack5, pq_gemm5*); version 1's calls
  *    are unchanged.
- * 3: adds pq_rotate_tokquant_noalloc; earlier calls are unchanged. */
-#define PQ_ABI_VERSION 4
+ * 3: adds pq_rotate_tokquant_noalloc; earlier calls are unchanged.
+ * 4: adds the test hook pq_test_set_wait_limit_ns.
+ * 5: adds pq_check_device_access and the status PQ_ERR_ACCESS. */
+#define PQ_ABI_VERSION 5
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
@@ -82,7 +84,8 @@ typedef enum pq_status {
     PQ_ERR_PAIRS = 4,     /* a pairs row is not a permutation of 0..127         */
     PQ_ERR_PARTITION = 5, /* P outside 1..3 or pb1/pb2 inconsistent with P      */
     PQ_ERR_ARCH = 6,      /* no device, or the current device is not sm_103     */
-    PQ_ERR_CUDA = 7       /* a CUDA runtime call or launch failed               */
+    PQ_ERR_CUDA = 7,      /* a CUDA runtime call or launch failed               */
+    PQ_ERR_ACCESS = 8     /* a pointer is not directly usable by the device     */
 } pq_status;
 
 /* ABI version of the loaded library (PQ_ABI_VERSION of its build). */
@@ -329,7 +332,7 @@ pq_status pq_gemm_tcn(const void *a, const float *asg, const float *rs, int M, i
  *   As    = max_g asg_g
  *   a[k]  = e4m3(fl(xr[k] / As))              (all 0 when As == 0; [CVT])
  *   rs_g  = sum_{k in g} dec(a[k])            (exact, then rounded to fp32)
-Two launches: pass A writes xr and the group scales (into rs); pass C reads
+ * Two launches: pass A writes xr and the group scales (into rs); pass C reads
  * them back and writes a, As and the row-sums over them.  Every step is a
  * separately rounded IEEE operation, so the outputs are bit-identical to a CPU
  * evaluation in that order.
@@ -435,6 +438,22 @@ pq_status pq_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stream);
  * on other threads.  Errors: PQ_ERR_SHAPE for ns > 2e9.
  */
 pq_status pq_test_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Whether kernels on the current device can dereference p directly (no
+ * counterpart in the pages; a helper for zero-copy inputs and outputs).  Every
+ * device pointer argument of the calls above may point to memory of the
+ * current device, to managed memory, or to page-locked host memory that is
+ * mapped into the device's address space at the same address (on this
+ * platform the host's memory is reached over a coherent link): the kernels
+ * then read x from, or write y to, host memory directly, and the bytes cross
+ * the link inside the kernels.  Such host buffers must stay allocated and
+ * page-locked until the kernels have finished.  This call checks the start
+ * address only (cudaPointerGetAttributes); it launches nothing.
+ * Returns PQ_OK, PQ_ERR_NULL, PQ_ERR_ACCESS (pageable host memory, host memory
+ * mapped at another address, or another device's memory) or PQ_ERR_CUDA.
+ */
+pq_status pq_check_device_access(const void *p);
 
 #ifdef __cplusplus
 }

@@ -824,6 +824,41 @@ def test_layer_graph_replays_the_step(pq, orc, M):
                      "graph M=%d" % M)
 
 
+@pytest.mark.parametrize("M,N", [(1, 256), (4, 17408), (40, 512)])
+def test_layer_graph_zero_copy(pq, orc, M, N):
+    """make_graph(zero_copy=True): the prologue reads x from the pinned host
+    buffer and the GEMM writes y into the pinned host buffer directly; every
+    replay must equal the eager call bit for bit, also after new values are
+    written into the pinned input, and the host buffers must pass the access
+    check that pageable memory fails."""
+    K = 512
+    prob = pqgen.make_problem(M, K, N, seed=75 + M)
+    layer = pq.PQLinear(prob.qweight, prob.qzeros, prob.scales, prob.pairs, prob.theta, prob.cs)
+    xh = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    pq.pq_check_device_access(xh)
+    pq.pq_check_device_access(yh)
+    pq.pq_check_device_access(layer.w)
+    with pytest.raises(pq.PQError) as e:
+        pq.pq_check_device_access(torch.empty((M, K), dtype=torch.bfloat16))   # pageable
+    assert e.value.status == 8
+    step = layer.make_graph(xh, yh, zero_copy=True)
+    for seed in (75 + M, 175 + M, 275 + M):
+        x = pqgen.make_problem(M, K, N, seed=seed).x
+        xh.copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+        yh.fill_(float("nan"))
+        step()
+        torch.cuda.synchronize()
+        y_eager = layer(dev_u16(x).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_eager.cpu().view(torch.int16)), seed
+    t = orc.pack(prob)
+    a_o, asg_o, rs_o = orc.rotate_quant(x, prob.cs, t["rec"])
+    ms, ns = _samples(M, N, N, N, 1000, 3)
+    y64 = orc.gemm_f64_sampled(ms, ns, a_o, asg_o, rs_o, t["codes"], t["sz"], N, N)
+    assert_close(yh.float().numpy()[ms, ns], y64, "zero-copy graph M=%d" % M)
+
+
 # ---------------------------------------------------------------- repeated launches
 @pytest.mark.parametrize("path", ["skinny", "tcn", "tc"])
 def test_gemm_repeated_graph_launches_status_clean(pq, orc, path):

@@ -28,11 +28,11 @@ EXPORTS = (
     "pq_gemm_tcn",
     "pq_rotate_tokquant", "pq_rotate_tokquant_noalloc", "pq_gemm_ptok",
     "pq_pack5", "pq_gemm5", "pq_gemm5_tc", "pq_gemm5_tcn",
-    "pq_e4m3_encode", "pq_test_set_wait_limit_ns",
+    "pq_e4m3_encode", "pq_test_set_wait_limit_ns", "pq_check_device_access",
 )
 
 STATUS = {0: "PQ_OK", 1: "PQ_ERR_NULL", 2: "PQ_ERR_SHAPE", 3: "PQ_ERR_ALIGN", 4: "PQ_ERR_PAIRS",
-          5: "PQ_ERR_PARTITION", 6: "PQ_ERR_ARCH", 7: "PQ_ERR_CUDA"}
+          5: "PQ_ERR_PARTITION", 6: "PQ_ERR_ARCH", 7: "PQ_ERR_CUDA", 8: "PQ_ERR_ACCESS"}
 
 
 class PQError(RuntimeError):
@@ -98,6 +98,8 @@ def lib() -> C.CDLL:
     L.pq_e4m3_encode.argtypes = [vp, vp, st, vp]
     L.pq_test_set_wait_limit_ns.restype = i32
     L.pq_test_set_wait_limit_ns.argtypes = [C.c_ulonglong]
+    L.pq_check_device_access.restype = i32
+    L.pq_check_device_access.argtypes = [vp]
     _lib = L
     return L
 
@@ -489,6 +491,15 @@ def pq_test_set_wait_limit_ns(ns):
     _check(lib().pq_test_set_wait_limit_ns(int(ns)), "pq_test_set_wait_limit_ns")
 
 
+def pq_check_device_access(t):
+    """Raise PQError unless kernels on the current device can dereference the
+    storage of tensor t (or the integer address t) directly: memory of the
+    current device, managed memory, or page-locked host memory mapped at the
+    same address."""
+    ptr = t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+    _check(lib().pq_check_device_access(C.c_void_p(ptr)), "pq_check_device_access")
+
+
 class PQLinear:
     """One packed projection resident in device memory: pq_pack once, then
     forward(x) = pq_rotate_quant + pq_gemm on the current stream."""
@@ -520,27 +531,49 @@ class PQLinear:
 
     __call__ = forward
 
-    def make_graph(self, x_host, y_host):
-        """One step as a CUDA graph on pinned host buffers: copy x_host (bf16
-        [M, K], pinned) to the device, the prologue and the GEMM, copy y back to
-        y_host (bf16 [M, N], pinned).  Returns a function that replays the step
-        on the current stream; each replay reads whatever x_host holds then.
-        The device buffers live as long as the returned function."""
+    def make_graph(self, x_host, y_host, zero_copy=False):
+        """One step as a CUDA graph on pinned host buffers x_host (bf16 [M, K])
+        and y_host (bf16 [M, N]).  Returns a function that replays the step on
+        the current stream; each replay reads whatever x_host holds then.  The
+        device buffers live as long as the returned function.
+
+        zero_copy=False: copy x_host to the device, the prologue and the GEMM,
+        copy y back to y_host.  zero_copy=True: the prologue reads x straight
+        from x_host and the GEMM writes y straight into y_host (page-locked
+        host memory mapped at the same device address, checked with
+        pq_check_device_access), so the bytes cross the host link inside the
+        kernels and the step has no copy operations."""
         torch = _torch()
         dev = self.w.device
         M, K = x_host.shape
         G = K // 128
-        x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-        y_dev = torch.empty((M, self.N), dtype=torch.bfloat16, device=dev)
+        if K != self.K or tuple(y_host.shape) != (M, self.N):
+            raise PQError("make_graph: x_host must be [M, %d] and y_host [M, %d]" % (self.K, self.N))
+        for t, what in ((x_host, "x_host"), (y_host, "y_host")):
+            if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+                raise PQError("make_graph: %s must be a contiguous page-locked bf16 host tensor" % what)
+            if zero_copy:
+                pq_check_device_access(t)
+        x_dev = None if zero_copy else torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        y_dev = None if zero_copy else torch.empty((M, self.N), dtype=torch.bfloat16, device=dev)
         a = torch.empty((self.P, M, K), dtype=torch.uint8, device=dev)
         asg = torch.empty((self.P, G, M), dtype=torch.float32, device=dev)
         rs = torch.empty((self.P, G, M), dtype=torch.float32, device=dev)
 
-        def body():
-            x_dev.copy_(x_host, non_blocking=True)
-            pq_rotate_quant(x_dev, self.rec, self.cs, a=a, asg=asg, rs=rs)
-            pq_gemm(a, asg, rs, self.w, self.sz, self.pb1, self.pb2, y=y_dev)
-            y_host.copy_(y_dev, non_blocking=True)
+        if zero_copy:
+            def body():
+                L, st = lib(), _stream(None)
+                _check(L.pq_rotate_quant(C.c_void_p(x_host.data_ptr()), M, K, K, self.P, _dptr(self.rec),
+                                         _dptr(self.cs), _dptr(a), _dptr(asg), _dptr(rs), st), "pq_rotate_quant")
+                _check(L.pq_gemm(_dptr(a), _dptr(asg), _dptr(rs), M, self.N, K, self.P, self.pb1, self.pb2,
+                                 _dptr(self.w), _dptr(self.sz), C.c_void_p(y_host.data_ptr()), self.N, st),
+                       "pq_gemm")
+        else:
+            def body():
+                x_dev.copy_(x_host, non_blocking=True)
+                pq_rotate_quant(x_dev, self.rec, self.cs, a=a, asg=asg, rs=rs)
+                pq_gemm(a, asg, rs, self.w, self.sz, self.pb1, self.pb2, y=y_dev)
+                y_host.copy_(y_dev, non_blocking=True)
 
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))

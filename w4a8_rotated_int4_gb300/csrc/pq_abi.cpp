@@ -31,6 +31,7 @@ const char *kStatusText[] = {
     "partition count or boundaries are inconsistent",
     "no sm_103 device is current",
     "a CUDA runtime call failed",
+    "a pointer is not directly usable by the device",
 };
 }  // namespace
 
@@ -171,7 +172,7 @@ using namespace pq;
 extern "C" int pq_abi_version(void) { return PQ_ABI_VERSION; }
 
 extern "C" const char *pq_status_string(int status) {
-    if (status < 0 || status > (int)PQ_ERR_CUDA) return "unknown status";
+    if (status < 0 || status > (int)PQ_ERR_ACCESS) return "unknown status";
     return kStatusText[status];
 }
 
@@ -557,4 +558,33 @@ extern "C" pq_status pq_test_set_wait_limit_ns(unsigned long long ns) {
     if (ns > pq::kWaitLimitNs) return pq::fail(PQ_ERR_SHAPE, "wait limit %llu ns above the product bound", ns);
     pq::g_test_wait_ns.store(ns, std::memory_order_relaxed);
     return PQ_OK;
+}
+
+extern "C" pq_status pq_check_device_access(const void *p) {
+    clear_error();
+    if (!p) return pq::fail(PQ_ERR_NULL, "NULL pointer");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return pq::fail(PQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    }
+    cudaPointerAttributes at{};
+    e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return pq::fail(PQ_ERR_CUDA, "cudaPointerGetAttributes: %s", cudaGetErrorString(e));
+    }
+    switch (at.type) {
+        case cudaMemoryTypeManaged:
+            return PQ_OK;
+        case cudaMemoryTypeDevice:
+            if (at.device == dev) return PQ_OK;
+            return pq::fail(PQ_ERR_ACCESS, "device memory of device %d, current device %d", at.device, dev);
+        case cudaMemoryTypeHost:
+            if (at.devicePointer == p) return PQ_OK;
+            return pq::fail(PQ_ERR_ACCESS, "page-locked host memory not mapped at the same device address");
+        default:
+            return pq::fail(PQ_ERR_ACCESS, "pageable host memory");
+    }
 }
