@@ -101,11 +101,11 @@ struct __align__(1024) StageT {
     uint8_t bh[kBits == 5 ? kBhBytes : 16];   // int5: fifth-bit planes (TMA)
 };
 
-// fp32 scales of one slab for the fold warps, in a ring of their own so a
-// stage is free as soon as its MMAs complete (the fold lags the MMA).  The
-// column part comes from the expansion warps; the row part is copied straight
-// from global memory by the row warps (cp.async), which run up to a ring's
-// depth ahead, so no global-load latency reaches the fold warps.
+// A slab's scales and zero-point operands, in a ring of their own so a stage
+// is free as soon as its MMAs complete (the fold lags the MMA).  The column
+// part comes from the expansion warps; the row part is loaded from global
+// memory by the row warps, which run up to a ring's depth ahead, so no
+// global-load latency reaches the fold warps.
 constexpr int kSzfRing = 4;
 // The zero-point MMA's operands: K = 16 bf16, K-major without swizzle, 8-row
 // x 16-byte core matrices 128 bytes apart along M/N.  The two core matrices

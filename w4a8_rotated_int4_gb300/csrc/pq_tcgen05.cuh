@@ -105,9 +105,8 @@ __device__ __forceinline__ void bf16_split3(float x, uint32_t &hi, uint32_t &mid
     lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
-// Non-blocking test of up to three mbarrier phases issued back to back, so
-// their shared-memory round trips overlap (acquire on success).  A null
-// barrier counts as complete.
+// Non-blocking test of three mbarrier phases issued back to back, so their
+// shared-memory round trips overlap (acquire on success).
 __device__ __forceinline__ uint32_t mbar_test3(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1,
                                                uint64_t *b2, uint32_t p2) {
     uint32_t r;
