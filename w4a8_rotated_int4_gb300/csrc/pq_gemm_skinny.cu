@@ -282,7 +282,10 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
             // (octet, group g) are contiguous, one 8-byte load
             const int cb = 4 * ((lane >> 1) & 1) + 2 * (lane & 1);
             const uint2 szp = *reinterpret_cast<const uint2 *>(st + prm.w_bytes + 32 * g + 4 * cb);
-            __syncwarp();                      // every read of this stage is done
+            // the stage is refilled by a bulk copy (the async proxy): order this
+            // warp's reads of it before that write, then release it
+            fence_proxy_async_smem();
+            __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             const float sc0 = half_lo(szp.x), zs0 = half_hi(szp.x);
             const float sc1 = half_lo(szp.y), zs1 = half_hi(szp.y);

@@ -404,6 +404,10 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         hb[i] = *reinterpret_cast<const uint16_t *>(wsl.bh + row * (kWSlabs * BK / 8) +
                                                                     wu * (BK / 8) + chunk * 2);
                 }
+                // the slot is refilled by the TMA (the async proxy): order these
+                // generic reads before that write, whether or not their values
+                // have reached the registers yet, then release it
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->w_empty[ws_i]);
                 // the operand slot free (its previous slab's MMAs complete; the
