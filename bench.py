@@ -442,7 +442,7 @@ NCU_TRAFFIC = {
     ("pq_gemm_skinny", "decode:1"): dict(
         bytes=47382016 + 0,
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
-        sha256="06cac57a7858cddd1fdabd12362a82b9009819143a9c35c46c9150c77ca3ea98"),
+        sha256="30b5e001742d6f159fc36fde0b914843c71dfb5e42715c436115521f9295de79"),
     ("pq_gemm_tc", "prefill"): dict(
         bytes=71116032 + 37804288,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
@@ -456,9 +456,9 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
         sha256="52e778010fe747ee49f2243c165ae8c6d3ec1431c859b42fc20ccf6ebc299485"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47476992 + 0,
+        bytes=47476992 + 256,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="b2f9f6f33b2779880f350f2eb73c2264793a58299d267c1115ec397b288af86d"),
+        sha256="1f37e9a5de95c3131cdfcb0b5b5366e59c11638a49607efc357a7bcfcbea420f"),
 }
 
 

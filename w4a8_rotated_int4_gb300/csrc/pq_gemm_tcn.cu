@@ -404,12 +404,17 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                         hb[i] = *reinterpret_cast<const uint16_t *>(wsl.bh + row * (kWSlabs * BK / 8) +
                                                                     wu * (BK / 8) + chunk * 2);
                 }
-                // the slot is refilled by the TMA (the async proxy): order these
-                // generic reads before that write, whether or not their values
-                // have reached the registers yet, then release it
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->w_empty[ws_i]);
+                // The slot is refilled by the TMA (the async proxy), so these
+                // generic reads must be ordered before that write by a proxy
+                // fence, which waits for them to land.  int5 (four weight
+                // slots) releases here, with a fence of its own; int4 (eight
+                // slots, where the later release costs nothing) releases after
+                // the operand stores, behind the fence those need anyway.
+                if constexpr (kBits == 5) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->w_empty[ws_i]);
+                }
                 // the operand slot free (its previous slab's MMAs complete; the
                 // phase before the first reads as complete)
                 if (xuse > 0 && !__all_sync(0xFFFFFFFFu, wait_or_abort(&ctl->x_empty[xs_i], (xuse - 1) & 1, abort_flag, prm.wait))) {
@@ -429,7 +434,10 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->x_full_b[xs_i]);
+                if (lane == 0) {
+                    mbar_arrive(&ctl->x_full_b[xs_i]);
+                    if constexpr (kBits != 5) mbar_arrive(&ctl->w_empty[ws_i]);
+                }
             }
             // the slab's SZ words for the fold (word j of the SZ box is octet
             // j / 8, column j % 8: column n = j), into the batch slot; every
