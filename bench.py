@@ -440,25 +440,25 @@ def e2e_graph_workload(pq, torch, wl, steps, warmup, stream, zero_copy=True):
 _CSRC = "w4a8_rotated_int4_gb300/csrc/"
 NCU_TRAFFIC = {
     ("pq_gemm_skinny", "decode:1"): dict(
-        bytes=47382016 + 0,
+        bytes=47381760 + 0,
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
-        sha256="30b5e001742d6f159fc36fde0b914843c71dfb5e42715c436115521f9295de79"),
+        sha256="ebf585e72de7ffe731635559c79391796330cff2feec4a082210b7f6de53525b"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=71116032 + 37804288,
+        bytes=71158528 + 37806848,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="52e778010fe747ee49f2243c165ae8c6d3ec1431c859b42fc20ccf6ebc299485"),
+        sha256="5d0430075c3b05214a4be042ad62211c67b798c374b8a6a3b22c97aaa7de700c"),
     ("pq_gemm_tc", "down"): dict(
-        bytes=99588864 + 54899200,
+        bytes=99590912 + 54865408,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="52e778010fe747ee49f2243c165ae8c6d3ec1431c859b42fc20ccf6ebc299485"),
+        sha256="5d0430075c3b05214a4be042ad62211c67b798c374b8a6a3b22c97aaa7de700c"),
     ("pq_gemm_tc", "qkv"): dict(
-        bytes=30700288 + 256,
+        bytes=30699520 + 11008,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="52e778010fe747ee49f2243c165ae8c6d3ec1431c859b42fc20ccf6ebc299485"),
+        sha256="5d0430075c3b05214a4be042ad62211c67b798c374b8a6a3b22c97aaa7de700c"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47476992 + 256,
+        bytes=47476480 + 0,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="1f37e9a5de95c3131cdfcb0b5b5366e59c11638a49607efc357a7bcfcbea420f"),
+        sha256="73e58f7633f4ea7e4a8ea717d4edf859efa5024df824677a86cf7b60436062cc"),
 }
 
 

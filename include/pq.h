@@ -68,8 +68,12 @@ extern "C" {
  *    are unchanged.
  * 3: adds pq_rotate_tokquant_noalloc; earlier calls are unchanged.
  * 4: adds the test hook pq_test_set_wait_limit_ns.
- * 5: adds pq_check_device_access and the status PQ_ERR_ACCESS. */
-#define PQ_ABI_VERSION 5
+ * 5: adds pq_check_device_access and the status PQ_ERR_ACCESS.
+ * 6: the byte layouts of w (pq_pack, pq_pack5) and whi (pq_pack5) change: a
+ *    word's low nibbles hold four consecutive k and its high nibbles the next
+ *    four, and whi is laid out in 32-k blocks; weights packed by an earlier
+ *    version must be packed again.  Signatures are unchanged. */
+#define PQ_ABI_VERSION 6
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
@@ -134,8 +138,10 @@ pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_t *sz_bytes
  *        half) at word index ((n / 8) * G + g) * 8 + n % 8, i.e. laid out
  *        [N/8][G][8]: the words of one column octet over all groups are
  *        contiguous (one 32-byte sector per group and octet).
- *   w    [N][K/2] bytes: byte k/2 of row n holds code c[k][n] in its low nibble
- *        (even k) and c[k+1][n] in its high nibble (raw codes 0..15).
+ *   w    [N][K/2] bytes (raw codes 0..15): each run of eight codes k = 8t ..
+ *        8t+7 of row n fills bytes 4t .. 4t+3, byte 4t + b holding c[8t+b][n]
+ *        in its low nibble and c[8t+b+4][n] in its high nibble (so a word's
+ *        low nibbles are four consecutive k, as are its high nibbles).
  *
  * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE (K, N not positive multiples of 128),
  * PQ_ERR_PARTITION (P outside 1..3), PQ_ERR_PAIRS (a pairs row is not a
@@ -155,8 +161,9 @@ pq_status pq_pack(int K, int N, int P, const int32_t *qweight, const int32_t *qz
  * so c = nibble + 16 * bit and zp likewise (0..31).  Outputs:
  *   rec, w   as pq_pack (w holds the low nibbles)
  *   sz       as pq_pack with zscale = f16(sc * (zp - 16))
- *   whi      [N][K/8] bytes (N * K / 8): bit k % 8 of byte k / 8 of row n is
- *            the fifth bit of c[k][n]
+ *   whi      [N][K/8] bytes (N * K / 8) in 4-byte blocks of 32 k: for
+ *            k = 32t + 4q + j (q in 0..7, j in 0..3) the fifth bit of c[k][n]
+ *            is bit q of byte 4t + j of row n
  * Errors: as pq_pack.
  */
 pq_status pq_pack5(int K, int N, int P, const int32_t *qweight, const int32_t *qzeros,

@@ -338,31 +338,36 @@ void orc_sz5(int G, int N, const uint16_t *scales, const int32_t *qzeros, const 
     free(zp);
 }
 
-/* Kernel weight layout w[n][k/2]: low nibble = code at even k, high = odd k. */
+/* Kernel weight layout w[n][K/2] (this build's choice; the pages fix only the
+ * AWQ input): each run of eight codes k = 8t .. 8t+7 of row n fills the four
+ * bytes 4t .. 4t+3, byte 4t + b holding code 8t + b in its low nibble and
+ * code 8t + b + 4 in its high nibble. */
 void orc_repack(int K, int N, const int32_t *qweight, uint8_t *w)
 {
     uint8_t *c = (uint8_t *)malloc((size_t)K * N);
     orc_unpack_awq(K, N, qweight, c);
     for (int n = 0; n < N; n++)
-        for (int k = 0; k < K; k += 2)
-            w[(size_t)n * (K / 2) + k / 2] =
-                (uint8_t)(c[(size_t)k * N + n] | (c[(size_t)(k + 1) * N + n] << 4));
+        for (int t = 0; t < K / 8; t++)
+            for (int b = 0; b < 4; b++)
+                w[(size_t)n * (K / 2) + 4 * t + b] =
+                    (uint8_t)(c[(size_t)(8 * t + b) * N + n] | (c[(size_t)(8 * t + b + 4) * N + n] << 4));
     free(c);
 }
 
-/* Kernel layouts of int5 weights: the low nibbles as orc_repack, and the
- * fifth bits whi[n][k/8], bit k % 8 of byte k / 8 = the fifth bit of (k, n). */
+/* Kernel layouts of int5 weights (this build's choice): the low nibbles as
+ * orc_repack, and the fifth bits whi[n][K/8] in 4-byte blocks of 32 k: for
+ * k = 32t + 16h + 4q + j (h in 0..1, q and j in 0..3) the fifth bit of (k, n)
+ * is bit 4h + q of byte 4t + j. */
 void orc_repack5(int K, int N, const int32_t *qweight, const int32_t *qweight_hi, uint8_t *w, uint8_t *whi)
 {
     orc_repack(K, N, qweight, w);
     uint8_t *bit = (uint8_t *)malloc((size_t)K * N);
     orc_unpack_plane(K, N, qweight_hi, bit);
+    memset(whi, 0, (size_t)N * (K / 8));
     for (int n = 0; n < N; n++)
-        for (int k = 0; k < K; k += 8) {
-            uint8_t b = 0;
-            for (int j = 0; j < 8; j++)
-                b |= (uint8_t)(bit[(size_t)(k + j) * N + n] << j);
-            whi[(size_t)n * (K / 8) + k / 8] = b;
+        for (int k = 0; k < K; k++) {
+            const int t = k / 32, h = (k % 32) / 16, q = (k % 16) / 4, j = k % 4;
+            whi[(size_t)n * (K / 8) + 4 * t + j] |= (uint8_t)(bit[(size_t)k * N + n] << (4 * h + q));
         }
     free(bit);
 }

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(pq.EXPORTS)
-    assert pq.pq_abi_version() == 5
+    assert pq.pq_abi_version() == 6
     for s in range(9):
         assert L.pq_status_string(s)
     assert L.pq_status_string(99) == b"unknown status"

@@ -87,11 +87,18 @@ def test_repack5_layout(orc):
     prob = pqgen.make_problem(4, 512, 256, seed=12, bits=5)
     codes = orc.codes5(prob.qweight, prob.qweight_hi, 256)      # [K, N]
     w, whi = orc.repack5(prob.qweight, prob.qweight_hi)
-    back = np.empty((256, 512), dtype=np.uint8)
-    back[:, 0::2] = w & 15
-    back[:, 1::2] = w >> 4
-    fifth = (whi[:, :, None] >> np.arange(8, dtype=np.uint8)[None, None, :]) & 1   # [N, K/8, 8]
-    back += 16 * fifth.reshape(256, 512).astype(np.uint8)
+    back = np.empty((256, 64, 8), dtype=np.uint8)      # byte 4t + b: codes 8t + b, 8t + b + 4
+    back[:, :, 0:4] = (w & 15).reshape(256, 64, 4)
+    back[:, :, 4:8] = (w >> 4).reshape(256, 64, 4)
+    back = back.reshape(256, 512)
+    # fifth bit of k = 32t + 16h + 4q + j: bit 4h + q of byte 4t + j
+    k = np.arange(512)
+    byte = 4 * (k // 32) + k % 4
+    sh = 4 * ((k % 32) // 16) + (k % 16) // 4
+    fifth = (whi[:, byte] >> sh[None, :].astype(np.uint8)) & 1                   # [N, K]
+    back += 16 * fifth.astype(np.uint8)
+    # one bit by hand: k = 53 = 32 + 16 + 4 + 1 sits in byte 5, bit 5
+    assert (whi[7, 5] >> 5) & 1 == codes[53, 7] >> 4
     assert np.array_equal(back, codes.T)
     assert 0.4 < (codes >= 16).mean() < 0.6
 

@@ -140,12 +140,15 @@ def test_repack_round_trip(orc):
     prob = pqgen.make_problem(4, 256, 128, seed=11)
     codes = orc.unpack_awq(prob.qweight, 128)          # [K, N]
     w = orc.repack(prob.qweight)                        # [N, K/2]
-    lo = (w & 15).astype(np.uint8)
-    hi = (w >> 4).astype(np.uint8)
-    back = np.empty((128, 256), dtype=np.uint8)
-    back[:, 0::2] = lo
-    back[:, 1::2] = hi
-    assert np.array_equal(back, codes.T)
+    # byte 4t + b of a row: code 8t + b (low nibble), code 8t + b + 4 (high)
+    lo = (w & 15).astype(np.uint8).reshape(128, 32, 4)
+    hi = (w >> 4).astype(np.uint8).reshape(128, 32, 4)
+    back = np.empty((128, 32, 8), dtype=np.uint8)
+    back[:, :, 0:4] = lo
+    back[:, :, 4:8] = hi
+    assert np.array_equal(back.reshape(128, 256), codes.T)
+    # one byte by hand: row 5, bytes 4..7 hold codes 8..15
+    assert w[5, 6] == codes[10, 5] | (codes[14, 5] << 4)
 
 
 # ------------------------------------------------------------------ records

@@ -253,31 +253,39 @@ static pq_status pack_layer(int K, int N, int P, const int32_t *qweight, const i
             }
         }
 
-    // weights: w[n][k/2] = c[k][n] | c[k+1][n] << 4
+    // weights: per run of eight k (k0 = 8t), byte 4t + b of row n holds
+    // c[k0 + b][n] (low nibble) and c[k0 + b + 4][n] (high nibble), so that
+    // masking a word's low and high nibbles yields k0..k0+3 and k0+4..k0+7 in
+    // byte order
     uint8_t *wo = static_cast<uint8_t *>(w);
-    for (int k = 0; k < K; k += 2) {
-        const int32_t *r0 = qweight + (size_t)k * W8;
-        const int32_t *r1 = r0 + W8;
-        for (int w8 = 0; w8 < W8; ++w8) {
-            const uint32_t a0 = (uint32_t)r0[w8], a1 = (uint32_t)r1[w8];
-            for (int s = 0; s < 8; ++s) {
-                const int n = 8 * w8 + kAwqOrder[s];
-                wo[(size_t)n * (K / 2) + k / 2] =
-                    (uint8_t)(((a0 >> (4 * s)) & 15u) | (((a1 >> (4 * s)) & 15u) << 4));
+    for (int k0 = 0; k0 < K; k0 += 8)
+        for (int b = 0; b < 4; ++b) {
+            const int32_t *r0 = qweight + (size_t)(k0 + b) * W8;
+            const int32_t *r1 = qweight + (size_t)(k0 + b + 4) * W8;
+            for (int w8 = 0; w8 < W8; ++w8) {
+                const uint32_t a0 = (uint32_t)r0[w8], a1 = (uint32_t)r1[w8];
+                for (int s = 0; s < 8; ++s) {
+                    const int n = 8 * w8 + kAwqOrder[s];
+                    wo[(size_t)n * (K / 2) + k0 / 2 + b] =
+                        (uint8_t)(((a0 >> (4 * s)) & 15u) | (((a1 >> (4 * s)) & 15u) << 4));
+                }
             }
         }
-    }
 
-    // int5: fifth bits whi[n][k/8], bit k % 8 of byte k / 8
+    // int5: fifth bits whi[n][K/8] in 4-byte blocks of 32 k.  Byte j of a
+    // block collects the bits of k = 4q + j (q = 0..7) at bit q, so that one
+    // left shift moves the bits of four consecutive k to the top bits of the
+    // four bytes (the expansion's byte masks)
     if (int5) {
         uint8_t *ho = static_cast<uint8_t *>(whi);
-        for (int k = 0; k < K; k += 8)
-            for (int n = 0; n < N; ++n) {
-                uint32_t b = 0;
-                for (int j = 0; j < 8; ++j)
-                    b |= (((uint32_t)qweight_hi[(size_t)(k + j) * W32 + n / 32] >> (n % 32)) & 1u) << j;
-                ho[(size_t)n * (K / 8) + k / 8] = (uint8_t)b;
-            }
+        for (int k32 = 0; k32 < K; k32 += 32)
+            for (int n = 0; n < N; ++n)
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t b = 0;
+                    for (int q = 0; q < 8; ++q)
+                        b |= (((uint32_t)qweight_hi[(size_t)(k32 + 4 * q + j) * W32 + n / 32] >> (n % 32)) & 1u) << q;
+                    ho[(size_t)n * (K / 8) + k32 / 8 + j] = (uint8_t)b;
+                }
     }
     return PQ_OK;
 }

@@ -230,9 +230,13 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        // bytes 8q..8q+7 -> pairs (k, k+4), (k+1, k+5), (k+2, k+6), (k+3, k+7)
-                        const uint32_t t01 = __byte_perm(u[2 * q], u[2 * q + 1], 0x5140);
-                        const uint32_t t23 = __byte_perm(u[2 * q], u[2 * q + 1], 0x7362);
+                        // activation bytes k0..k0+7 (k0 = 8q) -> the pairs of the
+                        // masked weight halves: word byte b holds k0 + b (low
+                        // nibble) and k0 + b + 4 (high nibble), so the masks below
+                        // give (k0, k0+2), 16 (k0+4, k0+6) and, after the 8-bit
+                        // shift, (k0+1, k0+3), 16 (k0+5, k0+7)
+                        const uint32_t t01 = __byte_perm(u[2 * q], u[2 * q + 1], 0x6420);
+                        const uint32_t t23 = __byte_perm(u[2 * q], u[2 * q + 1], 0x7531);
                         // the partners of the high nibbles (used in place as 16 c)
                         // are divided by 16 -- exact in f16 -- so every product is
                         // a * c * 2^-24

@@ -550,32 +550,40 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             Stage &st = stg[s];
             const uint32_t wcol = st.sz[et];   // column et's SZ word, read before full_b frees the stage
-            // all eight packed loads first (the stores below could alias them
-            // as far as the compiler knows), then expand and store
-            uint2 pk[8];
-            uint32_t hb[8];           // int5: the fifth bits of the same 16 k (bit i = k 16 chunk + i)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                pk[i] = *reinterpret_cast<const uint2 *>(st.bp + ((et >> 3) + 16 * i) * (BK / 2) + chunk * 8);
-                if constexpr (kBits == 5)
-                    hb[i] = *reinterpret_cast<const uint16_t *>(st.bh + ((et >> 3) + 16 * i) * (BK / 8) + chunk * 2);
-            }
             // A column with sc = 0 dequantizes to -zscale whatever its codes, so
             // its codes must not reach the MMA: the fold then scales it by
             // 2^9 * 1 and the zero-point MMA alone gives -zscale * rs.  Lane l
             // checks row 4w + l % 4 + 16 (l / 4) of this warp's 32 rows.
             const bool any_zero_sc = __any_sync(
                 0xFFFFFFFFu, (st.sz[4 * (et >> 5) + (lane & 3) + 16 * (lane >> 2)] & 0x7FFFu) == 0u);
+            // the packed loads of a batch first (the stores below could alias
+            // them as far as the compiler knows), then expand and store; int5
+            // takes its eight rows in two batches of four, which keeps its
+            // fifth-bit words within the role's 40 registers
+            constexpr int kLoadBatch = kBits == 5 ? 4 : 8;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int row = (et >> 3) + 16 * i;
-                uint4 e;
-                if constexpr (kBits == 5)
-                    e = expand16_int5(pk[i], hb[i]);
-                else
-                    e = expand16(pk[i]);
-                if (any_zero_sc && (st.sz[row] & 0x7FFFu) == 0u) e = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
+            for (int i0 = 0; i0 < 8; i0 += kLoadBatch) {
+                uint2 pk[kLoadBatch];
+                uint32_t hb[kLoadBatch];  // int5: the fifth-bit block word of the same 16 k, shifted for expand16_int5
+#pragma unroll
+                for (int u = 0; u < kLoadBatch; ++u) {
+                    const int row = (et >> 3) + 16 * (i0 + u);
+                    pk[u] = *reinterpret_cast<const uint2 *>(st.bp + row * (BK / 2) + chunk * 8);
+                    if constexpr (kBits == 5)
+                        hb[u] = *reinterpret_cast<const uint32_t *>(st.bh + row * (BK / 8) + (chunk >> 1) * 4) >>
+                                (4 * (chunk & 1));
+                }
+#pragma unroll
+                for (int u = 0; u < kLoadBatch; ++u) {
+                    const int row = (et >> 3) + 16 * (i0 + u);
+                    uint4 e;
+                    if constexpr (kBits == 5)
+                        e = expand16_int5(pk[u], hb[u]);
+                    else
+                        e = expand16(pk[u]);
+                    if (any_zero_sc && (st.sz[row] & 0x7FFFu) == 0u) e = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(st.bx + row * BK + ((chunk ^ (row & 7)) << 4)) = e;
+                }
             }
             // column et: the fold's 2^9 sc' (the MMA sums a * c * 2^-9, see
             // expand16; sc' = sc, or 1 where sc = 0) and the zero-point MMA's

@@ -394,15 +394,16 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 const WSlot &wsl = ws[ws_i];
                 wcol = wsl.sz[((et >> 3) * kWSlabs + wu) * 8 + (et & 7)];
                 uint2 pk[8];
-                uint32_t hb[8];           // int5: the fifth bits of the same 16 k
+                uint32_t hb[8];           // int5: the fifth-bit block word of the same 16 k, shifted for expand16_int5
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int row = (et >> 3) + 16 * i;
                     pk[i] = *reinterpret_cast<const uint2 *>(wsl.bp + row * (kWSlabs * BK / 2) + wu * (BK / 2) +
                                                              chunk * 8);
                     if constexpr (kBits == 5)
-                        hb[i] = *reinterpret_cast<const uint16_t *>(wsl.bh + row * (kWSlabs * BK / 8) +
-                                                                    wu * (BK / 8) + chunk * 2);
+                        hb[i] = *reinterpret_cast<const uint32_t *>(wsl.bh + row * (kWSlabs * BK / 8) +
+                                                                    wu * (BK / 8) + (chunk >> 1) * 4) >>
+                                (4 * (chunk & 1));
                 }
                 // The slot is refilled by the TMA (the async proxy), so these
                 // generic reads must be ordered before that write by a proxy

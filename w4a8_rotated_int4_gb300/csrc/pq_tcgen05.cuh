@@ -188,64 +188,42 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// Sixteen packed nibbles (byte j: code of k = 2j in bits 0..3, k = 2j + 1 in
-// bits 4..7) -> sixteen e4m3 bytes in k order, each the e4m3 value c * 2^-9:
-// a byte holding a nibble c alone is exactly that e4m3 number (bit 3 is the
-// lowest exponent bit, so codes 0..7 are the subnormals m * 2^-9 and 8..15
-// the normals (1 + m/8) * 2^-6).  One AND gives the even-k nibbles, a shift
-// and an AND the odd-k ones, and two byte permutes interleave them back into
-// k order: 10 instructions per 16 weights.  The MMA result is therefore
-// 2^-9 * sum a * c; the fold multiplies its weight scale by 2^9.
+// Sixteen packed nibbles -> sixteen e4m3 bytes in k order, each the e4m3
+// value c * 2^-9: a byte holding a nibble c alone is exactly that e4m3 number
+// (bit 3 is the lowest exponent bit, so codes 0..7 are the subnormals
+// m * 2^-9 and 8..15 the normals (1 + m/8) * 2^-6).  The packed layout puts
+// k0 + b in the low and k0 + b + 4 in the high nibble of byte b of each word
+// (k0 = 0, 8), so one AND gives k0..k0+3 in byte order and a shift and an AND
+// give k0+4..k0+7: 6 instructions per 16 weights.  The MMA result is
+// therefore 2^-9 * sum a * c; the fold multiplies its weight scale by 2^9.
 constexpr float kNibbleScale = 512.0f;
 
 __device__ __forceinline__ uint4 expand16(uint2 pk) {
-    const uint32_t lo0 = pk.x & 0x0F0F0F0Fu, hi0 = (pk.x >> 4) & 0x0F0F0F0Fu;
-    const uint32_t lo1 = pk.y & 0x0F0F0F0Fu, hi1 = (pk.y >> 4) & 0x0F0F0F0Fu;
-    uint4 o;
-    o.x = prmt(lo0, hi0, 0x5140u);     // k 0, 1, 2, 3
-    o.y = prmt(lo0, hi0, 0x7362u);     // k 4, 5, 6, 7
-    o.z = prmt(lo1, hi1, 0x5140u);
-    o.w = prmt(lo1, hi1, 0x7362u);
-    return o;
+    return make_uint4(pk.x & 0x0F0F0F0Fu, (pk.x >> 4) & 0x0F0F0F0Fu, pk.y & 0x0F0F0F0Fu,
+                      (pk.y >> 4) & 0x0F0F0F0Fu);
 }
 
-// 0xFF in byte j where bit 2j of b is set (j = 0..3), else 0x00.  The
-// multiply places bit 2j at bit 8j + 7 (shifts 7, 13, 19, 25); the other
-// partial products land on bits 9, 11, 13 (twice), 17, 19 (twice), 21, 25
-// (twice), 27 and 29, whose carries stop at the even bits 14, 20 and 26 that no
-// product reaches, so bits 7, 15, 23 and 31 hold exactly b0, b2, b4, b6.
-// The byte permute then replicates each byte's top bit over the byte.
-__device__ __forceinline__ uint32_t even_bit_mask(uint32_t b) {
-    return prmt((b & 0x55u) * 0x02082080u, 0u, 0xBA98u);
-}
-// The same for the odd bits 2j + 1: the constant is the even one halved, so
-// the products land on the same positions without a shift first.
-__device__ __forceinline__ uint32_t odd_bit_mask(uint32_t b) {
-    return prmt((b & 0xAAu) * 0x01041040u, 0u, 0xBA98u);
-}
-
-// int5 weights: sixteen packed low nibbles plus their sixteen fifth bits
-// (bit i of hb = the fifth bit of k = i) -> sixteen e4m3 bytes of value
-// (c - 16) * 2^-9, c = nibble + 16 * bit, in k order.  Fifth bit 1: c - 16 is
-// the nibble itself, the byte of expand16.  Fifth bit 0: c - 16 = -(16 -
-// nibble) with 16 - nibble in 1..16, and that magnitude alone in a byte is
-// again its own e4m3 value times 2^-9 (16 -> 0x10 = 2^-5), so the byte is
-// 0x80 | (16 - nibble) = 0x90 - nibble (no borrow leaves a byte).  The
-// selection runs on the even-k and odd-k nibble words before the interleave.
-__device__ __forceinline__ uint4 expand16_int5(uint2 pk, uint32_t hb) {
-    uint32_t nib[4] = {pk.x & 0x0F0F0F0Fu, (pk.x >> 4) & 0x0F0F0F0Fu, pk.y & 0x0F0F0F0Fu,
-                       (pk.y >> 4) & 0x0F0F0F0Fu};
-    // word q holds k = 8 (q / 2) + (q % 2) + 2j in byte j
-    const uint32_t hb8 = hb >> 8;
-    const uint32_t msk[4] = {even_bit_mask(hb), odd_bit_mask(hb), even_bit_mask(hb8), odd_bit_mask(hb8)};
+// int5 weights: sixteen packed low nibbles plus their sixteen fifth bits ->
+// sixteen e4m3 bytes of value (c - 16) * 2^-9, c = nibble + 16 * bit, in k
+// order.  Fifth bit 1: c - 16 is the nibble itself, the byte of expand16.
+// Fifth bit 0: c - 16 = -(16 - nibble) with 16 - nibble in 1..16, and that
+// magnitude alone in a byte is again its own e4m3 value times 2^-9 (16 ->
+// 0x10 = 2^-5), so the byte is 0x80 | (16 - nibble) = 0x90 - nibble (no
+// borrow leaves a byte).  hs is the 32-k fifth-bit block word shifted right by
+// 4h for the 16-k half h it covers, so that bit q of byte j is the fifth bit
+// of k = 4q + j of these sixteen (bit 4 + q: the other half's, or nothing).
+// Shifting it left by 7 - q puts the bits of word q's four k on the four
+// byte top bits (every other bit lands below a top bit), and the
+// sign-replicating byte permute widens them to byte masks.
+__device__ __forceinline__ uint4 expand16_int5(uint2 pk, uint32_t hs) {
+    const uint4 e = expand16(pk);
+    uint32_t nib[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) nib[q] = (nib[q] & msk[q]) | ((0x90909090u - nib[q]) & ~msk[q]);
-    uint4 o;
-    o.x = prmt(nib[0], nib[1], 0x5140u);
-    o.y = prmt(nib[0], nib[1], 0x7362u);
-    o.z = prmt(nib[2], nib[3], 0x5140u);
-    o.w = prmt(nib[2], nib[3], 0x7362u);
-    return o;
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t msk = prmt(hs << (7 - q), 0u, 0xBA98u);
+        nib[q] = (nib[q] & msk) | ((0x90909090u - nib[q]) & ~msk);
+    }
+    return make_uint4(nib[0], nib[1], nib[2], nib[3]);
 }
 
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFF))); }
