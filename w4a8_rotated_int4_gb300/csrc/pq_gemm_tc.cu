@@ -115,9 +115,25 @@ constexpr uint32_t kZLbo = 0, kZSbo = 128;
 struct __align__(128) SzfSlot {
     uint8_t za[BM * 16];      // row operand: (h, h, m, h, l, m, 0, 0) of -rs / 2 (row warps)
     uint8_t zb[BN * 16];      // column operand: (zh, zm, zh, zl, zh, zm, 0, 0) of zq (expand warps)
-    float2 col[BN / 2];       // column pair j: (2^9 sc', 2^9 sc'') of columns 2j, 2j + 1
-    float row[BM];            // asg of tile row i (0 past M); per-token: unused
+    // 2^9 sc' per column and asg per tile row (0 past M; per-token: unused),
+    // each stored in the order a fold thread reads them (col_slot, row_slot),
+    // so that it loads a 32-column step's scales and its four rows' asg with
+    // 16-byte loads, one conflict-free wavefront each
+    float col[BN];
+    float row[BM];
 };
+// column n: pair P = n / 2 is read by fold lane c4 = P % 4 in step cb = P / 16
+// as element j = (P / 4) % 4 of its eight floats at (4 cb + c4) * 8
+__device__ __forceinline__ int col_slot(int n) {
+    const int P = n >> 1;
+    return ((((P >> 4) * 4 + (P & 3)) * 4 + ((P >> 2) & 3)) << 1) + (n & 1);
+}
+// tile row 128 h + 32 q + 8 ri + g4 is read by fold warp (h, q), lane group g4,
+// as element ri of its four floats at ((4 h + q) * 8 + g4) * 4
+__device__ __forceinline__ int row_slot(int row) {
+    const int h = row >> 7, q = (row >> 5) & 3, ri = (row >> 3) & 3, g4 = row & 7;
+    return ((h * 4 + q) * 8 + g4) * 4 + ri;
+}
 
 struct Ctrl {
     uint64_t full_tma[kStages];
@@ -386,6 +402,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // loads of slab it + 1 are issued before slab it is stored, so their
         // latency overlaps the wait for the slab's slot.
         const int row0 = (BM / 2) * (warp - kRowWarp) + lane;
+        const int rslot0 = row_slot(row0);    // row row0 + 32 u sits at rslot0 + 32 u
         pdl_wait();        // asg and rs are the preceding prologue's output
         int ti = 0, kb = 0, n0 = 0, m0 = 0, p = 0;   // the slab whose rows are loaded next
         bool half_item;
@@ -430,7 +447,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int row = row0 + 32 * u;
-                if constexpr (!kTok) szf[r].row[row] = av[u];
+                if constexpr (!kTok) szf[r].row[rslot0 + 32 * u] = av[u];
                 // rs = h + m + l (bf16 parts): the row operand (h, h, m, h, l, m)
                 // of -rs / 2 against (zh, zm, zh, zl, zh, zm) in the column
                 // operand; the MMA reads the eight values twice (kZLbo = 0), so
@@ -601,7 +618,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 bf16_split3(zq, h, m, l);
                 *reinterpret_cast<uint4 *>(szf[r].zb + (et >> 3) * kZSbo + (et & 7) * 16) =
                     make_uint4(h | (m << 16), h | (l << 16), h | (m << 16), 0u);
-                reinterpret_cast<float *>(szf[r].col)[et] = kNibbleScale * sce;
+                szf[r].col[col_slot(et)] = kNibbleScale * sce;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -674,28 +691,29 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // four steps (32-column block cb), each two 16x256b.x4 loads
                 // (16-lane halves sh = 0, 1) in flight behind one wait
                 // per row: the asg splat (per-token: none, As is applied at the end)
-                uint64_t sa2[4];
-#pragma unroll
-                for (int ri = 0; ri < 4; ++ri) {
-                    if constexpr (kTok) {
-                        sa2[ri] = 0;
-                    } else {
-                        const float v = szf[r].row[row0 + 8 * ri];
-                        sa2[ri] = f2pack(v, v);
-                    }
+                uint64_t sa2[4] = {0, 0, 0, 0};
+                if constexpr (!kTok) {
+                    const float4 v = *reinterpret_cast<const float4 *>(szf[r].row + row_slot(row0));
+                    sa2[0] = f2pack(v.x, v.x);
+                    sa2[1] = f2pack(v.y, v.y);
+                    sa2[2] = f2pack(v.z, v.z);
+                    sa2[3] = f2pack(v.w, v.w);
                 }
-                // column pair 8 J + 2 c4 (J = 0..15) of the slab: col[4 J + c4]
-                const float2 *cf = szf[r].col + c4;
+                // column pairs 8 J + 2 c4 (J = 4 cb + j, j = 0..3) of step cb:
+                // eight floats at (4 cb + c4) * 8 (col_slot)
+                const float4 *cf = reinterpret_cast<const float4 *>(szf[r].col) + 2 * c4;
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t d0[16], d1[16];
                     tmem_issue256(taddr + 32 * cb, d0);
                     tmem_issue256(taddr + ((uint32_t)16 << 16) + 32 * cb, d1);
                     uint64_t z[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 v = cf[4 * (4 * cb + j)];
-                        z[j] = f2pack(v.x, v.y);
+                    {
+                        const float4 v01 = cf[8 * cb], v23 = cf[8 * cb + 1];
+                        z[0] = f2pack(v01.x, v01.y);
+                        z[1] = f2pack(v01.z, v01.w);
+                        z[2] = f2pack(v23.x, v23.y);
+                        z[3] = f2pack(v23.z, v23.w);
                     }
                     tmem_wait32(d0, d1);
                     if (cb == 3) {       // every load of this buffer has completed
