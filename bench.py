@@ -444,17 +444,17 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
         sha256="ebf585e72de7ffe731635559c79391796330cff2feec4a082210b7f6de53525b"),
     ("pq_gemm_tc", "prefill"): dict(
-        bytes=71158528 + 37806848,
+        bytes=72359936 + 38439168,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="5d0430075c3b05214a4be042ad62211c67b798c374b8a6a3b22c97aaa7de700c"),
+        sha256="8ddafd2a536289b0a8ed5973aaf82ef1ef18b8b88f9c1915bad3b72b25c01b08"),
     ("pq_gemm_tc", "down"): dict(
-        bytes=99590912 + 54865408,
+        bytes=99625472 + 54697728,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="5d0430075c3b05214a4be042ad62211c67b798c374b8a6a3b22c97aaa7de700c"),
+        sha256="8ddafd2a536289b0a8ed5973aaf82ef1ef18b8b88f9c1915bad3b72b25c01b08"),
     ("pq_gemm_tc", "qkv"): dict(
-        bytes=30699520 + 11008,
+        bytes=30699520 + 768,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="5d0430075c3b05214a4be042ad62211c67b798c374b8a6a3b22c97aaa7de700c"),
+        sha256="8ddafd2a536289b0a8ed5973aaf82ef1ef18b8b88f9c1915bad3b72b25c01b08"),
     ("pq_gemm_tcn", "decode:16"): dict(
         bytes=47476480 + 0,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
