@@ -243,7 +243,6 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    pdl_trigger();     // the next kernel may start its own load-time prefetch
 
     // the last block (weight producers) or slab (activation producer) issued
     // and the last slab an MMA warp committed, for the drain after a give-up
@@ -508,6 +507,13 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                 mbar_arrive(&ctl->row_empty[rr]);
             }
         }
+        // Dependent launch only now, as the CTA is about to finish: a CTA of
+        // this kernel fills its SM, so a dependent grid launched earlier
+        // crowds its CTAs onto the SMs this grid leaves idle (N/128 tiles
+        // against the SM count) and runs them there, several to an SM, once
+        // this grid completes.  A following prologue then took up to 3 us
+        // longer (decode M = 16: step 21.2 against 19.6 us).
+        pdl_trigger();
         // the sets meet in shared memory, in operand slot 0's expanded-weight
         // buffer: it is free only once BOTH sets have seen their last batch
         // (then every expansion and MMA has completed) -- a set that finishes
