@@ -1,3 +1,4 @@
+import gc
 import os
 import sys
 
@@ -18,3 +19,15 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _collect_cycles_after_test(request):
+    """GPU tests: after each test, free what reference cycles still hold.
+    A CUDA graph that a cycle keeps past its test is otherwise destroyed at the
+    next garbage collection, which may fall inside another test's stream
+    capture and invalidate it (graph destruction is not permitted while a
+    global-mode capture is running)."""
+    yield
+    if request.node.get_closest_marker("gpu") is not None:
+        gc.collect()

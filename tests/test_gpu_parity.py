@@ -392,6 +392,7 @@ def test_gemm_dispatch_beyond_skinny_k(pq, orc, M):
     with pytest.raises(pq.PQError) as e:
         pq.pq_gemm_skinny(a, asg, rs, L.w_d, L.sz_d)
     assert e.value.status == 2
+    del e      # the traceback holds this frame: no cycle may keep its CUDA objects alive
 
 
 @pytest.mark.parametrize("subnormal", [False, True])
@@ -842,6 +843,7 @@ def test_layer_graph_zero_copy(pq, orc, M, N):
     with pytest.raises(pq.PQError) as e:
         pq.pq_check_device_access(torch.empty((M, K), dtype=torch.bfloat16))   # pageable
     assert e.value.status == 8
+    del e      # the traceback holds this frame, and the frame will hold the graph
     step = layer.make_graph(xh, yh, zero_copy=True)
     for seed in (75 + M, 175 + M, 275 + M):
         x = pqgen.make_problem(M, K, N, seed=seed).x

@@ -542,7 +542,12 @@ class PQLinear:
         from x_host and the GEMM writes y straight into y_host (page-locked
         host memory mapped at the same device address, checked with
         pq_check_device_access), so the bytes cross the host link inside the
-        kernels and the step has no copy operations."""
+        kernels and the step has no copy operations.
+
+        The returned function owns a CUDA graph: release it (and anything that
+        keeps it alive, such as a reference cycle) outside any stream capture.
+        A graph destroyed while another global-mode capture is running
+        invalidates that capture."""
         torch = _torch()
         dev = self.w.device
         M, K = x_host.shape
