@@ -203,6 +203,7 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int M = prm.M, G = prm.K / BK;
     const int nbatch = (G + kBatch - 1) / kBatch;
+    const int nwb = (G + kWSlabs - 1) / kWSlabs;     // weight blocks of kWSlabs slabs
     const int n0 = blockIdx.x * NN;
     const int p = (n0 >= prm.pb1 ? 1 : 0) + (n0 >= prm.pb2 ? 1 : 0);
 
@@ -231,6 +232,20 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         for (int w = 0; w < kMmaWarps; ++w) mbar_init(&ctl->drain[w], 1);
         ctl->abort = 0;
         fence_mbar_init();
+        // The first ring's worth of weight blocks, before the tensor-memory
+        // allocation and the block-wide barrier: load-time tables that need no
+        // wait, so the first HBM round trip overlaps the CTA's setup.  The
+        // producers below continue from block kW on.
+        prefetch_map(&tmB);
+        prefetch_map(&tmS);
+        if constexpr (kBits == 5) prefetch_map(&tmH);
+        for (int wb = 0; wb < kW && wb < nwb; ++wb) {
+            const int it = wb * kWSlabs;
+            mbar_arrive_expect_tx(&ctl->w_full[wb], kTxW);
+            tma_load_2d(ws[wb].bp, &tmB, it * (BK / 2), n0, &ctl->w_full[wb]);
+            tma_load_2d(ws[wb].sz, &tmS, 8 * it, n0 / 8, &ctl->w_full[wb]);
+            if constexpr (kBits == 5) tma_load_2d(ws[wb].bh, &tmH, it * (BK / 8), n0, &ctl->w_full[wb]);
+        }
     }
     if (warp == kMmaWarp0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -253,13 +268,11 @@ tcn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         // the preceding kernel, so they stream without waiting for it.
         if (lane == 0) {
             const int tw = warp;
-            prefetch_map(&tmB);
-            prefetch_map(&tmS);
-            if constexpr (kBits == 5) prefetch_map(&tmH);
             // weight block wb = slabs kWSlabs wb .. +kWSlabs-1 (a box past K
-            // reads as zero)
-            const int nwb = (G + kWSlabs - 1) / kWSlabs;
-            for (int wb = tw; wb < nwb; wb += kTmaWWarps) {
+            // reads as zero); this warp owns the blocks wb = tw (mod
+            // kTmaWWarps), those below kW issued at the start by thread 0
+            for (int wb = tw; wb < kW && wb < nwb; wb += kTmaWWarps) last = wb;
+            for (int wb = tw + kW; wb < nwb; wb += kTmaWWarps) {
                 const int s = wb % kW, use = wb / kW;
                 if (use > 0 && !wait_or_abort(&ctl->w_empty[s], (use - 1) & 1, abort_flag, prm.wait)) {
                     set_abort(ctl, prm.status, kStatusWaitEmpty);
