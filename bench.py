@@ -456,9 +456,9 @@ NCU_TRAFFIC = {
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
         sha256="8ddafd2a536289b0a8ed5973aaf82ef1ef18b8b88f9c1915bad3b72b25c01b08"),
     ("pq_gemm_tcn", "decode:16"): dict(
-        bytes=47476224 + 0,
+        bytes=47479552 + 512,
         src=[_CSRC + "pq_gemm_tcn.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
-        sha256="9dd004344bd17d12cbaf8531ba44f9596ecc4afa488cde2a34fd851c89417c29"),
+        sha256="2d7ff27b4dafff28166a5aa77267241f542efa9f11d7e8942924852fa83fd60a"),
 }
 
 
