@@ -35,6 +35,10 @@
 //                consecutive slabs): one thread per output feature, one
 //                barrier test per batch, tcgen05.ld 32x32b.x16 per slab and
 //                acc[m] += asg[m] * (2^9 sc * D'[m] - zs8 * rs[m]) for m < M.
+// Thread 0 issues the first ring of weight copies as soon as the barriers are
+// initialised, ahead of the TMEM allocation, and the dependent launch is
+// triggered only after the fold loop: a CTA fills its SM, and a dependent grid
+// launched earlier crowds onto the SMs this grid leaves idle.
 // The weights are read exactly once, so the kernel is bound by HBM when the
 // grid covers the GPU.
 //
@@ -71,8 +75,9 @@ constexpr int BK = 128;           // one scale group per slab
 // larger copies and a slower stream).
 constexpr int kWSlabs = 1;
 // int5 weight slots carry the fifth-bit planes too, so int5 keeps four of them
-// to leave room for eight operand slots.  (An int5 layout with four operand
-// slots gave run-to-run differences in a few output columns; it is not used.)
+// to leave room for eight operand slots.  (Four operand slots measured slower;
+// a version with four once raced because a weight slot was released to the
+// TMA after generic reads with no proxy fence, which every release now has.)
 template <int kBits>
 constexpr int kWSlotsOf = kBits == 5 ? 4 : 8;   // weight ring (packed weights, SZ words, fifth bits), kWSlabs slabs each
 template <int kBits>
