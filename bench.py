@@ -233,10 +233,10 @@ class Workload:
         self.sz5 = [u16(sz) for _ in range(self.copies)]
         self.gemm5_bytes = self.gemm_bytes + whi.nbytes
 
-    def gemm5(self, pq, i, stream):
+    def gemm5(self, pq, i, stream, fn=None):
         j = i % self.copies
-        pq.pq_gemm5(self.a[j], self.asg[j], self.rs[j], self.w5[j], self.whi5[j], self.sz5[j], self.pb1, self.pb2,
-                    y=self.y[j], stream=stream)
+        (fn or pq.pq_gemm5)(self.a[j], self.asg[j], self.rs[j], self.w5[j], self.whi5[j], self.sz5[j], self.pb1,
+                            self.pb2, y=self.y[j], stream=stream)
 
     def gemm(self, pq, i, stream, fn=None):
         j = i % self.copies
@@ -349,6 +349,12 @@ def time_workload(pq, torch, wl, steps, warmup, stream, barrier=None, sampler=No
     # the same GEMM on int5 weights
     wl.int5_buffers(pq, torch, wl.x[0].device)
     out["int5_gemm_ms"] = time_each(wl.gemm5)
+    if wl.c["M"] <= 16:
+        # the two int5 decode kernels on their own (pq_gemm5 takes one of them)
+        out["int5_paths"] = {
+            "tcn": time_each(lambda pq_, j, s: wl.gemm5(pq_, j, s, fn=pq_.pq_gemm5_tcn)),
+            "skinny": time_each(lambda pq_, j, s: wl.gemm5(pq_, j, s, fn=pq_.pq_gemm5_skinny)),
+        }
     if wl.c["M"] > 16:
         # the per-token activation-scale path: its two-pass prologue, then its GEMM
         wl.ptok_buffers(torch, wl.x[0].device)
@@ -549,7 +555,8 @@ def summarize(wl, r, steps, peaks, clocks=None, sms=None):
         "int5": {"gemm_us": round(r["int5_gemm_ms"] * 1e3, 3),
                  "gemm_gbs": round(wl.gemm5_bytes / (r["int5_gemm_ms"] * 1e-3) / 1e9, 1),
                  "gemm_tflops": round(wl.flops / (r["int5_gemm_ms"] * 1e-3) / 1e12, 2),
-                 "vs_int4_time": round(r["int5_gemm_ms"] / r["gemm_ms"], 3)},
+                 "vs_int4_time": round(r["int5_gemm_ms"] / r["gemm_ms"], 3),
+                 "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("int5_paths", {}).items()}},
         "copies": wl.copies,
         "gemm_us_by_kernel": {k: round(v * 1e3, 3) for k, v in r.get("paths", {}).items()},
     }
@@ -805,6 +812,7 @@ def main():
         "producer_us": head["producer_us"], "silu_producer_us": head["silu_producer_us"],
         "roofline": head["roofline"],
         "gemm_us_by_kernel": head["gemm_us_by_kernel"],
+        "int5": head["int5"],
         "e2e": None if e2e_ms is None else {
             "value": round(e2e_graph_ms * 1e3, 3), "unit": "us", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "how": "public API PQLinear.make_graph(zero_copy=True): one CUDA "

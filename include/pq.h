@@ -72,8 +72,9 @@ extern "C" {
  * 6: the byte layouts of w (pq_pack, pq_pack5) and whi (pq_pack5) change: a
  *    word's low nibbles hold four consecutive k and its high nibbles the next
  *    four, and whi is laid out in 32-k blocks; weights packed by an earlier
- *    version must be packed again.  Signatures are unchanged. */
-#define PQ_ABI_VERSION 6
+ *    version must be packed again.  Signatures are unchanged.
+ * 7: adds pq_gemm5_skinny. */
+#define PQ_ABI_VERSION 7
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
@@ -409,10 +410,15 @@ pq_status pq_gemm_ptok(const void *a, const float *As, const float *rs, int M, i
  * and (sc, zs) from pq_pack5's SZ table.  The tensor cores take (c - 16) * 2^-9
  * itself, exact in e4m3.  Tolerance and arguments as pq_gemm, plus
  *   w, whi, sz  device copies of pq_pack5's outputs (whi 16-byte aligned)
- * pq_gemm5 dispatches: M <= 16 with at least half the SMs covered by the
- * 128-feature tiles runs the narrow tensor-core kernel (pq_gemm5_tcn), anything
- * else the prefill tensor-core kernel (pq_gemm5_tc).  pq_gemm5_tcn accepts
- * 1 <= M <= 16.  dev_status as for pq_gemm_tc.
+ * pq_gemm5 dispatches as pq_gemm: M = 1 to the CUDA-core kernel
+ * (pq_gemm5_skinny); 2 <= M <= 16 to the narrow tensor-core kernel
+ * (pq_gemm5_tcn) when its 128-feature tiles cover at least half the SMs, else
+ * to the CUDA-core kernel; any M <= 16 with K > 16384 to the narrow kernel;
+ * M > 16 to the prefill tensor-core kernel (pq_gemm5_tc).  pq_gemm5_tcn and
+ * pq_gemm5_skinny accept 1 <= M <= 16 (the CUDA-core kernel K <= 16384): it
+ * is pq_gemm_skinny with each fifth bit ORed into the f16 word of its nibble
+ * (bit 4 above a low nibble, bit 8 above a high one), so the same FMA takes
+ * the 5-bit code.  dev_status as for pq_gemm_tc.
  * Errors: PQ_ERR_NULL, PQ_ERR_SHAPE, PQ_ERR_ALIGN, PQ_ERR_PARTITION,
  * PQ_ERR_ARCH, PQ_ERR_CUDA.
  */
@@ -425,6 +431,9 @@ pq_status pq_gemm5_tc(const void *a, const float *asg, const float *rs, int M, i
 pq_status pq_gemm5_tcn(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
                        int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y,
                        int ldy, unsigned int *dev_status, void *stream);
+pq_status pq_gemm5_skinny(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
+                          int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y,
+                          int ldy, unsigned int *dev_status, void *stream);
 
 /*
  * The prologue's device e4m3 encoder applied to n fp32 values ([CVT]: NaN ->

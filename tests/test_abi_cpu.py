@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(pq.EXPORTS)
-    assert pq.pq_abi_version() == 6
+    assert pq.pq_abi_version() == 7
     for s in range(9):
         assert L.pq_status_string(s)
     assert L.pq_status_string(99) == b"unknown status"
@@ -137,6 +137,7 @@ def test_gemm_argument_checks(L, case, status):
     v5 = vals[:10] + [A] + vals[10:]             # whi after w
     assert L.pq_gemm5(*v5, None) == status
     assert L.pq_gemm5_tc(*v5, None, None) == status
+    assert L.pq_gemm5_skinny(*v5, None, None) == status
     assert L.pq_last_error()
 
 
@@ -227,6 +228,7 @@ def test_device_calls_without_gpu_report_arch(L):
     assert L.pq_gemm_ptok(*vals, None, None) == 6
     v5 = vals[:10] + [A] + vals[10:]
     assert L.pq_gemm5(*v5, None) == 6 and L.pq_gemm5_tcn(*v5, None, None) == 6
+    assert L.pq_gemm5_skinny(*v5, None, None) == 6
     assert L.pq_gemm5(*(vals[:10] + [None] + vals[10:]), None) == 1
     assert L.pq_e4m3_encode(S, A, 16, None) == 6
     with pytest.raises(pq.PQError) as e:

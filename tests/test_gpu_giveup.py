@@ -72,7 +72,7 @@ def build_case(pq, orc, path, M, K, N):
         f = orc.gemm5_f64 if bits == 5 else orc.gemm_f64
         y64 = f(a_o, s_o, rs_o, t["codes"], t["sz"], prob.pb1, prob.pb2)
     name = {"skinny": "pq_gemm_skinny", "tcn": "pq_gemm_tcn", "tc": "pq_gemm_tc", "ptok": "pq_gemm_ptok",
-            "tc5": "pq_gemm5_tc", "tcn5": "pq_gemm5_tcn"}[path]
+            "tc5": "pq_gemm5_tc", "tcn5": "pq_gemm5_tcn", "skinny5": "pq_gemm5_skinny"}[path]
     fn = getattr(pq.lib(), name)
     P = a.shape[0]
 
@@ -111,6 +111,7 @@ def is_nan_bf16(bits):
 GIVEUP_CASES = [  # path, M, K, N: several ring turns per CTA
     ("skinny", 1, 5120, 17408),
     ("skinny", 3, 2048, 16384),
+    ("skinny5", 1, 5120, 17408),
     ("tcn", 4, 5120, 8192),
     ("tcn5", 16, 2048, 4096),
     ("tc", 300, 4096, 2048),

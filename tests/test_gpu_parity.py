@@ -695,7 +695,8 @@ class Problem5:
 
 
 def run_gemm5(name, a, asg, rs, L, pb1, pb2, M, N, ldy=None):
-    """pq_gemm5_tc / pq_gemm5_tcn through the C ABI into a NaN-filled strided y."""
+    """An int5 GEMM path (pq_gemm5_tc, _tcn or _skinny) through the C ABI into a
+    NaN-filled strided y."""
     import ctypes as C
     import w4a8_rotated_int4_gb300 as m
     ldy = ldy or N
@@ -717,7 +718,7 @@ def run_gemm5(name, a, asg, rs, L, pb1, pb2, M, N, ldy=None):
 
 
 def gemm5_paths(M):
-    return ["pq_gemm5_tc"] + (["pq_gemm5_tcn"] if M <= 16 else [])
+    return ["pq_gemm5_tc"] + (["pq_gemm5_tcn", "pq_gemm5_skinny"] if M <= 16 else [])
 
 
 INT5_SMALL = [  # M, K, N, P, pb
@@ -779,7 +780,7 @@ def test_gemm5_all_fifth_bits_equal_int4(pq, orc):
     y4 = orc.gemm_f64(a_h, s_h, r_h, L4.t["codes"], L4.t["sz"], N, N)
     y64 = orc.gemm5_f64(a_h, s_h, r_h, L5.t["codes"], L5.t["sz"], N, N)
     assert orc.rel_err(y64, y4) < 1e-3
-    for name in ("pq_gemm5_tc", "pq_gemm5_tcn"):
+    for name in ("pq_gemm5_tc", "pq_gemm5_tcn", "pq_gemm5_skinny"):
         assert_close(run_gemm5(name, a, asg, rs, L5, N, N, M, N), y64, name)
 
 
@@ -797,6 +798,10 @@ def test_gemm5_full_workload_sampled(pq, orc, name, M):
     ms, ns = _samples(prob.M, prob.N, prob.pb1, prob.pb2, 3000, 17)
     y64 = orc.gemm5_f64_sampled(ms, ns, a_o, asg_o, rs_o, L.t["codes"], L.t["sz"], prob.pb1, prob.pb2)
     assert_close(y.float().cpu().numpy()[ms, ns], y64, "int5 %s M=%d" % (name, prob.M))
+    if prob.M <= 16:      # the CUDA-core int5 kernel on the same inputs
+        ys = pq.pq_gemm5_skinny(a, asg, rs, L.w_d, L.whi_d, L.sz_d, prob.pb1, prob.pb2)
+        torch.cuda.synchronize()
+        assert_close(ys.float().cpu().numpy()[ms, ns], y64, "int5 skinny %s M=%d" % (name, prob.M))
 
 
 # ---------------------------------------------------------------- graph API

@@ -27,7 +27,7 @@ EXPORTS = (
     "pq_gemm_tc",
     "pq_gemm_tcn",
     "pq_rotate_tokquant", "pq_rotate_tokquant_noalloc", "pq_gemm_ptok",
-    "pq_pack5", "pq_gemm5", "pq_gemm5_tc", "pq_gemm5_tcn",
+    "pq_pack5", "pq_gemm5", "pq_gemm5_tc", "pq_gemm5_tcn", "pq_gemm5_skinny",
     "pq_e4m3_encode", "pq_test_set_wait_limit_ns", "pq_check_device_access",
 )
 
@@ -90,7 +90,7 @@ def lib() -> C.CDLL:
     L.pq_pack5.argtypes = [i32, i32, i32] + [vp] * 11
     L.pq_gemm5.restype = i32
     L.pq_gemm5.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, vp, i32, vp]
-    for name in ("pq_gemm5_tc", "pq_gemm5_tcn"):
+    for name in ("pq_gemm5_tc", "pq_gemm5_tcn", "pq_gemm5_skinny"):
         f = getattr(L, name)
         f.restype = i32
         f.argtypes = [vp, vp, vp] + [i32] * 6 + [vp, vp, vp, vp, i32, vp, vp]
@@ -472,6 +472,11 @@ def pq_gemm5_tc(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, dev_status=N
 def pq_gemm5_tcn(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
     return _gemm5_path(lib().pq_gemm5_tcn, "pq_gemm5_tcn", a, asg, rs, w, whi, sz, pb1, pb2, y, dev_status,
                        stream)
+
+
+def pq_gemm5_skinny(a, asg, rs, w, whi, sz, pb1=None, pb2=None, y=None, dev_status=None, stream=None):
+    return _gemm5_path(lib().pq_gemm5_skinny, "pq_gemm5_skinny", a, asg, rs, w, whi, sz, pb1, pb2, y,
+                       dev_status, stream)
 
 
 def pq_e4m3_encode(x, out=None, stream=None):

@@ -519,6 +519,22 @@ extern "C" pq_status pq_gemm5_tcn(const void *a, const float *asg, const float *
     return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, whi);
 }
 
+extern "C" pq_status pq_gemm5_skinny(const void *a, const float *asg, const float *rs, int M, int N, int K,
+                                     int P, int pb1, int pb2, const void *w, const void *whi, const void *sz,
+                                     void *y, int ldy, unsigned int *dev_status, void *stream) {
+    clear_error();
+    pq_status st = check_gemm_args(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy);
+    if (st != PQ_OK) return st;
+    if (!whi) return fail(PQ_ERR_NULL, "NULL whi");
+    if (!aligned(whi, 16)) return fail(PQ_ERR_ALIGN, "whi needs 16-byte alignment");
+    if (M > kSkinnyMaxM) return fail(PQ_ERR_SHAPE, "pq_gemm5_skinny: M = %d > %d", M, kSkinnyMaxM);
+    if (dev_status && !aligned(dev_status, 4)) return fail(PQ_ERR_ALIGN, "dev_status alignment");
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != PQ_OK) return st;
+    return launch_gemm_skinny(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, dev_status, stream, sms, whi);
+}
+
 extern "C" pq_status pq_gemm5(const void *a, const float *asg, const float *rs, int M, int N, int K, int P,
                               int pb1, int pb2, const void *w, const void *whi, const void *sz, void *y,
                               int ldy, void *stream) {
@@ -530,10 +546,16 @@ extern "C" pq_status pq_gemm5(const void *a, const float *asg, const float *rs, 
     int sms = 0;
     st = check_device(&sms);
     if (st != PQ_OK) return st;
-    // M <= 16: the narrow tensor-core kernel when its 128-feature tiles cover at
-    // least half the SMs; otherwise (and for M > 16) the prefill kernel
-    if (M <= kTcnMaxM && 2 * (N / 128) >= sms)
-        return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, whi);
+    // As pq_gemm: M = 1 on the CUDA-core kernel (fewest instructions per
+    // weight); 2 <= M <= 16 on the narrow tensor-core kernel when its
+    // 128-feature tiles cover at least half the SMs, else on the CUDA-core
+    // kernel; any M <= 16 with K above the CUDA-core limit on the narrow
+    // kernel; M > 16 on the prefill kernel.
+    if (M <= kSkinnyMaxM) {
+        if ((M >= 2 && M <= kTcnMaxM && 2 * (N / 128) >= sms) || K > kSkinnyMaxK)
+            return launch_gemm_tcn(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, whi);
+        return launch_gemm_skinny(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, sms, whi);
+    }
     return launch_gemm_tc(a, asg, rs, M, N, K, P, pb1, pb2, w, sz, y, ldy, nullptr, stream, sms, false, whi);
 }
 

@@ -66,12 +66,15 @@ struct SkinnyParams {
     const float *asg;
     const float *rs;
     const uint8_t *w;
+    const uint8_t *whi;     // int5: fifth-bit planes [N][K/8] (else null)
     const uint32_t *sz;     // [N/8][G][8] words: f16 scale | f16 zscale << 16
     __nv_bfloat16 *y;
     unsigned int *status;
     int M, N, K, G, pb1, pb2, ldy;
     int oct_per_cta, n_oct, nkw, ngrp, stages;
-    uint32_t stage_bytes, w_bytes;
+    // a stage: the octet's nibble rows (w_bytes), its fifth-bit rows (h_bytes,
+    // int5 only) and its SZ words (from sz_off)
+    uint32_t stage_bytes, w_bytes, h_bytes, sz_off;
     WaitBound wait;           // the pipeline waits' bound
 };
 
@@ -87,6 +90,10 @@ __device__ __forceinline__ uint32_t hmul2_sixteenth(uint32_t a) {
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x2C002C00u));
     return r;
 }
+
+// v shifted left by s bits (right by -s when s < 0); s is a compile-time
+// constant after unrolling
+__device__ __forceinline__ uint32_t shift_bits(uint32_t v, int s) { return s >= 0 ? v << s : v >> -s; }
 
 // acc_lo += a.lo * b.lo, acc_hi += a.hi * b.hi with f16 operands and fp32 accumulators
 __device__ __forceinline__ void fma2_f32_f16(float &acc_lo, float &acc_hi, uint32_t a, uint32_t b) {
@@ -151,13 +158,14 @@ __device__ __forceinline__ int produce_octets(const SkinnyParams &prm, uint8_t *
         const int o = oct0 + i;
         mbar_arrive_expect_tx(&full[s], prm.stage_bytes);
         bulk_g2s(st, prm.w + (size_t)o * 8 * (K / 2), prm.w_bytes, &full[s]);
-        bulk_g2s(st + prm.w_bytes, prm.sz + (size_t)o * G * 8, 32u * (uint32_t)G, &full[s]);
+        if (prm.h_bytes) bulk_g2s(st + prm.w_bytes, prm.whi + (size_t)o * prm.h_bytes, prm.h_bytes, &full[s]);
+        bulk_g2s(st + prm.sz_off, prm.sz + (size_t)o * G * 8, 32u * (uint32_t)G, &full[s]);
         issued = i + 1;
     }
     return issued;
 }
 
-template <int MT>
+template <int MT, int kBits>
 __global__ void skinny_kernel(const SkinnyParams prm) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int nkw = prm.nkw, S = prm.stages, ngrp = prm.ngrp;
@@ -196,8 +204,11 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
         const int g = kvalid ? (k0 >> 7) : 0;
         pdl_wait();        // a, asg, rs are the preceding prologue's output
         uint32_t A[MT][16];
-        // per row of this lane's group: 2^24 asg, asg * rs and 8 * asg * rs
-        float asg24_r[MT], ar_r[MT], ar8_r[MT];
+        // per row of this lane's group: 2^24 asg, asg * rs and zo * asg * rs,
+        // zo = 8 (int4: the codes are summed raw, so zscale + 8 sc) or 16
+        // (int5: zscale + 16 sc)
+        constexpr float kZOff = kBits == 5 ? 16.0f : 8.0f;
+        float asg24_r[MT], ar_r[MT], arz_r[MT];
         int cur_p = -1;
         // s = i mod S and use = i / S, stepped without a division (S is a
         // multiple of ngrp, so s wraps back to grp)
@@ -216,7 +227,7 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                     uint32_t u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                     asg24_r[m] = 0.0f;
                     ar_r[m] = 0.0f;
-                    ar8_r[m] = 0.0f;
+                    arz_r[m] = 0.0f;
                     if (kvalid && row < M) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(
                             prm.a + ((size_t)p * M + row) * K + k0);
@@ -226,7 +237,7 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                         const float sa = __ldg(prm.asg + ((size_t)p * G + g) * M + row);
                         asg24_r[m] = sa * 16777216.0f;
                         ar_r[m] = sa * __ldg(prm.rs + ((size_t)p * G + g) * M + row);
-                        ar8_r[m] = 8.0f * ar_r[m];
+                        arz_r[m] = kZOff * ar_r[m];
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -266,11 +277,28 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0.0f;
                 const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+                // int5: the fifth bits of this lane's 32 k, one 32-k block word
+                // (bit 8j' + q' of the word: k = 4q' + j')
+                uint32_t hw = 0;
+                if constexpr (kBits == 5)
+                    if (kvalid) hw = *reinterpret_cast<const uint32_t *>(st + prm.w_bytes + (size_t)j * (K / 8) + (k0 >> 3));
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t x = wq[q], x8 = x >> 8;
-                    const uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
-                    const uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
+                    uint32_t lo = x & 0x000F000Fu, hi = x & 0x00F000F0u;
+                    uint32_t lo2 = x8 & 0x000F000Fu, hi2 = x8 & 0x00F000F0u;
+                    if constexpr (kBits == 5) {
+                        // Each fifth bit joins its nibble in the same f16 half: at
+                        // bit 4 above a low nibble (c = nibble + 16 b) and at bit 8
+                        // above a high nibble used as 16 nibble, so the one FMA
+                        // multiplies the 5-bit code (mantissa bits 0..8, still a
+                        // subnormal).  The shifts bring the bits of k = 8q + {0, 2},
+                        // {4, 6}, {1, 3}, {5, 7} to those places.
+                        lo |= shift_bits(hw, 4 - 2 * q) & 0x00100010u;
+                        hi |= shift_bits(hw, 7 - 2 * q) & 0x01000100u;
+                        lo2 |= (hw >> (4 + 2 * q)) & 0x00100010u;
+                        hi2 |= (hw >> (2 * q + 1)) & 0x01000100u;
+                    }
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         fma2_f32_f16(acc[m][0], acc[m][1], A[m][4 * q + 0], lo);
@@ -285,7 +313,7 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
             // this lane's group folds columns cb, cb+1 (cb even): the SZ words of
             // (octet, group g) are contiguous, one 8-byte load
             const int cb = 4 * ((lane >> 1) & 1) + 2 * (lane & 1);
-            const uint2 szp = *reinterpret_cast<const uint2 *>(st + prm.w_bytes + 32 * g + 4 * cb);
+            const uint2 szp = *reinterpret_cast<const uint2 *>(st + prm.sz_off + 32 * g + 4 * cb);
             // the stage is refilled by a bulk copy (the async proxy): order this
             // warp's reads of it before that write, then release it
             fence_proxy_async_smem();
@@ -300,11 +328,11 @@ __global__ void skinny_kernel(const SkinnyParams prm) {
                 float h4[4], h2[2];
                 split_step<8>(S[m], h4, lane, 2);
                 split_step<4>(h4, h2, lane, 1);
-                // fold (once per group and column): asg * (sc * D' - (zs + 8 sc) * rs)
+                // fold (once per group and column): asg * (sc * D' - (zs + zo sc) * rs)
                 // with D' = 2^24 * sum
                 float f[2];
-                f[0] = fmaf(sc0 * asg24_r[m], h2[0], -fmaf(sc0, ar8_r[m], zs0 * ar_r[m]));
-                f[1] = fmaf(sc1 * asg24_r[m], h2[1], -fmaf(sc1, ar8_r[m], zs1 * ar_r[m]));
+                f[0] = fmaf(sc0 * asg24_r[m], h2[0], -fmaf(sc0, arz_r[m], zs0 * ar_r[m]));
+                f[1] = fmaf(sc1 * asg24_r[m], h2[1], -fmaf(sc1, arz_r[m], zs1 * ar_r[m]));
                 // sum the 8 groups of the warp: bit 4 keeps 1 of 2, bits 3 and 2 add
                 float h1[1];
                 split_step<2>(f, h1, lane, 16);
@@ -409,7 +437,8 @@ pq_status launch_ring(SkinnyFn k, int mt, SkinnyParams prm, int sm_count, cudaSt
 
 pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, int M, int N, int K,
                              int P, int pb1, int pb2, const void *w, const void *sz, void *y,
-                             int ldy, unsigned int *dev_status, void *stream, int sm_count) {
+                             int ldy, unsigned int *dev_status, void *stream, int sm_count,
+                             const void *whi) {
     (void)P;
     if (K > kMaxK) return fail(PQ_ERR_SHAPE, "pq_gemm_skinny: K = %d > %d", K, kMaxK);
     SkinnyParams prm{};
@@ -417,6 +446,7 @@ pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, i
     prm.asg = asg;
     prm.rs = rs;
     prm.w = static_cast<const uint8_t *>(w);
+    prm.whi = static_cast<const uint8_t *>(whi);
     prm.sz = static_cast<const uint32_t *>(sz);
     prm.y = static_cast<__nv_bfloat16 *>(y);
     prm.status = dev_status;
@@ -431,18 +461,28 @@ pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, i
     prm.n_oct = N / 8;
     prm.nkw = (K + 1023) / 1024;
     prm.w_bytes = (uint32_t)(8 * (K / 2));
-    prm.stage_bytes = prm.w_bytes + 32u * (uint32_t)prm.G;
+    prm.h_bytes = whi ? (uint32_t)(8 * (K / 8)) : 0u;      // int5: the octet's fifth-bit rows
+    prm.sz_off = prm.w_bytes + prm.h_bytes;
+    prm.stage_bytes = prm.sz_off + 32u * (uint32_t)prm.G;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // rows per M-tile: the smallest power of two >= M (at most 8) whose
-    // instantiation fits the register file with one group of k-warps
+    // rows per M-tile: the smallest power of two >= M (at most 8; int5 at most
+    // 4) whose instantiation fits the register file with one group of k-warps
     const int w1 = prm.nkw + 1;
-    if (M == 1 && fits_registers(skinny_kernel<1>, w1)) return launch_ring(skinny_kernel<1>, 1, prm, sm_count, st);
-    if (M <= 2 && fits_registers(skinny_kernel<2>, w1)) return launch_ring(skinny_kernel<2>, 2, prm, sm_count, st);
-    if (M <= 4 && fits_registers(skinny_kernel<4>, w1)) return launch_ring(skinny_kernel<4>, 4, prm, sm_count, st);
-    if (fits_registers(skinny_kernel<8>, w1)) return launch_ring(skinny_kernel<8>, 8, prm, sm_count, st);
-    if (fits_registers(skinny_kernel<4>, w1)) return launch_ring(skinny_kernel<4>, 4, prm, sm_count, st);
-    if (fits_registers(skinny_kernel<2>, w1)) return launch_ring(skinny_kernel<2>, 2, prm, sm_count, st);
-    if (fits_registers(skinny_kernel<1>, w1)) return launch_ring(skinny_kernel<1>, 1, prm, sm_count, st);
+    if (whi) {
+        if (M == 1 && fits_registers(skinny_kernel<1, 5>, w1)) return launch_ring(skinny_kernel<1, 5>, 1, prm, sm_count, st);
+        if (M <= 2 && fits_registers(skinny_kernel<2, 5>, w1)) return launch_ring(skinny_kernel<2, 5>, 2, prm, sm_count, st);
+        if (fits_registers(skinny_kernel<4, 5>, w1)) return launch_ring(skinny_kernel<4, 5>, 4, prm, sm_count, st);
+        if (fits_registers(skinny_kernel<2, 5>, w1)) return launch_ring(skinny_kernel<2, 5>, 2, prm, sm_count, st);
+        if (fits_registers(skinny_kernel<1, 5>, w1)) return launch_ring(skinny_kernel<1, 5>, 1, prm, sm_count, st);
+        return fail(PQ_ERR_CUDA, "pq_gemm5_skinny: no instantiation fits K = %d", K);
+    }
+    if (M == 1 && fits_registers(skinny_kernel<1, 4>, w1)) return launch_ring(skinny_kernel<1, 4>, 1, prm, sm_count, st);
+    if (M <= 2 && fits_registers(skinny_kernel<2, 4>, w1)) return launch_ring(skinny_kernel<2, 4>, 2, prm, sm_count, st);
+    if (M <= 4 && fits_registers(skinny_kernel<4, 4>, w1)) return launch_ring(skinny_kernel<4, 4>, 4, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<8, 4>, w1)) return launch_ring(skinny_kernel<8, 4>, 8, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<4, 4>, w1)) return launch_ring(skinny_kernel<4, 4>, 4, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<2, 4>, w1)) return launch_ring(skinny_kernel<2, 4>, 2, prm, sm_count, st);
+    if (fits_registers(skinny_kernel<1, 4>, w1)) return launch_ring(skinny_kernel<1, 4>, 1, prm, sm_count, st);
     return fail(PQ_ERR_CUDA, "pq_gemm_skinny: no instantiation fits K = %d", K);
 }
 

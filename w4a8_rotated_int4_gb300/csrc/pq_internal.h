@@ -42,7 +42,7 @@ pq_status launch_e4m3_encode(const float *in, uint8_t *out, size_t n, void *stre
 pq_status launch_gemm_skinny(const void *a, const float *asg, const float *rs, int M, int N,
                              int K, int P, int pb1, int pb2, const void *w, const void *sz,
                              void *y, int ldy, unsigned int *dev_status, void *stream,
-                             int sm_count);
+                             int sm_count, const void *whi = nullptr);
 pq_status launch_gemm_tc(const void *a, const float *asg, const float *rs, int M, int N, int K,
                          int P, int pb1, int pb2, const void *w, const void *sz, void *y,
                          int ldy, unsigned int *dev_status, void *stream, int sm_count,
