@@ -446,9 +446,9 @@ def e2e_graph_workload(pq, torch, wl, steps, warmup, stream, zero_copy=True):
 _CSRC = "w4a8_rotated_int4_gb300/csrc/"
 NCU_TRAFFIC = {
     ("pq_gemm_skinny", "decode:1"): dict(
-        bytes=47381760 + 0,
+        bytes=47382528 + 0,
         src=[_CSRC + "pq_gemm_skinny.cu", _CSRC + "pq_device.cuh"],
-        sha256="ebf585e72de7ffe731635559c79391796330cff2feec4a082210b7f6de53525b"),
+        sha256="8ae33f144b01316d9ba3ed44a5a901a7adf157283aa932cb99984aba391671e7"),
     ("pq_gemm_tc", "prefill"): dict(
         bytes=72359936 + 38439168,
         src=[_CSRC + "pq_gemm_tc.cu", _CSRC + "pq_tcgen05.cuh", _CSRC + "pq_device.cuh"],
