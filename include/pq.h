@@ -73,8 +73,11 @@ extern "C" {
  *    word's low nibbles hold four consecutive k and its high nibbles the next
  *    four, and whi is laid out in 32-k blocks; weights packed by an earlier
  *    version must be packed again.  Signatures are unchanged.
- * 7: adds pq_gemm5_skinny. */
-#define PQ_ABI_VERSION 7
+ * 7: adds pq_gemm5_skinny.
+ * 8: the records of pq_pack and pq_pack5 are stored in chained order (see
+ *    pq_pack) with a keep flag in byte 2; records packed by an earlier
+ *    version must be packed again.  Signatures are unchanged. */
+#define PQ_ABI_VERSION 8
 
 /* Largest number of distinct rotations (partitions) one GEMM launch serves
  * ([Format] and the "Traps hit" note: the GEMM's limit applies to distinct
@@ -129,10 +132,25 @@ pq_status pq_pack_sizes(int K, int N, int P, size_t *rec_bytes, size_t *sz_bytes
  *   theta    f16   [P][8][K/2] angle of pair t of group g at index 64g + t
  *
  * Outputs:
- *   rec  [P][8][G][64] records of 8 bytes ([D3]): uint32 (i | j << 8), then
- *        uint16 f16(cos theta), uint16 f16(sin theta); cos/sin are evaluated in
- *        double precision (host libm) and rounded once to f16 (nearest, ties
- *        to even).
+ *   rec  [P][8][G][64] records of 8 bytes ([D3]): bytes u, v, keep, 0, then
+ *        uint16 f16(cos theta), uint16 f16(+-sin theta); cos/sin are evaluated
+ *        in double precision (host libm) and rounded once to f16 (nearest,
+ *        ties to even).  A record (u, v, c, s) rotates as
+ *            v[u], v[v] = fl(fl(c*v[u]) + fl(s*v[v])), fl(fl(c*v[v]) - fl(s*v[u]))
+ *        so a pages' pair (i, j) may be stored as (j, i) with its sine negated
+ *        (bit-identical results).  Chained order, per (p, g): layer 0 lists
+ *        the pairs in the pages' order t = 0..63 as (i, j); for r < 7, keep
+ *        (bit 0 of byte 2) names the output of slot t that the next layer
+ *        uses first (0: u, 1: v), and slot t of layer r + 1 holds the pair
+ *        containing that channel, with it as u.  Every pair of layer r + 1
+ *        receives exactly one kept channel: the kept channels are taken along
+ *        the alternating cycles of the two layers' pairings, each cycle walked
+ *        from its lowest channel c0 over its layer-r pair (c0, y0), keeping
+ *        y0, then from y0's layer-(r+1) partner over its layer-r pair, and so
+ *        on.  keep is 0 in layer 7.  Within a layer the order of the pairs
+ *        does not change the result (they are disjoint), but the prologues
+ *        rely on the chained order and the keep flags: records in another
+ *        order give wrong results.
  *   sz   the SZ table ([D1]): for column n and group g the f16 pair
  *        (sc, f16(sc * (zp - 8))) -- the product is taken in fp32 (exact) and
  *        rounded once to f16 -- stored as one 4-byte word (scale in the low

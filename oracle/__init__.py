@@ -166,6 +166,64 @@ def records(pairs: np.ndarray, theta: np.ndarray) -> np.ndarray:
     return out
 
 
+def chain_records(rec: np.ndarray) -> np.ndarray:
+    """The records [P, 8, G, 64, 8] rearranged into the library's chained
+    storage order (a layout of this library, not a step of the method).
+
+    Layer 0 keeps the given order.  Between layers r and r + 1 the two
+    pairings form alternating cycles; taking the cycles by their lowest
+    channel c0, the walk goes c0 -> its layer-r partner y (kept: byte 2 of
+    that layer-r record = 1 if y is its second channel) -> y's layer-(r+1)
+    partner -> ... until it is back at c0.  Slot t of layer r + 1 is the
+    layer-(r+1) pair holding the channel slot t kept, that channel first;
+    a pair stored reversed gets its sine's sign bit flipped, which leaves the
+    rotation unchanged because fl(-a) = -fl(a) and x - y = x + (-y) exactly.
+    """
+    rec = np.asarray(rec, dtype=np.uint8)
+    P, L, G, T, _ = rec.shape
+    out = np.zeros_like(rec)
+    for p in range(P):
+        for g in range(G):
+            # the current layer's slots as (first, second, cos bits, sin bits)
+            cur = [(int(rec[p, 0, g, t, 0]), int(rec[p, 0, g, t, 1]),
+                    int(rec[p, 0, g, t, 4]) | int(rec[p, 0, g, t, 5]) << 8,
+                    int(rec[p, 0, g, t, 6]) | int(rec[p, 0, g, t, 7]) << 8) for t in range(T)]
+            for r in range(L):
+                keep_second = [0] * T
+                if r + 1 < L:
+                    nxt = {}                 # channel -> (partner, cos, sin, is first in the given order)
+                    for t in range(T):
+                        i, j = int(rec[p, r + 1, g, t, 0]), int(rec[p, r + 1, g, t, 1])
+                        c = int(rec[p, r + 1, g, t, 4]) | int(rec[p, r + 1, g, t, 5]) << 8
+                        s = int(rec[p, r + 1, g, t, 6]) | int(rec[p, r + 1, g, t, 7]) << 8
+                        nxt[i] = (j, c, s, True)
+                        nxt[j] = (i, c, s, False)
+                    where = {}               # channel -> (slot, partner) in layer r
+                    for t, (u, v, _, _) in enumerate(cur):
+                        where[u] = (t, v)
+                        where[v] = (t, u)
+                    new = [None] * T
+                    done = set()
+                    for c0 in range(2 * T):
+                        if c0 in done:
+                            continue
+                        x = c0
+                        while True:
+                            t, y = where[x]
+                            done.update((x, y))
+                            keep_second[t] = 1 if y == cur[t][1] else 0
+                            partner, c, s, first = nxt[y]
+                            new[t] = (y, partner, c, s if first else s ^ 0x8000)
+                            x = partner
+                            if x == c0:
+                                break
+                for t, (u, v, c, s) in enumerate(cur):
+                    out[p, r, g, t] = (u, v, keep_second[t], 0, c & 0xFF, c >> 8, s & 0xFF, s >> 8)
+                if r + 1 < L:
+                    cur = new
+    return out
+
+
 def sz_table(scales: np.ndarray, qzeros: np.ndarray) -> np.ndarray:
     """SZ table [G, N, 2] f16 bit patterns (scale, scale*(zp-8))."""
     scales = _c(scales, np.uint16)
@@ -259,7 +317,8 @@ def pack5(prob) -> dict:
     """Oracle's own load-time tables for a generated int5 problem."""
     sz = sz5_table(prob["scales"], prob["qzeros"], prob["qzeros_hi"])
     w, whi = repack5(prob["qweight"], prob["qweight_hi"])
-    return dict(rec=records(prob["pairs"], prob["theta"]), sz=sz, sz_kernel=sz_kernel_layout(sz),
+    rec = records(prob["pairs"], prob["theta"])
+    return dict(rec=rec, rec_kernel=chain_records(rec), sz=sz, sz_kernel=sz_kernel_layout(sz),
                 w=w, whi=whi, codes=codes5(prob["qweight"], prob["qweight_hi"], prob["N"]),
                 zp=codes5(prob["qzeros"], prob["qzeros_hi"], prob["N"]))
 
@@ -453,7 +512,8 @@ def linear_rotw_f64(x, cs, pairs, theta, W, pb1, pb2) -> np.ndarray:
 def pack(prob) -> dict:
     """Oracle's own load-time tables for a generated problem."""
     sz = sz_table(prob["scales"], prob["qzeros"])
-    return dict(rec=records(prob["pairs"], prob["theta"]),
+    rec = records(prob["pairs"], prob["theta"])
+    return dict(rec=rec, rec_kernel=chain_records(rec),
                 sz=sz, sz_kernel=sz_kernel_layout(sz),
                 w=repack(prob["qweight"]),
                 codes=unpack_awq(prob["qweight"], prob["N"]),

@@ -53,7 +53,7 @@ class Problem:
                                                prob.pairs, prob.theta)
         self.t = orc.pack(prob)
         if check_pack:
-            assert np.array_equal(self.rec, self.t["rec"])
+            assert np.array_equal(self.rec, self.t["rec_kernel"])
             assert np.array_equal(self.sz, self.t["sz_kernel"])
             assert np.array_equal(self.w, self.t["w"])
         self.rec_d = torch.from_numpy(self.rec).cuda()
@@ -127,9 +127,9 @@ def test_prologue_bit_exact(pq, orc, name, over):
     P, M, K, G = prob.P, prob.M, prob.K, prob.G
     rec = orc.records(prob.pairs, prob.theta)
     rec_p, _, _ = pq.pq_pack(prob.qweight, prob.qzeros, prob.scales, prob.pairs, prob.theta)
-    assert np.array_equal(rec, rec_p)
+    assert np.array_equal(orc.chain_records(rec), rec_p)
     bufs, (a, asg, rs), pad = canary_outputs(P, M, K, G)
-    pq.pq_rotate_quant(dev_u16(prob.x).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+    pq.pq_rotate_quant(dev_u16(prob.x).view(torch.bfloat16), torch.from_numpy(orc.chain_records(rec)).cuda(),
                        dev_u16(prob.cs), a=a, asg=asg, rs=rs)
     torch.cuda.synchronize()
     a_o, asg_o, rs_o = orc.rotate_quant(prob.x, prob.cs, rec)
@@ -154,7 +154,7 @@ def test_prologue_tiny_and_huge_scales(pq, orc):
         xf[r] *= np.float32(f)
     x = pqgen.to_bf16_bits(xf)
     rec = orc.records(prob.pairs, prob.theta)
-    xd, rd, cd = dev_u16(x).view(torch.bfloat16), torch.from_numpy(rec).cuda(), dev_u16(prob.cs)
+    xd, rd, cd = dev_u16(x).view(torch.bfloat16), torch.from_numpy(orc.chain_records(rec)).cuda(), dev_u16(prob.cs)
     a, asg, rs = pq.pq_rotate_quant(xd, rd, cd)
     _, a2, As, rs2 = pq.pq_rotate_tokquant(xd, rd, cd)
     torch.cuda.synchronize()
@@ -173,7 +173,7 @@ def test_prologue_strided_x(pq, orc):
     xw = np.full((37, 384 + 64), 0x7FC0, dtype=np.uint16)     # NaN padding must never be read
     xw[:, :384] = prob.x
     rec = orc.records(prob.pairs, prob.theta)
-    a, asg, rs = pq.pq_rotate_quant(dev_u16(xw).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+    a, asg, rs = pq.pq_rotate_quant(dev_u16(xw).view(torch.bfloat16), torch.from_numpy(orc.chain_records(rec)).cuda(),
                                     dev_u16(prob.cs))
     a_o, asg_o, rs_o = orc.rotate_quant(xw, prob.cs, rec)
     assert np.array_equal(a.cpu().numpy(), a_o)
@@ -212,7 +212,7 @@ def test_add_rms_rotate_quant_bit_exact(pq, orc, M, K, P, pad):
     bufs, (a, asg, rs), gpad = canary_outputs(P, M, K, G)
     ro, h, a, asg, rs = pq.pq_add_rms_rotate_quant(
         dev_u16(xw).view(torch.bfloat16), dev_u16(res).view(torch.bfloat16), dev_u16(gamma).view(torch.bfloat16),
-        1e-6, torch.from_numpy(rec).cuda(), dev_u16(prob.cs), a=a, asg=asg, rs=rs)
+        1e-6, torch.from_numpy(orc.chain_records(rec)).cuda(), dev_u16(prob.cs), a=a, asg=asg, rs=rs)
     torch.cuda.synchronize()
     ro_o, h_o, a_o, asg_o, rs_o = orc.add_rms_rotate_quant(xw, res, gamma, 1e-6, prob.cs, rec)
     u16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
@@ -258,7 +258,7 @@ def test_silu_mul_rotate_quant_bit_exact(pq, orc, M, I, P, pad):
     rec = orc.records(prob.pairs, prob.theta)
     G = I // 128
     bufs, (a, asg, rs), gpad = canary_outputs(P, M, I, G)
-    act, a, asg, rs = pq.pq_silu_mul_rotate_quant(dev_u16(y).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+    act, a, asg, rs = pq.pq_silu_mul_rotate_quant(dev_u16(y).view(torch.bfloat16), torch.from_numpy(orc.chain_records(rec)).cuda(),
                                                   dev_u16(prob.cs), a=a, asg=asg, rs=rs)
     torch.cuda.synchronize()
     act_o, a_o, asg_o, rs_o = orc.silu_mul_rotate_quant(y, prob.cs, rec)
@@ -592,7 +592,7 @@ def test_rotate_tokquant_bit_exact(pq, orc, M, K, P, pb, zero_rows, knobs):
     bufs, (a, _, rs), _ = canary_outputs(P, M, K, G, pad)
     xr = xr_buf[pad:pad + P * M * K].view(P, M, K).view(torch.bfloat16)
     As = as_buf[pad:pad + P * M].view(P, M)
-    pq.pq_rotate_tokquant(dev_u16(x).view(torch.bfloat16), torch.from_numpy(rec).cuda(), dev_u16(prob.cs),
+    pq.pq_rotate_tokquant(dev_u16(x).view(torch.bfloat16), torch.from_numpy(orc.chain_records(rec)).cuda(), dev_u16(prob.cs),
                           xr=xr, a=a, As=As, rs=rs)
     torch.cuda.synchronize()
     xr_o, a_o, As_o, rs_o = orc.rotate_tokquant(x, prob.cs, rec)
@@ -621,7 +621,7 @@ def test_rotate_tokquant_long_rows(pq, orc):
     M, K = 3, 118784
     prob = pqgen.make_problem(M, K, 128, seed=K + M)
     rec = orc.records(prob.pairs, prob.theta)
-    xr, a, As, rs = pq.pq_rotate_tokquant(dev_u16(prob.x).view(torch.bfloat16), torch.from_numpy(rec).cuda(),
+    xr, a, As, rs = pq.pq_rotate_tokquant(dev_u16(prob.x).view(torch.bfloat16), torch.from_numpy(orc.chain_records(rec)).cuda(),
                                           dev_u16(prob.cs))
     torch.cuda.synchronize()
     xr_o, a_o, As_o, rs_o = orc.rotate_tokquant(prob.x, prob.cs, rec)
@@ -682,7 +682,7 @@ class Problem5:
                                                           prob.qzeros_hi, prob.scales, prob.pairs, prob.theta)
         self.t = orc.pack5(prob)
         if check_pack:
-            assert np.array_equal(self.rec, self.t["rec"])
+            assert np.array_equal(self.rec, self.t["rec_kernel"])
             assert np.array_equal(self.sz, self.t["sz_kernel"])
             assert np.array_equal(self.w, self.t["w"])
             assert np.array_equal(self.whi, self.t["whi"])

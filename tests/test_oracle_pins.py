@@ -203,6 +203,103 @@ def test_pairs_validation(orc):
     assert not orc.check_pairs(bad2)
 
 
+# ------------------------------------------------- chained record order
+def _check_chain(plain, chained):
+    """The chained records hold the same rotation as the plain ones: per
+    layer the same pairs with the same cosines and the sines of reversed
+    pairs negated, layer 0 unchanged, and every kept channel leads the next
+    layer's slot, one kept channel per next-layer pair."""
+    pi, pj, pup, pc, ps = _rec_fields(plain)
+    ci, cj, cup, cc, cs_ = _rec_fields(chained)
+    assert np.all(pup == 0)
+    keep = cup & 0xFF
+    assert np.all(cup >> 8 == 0) and np.all((keep == 0) | (keep == 1)) and np.all(keep[:, 7] == 0)
+    P, L, G, T = pi.shape
+    for p in range(P):
+        for g in range(G):
+            for r in range(L):
+                want = {}
+                for t in range(T):
+                    want[(int(pi[p, r, g, t]), int(pj[p, r, g, t]))] = (int(pc[p, r, g, t]), int(ps[p, r, g, t]))
+                for t in range(T):
+                    u, v = int(ci[p, r, g, t]), int(cj[p, r, g, t])
+                    if (u, v) in want:
+                        assert want.pop((u, v)) == (int(cc[p, r, g, t]), int(cs_[p, r, g, t]))
+                    else:
+                        assert want.pop((v, u)) == (int(cc[p, r, g, t]), int(cs_[p, r, g, t]) ^ 0x8000)
+                assert not want
+                if r + 1 < L:
+                    kept = [int(cj[p, r, g, t]) if keep[p, r, g, t] else int(ci[p, r, g, t]) for t in range(T)]
+                    assert [int(ci[p, r + 1, g, t]) for t in range(T)] == kept
+
+
+def test_chain_records_valid(orc):
+    prob = pqgen.make_problem(1, 384, 128, P=3, seed=21)
+    plain = orc.records(prob.pairs, prob.theta)
+    chained = orc.chain_records(plain)
+    _check_chain(plain, chained)
+    assert np.array_equal(chained[:, 0, ..., :2], plain[:, 0, ..., :2])
+    assert np.array_equal(chained[:, 0, ..., 4:], plain[:, 0, ..., 4:])
+
+
+def test_chain_records_hand_examples(orc):
+    """Small pairings worked by hand."""
+    theta = np.zeros((1, 8, 64), dtype=np.uint16)
+    theta[0, :, :] = np.float16(0.25).view(np.uint16)
+    sin_bits = int(np.float16(np.sin(np.float64(np.float16(0.25)))).view(np.uint16))
+    neg = sin_bits ^ 0x8000
+    t = np.arange(64)
+    ident = np.arange(128, dtype=np.int16)                      # (0,1), (2,3), ...
+    shifted = np.roll(ident, -1)                                # (1,2), (3,4), ..., (127,0)
+    swapped = ident.reshape(64, 2)[:, ::-1].reshape(-1).copy()  # (1,0), (3,2), ...
+
+    # identity / shifted alternating: one cycle through all channels.
+    # 0 -> 1: the walk from 0 keeps 1, 3, 5, ... (each slot's second channel);
+    #   slot t of layer 1 is shifted's pair (2t+1, 2t+2) in its own order.
+    # 1 -> 2: the walk from 0 meets slot 63 = (127, 0) and keeps 127, then
+    #   125, ...: every slot keeps its first channel 2t+1, which leads
+    #   identity's pair (2t, 2t+1) reversed (sine negated).
+    # 2 -> 3: the walk from 0 meets slot 0 = (1, 0) and keeps 1: first again.
+    ch = orc.chain_records(orc.records(np.stack([ident, shifted] * 4)[None], theta))
+    i, j, up, c16, s16 = _rec_fields(ch)
+    assert np.array_equal(up[0, :, 0], np.array([1] + [0] * 7)[:, None] * np.ones((1, 64), np.int64))
+    for r in (1, 3, 5, 7):
+        assert np.array_equal(i[0, r, 0], 2 * t + 1) and np.array_equal(j[0, r, 0], (2 * t + 2) % 128)
+        assert np.all(s16[0, r, 0] == sin_bits)
+    for r in (2, 4, 6):
+        assert np.array_equal(i[0, r, 0], 2 * t + 1) and np.array_equal(j[0, r, 0], 2 * t)
+        assert np.all(s16[0, r, 0] == neg)
+
+    # the same pairs, the odd layers given reversed: cycles of length two;
+    # 0 -> 1 keeps 2t+1, which is first in swapped's (2t+1, 2t): no negation
+    ch = orc.chain_records(orc.records(np.stack([ident, swapped] * 4)[None], theta))
+    i, j, up, c16, s16 = _rec_fields(ch)
+    assert np.all(up[0, 0, 0] == 1)
+    assert np.array_equal(i[0, 1, 0], 2 * t + 1) and np.array_equal(j[0, 1, 0], 2 * t)
+    assert np.all(s16[0, 1, 0] == sin_bits)
+
+    # the same pairs in the same order in every layer: layer 0 keeps 2t+1,
+    # which then leads (2t+1, 2t) in every later layer, kept as the first
+    ch = orc.chain_records(orc.records(np.stack([ident] * 8)[None], theta))
+    i, j, up, c16, s16 = _rec_fields(ch)
+    assert np.all(up[0, 0, 0] == 1) and np.all(up[0, 1:, 0] == 0)
+    for r in range(1, 8):
+        assert np.array_equal(i[0, r, 0], 2 * t + 1) and np.array_equal(j[0, r, 0], 2 * t)
+        assert np.all(s16[0, r, 0] == neg)
+    assert np.all(c16 == c16[0, 0, 0, 0])
+
+
+def test_chain_records_rotate_identically(orc):
+    """The oracle's prologue gives the same bits with the chained records as
+    with the pages' order (the reversal with a negated sine is exact)."""
+    prob = pqgen.make_problem(37, 640, 128, P=2, seed=8)
+    plain = orc.records(prob.pairs, prob.theta)
+    chained = orc.chain_records(plain)
+    assert not np.array_equal(plain, chained)
+    for x1, x2 in zip(orc.rotate_quant(prob.x, prob.cs, plain), orc.rotate_quant(prob.x, prob.cs, chained)):
+        assert np.array_equal(np.asarray(x1).view(np.uint8), np.asarray(x2).view(np.uint8))
+
+
 # ------------------------------------------------------------------ SZ table
 def test_sz_exhaustive_against_numpy(orc):
     """(sc, f16(sc*(zp-8))) for every positive finite f16 scale and zp 0..15."""

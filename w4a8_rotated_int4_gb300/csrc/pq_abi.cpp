@@ -216,25 +216,82 @@ static pq_status pack_layer(int K, int N, int P, const int32_t *qweight, const i
         }
     }
 
-    // rotation records: [p][layer][g][t] = {i | j<<8, f16 cos, f16 sin}
+    // rotation records: [p][layer][g][slot] = {u, v, keep, 0, f16 cos, f16 sin},
+    // in chained order (pq.h): layer 0 in the pages' order; slot t of layer
+    // r + 1 holds the pair of the channel that slot t keeps from layer r, that
+    // channel first (u), the sine negated where this reverses the pages' pair.
+    // The kept channels of a layer are chosen along the alternating cycles of
+    // the two layers' pairings, walked from the lowest unvisited channel:
+    // cycle x0 -r- y0 -(r+1)- x1 -r- y1 ... keeps y0, y1, ..., so that every
+    // pair of layer r + 1 receives exactly one kept channel.
     uint8_t *ro = static_cast<uint8_t *>(rec);
-    for (int pl = 0; pl < P * 8; ++pl)
-        for (int g = 0; g < G; ++g)
+    for (int p = 0; p < P; ++p)
+        for (int g = 0; g < G; ++g) {
+            int u[64], v[64], src[64];      // this layer's slots: channels, pages' pair index
+            bool rev[64];                   // (u, v) is the pages' pair reversed
+            const int16_t *p0 = pairs + (size_t)p * 8 * K + 128 * g;
             for (int t = 0; t < 64; ++t) {
-                const int16_t *pr = pairs + (size_t)pl * K + 128 * g;
-                const double th = half_value(theta[(size_t)pl * (K / 2) + 64 * g + t]);
-                const uint16_t c = half_bits_rne(std::cos(th));
-                const uint16_t s = half_bits_rne(std::sin(th));
-                uint8_t *o = ro + (((size_t)pl * G + g) * 64 + t) * 8;
-                o[0] = (uint8_t)pr[2 * t];
-                o[1] = (uint8_t)pr[2 * t + 1];
-                o[2] = 0;
-                o[3] = 0;
-                o[4] = (uint8_t)(c & 0xFF);
-                o[5] = (uint8_t)(c >> 8);
-                o[6] = (uint8_t)(s & 0xFF);
-                o[7] = (uint8_t)(s >> 8);
+                u[t] = p0[2 * t];
+                v[t] = p0[2 * t + 1];
+                src[t] = t;
+                rev[t] = false;
             }
+            for (int r = 0; r < 8; ++r) {
+                const size_t pl = (size_t)p * 8 + r;
+                uint8_t keep_v[64] = {};
+                int nu[64], nv[64], nsrc[64];
+                bool nrev[64];
+                if (r < 7) {
+                    const int16_t *pn = pairs + (pl + 1) * K + 128 * g;
+                    int mate[128], slot[128], mate_n[128], pair_n[128];
+                    for (int t = 0; t < 64; ++t) {
+                        mate[u[t]] = v[t];
+                        mate[v[t]] = u[t];
+                        slot[u[t]] = slot[v[t]] = t;
+                        const int a = pn[2 * t], b = pn[2 * t + 1];
+                        mate_n[a] = b;
+                        mate_n[b] = a;
+                        pair_n[a] = pair_n[b] = t;
+                    }
+                    bool seen[128] = {};
+                    for (int c0 = 0; c0 < 128; ++c0) {
+                        if (seen[c0]) continue;
+                        int x = c0;
+                        do {
+                            const int y = mate[x], t = slot[x], tn = pair_n[y];
+                            seen[x] = seen[y] = true;
+                            keep_v[t] = (uint8_t)(y == v[t]);
+                            nu[t] = y;
+                            nv[t] = mate_n[y];
+                            nsrc[t] = tn;
+                            nrev[t] = pn[2 * tn] != y;
+                            x = mate_n[y];
+                        } while (x != c0);
+                    }
+                }
+                for (int t = 0; t < 64; ++t) {
+                    const double th = half_value(theta[pl * (K / 2) + 64 * g + src[t]]);
+                    const uint16_t c = half_bits_rne(std::cos(th));
+                    const uint16_t s = (uint16_t)(half_bits_rne(std::sin(th)) ^ (rev[t] ? 0x8000u : 0u));
+                    uint8_t *o = ro + ((pl * G + g) * 64 + t) * 8;
+                    o[0] = (uint8_t)u[t];
+                    o[1] = (uint8_t)v[t];
+                    o[2] = keep_v[t];
+                    o[3] = 0;
+                    o[4] = (uint8_t)(c & 0xFF);
+                    o[5] = (uint8_t)(c >> 8);
+                    o[6] = (uint8_t)(s & 0xFF);
+                    o[7] = (uint8_t)(s >> 8);
+                }
+                if (r < 7)
+                    for (int t = 0; t < 64; ++t) {
+                        u[t] = nu[t];
+                        v[t] = nv[t];
+                        src[t] = nsrc[t];
+                        rev[t] = nrev[t];
+                    }
+            }
+        }
 
     // SZ table: (sc, f16(sc * (zp - offset))), the product exact in fp32, one
     // word per (column, group) at [n/8][g][n%8]

@@ -12,18 +12,21 @@
 // saturate at 448).
 //
 // Layout on the GPU (M > 16).  One CTA owns a tile of 64 tokens x one
-// 128-group x one partition (the partition is the grid's z dimension); the
-// records of (p, g) are decoded once into shared-memory byte offsets and f16
-// cos/sin.  The tile is held in shared memory as v[k][token pair] (two fp32
-// values, tokens 2l and 2l+1, per 8-byte word): in a Givens layer lane l of a
-// warp works on its two tokens of one pair (i, j) at a time, so the 32 lanes
-// read v[i][0..31] and v[j][0..31] -- consecutive 8-byte words, free of bank
-// conflicts whatever the pair permutation is.  Each of the 8 warps takes 8
-// of the 64 disjoint pairs of a layer (in two batches of 4: all loads, then
-// all stores); the layers are separated by __syncthreads.  Every multiply, add,
-// subtract and divide is a separately rounded IEEE operation (explicit .rn
-// intrinsics), so results are bit-identical to an fp32 CPU evaluation in the
-// same order.
+// 128-group x one partition (the partition is the grid's z dimension).  The
+// tile is held in shared memory as v[k][token pair] (two fp32 values, tokens
+// 2l and 2l+1, per 8-byte word): in a Givens layer lane l of a warp works on
+// its two tokens of one pair at a time, so the 32 lanes touch consecutive
+// 8-byte words, free of bank conflicts whatever the pair permutation is.
+// Each of the 8 warps owns 8 of the 64 slots of every layer.  The records come
+// in the packer's chained order: the channel a slot keeps from one layer is
+// the first channel of its pair in the next, so each slot holds that value in
+// registers and exchanges only the other one through shared memory -- one
+// 8-byte load and one store per slot and layer instead of two of each.  The
+// records of (p, g) are decoded once into byte offsets and fp32 coefficient
+// pairs, one per output, in the space of the consumed x tile.  The layers are
+// separated by __syncthreads.  Every multiply, add, subtract and divide is a
+// separately rounded IEEE operation (explicit .rn intrinsics), so results are
+// bit-identical to an fp32 CPU evaluation in the same order.
 //
 // Decode band (M <= 16): 64 threads per token, thread t owns pair t of every
 // layer and keeps its 8 records in registers; one CTA per (token block, group,
@@ -65,17 +68,23 @@ static_assert(kPairsPerWarp % kBatch == 0 && kChPerWarp % 16 == 0, "work split")
 constexpr int kXsStride = 65;         // words per staged x row (64 + 1 pad)
 constexpr int kCodeStride = 144;      // bytes per staged code row
 
+// A decoded record: per slot the two outputs as coefficient pairs on the
+// slot's two operands, out1 = fl(fl(x1 a) + fl(y1 b)), out2 = fl(fl(x2 a) +
+// fl(y2 b)), and two byte offsets into v (see rotate_quant_kernel).
 struct __align__(16) Smem {
     float2 v[128][kTok / 2];          // 32 KB, v[k][token pair]: (token 2l, token 2l+1)
     union {
-        uint32_t xs[kTok][kXsStride]; // x tile, two bf16 per word (before the layers)
-        struct {                      // after them
+        uint32_t xs[kTok][kXsStride]; // x tile, two bf16 per word (before the fill)
+        struct {                      // the records of (p, g), during the layers
+            float4 coef[8][64];       // (x1, y1, x2, y2)
+            uint2 off[8][64];         // byte offsets of v rows
+        } rec;
+        struct {                      // after the layers
             uint8_t codes[kTok][kCodeStride];   // e4m3 codes
             float red_max[kWarps][kTok];        // per-warp amax
             int red_sum[kWarps][kTok];          // per-warp row-sums (x 2^9)
         };
     };
-    uint2 rec[8][64];                 // records of (p, g): byte offsets of v[i] | v[j] << 16; f16 cos | sin << 16
     float cs[128];
 };
 
@@ -172,6 +181,13 @@ __device__ __forceinline__ void givens(float c, float s, float &vi, float &vj) {
     vj = nj;
 }
 
+// (fl(fl(x a.x) + fl(y b.x)), fl(fl(x a.y) + fl(y b.y))): one output of a
+// Givens pair for two tokens, each product and the sum rounded on its own
+__device__ __forceinline__ float2 rot2(float x, float y, float2 a, float2 b) {
+    return make_float2(__fadd_rn(__fmul_rn(x, a.x), __fmul_rn(y, b.x)),
+                       __fadd_rn(__fmul_rn(x, a.y), __fmul_rn(y, b.y)));
+}
+
 // kRot = false: the per-group quantisation (codes, asg, rs).
 // kRot = true: pass A of the per-token path -- the rotated rows rounded to
 // bf16 into xr [P][M][K] and each group's scale fl(max |xr| * fl(1/448)) into
@@ -217,17 +233,6 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
             uint32_t *d = &sm.xs[row][4 * q];
             d[0] = xv[it].x; d[1] = xv[it].y; d[2] = xv[it].z; d[3] = xv[it].w;
         }
-        // decoded records: shared-memory byte offsets of v[i][0], v[j][0]; f16 cos, sin
-#pragma unroll
-        for (int it = 0; it < kRv; ++it) {
-            const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
-            const uint32_t w0[2] = {rv[it].x, rv[it].z}, w1[2] = {rv[it].y, rv[it].w};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t i = w0[h] & 0xFF, j = (w0[h] >> 8) & 0xFF;
-                sm.rec[r][2 * q + h] = make_uint2(i * (uint32_t)(kTok * 4) | (j * (uint32_t)(kTok * 4)) << 16, w1[h]);
-            }
-        }
         if (tid < 128) sm.cs[tid] = half_to_float(csv);
         __syncthreads();
 
@@ -241,37 +246,119 @@ rotate_quant_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx, int P
             sm.v[2 * kw + 1][lane] = make_float2(__fmul_rn(bf16hi(w0), sm.cs[2 * kw + 1]),
                                                  __fmul_rn(bf16hi(w1), sm.cs[2 * kw + 1]));
         }
+        __syncthreads();     // the x tile is consumed: its space takes the records
+
+        // Records in chained order (pq_pack): slot t of a layer rotates the
+        // pair (u, v); from layer 1 on, u is the channel slot t kept in
+        // registers from the layer before.  Decoded per layer kind, with
+        // u' = c u + s v -> (c, s) and v' = c v - s u -> (-s, c) on (u, v):
+        //   layer 0:  operands (kept channel, other) both loaded: off = (kept,
+        //             other); out1 is kept, out2 stored at the other;
+        //   1..6:     operands (u held, v loaded from off.x); out1 is kept,
+        //             out2 (the other channel's output) stored at off.y;
+        //   7:        operands (u held, v from off.x); u' stored at off.y, v'
+        //             at off.x.
+        // The reversals are exact: fl(-s a) = -fl(s a) and x - y = x + (-y).
+        // Channel bytes are masked to 0..127, so every offset stays in v.
+#pragma unroll
+        for (int it = 0; it < kRv; ++it) {
+            const int c = tid + it * kThreads, r = c >> 5, q = c & 31;
+            const uint32_t w0[2] = {rv[it].x, rv[it].z}, w1[2] = {rv[it].y, rv[it].w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t u = (w0[h] & 0x7F) * (uint32_t)(kTok * 4);
+                const uint32_t v = ((w0[h] >> 8) & 0x7F) * (uint32_t)(kTok * 4);
+                const bool keep_v = (w0[h] >> 16) & 1;
+                const float cc = half_to_float((uint16_t)(w1[h] & 0xFFFFu));
+                const float ss = half_to_float((uint16_t)(w1[h] >> 16));
+                float4 cf;
+                uint2 of;
+                if (r == 0) {
+                    of = keep_v ? make_uint2(v, u) : make_uint2(u, v);
+                    cf = keep_v ? make_float4(cc, -ss, ss, cc) : make_float4(cc, ss, -ss, cc);
+                } else if (r < 7) {
+                    of = make_uint2(v, keep_v ? u : v);
+                    cf = keep_v ? make_float4(-ss, cc, cc, ss) : make_float4(cc, ss, -ss, cc);
+                } else {
+                    of = make_uint2(v, u);
+                    cf = make_float4(cc, ss, -ss, cc);
+                }
+                sm.rec.coef[r][2 * q + h] = cf;
+                sm.rec.off[r][2 * q + h] = of;
+            }
+        }
         __syncthreads();
 
-        // eight Givens layers; the pairs of one layer are disjoint, so a warp
-        // reads all operands of a batch of pairs before writing any result
+        // eight Givens layers.  Warp w owns slots 8w..8w+7 of every layer and
+        // keeps one value per slot (for both tokens of the lane) in kv; the
+        // pairs of one layer are disjoint, so a warp reads all operands of a
+        // batch of slots before writing any result.
         const uint32_t vlane = smem_addr(&sm.v[0][lane]);
-        for (int r = 0; r < 8; ++r) {
+        const int s0 = kPairsPerWarp * warp;
+        float2 kv[kPairsPerWarp];
+#pragma unroll
+        for (int half = 0; half < kPairsPerWarp / kBatch; ++half) {
+            float2 va[kBatch], vb[kBatch];
+            float4 cf[kBatch];
+            uint32_t ob[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const uint2 o = sm.rec.off[0][s0 + kBatch * half + q];
+                cf[q] = sm.rec.coef[0][s0 + kBatch * half + q];
+                ob[q] = vlane + o.y;
+                va[q] = lds_f32x2(vlane + o.x);
+                vb[q] = lds_f32x2(ob[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                kv[kBatch * half + q] = rot2(cf[q].x, cf[q].y, va[q], vb[q]);
+                sts_f32x2(ob[q], rot2(cf[q].z, cf[q].w, va[q], vb[q]));
+            }
+        }
+        __syncthreads();
+        for (int r = 1; r < 7; ++r) {
 #pragma unroll
             for (int half = 0; half < kPairsPerWarp / kBatch; ++half) {
-                float2 vi[kBatch], vj[kBatch];
-                float cc[kBatch], ss[kBatch];
-                uint32_t ai[kBatch], aj[kBatch];
+                float2 vb[kBatch];
+                float4 cf[kBatch];
+                uint32_t os[kBatch];
 #pragma unroll
                 for (int q = 0; q < kBatch; ++q) {
-                    const uint2 rr = sm.rec[r][kPairsPerWarp * warp + kBatch * half + q];
-                    ai[q] = vlane + (rr.x & 0xFFFFu);
-                    aj[q] = vlane + (rr.x >> 16);
-                    cc[q] = half_to_float((uint16_t)(rr.y & 0xFFFFu));
-                    ss[q] = half_to_float((uint16_t)(rr.y >> 16));
-                    vi[q] = lds_f32x2(ai[q]);
-                    vj[q] = lds_f32x2(aj[q]);
+                    const uint2 o = sm.rec.off[r][s0 + kBatch * half + q];
+                    cf[q] = sm.rec.coef[r][s0 + kBatch * half + q];
+                    os[q] = vlane + o.y;
+                    vb[q] = lds_f32x2(vlane + o.x);
                 }
 #pragma unroll
                 for (int q = 0; q < kBatch; ++q) {
-                    givens(cc[q], ss[q], vi[q].x, vj[q].x);
-                    givens(cc[q], ss[q], vi[q].y, vj[q].y);
-                    sts_f32x2(ai[q], vi[q]);
-                    sts_f32x2(aj[q], vj[q]);
+                    const float2 va = kv[kBatch * half + q];
+                    kv[kBatch * half + q] = rot2(cf[q].x, cf[q].y, va, vb[q]);
+                    sts_f32x2(os[q], rot2(cf[q].z, cf[q].w, va, vb[q]));
                 }
             }
             __syncthreads();
         }
+#pragma unroll
+        for (int half = 0; half < kPairsPerWarp / kBatch; ++half) {
+            float2 vb[kBatch];
+            float4 cf[kBatch];
+            uint32_t oa[kBatch], os[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const uint2 o = sm.rec.off[7][s0 + kBatch * half + q];
+                cf[q] = sm.rec.coef[7][s0 + kBatch * half + q];
+                oa[q] = vlane + o.x;
+                os[q] = vlane + o.y;
+                vb[q] = lds_f32x2(oa[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const float2 va = kv[kBatch * half + q];
+                sts_f32x2(os[q], rot2(cf[q].x, cf[q].y, va, vb[q]));
+                sts_f32x2(oa[q], rot2(cf[q].z, cf[q].w, va, vb[q]));
+            }
+        }
+        __syncthreads();
 
         // quantise: warp w takes channels kChPerWarp w .. + kChPerWarp - 1 of
         // both tokens of the lane
