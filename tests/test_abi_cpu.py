@@ -67,6 +67,31 @@ def test_pack5_byte_equal_to_oracle(L, orc, shape):
     assert L.pq_pack5(K, N, P, *([nul] * 11)) == 1
 
 
+@pytest.mark.parametrize("pattern", ["identity", "alternate", "reversed", "mixed"])
+def test_pack_chained_records_structured_pairings(L, orc, pattern):
+    """The packer's chained record order against the oracle's on pairings with
+    structure: the same pairs in every layer, an alternation that makes one
+    cycle through all channels, reversed repeats, and random rows between them."""
+    K, N, P = 256, 128, 2
+    prob = pqgen.make_problem(1, K, N, P=P, seed=41)
+    ident = np.arange(128, dtype=np.int16)
+    shifted = np.roll(ident, -1)
+    swapped = ident.reshape(64, 2)[:, ::-1].reshape(-1).copy()
+    rows = {"identity": [ident] * 8, "alternate": [ident, shifted] * 4,
+            "reversed": [ident, swapped] * 4}
+    pairs = prob.pairs.copy()
+    for p in range(P):
+        for g in range(K // 128):
+            seq = rows.get(pattern)
+            for r in range(8):
+                if seq is not None:
+                    pairs[p, r, 128 * g:128 * g + 128] = seq[r]
+                elif r % 2 == 0:
+                    pairs[p, r, 128 * g:128 * g + 128] = [ident, shifted, swapped][(p + g + r // 2) % 3]
+    rec, _, _ = pq.pq_pack(prob.qweight, prob.qzeros, prob.scales, pairs, prob.theta)
+    assert np.array_equal(rec, orc.chain_records(orc.records(pairs, prob.theta)))
+
+
 def test_pack_special_angles_and_scales(L, orc):
     """Angles and scales at the edges of f16: zero, subnormal, large, negative."""
     prob = pqgen.make_problem(1, 256, 256, seed=3)
